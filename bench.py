@@ -1,0 +1,329 @@
+"""Benchmark: fixed-m attention forward on the Wan2.2-DiT-shaped workload.
+
+One step = the whole hot path on one batch of synthetic input:
+    fm_bounds (norms, key mean, m, flags over all 75,600 keys)
+    fm_attn_chunk x 2 (two KV chunks of 37,800, the ring's steps run sequentially)
+    fm_finalize
+at B=1, H=40, S_q=S_k=75,600, D=128, bf16, virtual K-centering on.
+TFLOP/s = 4*H*S_q*S_k*D / t (the two contractions), t from CUDA events on the launch stream.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (plain fp64 C, all host cores) on a bounded sample
+of the same workload.  Under torchrun (N > 1) every rank runs an independent replica
+(weak scaling; the path needs no collective); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fixed-m attn fwd TFLOP/s (bf16, S=75,600, H=40, D=128) and % of BF16 tensor peak"
+WORKLOAD = "wan"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sms, maxs, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxs.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sms:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
+                "samples": len(sms)}
+
+
+def cpu_oracle_sample(target_s: float = 12.0, max_rows: int = 4096):
+    """Time the fp64 CPU oracle on 1 head x R query rows x all 75,600 keys of the workload.
+
+    R grows until one timed call takes about target_s seconds.  Returns (TFLOP/s, dict)."""
+    import oracle
+    import workloads
+
+    oracle.build()
+    w = workloads.WORKLOADS[WORKLOAD]
+    q, k, v = workloads.make_inputs(WORKLOAD, device="cpu", heads=[0])
+    threads = oracle.num_threads()
+    rows = 16
+    while True:
+        t0 = time.perf_counter()
+        oracle.attention(q[0, :, :rows], k[0], v[0], threads=threads)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or rows >= max_rows:
+            break
+        rows = min(max_rows, max(rows * 2, int(rows * target_s / max(dt, 1e-3))))
+    flops = w.flops(heads=1, rows=rows)
+    return flops / dt / 1e12, {"rows": rows, "seconds": dt, "threads": threads}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle as it stands, timed on a bounded sample per step."""
+    if rank != 0:
+        return
+    import oracle
+    import workloads
+
+    oracle.build()
+    w = workloads.WORKLOADS[WORKLOAD]
+    q, k, v = workloads.make_inputs(WORKLOAD, device="cpu", heads=[0])
+    threads = oracle.num_threads()
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle.attention(q[0, :, :rows], k[0], v[0], threads=threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.attention(q[0, :, :rows], k[0], v[0], threads=threads)
+        times.append(time.perf_counter() - t0)
+    t = sum(times)
+    flops = w.flops(heads=1, rows=rows) * args.steps
+    value = flops / t / 1e12
+    sample = f"1 head x {rows} query rows x all {w.N} keys per step (fp64 oracle, {threads} threads)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} H={w.H} S={w.Sq} D={w.D} bf16 inputs, sampled rows",
+                   "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import fixed_max_softmax_gb300 as fm
+    import workloads
+
+    fm.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = workloads.WORKLOADS[WORKLOAD]
+    chunks = workloads.chunk_bounds(w)
+    H = w.H if args.heads is None else args.heads
+    q, k, v = workloads.make_inputs(WORKLOAD, device=dev, heads=range(H))
+    fa = fm.FixedMAttention(w.B, H, w.Sq, w.N, w.D, dev, centering=True, out_dtype=torch.bfloat16)
+    stream = torch.cuda.current_stream(dev)
+    step_flops = w.flops(heads=w.B * H)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def step(ev=None):
+        fm.fm_bounds(q, k, v, fa.opt, fa.bounds, fa.workspace, stream)
+        for i, (s, n) in enumerate(chunks):
+            if ev is not None:
+                ev.append(torch.cuda.Event(enable_timing=True))
+                ev[-1].record(stream)
+            fm.fm_attn_chunk(q, k[:, :, s:s + n], v[:, :, s:s + n], fa.bounds, fa.opt, fa.acc_o, fa.acc_sum,
+                             fa.acc_max, i > 0, stream)
+            if ev is not None:
+                ev.append(torch.cuda.Event(enable_timing=True))
+                ev[-1].record(stream)
+        fm.fm_finalize(fa.acc_o, fa.acc_sum, fa.out, stream)
+
+    launches_per_step = 4 + len(chunks) + 1  # bounds: ksum, kmean, norms, finish; chunks; finalize
+    for _ in range(args.warmup):
+        step()
+    fm.fm_sync_status(stream)
+    flags = fa.bounds.flag
+    eligible = float(flags.float().mean().item())
+
+    # ---- timed region: inputs resident in HBM (each tensor 774 MB > L2)
+    chunk_events = []
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clk:
+        start.record(stream)
+        for _ in range(args.steps):
+            step(chunk_events)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier()
+    fm.fm_sync_status(stream)
+    t_ms = start.elapsed_time(end)
+    chunk_ms = [chunk_events[i].elapsed_time(chunk_events[i + 1]) for i in range(0, len(chunk_events), 2)]
+    if dist is not None:
+        tt = torch.tensor([t_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms = float(tt.item())
+    ms_per_step = t_ms / args.steps
+    value = world * step_flops * args.steps / (t_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers (pinned), copies timed
+    e2e = None
+    if args.e2e_steps > 0:
+        qh = q.cpu().pin_memory()
+        kh = k.cpu().pin_memory()
+        vh = v.cpu().pin_memory()
+        oh = torch.empty(fa.out.shape, dtype=fa.out.dtype).pin_memory()
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            fa.forward(qd, kd, vd, chunks, stream)
+            oh.copy_(fa.out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        fm.fm_sync_status(stream)
+        te = e0.elapsed_time(e1)
+        if dist is not None:
+            tt = torch.tensor([te], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            te = float(tt.item())
+        e2e = {"value": world * step_flops * args.e2e_steps / (te * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(3 * q.numel() * q.element_size()),
+               "d2h_bytes_per_step": int(fa.out.numel() * fa.out.element_size()),
+               "ms_per_step": te / args.e2e_steps, "steps": args.e2e_steps}
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    chunk_flops = [w.flops(heads=w.B * H, keys=n) for _, n in chunks]
+    per_launch_flops = statistics.mean(chunk_flops)
+    chunk_avg_ms = statistics.mean(chunk_ms)
+    achieved = per_launch_flops / (chunk_avg_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops_sustained"]
+    roofline = {"bound": "tensor", "kernel": "fm_chunk_tc_kernel", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": args.traffic,
+                "peak_kind": f"bf16 sustained ({peak_src})",
+                "frac_of_burst_peak": achieved / peaks["bf16_tflops"], "launch_ms": chunk_avg_ms}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cv, info = cpu_oracle_sample(args.cpu_seconds)
+        cpu = {"value": cv, "unit": "TFLOP/s", "cores": info["threads"], "kind": "oracle",
+               "sample": f"1 head x {info['rows']} query rows x all {w.N} keys, fp64, "
+                         f"{info['seconds']:.1f} s"}
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} H={H} S_q=S_k={w.Sq} D={w.D} bf16, "
+                               f"{len(chunks)} KV chunks of {chunks[0][1]}, virtual K-centering",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (774 MB per tensor), no flush",
+                   "fixed_m_tile_fraction": eligible},
+        "pct_of_peak": 100.0 * value / peak,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": {k2: clocks[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons")},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=256, help="query rows per reference step")
+    ap.add_argument("--heads", type=int, default=None, help="first N heads only (profiling a smaller case)")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per chunk launch from an ncu capture of the current kernel")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank, world, local_rank = dist_env()
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,235 @@
+"""fixed_max_softmax_gb300 -- fixed-m (const-max) attention forward on GB300.
+
+A thin ctypes binding of ``libfm.so`` (C ABI: ``include/fm.h``).  Every step of the
+path -- bounds, chunk folding, finalize -- runs in the library's CUDA kernels; this
+module only marshals torch tensors into ``fm_tensor`` descriptors, passes raw
+pointers and the current CUDA stream, and turns error codes into exceptions.
+PyTorch provides device memory and streams and nothing else.
+
+Functions with the ABI's names (same arguments, torch tensors in place of pointers):
+``fm_bounds_workspace_size``, ``fm_bounds``, ``fm_attn_chunk``, ``fm_finalize``,
+``fm_sync_status``, ``fm_last_error``, ``fm_version``.
+
+``FixedMAttention`` owns the buffers of one problem shape and runs the whole path
+(bounds, one ``fm_attn_chunk`` per KV chunk, finalize); ``attention()`` is the
+one-call form.
+
+There is no CPU path: if the library is not built, ``load()`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libfm.so")
+
+FM_F32, FM_BF16, FM_F16, FM_F8E4M3, FM_F8E5M2 = 0, 1, 2, 3, 4
+FM_OK, FM_ERR_ARG, FM_ERR_SHAPE, FM_ERR_DTYPE, FM_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
+FM_ERR_BOUNDS_MISMATCH, FM_ERR_CUDA, FM_ERR_TIMEOUT = 5, 6, 7
+FM_BOUNDS_MAGIC = 0x314D4246
+FM_BLOCK_Q = 128
+ERROR_NAMES = {0: "FM_OK", 1: "FM_ERR_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_DTYPE", 4: "FM_ERR_UNSUPPORTED",
+               5: "FM_ERR_BOUNDS_MISMATCH", 6: "FM_ERR_CUDA", 7: "FM_ERR_TIMEOUT"}
+ABI_SYMBOLS = ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
+               "fm_last_error", "fm_version")
+
+
+class FMError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{ERROR_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class fm_tensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("S", ctypes.c_int64), ("D", ctypes.c_int64),
+                ("stride", ctypes.c_int64 * 4)]
+
+
+class fm_opts(ctypes.Structure):
+    _fields_ = [("softmax_scale", ctypes.c_float), ("centering", ctypes.c_int32),
+                ("force_online", ctypes.c_int32)]
+
+
+class fm_bounds_out(ctypes.Structure):
+    _fields_ = [("m", ctypes.c_void_p), ("flag", ctypes.c_void_p), ("qmax_sq", ctypes.c_void_p),
+                ("kmax_sq", ctypes.c_void_p), ("kbar", ctypes.c_void_p), ("qkbar", ctypes.c_void_p),
+                ("vmax_sq", ctypes.c_void_p),
+                ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("Sq", ctypes.c_int64), ("D", ctypes.c_int64),
+                ("n_qblocks", ctypes.c_int64), ("N_total", ctypes.c_int64),
+                ("C", ctypes.c_int32), ("W", ctypes.c_int32), ("gate", ctypes.c_int32),
+                ("centered", ctypes.c_int32), ("alpha", ctypes.c_float), ("dtype", ctypes.c_int32),
+                ("kv_seen", ctypes.c_int64), ("online_lock", ctypes.c_int32), ("magic", ctypes.c_uint32)]
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load libfm.so (build it first with fixed_max_softmax_gb300.build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise FMError(FM_ERR_CUDA, f"{p} is missing: the CUDA library is not built "
+                                   "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(p)
+    P, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.fm_bounds_workspace_size.argtypes = [i64, i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)]
+    lib.fm_bounds.argtypes = [P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.fm_attn_chunk.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_int, P]
+    lib.fm_finalize.argtypes = [P, P, P, P]
+    lib.fm_sync_status.argtypes = [P]
+    lib.fm_last_error.restype = ctypes.c_char_p
+    lib.fm_last_error.argtypes = []
+    lib.fm_version.argtypes = []
+    for name in ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
+                 "fm_version"):
+        getattr(lib, name).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+_DTYPES = {torch.float32: FM_F32, torch.bfloat16: FM_BF16, torch.float16: FM_F16}
+if hasattr(torch, "float8_e4m3fn"):
+    _DTYPES[torch.float8_e4m3fn] = FM_F8E4M3
+if hasattr(torch, "float8_e5m2"):
+    _DTYPES[torch.float8_e5m2] = FM_F8E5M2
+
+
+def tensor(t: torch.Tensor) -> fm_tensor:
+    """Describe a 4-D [B, H, S, D] torch tensor (any strides) as an fm_tensor."""
+    if t.dim() != 4:
+        raise FMError(FM_ERR_SHAPE, f"expected a 4-D [B, H, S, D] tensor, got shape {tuple(t.shape)}")
+    d = fm_tensor()
+    d.ptr = t.data_ptr() or None
+    d.dtype = _DTYPES.get(t.dtype, -1)
+    d.B, d.H, d.S, d.D = t.shape
+    for i, s in enumerate(t.stride()):
+        d.stride[i] = s
+    return d
+
+
+def opts(softmax_scale: float = 0.0, centering: bool = False, force_online: bool = False) -> fm_opts:
+    return fm_opts(float(softmax_scale), int(bool(centering)), int(bool(force_online)))
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(rc: int):
+    if rc != FM_OK:
+        raise FMError(rc, load().fm_last_error().decode())
+    return rc
+
+
+def fm_version() -> int:
+    return load().fm_version()
+
+
+def fm_last_error() -> str:
+    return load().fm_last_error().decode()
+
+
+def fm_bounds_workspace_size(B: int, H: int, N_total: int, D: int) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fm_bounds_workspace_size(B, H, N_total, D, ctypes.byref(n)))
+    return n.value
+
+
+class Bounds:
+    """Device arrays of one fm_bounds_out (allocated with torch) plus the struct itself."""
+
+    def __init__(self, B: int, H: int, Sq: int, D: int, device):
+        nqb = (Sq + FM_BLOCK_Q - 1) // FM_BLOCK_Q
+        kw = dict(device=device)
+        self.m = torch.zeros(B, H, nqb, dtype=torch.int32, **kw)
+        self.flag = torch.zeros(B, H, nqb, dtype=torch.uint8, **kw)
+        self.qmax_sq = torch.zeros(B, H, nqb, dtype=torch.float32, **kw)
+        self.kmax_sq = torch.zeros(B, H, dtype=torch.float32, **kw)
+        self.kbar = torch.zeros(B, H, D, dtype=torch.float32, **kw)
+        self.qkbar = torch.zeros(B, H, max(Sq, 1), dtype=torch.float32, **kw)
+        self.vmax_sq = torch.zeros(1, dtype=torch.float32, **kw)
+        self.out = fm_bounds_out()
+        self.out.m, self.out.flag = self.m.data_ptr(), self.flag.data_ptr()
+        self.out.qmax_sq, self.out.kmax_sq = self.qmax_sq.data_ptr(), self.kmax_sq.data_ptr()
+        self.out.kbar, self.out.qkbar, self.out.vmax_sq = (self.kbar.data_ptr(), self.qkbar.data_ptr(),
+                                                           self.vmax_sq.data_ptr())
+
+
+def fm_bounds(q, k_full, v_full, opt: fm_opts, bounds: Bounds, workspace: torch.Tensor | None, stream=None):
+    tq, tk, tv = tensor(q), tensor(k_full), tensor(v_full)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check(load().fm_bounds(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), ctypes.byref(opt),
+                                   ctypes.byref(bounds.out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fm_attn_chunk(q, k_chunk, v_chunk, bounds: Bounds, opt: fm_opts, acc_o, acc_sum, acc_max,
+                  accumulate: bool, stream=None):
+    tq, tk, tv = tensor(q), tensor(k_chunk), tensor(v_chunk)
+    return _check(load().fm_attn_chunk(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                       ctypes.byref(bounds.out), ctypes.byref(opt), _ptr(acc_o), _ptr(acc_sum),
+                                       _ptr(acc_max), int(bool(accumulate)), _stream(stream)))
+
+
+def fm_finalize(acc_o, acc_sum, o_out, stream=None):
+    to = tensor(o_out)
+    return _check(load().fm_finalize(_ptr(acc_o), _ptr(acc_sum), ctypes.byref(to), _stream(stream)))
+
+
+def fm_sync_status(stream=None):
+    return _check(load().fm_sync_status(_stream(stream)))
+
+
+class FixedMAttention:
+    """Buffers and the call sequence of one fixed-m attention forward of a fixed shape.
+
+    forward(q, k, v, chunks) runs fm_bounds over all of K/V, one fm_attn_chunk per
+    (start, length) slice of the key sequence (the ring's steps, sequentially), and
+    fm_finalize into `out` (fp32 or the input dtype).
+    """
+
+    def __init__(self, B, H, Sq, N, D, device="cuda", centering=False, softmax_scale=0.0,
+                 force_online=False, out_dtype=torch.float32):
+        self.shape = (B, H, Sq, N, D)
+        self.opt = opts(softmax_scale, centering, force_online)
+        self.bounds = Bounds(B, H, Sq, D, device)
+        nbytes = fm_bounds_workspace_size(B, H, N, D)
+        self.workspace = torch.empty(max(nbytes, 16) // 4 + 4, dtype=torch.float32, device=device)
+        self.acc_o = torch.empty(B, H, Sq, D, dtype=torch.float32, device=device)
+        self.acc_sum = torch.empty(B, H, Sq, dtype=torch.float32, device=device)
+        self.acc_max = torch.empty(B, H, Sq, dtype=torch.float32, device=device)
+        self.out = torch.empty(B, H, Sq, D, dtype=out_dtype, device=device)
+
+    def forward(self, q, k, v, chunks=None, stream=None):
+        N = k.shape[2]
+        chunks = [(0, N)] if chunks is None else chunks
+        fm_bounds(q, k, v, self.opt, self.bounds, self.workspace, stream)
+        for i, (s, n) in enumerate(chunks):
+            fm_attn_chunk(q, k[:, :, s:s + n], v[:, :, s:s + n], self.bounds, self.opt, self.acc_o,
+                          self.acc_sum, self.acc_max, i > 0, stream)
+        fm_finalize(self.acc_o, self.acc_sum, self.out, stream)
+        return self.out
+
+    __call__ = forward
+
+
+def attention(q, k, v, chunks=None, centering=False, softmax_scale=0.0, force_online=False,
+              out_dtype=torch.float32, stream=None):
+    """One-call fixed-m attention forward: returns o [B, H, Sq, D]."""
+    B, H, Sq, D = q.shape
+    fa = FixedMAttention(B, H, Sq, k.shape[2], D, q.device, centering, softmax_scale, force_online, out_dtype)
+    return fa.forward(q, k, v, chunks, stream).clone()

@@ -1,0 +1,341 @@
+// fm_api.cu -- the C ABI of libfm: argument validation, constants, dispatch.
+//
+// Every entry point validates its arguments on the host, returns an error code without
+// enqueuing anything when they are wrong, and otherwise enqueues kernels on the caller's
+// stream and returns immediately.  The only state kept is a thread-local error message
+// and, per GPU, one device word where kernels record a pipeline wait that gave up.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+#include <string>
+
+#include "fm_internal.h"
+
+namespace fm {
+
+// Per-GPU error word: set by a kernel whose pipeline wait ran past its limit.
+__device__ unsigned int g_dev_error;
+
+namespace {
+
+thread_local std::string t_err;
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char *what) {
+  return fail(FM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+unsigned int *dev_error_ptr() {
+  static unsigned int *ptrs[kMaxDevices] = {};
+  static std::once_flag once[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::call_once(once[dev], [dev] {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dev_error) == cudaSuccess) ptrs[dev] = static_cast<unsigned int *>(p);
+  });
+  return ptrs[dev];
+}
+
+// ceil(log2 n) for n >= 1 (0 for n <= 1): the number of bits of n - 1.
+int ceil_log2_i64(int64_t n) {
+  if (n <= 1) return 0;
+  uint64_t x = (uint64_t)(n - 1);
+  int bits = 0;
+  while (x) {
+    ++bits;
+    x >>= 1;
+  }
+  return bits;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Validate one fm_tensor and turn it into a View.  `what` names it in messages.
+int to_view(const fm_tensor *t, const char *what, View *v) {
+  if (!t) return fail(FM_ERR_ARG, "%s: NULL tensor", what);
+  if (t->dtype == FM_F16 || t->dtype == FM_F8E4M3 || t->dtype == FM_F8E5M2)
+    return fail(FM_ERR_DTYPE,
+                "%s: fp16/fp8 inputs are rejected: 2^C-scale fixed-m terms overflow their exponent range",
+                what);
+  if (t->dtype != FM_F32 && t->dtype != FM_BF16) return fail(FM_ERR_ARG, "%s: unknown dtype %d", what, t->dtype);
+  if (t->B < 0 || t->H < 0 || t->S < 0 || t->D < 0)
+    return fail(FM_ERR_ARG, "%s: negative dimension [%lld,%lld,%lld,%lld]", what, (long long)t->B,
+                (long long)t->H, (long long)t->S, (long long)t->D);
+  for (int i = 0; i < 4; ++i)
+    if (t->stride[i] < 0) return fail(FM_ERR_ARG, "%s: negative stride", what);
+  if (t->D != 64 && t->D != 128)
+    return fail(FM_ERR_UNSUPPORTED, "%s: head dimension %lld not supported (64 or 128)", what, (long long)t->D);
+  if (t->B > 65535 || t->H > 65535) return fail(FM_ERR_UNSUPPORTED, "%s: B or H above 65535", what);
+  const int64_t n = t->B * t->H * t->S * t->D;
+  const size_t es = t->dtype == FM_F32 ? 4 : 2;
+  if (n > 0 && !t->ptr) return fail(FM_ERR_ARG, "%s: NULL data pointer", what);
+  if (reinterpret_cast<uintptr_t>(t->ptr) % es) return fail(FM_ERR_UNSUPPORTED, "%s: misaligned data", what);
+  v->ptr = t->ptr;
+  v->dtype = t->dtype;
+  v->B = t->B;
+  v->H = t->H;
+  v->S = t->S;
+  v->D = t->D;
+  v->sB = t->stride[0];
+  v->sH = t->stride[1];
+  v->sS = t->stride[2];
+  v->sD = t->stride[3];
+  return FM_OK;
+}
+
+// softmax_scale -> alpha = scale * log2(e) (fp64), or an error.
+int make_alpha(const fm_opts *opts, int64_t D, double *alpha) {
+  double scale = (opts && opts->softmax_scale > 0.f) ? (double)opts->softmax_scale : 1.0 / sqrt((double)D);
+  if (!(scale > 0.0) || !isfinite(scale)) return fail(FM_ERR_ARG, "softmax_scale must be finite");
+  *alpha = scale * 1.4426950408889634;  // log2(e)
+  return FM_OK;
+}
+
+int check_qkv(const View &q, const View &k, const View &v) {
+  if (q.dtype != k.dtype || q.dtype != v.dtype) return fail(FM_ERR_DTYPE, "q, k and v must share one dtype");
+  if (k.H != q.H || v.H != q.H)
+    return fail(FM_ERR_UNSUPPORTED, "k/v heads (%lld/%lld) differ from q heads (%lld): GQA/MQA not supported",
+                (long long)k.H, (long long)v.H, (long long)q.H);
+  if (k.B != q.B || v.B != q.B) return fail(FM_ERR_SHAPE, "batch sizes of q, k, v differ");
+  if (k.S != v.S) return fail(FM_ERR_SHAPE, "k and v lengths differ (%lld vs %lld)", (long long)k.S, (long long)v.S);
+  if (k.D != q.D || v.D != q.D) return fail(FM_ERR_SHAPE, "head dimensions of q, k, v differ");
+  return FM_OK;
+}
+
+}  // namespace
+
+int current_device_sm_count() {
+  static int counts[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+  if (!counts[dev]) {
+    int c = 0;
+    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+    counts[dev] = c > 0 ? c : 148;
+  }
+  return counts[dev];
+}
+
+}  // namespace fm
+
+using namespace fm;
+
+extern "C" {
+
+int fm_version(void) { return (1 << 16) | 0; }
+
+const char *fm_last_error(void) { return t_err.c_str(); }
+
+int fm_bounds_workspace_size(int64_t B, int64_t H, int64_t N_total, int64_t D, size_t *bytes) {
+  t_err.clear();
+  if (!bytes) return fail(FM_ERR_ARG, "bytes is NULL");
+  if (B < 0 || H < 0 || N_total < 0 || D < 0) return fail(FM_ERR_ARG, "negative size");
+  *bytes = bounds_workspace_bytes(B, H, N_total, D);
+  return FM_OK;
+}
+
+int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_full, const fm_opts *opts,
+              fm_bounds_out *out, void *workspace, size_t workspace_bytes, fm_stream_t stream) {
+  t_err.clear();
+  View vq, vk, vv;
+  int rc;
+  if ((rc = to_view(q, "q", &vq)) || (rc = to_view(k_full, "k_full", &vk)) || (rc = to_view(v_full, "v_full", &vv)))
+    return rc;
+  if ((rc = check_qkv(vq, vk, vv))) return rc;
+  if (!out) return fail(FM_ERR_ARG, "out is NULL");
+  if (opts && opts->centering != 0 && opts->centering != 1) return fail(FM_ERR_ARG, "centering must be 0 or 1");
+  const int centering = opts ? opts->centering : 0;
+  double alpha;
+  if ((rc = make_alpha(opts, vq.D, &alpha))) return rc;
+  const int64_t B = vq.B, H = vq.H, Sq = vq.S, D = vq.D, N = vk.S;
+  const int64_t nqb = ceil_div(Sq, FM_BLOCK_Q);
+  // every non-empty device array must be given (torch hands out NULL for empty ones)
+  if ((B * H * nqb > 0 && (!out->m || !out->flag || !out->qmax_sq)) || (B * H * Sq > 0 && !out->qkbar) ||
+      (B * H > 0 && (!out->kmax_sq || !out->kbar || !out->vmax_sq)))
+    return fail(FM_ERR_ARG, "fm_bounds_out: every device array pointer must be set");
+  const size_t need = bounds_workspace_bytes(B, H, N, D);
+  if (workspace_bytes < need) return fail(FM_ERR_ARG, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  if (need > 0 && !workspace) return fail(FM_ERR_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) % 16) return fail(FM_ERR_ARG, "workspace must be 16-byte aligned");
+
+  // C(N) = 127 - ceil(log2 N) - ceil(log2 Vmax), W = C + 125, gate = floor(W / 2)
+  // ("feat(attention): fixed-m splash attention kernel with dynamic bounds and safety
+  // fallbacks", Summary).
+  const int C = 127 - ceil_log2_i64(N) - ceil_log2_i64(FM_VMAX);
+  const int W = C + 125;
+  const int gate = W >= 0 ? W / 2 : -((-W + 1) / 2);
+
+  out->B = B;
+  out->H = H;
+  out->Sq = Sq;
+  out->D = D;
+  out->n_qblocks = nqb;
+  out->N_total = N;
+  out->C = C;
+  out->W = W;
+  out->gate = gate;
+  out->centered = centering;
+  out->alpha = (float)alpha;
+  out->dtype = vq.dtype;
+  out->kv_seen = 0;
+  out->online_lock = -1;
+  out->magic = 0;
+  if (B * H == 0) {
+    out->magic = FM_BOUNDS_MAGIC;
+    return FM_OK;
+  }
+  BoundsArgs a;
+  a.q = vq;
+  a.k = vk;
+  a.v = vv;
+  a.centering = centering;
+  a.alpha = alpha;
+  a.C = C;
+  a.gate = gate;
+  a.nqb = nqb;
+  a.m = out->m;
+  a.flag = out->flag;
+  a.qmax_sq = out->qmax_sq;
+  a.kmax_sq = out->kmax_sq;
+  a.kbar = out->kbar;
+  a.qkbar = out->qkbar;
+  a.vmax_sq = out->vmax_sq;
+  a.ws = workspace;
+  a.ws_bytes = workspace_bytes;
+  cudaError_t e = launch_bounds(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fm_bounds launch");
+  out->magic = FM_BOUNDS_MAGIC;
+  return FM_OK;
+}
+
+int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk, fm_bounds_out *bounds,
+                  const fm_opts *opts, float *acc_o, float *acc_sum, float *acc_max, int accumulate,
+                  fm_stream_t stream) {
+  t_err.clear();
+  View vq, vk, vv;
+  int rc;
+  if ((rc = to_view(q, "q", &vq)) || (rc = to_view(k_chunk, "k_chunk", &vk)) ||
+      (rc = to_view(v_chunk, "v_chunk", &vv)))
+    return rc;
+  if ((rc = check_qkv(vq, vk, vv))) return rc;
+  if (!bounds) return fail(FM_ERR_ARG, "bounds is NULL");
+  if (accumulate != 0 && accumulate != 1) return fail(FM_ERR_ARG, "accumulate must be 0 or 1");
+  if (opts && ((opts->centering != 0 && opts->centering != 1) || (opts->force_online != 0 && opts->force_online != 1)))
+    return fail(FM_ERR_ARG, "centering and force_online must be 0 or 1");
+  const int centering = opts ? opts->centering : 0;
+  const int force_online = opts ? opts->force_online : 0;
+  // the bounds must belong to this call
+  if (bounds->magic != FM_BOUNDS_MAGIC)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "bounds were not produced by fm_bounds (magic 0x%08x)", bounds->magic);
+  const int64_t nqb = ceil_div(vq.S, FM_BLOCK_Q);
+  if (bounds->B != vq.B || bounds->H != vq.H || bounds->Sq != vq.S || bounds->n_qblocks != nqb ||
+      bounds->D != vq.D)
+    return fail(FM_ERR_BOUNDS_MISMATCH,
+                "bounds shape [B=%lld,H=%lld,nqb=%lld] (Sq=%lld, D=%lld) does not match q [%lld,%lld,%lld] (Sq=%lld, "
+                "D=%lld)",
+                (long long)bounds->B, (long long)bounds->H, (long long)bounds->n_qblocks, (long long)bounds->Sq,
+                (long long)bounds->D, (long long)vq.B, (long long)vq.H, (long long)nqb, (long long)vq.S,
+                (long long)vq.D);
+  if (bounds->centered != centering)
+    return fail(FM_ERR_BOUNDS_MISMATCH,
+                "bounds measured with centering=%d cannot serve a call with centering=%d: raw-key norms do not "
+                "bound centered logits",
+                bounds->centered, centering);
+  if (bounds->dtype != vq.dtype) return fail(FM_ERR_BOUNDS_MISMATCH, "bounds were computed for another dtype");
+  double alpha;
+  if ((rc = make_alpha(opts, vq.D, &alpha))) return rc;
+  if ((float)alpha != bounds->alpha)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "softmax scale differs from the one the bounds were computed with");
+  const int64_t seen = accumulate ? bounds->kv_seen + vk.S : vk.S;
+  if (seen > bounds->N_total)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "%lld keys folded in exceed the %lld keys the bounds cover",
+                (long long)seen, (long long)bounds->N_total);
+  if (accumulate && bounds->online_lock >= 0 && bounds->online_lock != force_online)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "force_online must stay the same across the chunks of one call");
+  if (accumulate && bounds->online_lock < 0)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "accumulate=1 before any accumulate=0 chunk for these bounds");
+  const int64_t rows = vq.B * vq.H * vq.S;
+  if (rows > 0 && (!acc_o || !acc_sum || !acc_max)) return fail(FM_ERR_ARG, "accumulator pointer is NULL");
+  if (reinterpret_cast<uintptr_t>(acc_o) % 16 || reinterpret_cast<uintptr_t>(acc_sum) % 4 ||
+      reinterpret_cast<uintptr_t>(acc_max) % 4)
+    return fail(FM_ERR_ARG, "acc_o must be 16-byte aligned, acc_sum/acc_max 4-byte aligned");
+
+  unsigned int *err = dev_error_ptr();
+  if (!err) return fail(FM_ERR_CUDA, "cannot resolve the device error word (no CUDA device?)");
+  ChunkArgs a;
+  a.q = vq;
+  a.k = vk;
+  a.v = vv;
+  a.alpha = (float)alpha;
+  a.force_online = force_online;
+  a.accumulate = accumulate;
+  a.nqb = nqb;
+  a.m = bounds->m;
+  a.flag = bounds->flag;
+  a.qkbar = bounds->qkbar;
+  a.acc_o = acc_o;
+  a.acc_sum = acc_sum;
+  a.acc_max = acc_max;
+  a.err = err;
+  a.timeout_ns = kWaitTimeoutNs;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (rows > 0) {
+    if (vk.S == 0) {
+      if (!accumulate) e = launch_chunk_empty_init(a, st);
+    } else if (chunk_tc_supported(a)) {
+      e = launch_chunk_tc(a, st);
+      if (e == cudaErrorNotSupported) e = launch_chunk_simt(a, st);
+    } else {
+      e = launch_chunk_simt(a, st);
+    }
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "fm_attn_chunk launch");
+  bounds->kv_seen = seen;
+  bounds->online_lock = force_online;
+  return FM_OK;
+}
+
+int fm_finalize(const float *acc_o, const float *acc_sum, const fm_tensor *o_out, fm_stream_t stream) {
+  t_err.clear();
+  View vo;
+  int rc;
+  if ((rc = to_view(o_out, "o_out", &vo))) return rc;
+  const int64_t rows = vo.B * vo.H * vo.S;
+  if (rows > 0 && (!acc_o || !acc_sum)) return fail(FM_ERR_ARG, "accumulator pointer is NULL");
+  if (reinterpret_cast<uintptr_t>(acc_o) % 16) return fail(FM_ERR_ARG, "acc_o must be 16-byte aligned");
+  cudaError_t e = launch_finalize(acc_o, acc_sum, vo, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fm_finalize launch");
+  return FM_OK;
+}
+
+int fm_sync_status(fm_stream_t stream) {
+  t_err.clear();
+  cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_dev_error, sizeof word);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+  if (word != 0) {
+    const unsigned int zero = 0;
+    cudaMemcpyToSymbol(g_dev_error, &zero, sizeof zero);
+    return fail(FM_ERR_TIMEOUT, "a kernel pipeline wait ran past its limit (code %u); outputs are invalid", word);
+  }
+  return FM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,295 @@
+// fm_bounds.cu -- the bounds pass of fixed-m attention.
+//
+// Computes, per (batch, head): the key mean kbar (when centering), the maximum key norm
+// (of k_j - kbar, or of k_j), per 128-row Q-block the maximum query norm, per row the
+// centering term alpha*q_i.kbar, the global max of v^2, and from those the shift
+// m = ceil(U) - C(N) and the eligibility flag v_ok && U <= gate, with
+// U = alpha*sqrt(max|q|^2)*sqrt(max|k|^2).
+// Sources: "feat(attention): fixed-m splash attention kernel with dynamic bounds and
+// safety fallbacks" (PR #477), Summary; the fused norm reduction of "Kernel reference:
+// ring_attention_const_max_fwd", section "Transpose prologue with fused norms"; the key
+// mean over real tokens of PR #478, Summary.
+//
+// Launches (all deterministic: fixed-order sums, maxima without atomics):
+//   1. ksum    (centering only) partial key sums, P row ranges per head  -> workspace
+//   2. kmean   (centering only) ordered sum of the P partials / N          -> kbar
+//   3. main    one grid over Q-blocks, K row-blocks and V row-blocks: row norms via warp
+//              shuffles; per-block maxima -> qmax_sq (Q) and the workspace (K, V);
+//              qkbar per row
+//   4. finish  per head: key max, global V max, U, m, flag
+// Bytes: Q + K + V once each, plus K once more for the mean when centering.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fm_internal.h"
+
+namespace fm {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kQRows = FM_BLOCK_Q;  // rows per Q-block
+constexpr int kKVRows = 256;        // rows per K / V block of the main pass
+constexpr int kMaxPartials = 64;    // row ranges per head for the key sum
+
+__host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline int64_t num_partials(int64_t N) {
+  int64_t p = ceil_div(N, 1024);
+  return p < 1 ? 1 : (p > kMaxPartials ? kMaxPartials : p);
+}
+
+struct WsLayout {
+  int64_t P, nkb, nvb;
+  size_t off_part, off_kb, off_vb, total;
+};
+
+WsLayout ws_layout(int64_t B, int64_t H, int64_t N, int64_t D) {
+  WsLayout w;
+  w.P = num_partials(N);
+  w.nkb = ceil_div(N, kKVRows);
+  w.nvb = w.nkb;
+  w.off_part = 0;
+  w.off_kb = w.off_part + sizeof(float) * (size_t)(B * H * w.P * D);
+  w.off_vb = w.off_kb + sizeof(float) * (size_t)(B * H * w.nkb);
+  w.total = w.off_vb + sizeof(float) * (size_t)(B * H * w.nvb);
+  w.total = (w.total + 255) & ~(size_t)255;
+  return w;
+}
+
+// Load the EPL elements of row `row` that lane `lane` owns (d = lane*EPL + e) as fp32.
+template <typename T, int EPL, bool CONTIG>
+__device__ __forceinline__ void load_row(const T *base, int64_t sD, int lane, float (&x)[EPL]) {
+  if constexpr (CONTIG && sizeof(T) == 2 && EPL == 4) {
+    uint2 u = *reinterpret_cast<const uint2 *>(base + lane * 4);
+    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162 *>(&u.x);
+    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162 *>(&u.y);
+    float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+    x[0] = fa.x; x[1] = fa.y; x[2] = fb.x; x[3] = fb.y;
+  } else if constexpr (CONTIG && sizeof(T) == 2 && EPL == 2) {
+    __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(base + lane * 2);
+    float2 fa = __bfloat1622float2(a);
+    x[0] = fa.x; x[1] = fa.y;
+  } else if constexpr (CONTIG && sizeof(T) == 4 && EPL == 4) {
+    float4 f = *reinterpret_cast<const float4 *>(base + lane * 4);
+    x[0] = f.x; x[1] = f.y; x[2] = f.z; x[3] = f.w;
+  } else if constexpr (CONTIG && sizeof(T) == 4 && EPL == 2) {
+    float2 f = *reinterpret_cast<const float2 *>(base + lane * 2);
+    x[0] = f.x; x[1] = f.y;
+  } else {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      T t = base[(int64_t)(lane * EPL + e) * sD];
+      if constexpr (sizeof(T) == 2) x[e] = __bfloat162float(t); else x[e] = (float)t;
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// 1. Partial key sums: CTA (p, h, b) sums rows [p*len, (p+1)*len) of head (b, h).
+template <typename T, int EPL, bool CONTIG>
+__global__ void __launch_bounds__(kThreads) ksum_kernel(View k, int64_t P, float *part) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t b = blockIdx.z, h = blockIdx.y, p = blockIdx.x;
+  const int64_t len = ceil_div(k.S, P);
+  const int64_t r0 = p * len, r1 = min(k.S, r0 + len);
+  const T *base = reinterpret_cast<const T *>(k.ptr) + b * k.sB + h * k.sH;
+  float acc[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+  for (int64_t r = r0 + warp; r < r1; r += kWarps) {
+    float x[EPL];
+    load_row<T, EPL, CONTIG>(base + r * k.sS, k.sD, lane, x);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] += x[e];
+  }
+  __shared__ float red[kWarps][128];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) red[warp][lane * EPL + e] = acc[e];
+  __syncthreads();
+  const int D = 32 * EPL;
+  if (threadIdx.x < D) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += red[w][threadIdx.x];
+    part[((b * k.H + h) * P + p) * D + threadIdx.x] = s;
+  }
+}
+
+// 2. Key mean: ordered sum of the P partials of head (b, h), divided by N.
+__global__ void kmean_kernel(const float *part, int64_t H, int64_t P, int D, int64_t N, float *kbar) {
+  const int64_t bh = blockIdx.y * H + blockIdx.x;
+  const int d = threadIdx.x;
+  if (d >= D) return;
+  float s = 0.f;
+  for (int64_t p = 0; p < P; ++p) s += part[(bh * P + p) * D + d];
+  kbar[bh * D + d] = N > 0 ? s / (float)N : 0.f;
+}
+
+// 3. Norms.  blockIdx.x in [0, nqb) -> Q-block; [nqb, nqb+nkb) -> K rows; then V rows.
+template <typename T, int EPL, bool CONTIG>
+__global__ void __launch_bounds__(kThreads)
+    norms_kernel(View q, View k, View v, int64_t nqb, int64_t nkb, int centering, float alpha,
+                 const float *kbar, float *qmax_sq, float *qkbar, float *kblk, float *vblk) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t b = blockIdx.z, h = blockIdx.y, bx = blockIdx.x;
+  const int64_t bh = b * q.H + h;
+  const int D = 32 * EPL;
+  __shared__ float wmax[kWarps];
+  float kb[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) kb[e] = centering ? kbar[bh * D + lane * EPL + e] : 0.f;
+
+  float best = 0.f;  // maxima of non-negative quantities start at 0
+  if (bx < nqb) {
+    // Q-block: per-row |q|^2 and alpha * q.kbar
+    const T *base = reinterpret_cast<const T *>(q.ptr) + b * q.sB + h * q.sH;
+    const int64_t r0 = bx * kQRows, r1 = min(q.S, r0 + kQRows);
+    for (int64_t r = r0 + warp; r < r1; r += kWarps) {
+      float x[EPL];
+      load_row<T, EPL, CONTIG>(base + r * q.sS, q.sD, lane, x);
+      float ss = 0.f, dk = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        ss = fmaf(x[e], x[e], ss);
+        dk = fmaf(x[e], kb[e], dk);
+      }
+      ss = warp_sum(ss);
+      dk = warp_sum(dk);
+      best = fmaxf(best, ss);
+      if (lane == 0) qkbar[bh * q.S + r] = alpha * dk;
+    }
+  } else if (bx < nqb + nkb) {
+    // K rows: |k - kbar|^2 (kbar = 0 when not centering)
+    const T *base = reinterpret_cast<const T *>(k.ptr) + b * k.sB + h * k.sH;
+    const int64_t r0 = (bx - nqb) * kKVRows, r1 = min(k.S, r0 + kKVRows);
+    for (int64_t r = r0 + warp; r < r1; r += kWarps) {
+      float x[EPL];
+      load_row<T, EPL, CONTIG>(base + r * k.sS, k.sD, lane, x);
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        float c = x[e] - kb[e];
+        ss = fmaf(c, c, ss);
+      }
+      best = fmaxf(best, warp_sum(ss));
+    }
+  } else {
+    // V rows: max element square
+    const T *base = reinterpret_cast<const T *>(v.ptr) + b * v.sB + h * v.sH;
+    const int64_t r0 = (bx - nqb - nkb) * kKVRows, r1 = min(v.S, r0 + kKVRows);
+    for (int64_t r = r0 + warp; r < r1; r += kWarps) {
+      float x[EPL];
+      load_row<T, EPL, CONTIG>(base + r * v.sS, v.sD, lane, x);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) best = fmaxf(best, x[e] * x[e]);
+    }
+    best = warp_max(best);
+  }
+  if (lane == 0) wmax[warp] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, wmax[w]);
+    if (bx < nqb) qmax_sq[bh * nqb + bx] = mx;
+    else if (bx < nqb + nkb) kblk[bh * nkb + (bx - nqb)] = mx;
+    else vblk[bh * nkb + (bx - nqb - nkb)] = mx;
+  }
+}
+
+// 4. Per head: key max, global V max, then U, m, flag for every Q-block.
+__global__ void __launch_bounds__(kThreads)
+    finish_kernel(int64_t H, int64_t nqb, int64_t nkb, int64_t n_heads_total, const float *kblk,
+                  const float *vblk, double alpha, int C, int gate, const float *qmax_sq,
+                  float *kmax_sq, float *vmax_sq, int32_t *m, uint8_t *flag) {
+  const int64_t bh = blockIdx.y * H + blockIdx.x;
+  __shared__ float red[2][kWarps];
+  float km = 0.f, vm = 0.f;
+  for (int64_t i = threadIdx.x; i < nkb; i += kThreads) km = fmaxf(km, kblk[bh * nkb + i]);
+  for (int64_t i = threadIdx.x; i < n_heads_total * nkb; i += kThreads) vm = fmaxf(vm, vblk[i]);
+  km = warp_max(km);
+  vm = warp_max(vm);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) { red[0][warp] = km; red[1][warp] = vm; }
+  __syncthreads();
+  km = 0.f; vm = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) { km = fmaxf(km, red[0][w]); vm = fmaxf(vm, red[1][w]); }
+  if (threadIdx.x == 0) {
+    kmax_sq[bh] = km;
+    if (bh == 0) vmax_sq[0] = vm;
+  }
+  const bool v_ok = vm <= (float)FM_VMAX * (float)FM_VMAX;
+  const double ksq = sqrt((double)km);
+  for (int64_t i = threadIdx.x; i < nqb; i += kThreads) {
+    const double U = alpha * sqrt((double)qmax_sq[bh * nqb + i]) * ksq;
+    m[bh * nqb + i] = (int32_t)ceil(U) - C;
+    flag[bh * nqb + i] = (uint8_t)(v_ok && U <= (double)gate);
+  }
+}
+
+template <typename T, int EPL, bool CONTIG>
+cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st) {
+  const int64_t B = a.q.B, H = a.q.H, N = a.k.S;
+  char *ws = reinterpret_cast<char *>(a.ws);
+  float *part = reinterpret_cast<float *>(ws + w.off_part);
+  float *kblk = reinterpret_cast<float *>(ws + w.off_kb);
+  float *vblk = reinterpret_cast<float *>(ws + w.off_vb);
+  const int D = (int)a.q.D;
+  if (a.centering && N > 0) {
+    ksum_kernel<T, EPL, CONTIG><<<dim3((unsigned)w.P, (unsigned)H, (unsigned)B), kThreads, 0, st>>>(a.k, w.P, part);
+    kmean_kernel<<<dim3((unsigned)H, (unsigned)B), 128, 0, st>>>(part, H, w.P, D, N, a.kbar);
+  } else {
+    cudaError_t e = cudaMemsetAsync(a.kbar, 0, sizeof(float) * (size_t)(B * H * D), st);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t nx = a.nqb + 2 * w.nkb;
+  if (nx > 0) {
+    norms_kernel<T, EPL, CONTIG><<<dim3((unsigned)nx, (unsigned)H, (unsigned)B), kThreads, 0, st>>>(
+        a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, kblk, vblk);
+  }
+  finish_kernel<<<dim3((unsigned)H, (unsigned)B), kThreads, 0, st>>>(
+      H, a.nqb, w.nkb, B * H, kblk, vblk, a.alpha, a.C, a.gate, a.qmax_sq, a.kmax_sq, a.vmax_sq, a.m, a.flag);
+  return cudaGetLastError();
+}
+
+bool contiguous_rows(const View &t) {
+  const size_t es = t.dtype == FM_F32 ? 4 : 2;
+  const size_t vec = es * (size_t)(t.D / 32);  // bytes a lane loads
+  if (t.sD != 1) return false;
+  if (reinterpret_cast<uintptr_t>(t.ptr) % vec) return false;
+  return ((t.sB * es) % vec == 0 || t.B == 1) && ((t.sH * es) % vec == 0 || t.H == 1) &&
+         ((t.sS * es) % vec == 0 || t.S <= 1);
+}
+
+}  // namespace
+
+size_t bounds_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D) {
+  return ws_layout(B, H, N, D).total;
+}
+
+cudaError_t launch_bounds(const BoundsArgs &a, cudaStream_t st) {
+  const WsLayout w = ws_layout(a.q.B, a.q.H, a.k.S, a.q.D);
+  const bool contig = contiguous_rows(a.q) && contiguous_rows(a.k) && contiguous_rows(a.v);
+  const bool bf16 = a.q.dtype == FM_BF16;
+  const bool d128 = a.q.D == 128;
+  if (bf16) {
+    if (d128) return contig ? launch_typed<__nv_bfloat16, 4, true>(a, w, st) : launch_typed<__nv_bfloat16, 4, false>(a, w, st);
+    return contig ? launch_typed<__nv_bfloat16, 2, true>(a, w, st) : launch_typed<__nv_bfloat16, 2, false>(a, w, st);
+  }
+  if (d128) return contig ? launch_typed<float, 4, true>(a, w, st) : launch_typed<float, 4, false>(a, w, st);
+  return contig ? launch_typed<float, 2, true>(a, w, st) : launch_typed<float, 2, false>(a, w, st);
+}
+
+}  // namespace fm

@@ -1,0 +1,643 @@
+// fm_chunk_tc.cu -- tensor-core chunk kernel of fixed-m attention (sm_103a).
+//
+// Folds one KV chunk into the fp32 accumulators for bf16 inputs with D = 128:
+//   S = Q K^T             tcgen05.mma kind::f16, A = Q and B = K from swizzled shared
+//                         memory (TMA), fp32 accumulator in tensor memory (TMEM)
+//   P = 2^(alpha*S - b)   softmax warps: tcgen05.ld of S, FFMA + ex2, row sums in
+//                         registers, bf16 P written back over S in TMEM (tcgen05.st)
+//   O += P V              tcgen05.mma with A = P read from TMEM, B = V from shared memory
+//   epilogue              O and the row sums are added into (or initialise) acc_o/acc_sum
+// For an eligible Q-block the shift b_i = m + qkbar_i is fixed before the chunk starts,
+// so there is no row max, no rescale of O and the cross-chunk merge is a pure add
+// ("Kernel reference: ring_attention_const_max_fwd", sections "Dropping the online max
+// buys a better layout", "A static bound makes the ring reduction pure addition",
+// "Accumulate, then normalize once"; PR #477 Summary for m, the exp2 form and the
+// virtual centering term applied in registers).  A Q-block that failed the gate runs
+// online softmax in the same pipeline (PR #478, "Cross-Ring Safety Fallback"): its
+// softmax warps keep a running row max, rescale O in TMEM when the max grows by more
+// than 2^8 (lazy rescale: exact, since the final shift is whatever the running max is),
+// and merge with the previous chunks through acc_max.
+//
+// CTA = two 128-row Q tiles of one (batch, head) (256 rows) against every KV tile of the
+// chunk; 12 warps:
+//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a 4-stage ring
+//   warp 1      TMEM allocator; lane 0 issues every MMA and commit
+//   warps 4-7   softmax + epilogue of Q tile 0 (TMEM lanes 0-127)
+//   warps 8-11  softmax + epilogue of Q tile 1
+// TMEM (512 columns): S0/P0 [0,128) S1/P1 [128,256) O0 [256,384) O1 [384,512).
+// MMA issue order per KV tile j:  S0(j), PV1(j-1), S1(j), PV0(j) -- each softmax group
+// works on its tile while the tensor core runs the other group's two MMAs.
+// Every wait on an mbarrier is bounded in time; on expiry the kernel records the failure
+// in the device error word, waits (bounded) for its own copies and MMAs, frees TMEM and
+// returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include <mutex>
+
+#include "fm_internal.h"
+
+namespace fm {
+namespace {
+
+constexpr int kBQ = 128;   // rows per Q tile = TMEM lanes
+constexpr int kBK = 128;   // keys per KV tile
+constexpr int kHD = 128;   // head dimension
+constexpr int kStages = 4; // K/V ring: K_j in stage (2j)%4, V_j in stage (2j+1)%4
+constexpr int kTileBytes = kBK * kHD * 2;     // 32 KiB
+constexpr int kPanelBytes = 128 * 64 * 2;     // 128 rows x 64 bf16 (one 128-byte swizzle span)
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLazyRescale = 8.0f;          // online path: rescale when the max grows by > 2^8
+
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffKV = 2 * kTileBytes;
+constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+constexpr int kBarQFull = 0;
+constexpr int kBarKVFull = 1;
+constexpr int kBarKVEmpty = kBarKVFull + kStages;
+constexpr int kBarSFull = kBarKVEmpty + kStages;
+constexpr int kBarPReady = kBarSFull + 2;
+constexpr int kBarODone = kBarPReady + 2;
+constexpr int kBarDrain = kBarODone + 2;
+constexpr int kNumBars = kBarDrain + 1;
+constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 8;
+constexpr int kSmemUsed = kOffAbort + 8;
+constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), A K-major, B K-major (bit 16 = 0) or
+// MN-major (bit 16 = 1), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+constexpr uint32_t kIdescQK = idesc_bf16(kBQ, kBK, false);  // S = Q K^T: K is [keys, D], K-major
+constexpr uint32_t kIdescPV = idesc_bf16(kBQ, kHD, true);   // O = P V:   V is [keys, D], MN-major
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Slow path of wait_phase: poll until the phase completes, the time limit passes (the
+// failure is recorded and the CTA's abort flag raised) or, if `abort_flag` is given,
+// another role of the CTA has already given up.
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             unsigned long long timeout_ns, unsigned int *err,
+                                             unsigned int code) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_test(bar, parity)) return true;
+    if ((it & 31) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer() - t0 > timeout_ns) {
+        if (abort_flag) *abort_flag = 1;
+        atomicCAS(err, 0u, code);
+        return false;
+      }
+    }
+  }
+}
+// Wait for the phase of `bar` with parity `parity`; false when the wait gave up.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           unsigned long long timeout_ns, unsigned int *err,
+                                           unsigned int code) {
+  if (mbar_test(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, abort_flag, timeout_ns, err, code);
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm, uint32_t bar, int c0,
+                                            int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d),
+      "r"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+// Shared-memory matrix descriptor: start, leading and stride byte offsets (>> 4), the
+// fixed version bits (46-48 = 0b001) and the 128-byte swizzle mode (bits 61-63 = 2).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo & 0x3FFFFu) >> 4) << 16) |
+         ((uint64_t)((sbo & 0x3FFFFu) >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+#define FM_R8(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
+                 "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+// 32 consecutive 32-bit TMEM columns of this thread's lane, waited for.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+      "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+      "[%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : FM_R8(0), FM_R8(8), FM_R8(16), FM_R8(24)
+      : "r"(taddr)
+      : "memory");
+}
+#undef FM_R8
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+      "%13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+      "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// two fp32 -> one bf16x2 word, `lo` in the low half (the lower column index)
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+struct TcParams {
+  int64_t Sq, nqb;
+  int Nc, H, n_kv;
+  float alpha;
+  int force_online, accumulate;
+  const int32_t *m;
+  const uint8_t *flag;
+  const float *qkbar;
+  float *acc_o, *acc_sum, *acc_max;
+  unsigned int *err;
+  unsigned long long timeout_ns;
+};
+
+// Fixed-m softmax of one 128x128 S tile for this thread's row; P overwrites S.
+__device__ __forceinline__ void softmax_fixed_tile(uint32_t tS, int nvalid, float alpha, float nbias,
+                                                   float (&l)[4]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t s[32];
+    tmem_ld32(tS + c * 32, s);
+    uint32_t pk[16];
+    if (nvalid >= kBK) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), alpha, nbias));
+        const float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), alpha, nbias));
+        l[e & 3] += p0;
+        l[(e + 2) & 3] += p1;
+        pk[e] = pack_bf16(p0, p1);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int col = c * 32 + 2 * e;
+        const float p0 = col < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e]), alpha, nbias)) : 0.f;
+        const float p1 = col + 1 < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e + 1]), alpha, nbias)) : 0.f;
+        l[e & 3] += p0;
+        l[(e + 2) & 3] += p1;
+        pk[e] = pack_bf16(p0, p1);
+      }
+    }
+    tmem_st16(tS + c * 16, pk);  // P columns [16c, 16c+16) lie in S columns already read
+  }
+}
+
+// Online softmax of one S tile: running max `run` (base-2 units), lazy rescale of O.
+__device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, int nvalid, float alpha,
+                                                    bool have_o, float &run, float (&l)[4]) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t s[32];
+    tmem_ld32(tS + c * 32, s);
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (c * 32 + e < nvalid) mx = fmaxf(mx, __uint_as_float(s[e]));
+  }
+  const float zmax = mx * alpha;
+  if (run == -INFINITY || zmax > run + kLazyRescale) {
+    const float nr = fmaxf(run, zmax);
+    if (have_o && run != -INFINITY) {
+      const float sc = ex2(run - nr);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) l[i] *= sc;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * sc);
+        tmem_st32(tO + c * 32, o);
+      }
+    }
+    run = nr;
+  }
+  const float nb = -run;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t s[32];
+    tmem_ld32(tS + c * 32, s);
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int col = c * 32 + 2 * e;
+      const float p0 = col < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e]), alpha, nb)) : 0.f;
+      const float p1 = col + 1 < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e + 1]), alpha, nb)) : 0.f;
+      l[e & 3] += p0;
+      l[(e + 2) & 3] += p1;
+      pk[e] = pack_bf16(p0, p1);
+    }
+    tmem_st16(tS + c * 16, pk);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    fm_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (base - raw);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffAbort);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffTmemSlot);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int64_t qb0 = 2 * (int64_t)blockIdx.x;
+  auto bar = [&](int i) -> uint32_t { return base + (uint32_t)(kOffBar + 8 * i); };
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(kBarQFull), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarKVFull + s), 1);
+      mbar_init(bar(kBarKVEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(kBarSFull + t), 1);
+      mbar_init(bar(kBarPReady + t), 128);
+      mbar_init(bar(kBarODone + t), 1);
+    }
+    mbar_init(bar(kBarDrain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_kv = p.n_kv;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int last_round[kStages];
+      for (int s = 0; s < kStages; ++s) last_round[s] = -1;
+      mbar_expect_tx(bar(kBarQFull), 4 * kPanelBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int pn = 0; pn < 2; ++pn)
+          tma_load_4d(base + kOffQ + t * kTileBytes + pn * kPanelBytes, &tmQ, bar(kBarQFull), pn * 64,
+                      (int)((qb0 + t) * kBQ), h, b);
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        for (int w = 0; w < 2 && ok; ++w) {
+          const int idx = 2 * j + w, s = idx % kStages, round = idx / kStages;
+          ok = wait_phase(bar(kBarKVEmpty + s), (uint32_t)((round & 1) ^ 1), abort_flag, p.timeout_ns, p.err,
+                          kDevErrTimeoutProducer);
+          if (!ok) break;
+          mbar_expect_tx(bar(kBarKVFull + s), kTileBytes);
+          const CUtensorMap *tm = w ? &tmV : &tmK;
+          for (int pn = 0; pn < 2; ++pn)
+            tma_load_4d(base + kOffKV + s * kTileBytes + pn * kPanelBytes, tm, bar(kBarKVFull + s), pn * 64,
+                        j * kBK, h, b);
+          last_round[s] = round;
+        }
+      }
+      if (!ok) {
+        // let every copy already issued land before the CTA can exit
+        wait_phase(bar(kBarQFull), 0, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain);
+        for (int s = 0; s < kStages; ++s)
+          if (last_round[s] >= 0)
+            wait_phase(bar(kBarKVFull + s), (uint32_t)(last_round[s] & 1), nullptr, p.timeout_ns, p.err,
+                       kDevErrTimeoutDrain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t tS0 = tmem + 0, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+      auto q_desc = [&](int t, int kk) {
+        return smem_desc(base + kOffQ + t * kTileBytes + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
+      };
+      auto k_desc = [&](int s, int kk) {
+        return smem_desc(base + kOffKV + s * kTileBytes + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
+      };
+      auto v_desc = [&](int s, int kk) {
+        return smem_desc(base + kOffKV + s * kTileBytes + kk * 2048, kPanelBytes, 1024);
+      };
+      bool ok = wait_phase(bar(kBarQFull), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma);
+      int vs_prev = 0;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int ki = 2 * j, ks = ki % kStages;
+        ok = wait_phase(bar(kBarKVFull + ks), (uint32_t)((ki / kStages) & 1), abort_flag, p.timeout_ns, p.err,
+                        kDevErrTimeoutMma);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tS0, q_desc(0, kk), k_desc(ks, kk), kIdescQK, kk > 0);
+        mma_commit(bar(kBarSFull + 0));
+        if (j > 0) {
+          ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((j - 1) & 1), abort_flag, p.timeout_ns, p.err,
+                          kDevErrTimeoutMma);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tO1, tS1 + kk * 8, v_desc(vs_prev, kk), kIdescPV, (j - 1 > 0 || kk > 0));
+          mma_commit(bar(kBarKVEmpty + vs_prev));
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tS1, q_desc(1, kk), k_desc(ks, kk), kIdescQK, kk > 0);
+        mma_commit(bar(kBarSFull + 1));
+        mma_commit(bar(kBarKVEmpty + ks));
+        const int vi = 2 * j + 1, vs = vi % kStages;
+        ok = wait_phase(bar(kBarKVFull + vs), (uint32_t)((vi / kStages) & 1), abort_flag, p.timeout_ns, p.err,
+                        kDevErrTimeoutMma) &&
+             wait_phase(bar(kBarPReady + 0), (uint32_t)(j & 1), abort_flag, p.timeout_ns, p.err,
+                        kDevErrTimeoutMma);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ts(tO0, tS0 + kk * 8, v_desc(vs, kk), kIdescPV, (j > 0 || kk > 0));
+        if (j == n_kv - 1) mma_commit(bar(kBarODone + 0));
+        vs_prev = vs;
+      }
+      if (ok) {
+        ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((n_kv - 1) & 1), abort_flag, p.timeout_ns, p.err,
+                        kDevErrTimeoutMma);
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tO1, tS1 + kk * 8, v_desc(vs_prev, kk), kIdescPV, (n_kv - 1 > 0 || kk > 0));
+          mma_commit(bar(kBarKVEmpty + vs_prev));
+          mma_commit(bar(kBarODone + 1));
+        }
+      }
+      if (!ok) {
+        // every MMA issued so far must finish reading shared memory and TMEM before exit
+        mma_commit(bar(kBarDrain));
+        wait_phase(bar(kBarDrain), 0, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax groups
+    const int t = (warp - 4) >> 2;   // Q tile of this group
+    const int wq = warp & 3;         // TMEM lane quarter of this warp
+    const int r = wq * 32 + lane;    // row within the tile
+    const int64_t qb = qb0 + t;
+    const bool tile_ok = qb < p.nqb;
+    const int64_t row = qb * kBQ + r;
+    const bool row_ok = tile_ok && row < p.Sq;
+    const int64_t bh = (int64_t)b * p.H + h;
+    const bool fixed = !tile_ok || (!p.force_online && p.flag[bh * p.nqb + qb] != 0);
+    float bias = 0.f;
+    if (fixed && tile_ok) bias = (float)p.m[bh * p.nqb + qb] + (row_ok ? p.qkbar[bh * p.Sq + row] : 0.f);
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (uint32_t)(t * 128);
+    const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(t * 128);
+    float l[4] = {0.f, 0.f, 0.f, 0.f};
+    float run = -INFINITY;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      ok = wait_phase(bar(kBarSFull + t), (uint32_t)(j & 1), abort_flag, p.timeout_ns, p.err,
+                      kDevErrTimeoutSoftmax);
+      ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
+      if (!ok) break;
+      tc_fence_after();
+      const int nvalid = min(kBK, p.Nc - j * kBK);
+      if (fixed) softmax_fixed_tile(tS, nvalid, p.alpha, -bias, l);
+      else softmax_online_tile(tS, tO, nvalid, p.alpha, j > 0, run, l);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kBarPReady + t));
+    }
+    if (ok) {
+      ok = wait_phase(bar(kBarODone + t), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutSoftmax);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float lsum = (l[0] + l[1]) + (l[2] + l[3]);
+      const int64_t rflat = bh * p.Sq + row;
+      float cprev = 0.f, cnew = 1.f, nr = run;
+      if (!fixed && row_ok && p.accumulate) {
+        const float R = p.acc_max[rflat];
+        nr = fmaxf(R, run);
+        cprev = (R == -INFINITY) ? 0.f : exp2f(R - nr);
+        cnew = (run == -INFINITY) ? 0.f : exp2f(run - nr);
+      }
+      float4 *dst = reinterpret_cast<float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        if (row_ok) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float4 x = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
+                                   __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
+            if (p.accumulate) {
+              const float4 y = dst[c * 8 + q4];
+              if (fixed) {
+                x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+              } else {
+                x.x = fmaf(y.x, cprev, x.x * cnew); x.y = fmaf(y.y, cprev, x.y * cnew);
+                x.z = fmaf(y.z, cprev, x.z * cnew); x.w = fmaf(y.w, cprev, x.w * cnew);
+              }
+            }
+            dst[c * 8 + q4] = x;
+          }
+        }
+      }
+      if (row_ok) {
+        if (fixed) {
+          p.acc_sum[rflat] = p.accumulate ? p.acc_sum[rflat] + lsum : lsum;
+          p.acc_max[rflat] = bias;
+        } else {
+          p.acc_sum[rflat] = p.accumulate ? fmaf(p.acc_sum[rflat], cprev, lsum * cnew) : lsum;
+          p.acc_max[rflat] = nr;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// [B, H, S, D] bf16 view -> 4-D tensor map (D, S, H, B) with 64 x 128 boxes, 128-byte swizzle.
+bool encode_map(CUtensorMap *map, const View &t) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  const uint64_t es = 2;
+  cuuint64_t dims[4] = {(cuuint64_t)t.D, (cuuint64_t)t.S, (cuuint64_t)t.H, (cuuint64_t)t.B};
+  // strides of size-1 dimensions are never stepped; give them a well-formed value
+  const int64_t sS = t.S > 1 ? t.sS : t.D;
+  const int64_t sH = t.H > 1 ? t.sH : t.S * sS;
+  const int64_t sB = t.B > 1 ? t.sB : t.H * sH;
+  cuuint64_t strides[3] = {(cuuint64_t)(sS * es), (cuuint64_t)(sH * es), (cuuint64_t)(sB * es)};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(t.ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool tma_view_ok(const View &t) {
+  if (t.dtype != FM_BF16 || t.D != kHD || t.sD != 1) return false;
+  if (reinterpret_cast<uintptr_t>(t.ptr) % 16) return false;
+  if (t.S < 1 || t.B < 1 || t.H < 1) return false;
+  auto ok16 = [](int64_t s, int64_t n) { return n <= 1 || ((s * 2) % 16 == 0 && s > 0); };
+  return ok16(t.sS, t.S) && ok16(t.sH, t.H) && ok16(t.sB, t.B);
+}
+
+}  // namespace
+
+bool chunk_tc_supported(const ChunkArgs &a) {
+  return tma_view_ok(a.q) && tma_view_ok(a.k) && tma_view_ok(a.v) &&
+         reinterpret_cast<uintptr_t>(a.acc_o) % 16 == 0 && a.q.B <= 65535 && a.q.H <= 65535 &&
+         a.k.S <= (int64_t)1 << 30 && a.q.S <= (int64_t)1 << 30;
+}
+
+cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  // a layout the driver's tensor-map encoder refuses is reported so the caller can use
+  // the CUDA-core kernel instead; nothing has been launched then
+  if (!encode_map(&mq, a.q) || !encode_map(&mk, a.k) || !encode_map(&mv, a.v)) return cudaErrorNotSupported;
+  cudaError_t e =
+      cudaFuncSetAttribute(fm_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  TcParams p;
+  p.Sq = a.q.S;
+  p.nqb = a.nqb;
+  p.Nc = (int)a.k.S;
+  p.H = (int)a.q.H;
+  p.n_kv = (int)((a.k.S + kBK - 1) / kBK);
+  p.alpha = a.alpha;
+  p.force_online = a.force_online;
+  p.accumulate = a.accumulate;
+  p.m = a.m;
+  p.flag = a.flag;
+  p.qkbar = a.qkbar;
+  p.acc_o = a.acc_o;
+  p.acc_sum = a.acc_sum;
+  p.acc_max = a.acc_max;
+  p.err = a.err;
+  p.timeout_ns = a.timeout_ns;
+  dim3 grid((unsigned)((a.nqb + 1) / 2), (unsigned)a.q.H, (unsigned)a.q.B);
+  fm_chunk_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fm

@@ -1,0 +1,80 @@
+// fm_internal.h -- declarations shared by the CUDA translation units of libfm.
+// Not part of the public ABI (include/fm.h is).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fm.h"
+
+namespace fm {
+
+// Device error codes written to the per-GPU error word.
+enum : unsigned int {
+  kDevErrNone = 0,
+  kDevErrTimeoutProducer = 1,
+  kDevErrTimeoutMma = 2,
+  kDevErrTimeoutSoftmax = 3,
+  kDevErrTimeoutDrain = 4,
+};
+
+// Default limit of a pipeline wait inside a kernel.  One CTA of the chunk kernel runs
+// for well under 10 ms at the largest sizes, so a wait that lasts seconds means a
+// broken pipeline; the kernel then records the failure and returns.
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+// A validated view of an fm_tensor (element strides; D stride may be any value).
+struct View {
+  const void *ptr;
+  int dtype;
+  int64_t B, H, S, D;
+  int64_t sB, sH, sS, sD;
+};
+
+// ---- bounds (fm_bounds.cu) -------------------------------------------------
+struct BoundsArgs {
+  View q, k, v;
+  int centering;
+  double alpha;   // softmax_scale * log2(e), fp64 for the bound
+  int C, gate;
+  int64_t nqb;    // ceil(Sq / 128)
+  int32_t *m;
+  uint8_t *flag;
+  float *qmax_sq, *kmax_sq, *kbar, *qkbar, *vmax_sq;
+  void *ws;
+  size_t ws_bytes;
+};
+size_t bounds_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D);
+cudaError_t launch_bounds(const BoundsArgs &a, cudaStream_t st);
+
+// ---- chunk kernels ----------------------------------------------------------
+struct ChunkArgs {
+  View q, k, v;            // k, v: this chunk
+  float alpha;
+  int force_online;
+  int accumulate;
+  int64_t nqb;
+  const int32_t *m;
+  const uint8_t *flag;
+  const float *qkbar;      // [B,H,Sq] (zeros when not centering)
+  float *acc_o, *acc_sum, *acc_max;
+  unsigned int *err;       // device error word
+  unsigned long long timeout_ns;
+};
+// SIMT path: fp32 inputs (exact fp32 arithmetic), any D in {64,128}, any strides.
+cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st);
+// tcgen05/TMEM/TMA path: bf16, D = 128, unit D stride, 16-byte aligned rows.  Returns
+// cudaErrorNotSupported, launching nothing, when the tensor maps cannot be encoded.
+bool chunk_tc_supported(const ChunkArgs &a);
+cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
+// Empty chunk (Nc == 0) with accumulate == 0: write the empty state.
+cudaError_t launch_chunk_empty_init(const ChunkArgs &a, cudaStream_t st);
+
+// ---- finalize (fm_finalize.cu) ---------------------------------------------
+cudaError_t launch_finalize(const float *acc_o, const float *acc_sum, const View &o,
+                            cudaStream_t st);
+
+// ---- helpers shared by host code -------------------------------------------
+int current_device_sm_count();
+
+}  // namespace fm

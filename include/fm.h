@@ -1,0 +1,190 @@
+/*
+ * fm.h -- C ABI of the fixed-m (const-max) attention forward for GB300 (sm_103a).
+ *
+ * The method replaces softmax's running row maximum by a shift fixed before any
+ * score is computed, so that the base-2 numerator and denominator of every row
+ * build up as plain fp32 sums across KV chunks, with one divide at the end.
+ * Page references (title, section):
+ *   [NKI]   "Kernel reference: ring_attention_const_max_fwd const-max ring attention"
+ *   [PR477] "feat(attention): fixed-m splash attention kernel with dynamic bounds and
+ *            safety fallbacks" (maxdiffusion PR #477)
+ *   [PR478] "feat(attention): 2D Ulysses+Ring attention with Global Virtual
+ *            K-Centering" (maxdiffusion PR #478)
+ *
+ * Call sequence for one attention forward over a key sequence split into chunks
+ * (the ring's KV steps, run one after another on one GPU):
+ *     fm_bounds(q, k_full, v_full)                       once
+ *     fm_attn_chunk(q, k_c, v_c, accumulate = c > 0)     once per chunk c
+ *     fm_finalize(acc_o, acc_sum -> o)                   once
+ *
+ * Conventions shared by every call:
+ *   - Tensors are described by fm_tensor: a logical [B, H, S, D] array with element
+ *     strides (any order, e.g. [B,H,S,D] or the pages' token-major [B,S,H,D]).
+ *   - All buffers are device memory owned by the caller; the library allocates
+ *     nothing and keeps no state besides a thread-local error string and one
+ *     device-side error word per GPU.
+ *   - Calls validate on the host, enqueue kernels on `stream` and return without
+ *     synchronising.  On any error code nothing is enqueued and no output buffer is
+ *     touched; fm_last_error() returns a message for the calling thread.
+ *   - Device-side failures (a pipeline wait that exceeded its time limit) are
+ *     reported by fm_sync_status().
+ */
+#ifndef FM_H_
+#define FM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FM_API __attribute__((visibility("default")))
+#else
+#define FM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *fm_stream_t;
+
+/* Element types.  Only FM_F32 and FM_BF16 are accepted: [PR477]'s commit message
+ * rejects fp16 (and fp8) because 2^C-scale terms overflow their exponent range
+ * (Q = K = 0, V = 1 gives inf instead of 1.0); here they fail with FM_ERR_DTYPE. */
+enum { FM_F32 = 0, FM_BF16 = 1, FM_F16 = 2, FM_F8E4M3 = 3, FM_F8E5M2 = 4 };
+
+/* Return codes. */
+enum {
+  FM_OK = 0,
+  FM_ERR_ARG = 1,             /* NULL pointer, negative size, bad flag value */
+  FM_ERR_SHAPE = 2,           /* shapes of q / k / v / outputs disagree */
+  FM_ERR_DTYPE = 3,           /* fp16 / fp8, or q, k, v of different types */
+  FM_ERR_UNSUPPORTED = 4,     /* D not in {64, 128}; GQA (k.H != q.H); misaligned data */
+  FM_ERR_BOUNDS_MISMATCH = 5, /* bounds do not belong to this call (see fm_attn_chunk) */
+  FM_ERR_CUDA = 6,            /* a CUDA runtime call or kernel launch failed */
+  FM_ERR_TIMEOUT = 7          /* a kernel's pipeline wait ran past its limit */
+};
+
+#define FM_BOUNDS_MAGIC 0x314D4246u /* tag written by fm_bounds ("FBM1") */
+#define FM_BLOCK_Q 128              /* rows per Q-block: the granularity of m and flag */
+#define FM_VMAX 256                 /* the V bound of [PR477]'s commit message */
+#define FM_SUM_CLAMP 1e-37f         /* [NKI] "Accumulate, then normalize once" */
+
+/* A logical [B, H, S, D] tensor: element (b,h,s,d) lives at
+ * ptr + (b*stride[0] + h*stride[1] + s*stride[2] + d*stride[3]) * elemsize. */
+typedef struct {
+  void *ptr;
+  int32_t dtype; /* FM_F32 or FM_BF16 */
+  int32_t reserved;
+  int64_t B, H, S, D;
+  int64_t stride[4]; /* element strides, >= 0 */
+} fm_tensor;
+
+typedef struct {
+  float softmax_scale;  /* <= 0 selects 1/sqrt(D) ([NKI] Interface table) */
+  int32_t centering;    /* 1: virtual K-centering ([PR477] "Virtual K-centering") */
+  int32_t force_online; /* 1: every Q-block takes the online-softmax fallback */
+} fm_opts;
+
+/* Bounds of one attention call ([PR477] Summary, "Dynamic eligibility bounding").
+ * The caller allocates the device arrays and fills the pointers; fm_bounds fills
+ * every other field.  nqb = ceil(Sq / FM_BLOCK_Q).
+ *   m       int32 [B, H, nqb]  per-(head, Q-block) shift m = ceil(U) - C(N)
+ *   flag    uint8 [B, H, nqb]  1 = eligible for fixed-m: v_ok && U <= gate
+ *   qmax_sq f32   [B, H, nqb]  max over the block's rows of ||q_i||^2
+ *   kmax_sq f32   [B, H]       max_j ||k_j - kbar||^2 (centered) or ||k_j||^2
+ *   kbar    f32   [B, H, D]    mean key over all real keys ([PR478] Summary); 0 if
+ *                              not centering
+ *   qkbar   f32   [B, H, Sq]   alpha * q_i . kbar, the per-row centering term applied
+ *                              in registers by the chunk kernels; 0 if not centering
+ *   vmax_sq f32   [1]          max over all of V of v^2 (v_ok = vmax_sq <= 256^2)
+ * with alpha = softmax_scale * log2(e) (base-2 logits, [PR477]'s exp2 formulation)
+ * and U = alpha * sqrt(qmax_sq) * sqrt(kmax_sq), the Cauchy-Schwarz bound on the
+ * base-2 logit ([NKI] "Picking a max that is safe without measuring it"). */
+typedef struct {
+  int32_t *m;
+  uint8_t *flag;
+  float *qmax_sq;
+  float *kmax_sq;
+  float *kbar;
+  float *qkbar;
+  float *vmax_sq;
+  /* filled by fm_bounds */
+  int64_t B, H, Sq, D, n_qblocks;
+  int64_t N_total;   /* total KV length over every chunk of the call */
+  int32_t C, W, gate; /* C(N) = 127 - ceil(log2 N) - 8, W = C + 125, gate = floor(W/2) */
+  int32_t centered;  /* the opts.centering the bounds were measured with */
+  float alpha;
+  int32_t dtype;
+  /* updated by fm_attn_chunk (host-side bookkeeping of the chunk sequence) */
+  int64_t kv_seen;
+  int32_t online_lock;
+  uint32_t magic; /* FM_BOUNDS_MAGIC once fm_bounds has succeeded */
+} fm_bounds_out;
+
+/* Scratch bytes fm_bounds needs for k_full of shape [B, H, N_total, D] (partial
+ * key sums for the mean, per-block key and value maxima).  Returns FM_OK. */
+FM_API int fm_bounds_workspace_size(int64_t B, int64_t H, int64_t N_total, int64_t D, size_t *bytes);
+
+/* fm_bounds -- norms, key mean, m and the per-tile flag ([PR477] Summary; the
+ * fused norm reduction of [NKI] "Transpose prologue with fused norms" and [PR478]).
+ *   q      [B, H, Sq, D]  queries (all rows of the call)
+ *   k_full [B, H, N, D]   ALL keys of the call (every chunk), N = N_total
+ *   v_full [B, H, N, D]   all values
+ *   opts   softmax_scale and centering (force_online is ignored here)
+ *   out    caller-filled pointers; every other field is written
+ *   workspace, workspace_bytes  device scratch of at least fm_bounds_workspace_size
+ * Device results are deterministic (fixed-order reductions).  Errors: FM_ERR_ARG,
+ * FM_ERR_SHAPE, FM_ERR_DTYPE, FM_ERR_UNSUPPORTED, FM_ERR_CUDA. */
+FM_API int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_full,
+              const fm_opts *opts, fm_bounds_out *out, void *workspace, size_t workspace_bytes,
+              fm_stream_t stream);
+
+/* fm_attn_chunk -- fold one KV chunk into the unnormalised fp32 accumulators
+ * ([NKI] "A static bound makes the ring reduction pure addition", "Accumulate, then
+ * normalize once").  For an eligible Q-block (flag = 1, force_online = 0) each row i
+ * adds p_ij = 2^(alpha*q_i.k_j - m - qkbar_i) to acc_sum and p_ij*v_j to acc_o: pure
+ * addition across chunks.  Other Q-blocks take the online-softmax fallback ([PR478]
+ * "Cross-Ring Safety Fallback"): a running row max kept in acc_max, with rescaling.
+ *   q        [B, H, Sq, D]   the same queries given to fm_bounds
+ *   k_chunk  [B, H, Nc, D]   this chunk's keys (Nc >= 0, any Nc, ragged tails allowed)
+ *   v_chunk  [B, H, Nc, D]
+ *   bounds   from fm_bounds for this call; kv_seen/online_lock are updated
+ *   acc_o    f32 [B, H, Sq, D] contiguous;  acc_sum, acc_max f32 [B, H, Sq] contiguous.
+ *            acc_max holds each row's current base-2 shift (m + qkbar_i on fixed-m
+ *            rows, the running max on fallback rows), so acc_sum * 2^acc_max is the
+ *            row's sum of 2^z.
+ *   accumulate  0: overwrite the accumulators (first chunk); 1: add into them
+ * Errors: FM_ERR_BOUNDS_MISMATCH when bounds->magic is wrong, the bounds' shape is
+ * not [B, H, ceil(Sq/128)], bounds->centered != opts->centering (raw-key bounds must
+ * never pair with centered logits: [PR477] "matched pair"), the softmax scale
+ * differs, more keys arrive than bounds->N_total, or force_online changes within a
+ * call; plus the errors of fm_bounds. */
+FM_API int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk,
+                  fm_bounds_out *bounds, const fm_opts *opts, float *acc_o, float *acc_sum,
+                  float *acc_max, int accumulate, fm_stream_t stream);
+
+/* fm_finalize -- o = acc_o / max(acc_sum, 1e-37) ([NKI] "Accumulate, then normalize
+ * once": one divide, sum floored near the smallest fp32 normal).
+ *   acc_o f32 [B, H, Sq, D] and acc_sum f32 [B, H, Sq], contiguous
+ *   o_out [B, H, Sq, D] (its B, H, S, D give the shape), FM_F32 or FM_BF16, any strides
+ * Errors: FM_ERR_ARG, FM_ERR_DTYPE, FM_ERR_CUDA. */
+FM_API int fm_finalize(const float *acc_o, const float *acc_sum, const fm_tensor *o_out,
+                fm_stream_t stream);
+
+/* fm_sync_status -- synchronise `stream`, then report and clear this GPU's device
+ * error word: FM_ERR_TIMEOUT if a kernel gave up on a pipeline wait (its outputs are
+ * then invalid), FM_ERR_CUDA on an asynchronous CUDA error, else FM_OK. */
+FM_API int fm_sync_status(fm_stream_t stream);
+
+/* Message of the last failing call on this thread ("" if none).  Valid until the
+ * thread's next fm_* call. */
+FM_API const char *fm_last_error(void);
+
+/* ABI version of this header: (major << 16) | minor. */
+FM_API int fm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FM_H_ */

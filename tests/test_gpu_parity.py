@@ -1,0 +1,236 @@
+"""GPU parity of the CUDA path (through the C ABI) against the fp64 CPU oracle.
+
+Bars: m and flag bit-exact outside the tie band (|U - nearest integer| or |U - gate|
+below 1e-4*max(1,U), where fp32 device sums may legitimately round the other way);
+outputs within max-abs 1e-5 for fp32 inputs and 2e-2 for bf16 inputs; the fixed-m and
+the online-fallback path within the same tolerance of each other.  Small cases are
+compared element by element; the full-size workloads on sampled (head, row) sets that
+include every ragged tail.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fixed_max_softmax_gb300 as fm
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+TOL_F32 = 1e-5
+
+
+@pytest.fixture(scope="session")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fixed_max_softmax_gb300 import build as fmbuild
+
+    fmbuild.build()
+    fm.load()
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")
+
+
+def run(q, k, v, chunks=None, centering=False, force_online=False, out_dtype=torch.float32):
+    B, H, Sq, D = q.shape
+    fa = fm.FixedMAttention(B, H, Sq, k.shape[2], D, q.device, centering=centering, force_online=force_online,
+                            out_dtype=out_dtype)
+    o = fa.forward(q, k, v, chunks)
+    fm.fm_sync_status()
+    return fa, o
+
+
+def maxerr(a, b):
+    a = a.detach().cpu().double().numpy() if hasattr(a, "detach") else np.asarray(a)
+    b = b.detach().cpu().double().numpy() if hasattr(b, "detach") else np.asarray(b)
+    assert a.shape == b.shape, (a.shape, b.shape)
+    return float(np.max(np.abs(a - b))) if a.size else 0.0
+
+
+def check_bounds(fa, ob, heads=None, check_vmax=True):
+    """GPU bounds vs oracle bounds (optionally for a subset of heads of batch 0)."""
+    sel = (lambda x: x) if heads is None else (lambda x: x[:, heads])
+    m_g = sel(fa.bounds.m.cpu().numpy())
+    f_g = sel(fa.bounds.flag.cpu().numpy())
+    U = ob["U"]
+    safe = ob["margin"] > 1e-4 * np.maximum(1.0, U)
+    assert np.array_equal(m_g[safe], ob["m"][safe]), "m differs outside the tie band"
+    assert np.array_equal(f_g[safe], ob["flag"][safe]), "flag differs outside the tie band"
+    assert np.all(np.abs(m_g.astype(np.int64) - ob["m"]) <= 1)
+    np.testing.assert_allclose(sel(fa.bounds.qmax_sq.cpu().numpy()), ob["qmax_sq"], rtol=2e-5, atol=1e-30)
+    np.testing.assert_allclose(sel(fa.bounds.kmax_sq.cpu().numpy()), ob["kmax_sq"], rtol=2e-5, atol=1e-12)
+    np.testing.assert_allclose(sel(fa.bounds.kbar.cpu().numpy()), ob["kbar"], rtol=1e-5, atol=2e-6)
+    qk = sel(fa.bounds.qkbar.cpu().numpy())[..., : ob["qkbar"].shape[-1]]
+    np.testing.assert_allclose(qk, ob["qkbar"], rtol=1e-4, atol=1e-4)
+    if check_vmax:
+        # v^2 of a bf16 value is exact in fp32; of an fp32 value it takes one rounding
+        g = float(fa.bounds.vmax_sq.item())
+        assert abs(g - ob["vmax_sq"]) <= 2.0 ** -23 * ob["vmax_sq"], (g, ob["vmax_sq"])
+    b = fa.bounds.out
+    assert (b.C, b.W, b.gate) == (ob["C"], ob["W"], ob["gate"])
+    assert b.magic == fm.FM_BOUNDS_MAGIC
+    return int((~safe).sum())
+
+
+# ------------------------------------------------------------------ small, element by element
+
+def test_tiny_fp32_element_by_element(dev):
+    w = workloads.WORKLOADS["tiny"]
+    q, k, v = workloads.make_inputs("tiny", device=dev)
+    fa, o = run(q, k, v, workloads.chunk_bounds(w), centering=False)
+    ref = oracle.attention(q.cpu(), k.cpu(), v.cpu())
+    assert maxerr(o, ref) <= TOL_F32
+    check_bounds(fa, oracle.bounds(q.cpu(), k.cpu(), v.cpu(), centering=False))
+    _, o2 = run(q, k, v, workloads.chunk_bounds(w), force_online=True)
+    assert maxerr(o2, ref) <= TOL_F32
+
+
+@pytest.mark.parametrize("centering", [False, True])
+@pytest.mark.parametrize("force_online", [False, True])
+@pytest.mark.parametrize("shape", [(1, 3, 300, 333, [(0, 128), (128, 100), (228, 105)]),
+                                   (2, 2, 128, 128, [(0, 128)]),
+                                   (1, 2, 77, 1000, [(0, 999), (999, 1)]),
+                                   (1, 1, 513, 257, [(0, 129), (129, 128)])])
+def test_bf16_ragged_chunks_element_by_element(dev, shape, centering, force_online):
+    B, H, Sq, N, chunks = shape
+    q, k, v = workloads.make_inputs("wan", device="cpu", heads=range(H), Sq=Sq, N=N)
+    if B > 1:
+        q2, k2, v2 = workloads.make_inputs("h40_s4096", device="cpu", heads=range(H), Sq=Sq, N=N)
+        q, k, v = torch.cat([q, q2]), torch.cat([k, k2]), torch.cat([v, v2])
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    fa, o = run(qd, kd, vd, chunks, centering=centering, force_online=force_online)
+    ref = oracle.attention(q, k, v)
+    err = maxerr(o, ref)
+    assert err <= TOL_BF16, err
+    check_bounds(fa, oracle.bounds(q, k, v, centering=centering))
+
+
+def test_fp32_d128_and_bf16_d64_use_the_cuda_core_path(dev):
+    for name, D in (("tiny", 64), ("h40_s4096", 128)):
+        q, k, v = workloads.make_inputs(name, device="cpu", heads=[0, 1], Sq=200, N=300)
+        for dt, tol in ((torch.float32, TOL_F32), (torch.bfloat16, TOL_BF16)):
+            qq, kk, vv = q.to(dt), k.to(dt), v.to(dt)
+            _, o = run(qq.to(dev), kk.to(dev), vv.to(dev), [(0, 150), (150, 150)], centering=True)
+            assert maxerr(o, oracle.attention(qq, kk, vv)) <= tol, (name, dt)
+
+
+def test_token_major_layout_and_bf16_output(dev):
+    """Inputs laid out [B, S, H, D] (the pages' token-major layout) seen through strides."""
+    q, k, v = workloads.make_inputs("wan", device="cpu", heads=range(4), Sq=260, N=390)
+    tq = q.permute(0, 2, 1, 3).contiguous().to(dev).permute(0, 2, 1, 3)
+    tk = k.permute(0, 2, 1, 3).contiguous().to(dev).permute(0, 2, 1, 3)
+    tv = v.permute(0, 2, 1, 3).contiguous().to(dev).permute(0, 2, 1, 3)
+    assert not tq.is_contiguous()
+    ref = oracle.attention(q, k, v)
+    _, o = run(tq, tk, tv, [(0, 200), (200, 190)], centering=True, out_dtype=torch.bfloat16)
+    assert o.dtype == torch.bfloat16
+    assert maxerr(o, ref) <= TOL_BF16
+
+
+def test_empty_and_degenerate_inputs(dev):
+    # a single key: output equals its value (up to bf16 P rounding, exact here: p=1 scale)
+    q, k, v = workloads.make_inputs("wan", device="cpu", heads=[0], Sq=5, N=1)
+    _, o = run(q.to(dev), k.to(dev), v.to(dev))
+    assert maxerr(o, v.expand(1, 1, 5, 128).float()) <= TOL_BF16
+    # an empty first chunk initialises; the next one accumulates
+    q, k, v = workloads.make_inputs("wan", device="cpu", heads=[0, 1], Sq=140, N=200)
+    _, o = run(q.to(dev), k.to(dev), v.to(dev), [(0, 0), (0, 200)], centering=True)
+    assert maxerr(o, oracle.attention(q, k, v)) <= TOL_BF16
+    # Sq = 0 and H = 0 are no-ops
+    z = torch.empty(1, 2, 0, 128, dtype=torch.bfloat16, device=dev)
+    kk = torch.randn(1, 2, 10, 128, device=dev).bfloat16()
+    run(z, kk, kk)
+    # Q = K = 0, V = 1 gives exactly 1 (the case fp16 fixed-m gets wrong)
+    zq = torch.zeros(1, 1, 130, 128, dtype=torch.bfloat16, device=dev)
+    ones = torch.ones(1, 1, 300, 128, dtype=torch.bfloat16, device=dev)
+    _, o = run(zq, torch.zeros_like(ones), ones, [(0, 150), (150, 150)])
+    assert torch.all(torch.isfinite(o)) and maxerr(o, torch.ones_like(o)) <= TOL_BF16
+
+
+def test_schedule_invariance_bitwise(dev):
+    """Repeated runs are bit-identical (deterministic reductions, fixed tile order)."""
+    q, k, v = workloads.make_inputs("mix", device=dev, heads=range(6), Sq=700, N=900)
+    outs = []
+    for _ in range(2):
+        fa, o = run(q, k, v, [(0, 450), (450, 450)], centering=True)
+        outs.append((o.clone(), fa.bounds.m.clone(), fa.bounds.kbar.clone(), fa.acc_sum.clone()))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
+# ------------------------------------------------------------------ full-size workloads (sampled rows)
+
+def sampled(q, k, v, o, heads, rows):
+    qs = q[0, heads][:, rows].cpu()
+    ks, vs = k[0, heads].cpu(), v[0, heads].cpu()
+    ref = oracle.attention(qs, ks, vs)
+    got = o[0, heads][:, rows]
+    return maxerr(got, ref)
+
+
+def test_h40_s4096_full(dev):
+    w = workloads.WORKLOADS["h40_s4096"]
+    q, k, v = workloads.make_inputs("h40_s4096", device=dev)
+    fa, o = run(q, k, v, workloads.chunk_bounds(w), centering=False)
+    check_bounds(fa, oracle.bounds(q.cpu(), k.cpu(), v.cpu(), centering=False))
+    assert bool(fa.bounds.flag.all())
+    rows = list(range(0, 128)) + list(range(2000, 2100)) + list(range(3968, 4096))
+    assert sampled(q, k, v, o, [0, 39], rows) <= TOL_BF16
+    _, o2 = run(q, k, v, workloads.chunk_bounds(w), force_online=True)
+    assert maxerr(o2[0, [0, 39]][:, rows], o[0, [0, 39]][:, rows]) <= TOL_BF16
+
+
+def test_wan_full_size(dev):
+    w = workloads.WORKLOADS["wan"]
+    q, k, v = workloads.make_inputs("wan", device=dev)
+    fa, o = run(q, k, v, workloads.chunk_bounds(w), centering=True)
+    heads = [0, 17, 39]
+    ob = oracle.bounds(q[:, heads].cpu(), k[:, heads].cpu(), v[:, heads].cpu(), centering=True)
+    check_bounds(fa, ob, heads=heads, check_vmax=False)
+    # the V maximum spans every head: the oracle's, over groups of heads (keys stand in
+    # for nothing here, they only give the call the shape it wants)
+    vmax = max(oracle.bounds(q[:, h0:h0 + 4, :1].cpu(), v[:, h0:h0 + 4].cpu(), v[:, h0:h0 + 4].cpu())["vmax_sq"]
+               for h0 in range(0, 40, 4))
+    assert float(fa.bounds.vmax_sq.item()) == vmax
+    nqb = fa.bounds.out.n_qblocks
+    assert nqb == 591
+    # rows: first Q-block pair, one block in the middle, the ragged 80-row tail
+    rows = list(range(0, 256)) + list(range(37760, 37888)) + list(range(75520, 75600))
+    assert sampled(q, k, v, o, [0, 17], rows) <= TOL_BF16
+    _, o2 = run(q, k, v, workloads.chunk_bounds(w), centering=True, force_online=True)
+    assert maxerr(o2[0, [0, 17]][:, rows], o[0, [0, 17]][:, rows]) <= TOL_BF16
+
+
+@pytest.mark.parametrize("centering", [False, True])
+def test_mix_fallback_full(dev, centering):
+    q, k, v = workloads.make_inputs("mix", device=dev)
+    fa, o = run(q, k, v, None, centering=centering)
+    ob = oracle.bounds(q.cpu(), k.cpu(), v.cpu(), centering=centering)
+    check_bounds(fa, ob)
+    flags = fa.bounds.flag.cpu().numpy()[0]
+    heads_on = [h for h in range(40) if flags[h].all()][:1]
+    heads_off = [h for h in range(40) if not flags[h].any()][:1]
+    if not centering:
+        assert heads_off, "without centering some heads must fall back"
+    rows = list(range(0, 128)) + list(range(16256, 16384))
+    for hs in (heads_on, heads_off):
+        if hs:
+            assert sampled(q, k, v, o, hs, rows) <= TOL_BF16, hs
+
+
+def test_adversarial_full(dev):
+    w = workloads.WORKLOADS["adversarial"]
+    q, k, v = workloads.make_inputs("adversarial", device=dev)
+    fa, o = run(q, k, v, None, centering=True)
+    ob = oracle.bounds(q.cpu(), k.cpu(), v.cpu(), centering=True)
+    check_bounds(fa, ob)
+    flags = fa.bounds.flag.cpu().numpy()[0]
+    adv = w.extra["adv_heads"]
+    assert not flags[:adv, 0].any(), "the query with bound 231.01 must be rejected"
+    assert flags[:adv, 1:].all() and flags[adv:].all()
+    rows = list(range(0, 256))
+    assert sampled(q, k, v, o, [0, 25], rows) <= TOL_BF16
+    _, o2 = run(q, k, v, None, centering=True, force_online=True)
+    assert maxerr(o2[0, [0, 25]][:, rows], o[0, [0, 25]][:, rows]) <= TOL_BF16
