@@ -7,6 +7,7 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 
 #include <mutex>
 #include <string>
@@ -15,8 +16,10 @@
 
 namespace fm {
 
-// Per-GPU error word: set by a kernel whose pipeline wait ran past its limit.
-__device__ unsigned int g_dev_error;
+// Per-GPU error record: word 0 is set by the first kernel wait that ran past its limit
+// (the role code); words 1-5 say where (barrier << 16 | tile, block x, y, z, thread).
+constexpr int kErrWords = 8;
+__device__ unsigned int g_dev_error[kErrWords];
 
 namespace {
 
@@ -63,6 +66,17 @@ int ceil_log2_i64(int64_t n) {
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Limit of one pipeline wait inside a kernel: kWaitTimeoutNs, or FM_WAIT_TIMEOUT_MS
+// milliseconds from the environment (1 ms to 60 s).
+unsigned long long wait_timeout_ns() {
+  const char *s = getenv("FM_WAIT_TIMEOUT_MS");
+  if (s && *s) {
+    const long long ms = atoll(s);
+    if (ms >= 1 && ms <= 60000) return (unsigned long long)ms * 1000000ull;
+  }
+  return kWaitTimeoutNs;
+}
 
 // Validate one fm_tensor and turn it into a View.  `what` names it in messages.
 int to_view(const fm_tensor *t, const char *what, View *v) {
@@ -291,7 +305,7 @@ int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor 
   a.acc_sum = acc_sum;
   a.acc_max = acc_max;
   a.err = err;
-  a.timeout_ns = kWaitTimeoutNs;
+  a.timeout_ns = wait_timeout_ns();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (rows > 0) {
@@ -327,15 +341,19 @@ int fm_sync_status(fm_stream_t stream) {
   t_err.clear();
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-  unsigned int word = 0;
-  e = cudaMemcpyFromSymbol(&word, g_dev_error, sizeof word);
+  unsigned int w[kErrWords] = {};
+  e = cudaMemcpyFromSymbol(w, g_dev_error, sizeof w);
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-  if (word != 0) {
-    const unsigned int zero = 0;
-    cudaMemcpyToSymbol(g_dev_error, &zero, sizeof zero);
-    return fail(FM_ERR_TIMEOUT, "a kernel pipeline wait ran past its limit (code %u); outputs are invalid", word);
+  if (w[0] != 0) {
+    const unsigned int zero[kErrWords] = {};
+    cudaMemcpyToSymbol(g_dev_error, zero, sizeof zero);
+    return fail(FM_ERR_TIMEOUT,
+                "a kernel pipeline wait ran past its limit (role %u, barrier %u, tile %u, block (%u,%u,%u), "
+                "thread %u); outputs are invalid",
+                w[0], w[1] >> 16, w[1] & 0xFFFFu, w[2], w[3], w[4], w[5]);
   }
   return FM_OK;
 }
 
 }  // extern "C"
+

@@ -112,12 +112,14 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
-// Slow path of wait_phase: poll until the phase completes, the time limit passes (the
-// failure is recorded and the CTA's abort flag raised) or, if `abort_flag` is given,
-// another role of the CTA has already given up.
+// Slow path of wait_phase: poll until the phase completes, the time limit passes or, if
+// `abort_flag` is given, another role of the CTA has already given up.  On expiry the
+// first failing wait of the launch records itself in err[0..5]: role code, `tag`
+// (barrier index << 16 | tile index j), block x, y, z and thread, and raises the CTA's
+// abort flag.
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                              unsigned long long timeout_ns, unsigned int *err,
-                                             unsigned int code) {
+                                             unsigned int code, unsigned int tag) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_test(bar, parity)) return true;
@@ -125,7 +127,13 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, vola
       if (abort_flag && *abort_flag) return false;
       if (globaltimer() - t0 > timeout_ns) {
         if (abort_flag) *abort_flag = 1;
-        atomicCAS(err, 0u, code);
+        if (atomicCAS(err, 0u, code) == 0u) {
+          err[1] = tag;
+          err[2] = blockIdx.x;
+          err[3] = blockIdx.y;
+          err[4] = blockIdx.z;
+          err[5] = threadIdx.x;
+        }
         return false;
       }
     }
@@ -134,9 +142,12 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, vola
 // Wait for the phase of `bar` with parity `parity`; false when the wait gave up.
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                            unsigned long long timeout_ns, unsigned int *err,
-                                           unsigned int code) {
+                                           unsigned int code, unsigned int tag = 0) {
   if (mbar_test(bar, parity)) return true;
-  return wait_phase_slow(bar, parity, abort_flag, timeout_ns, err, code);
+  return wait_phase_slow(bar, parity, abort_flag, timeout_ns, err, code, tag);
+}
+__device__ __forceinline__ unsigned int wtag(int bar_index, int j) {
+  return ((unsigned int)bar_index << 16) | ((unsigned int)j & 0xFFFFu);
 }
 
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm, uint32_t bar, int c0,
@@ -296,10 +307,13 @@ __device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, in
       if (c * 32 + e < nvalid) mx = fmaxf(mx, __uint_as_float(s[e]));
   }
   const float zmax = mx * alpha;
-  if (run == -INFINITY || zmax > run + kLazyRescale) {
-    const float nr = fmaxf(run, zmax);
-    if (have_o && run != -INFINITY) {
-      const float sc = ex2(run - nr);
+  // The decision is per row, but tcgen05.ld/st are warp-collective: the warp rescales
+  // when any of its rows needs it, and rows that do not keep their max (scale 1).
+  const bool need = run == -INFINITY || zmax > run + kLazyRescale;
+  if (__any_sync(0xffffffffu, need)) {
+    const float nr = need ? fmaxf(run, zmax) : run;
+    if (have_o) {  // O holds earlier tiles (j > 0): every row's run is finite then
+      const float sc = need ? ex2(run - nr) : 1.0f;
 #pragma unroll
       for (int i = 0; i < 4; ++i) l[i] *= sc;
 #pragma unroll
@@ -383,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int w = 0; w < 2 && ok; ++w) {
           const int idx = 2 * j + w, s = idx % kStages, round = idx / kStages;
           ok = wait_phase(bar(kBarKVEmpty + s), (uint32_t)((round & 1) ^ 1), abort_flag, p.timeout_ns, p.err,
-                          kDevErrTimeoutProducer);
+                          kDevErrTimeoutProducer, wtag(kBarKVEmpty + s, j));
           if (!ok) break;
           mbar_expect_tx(bar(kBarKVFull + s), kTileBytes);
           const CUtensorMap *tm = w ? &tmV : &tmK;
@@ -395,11 +409,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         // let every copy already issued land before the CTA can exit
-        wait_phase(bar(kBarQFull), 0, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain);
+        wait_phase(bar(kBarQFull), 0, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain, wtag(kBarQFull, 0));
         for (int s = 0; s < kStages; ++s)
           if (last_round[s] >= 0)
             wait_phase(bar(kBarKVFull + s), (uint32_t)(last_round[s] & 1), nullptr, p.timeout_ns, p.err,
-                       kDevErrTimeoutDrain);
+                       kDevErrTimeoutDrain, wtag(kBarKVFull + s, 0));
       }
     }
   } else if (warp == 1) {
@@ -415,12 +429,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto v_desc = [&](int s, int kk) {
         return smem_desc(base + kOffKV + s * kTileBytes + kk * 2048, kPanelBytes, 1024);
       };
-      bool ok = wait_phase(bar(kBarQFull), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma);
+      bool ok = wait_phase(bar(kBarQFull), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma, wtag(kBarQFull, 0));
       int vs_prev = 0;
       for (int j = 0; j < n_kv && ok; ++j) {
         const int ki = 2 * j, ks = ki % kStages;
         ok = wait_phase(bar(kBarKVFull + ks), (uint32_t)((ki / kStages) & 1), abort_flag, p.timeout_ns, p.err,
-                        kDevErrTimeoutMma);
+                        kDevErrTimeoutMma, wtag(kBarKVFull + ks, j));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -428,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(kBarSFull + 0));
         if (j > 0) {
           ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((j - 1) & 1), abort_flag, p.timeout_ns, p.err,
-                          kDevErrTimeoutMma);
+                          kDevErrTimeoutMma, wtag(kBarPReady + 1, j));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -442,9 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(kBarKVEmpty + ks));
         const int vi = 2 * j + 1, vs = vi % kStages;
         ok = wait_phase(bar(kBarKVFull + vs), (uint32_t)((vi / kStages) & 1), abort_flag, p.timeout_ns, p.err,
-                        kDevErrTimeoutMma) &&
+                        kDevErrTimeoutMma, wtag(kBarKVFull + vs, j)) &&
              wait_phase(bar(kBarPReady + 0), (uint32_t)(j & 1), abort_flag, p.timeout_ns, p.err,
-                        kDevErrTimeoutMma);
+                        kDevErrTimeoutMma, wtag(kBarPReady + 0, j));
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -454,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (ok) {
         ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((n_kv - 1) & 1), abort_flag, p.timeout_ns, p.err,
-                        kDevErrTimeoutMma);
+                        kDevErrTimeoutMma, wtag(kBarPReady + 1, n_kv));
         if (ok) {
           tc_fence_after();
 #pragma unroll
@@ -467,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         // every MMA issued so far must finish reading shared memory and TMEM before exit
         mma_commit(bar(kBarDrain));
-        wait_phase(bar(kBarDrain), 0, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain);
+        wait_phase(bar(kBarDrain), 0, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain, wtag(kBarDrain, 0));
       }
     }
   } else if (warp >= 4) {
@@ -491,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       ok = wait_phase(bar(kBarSFull + t), (uint32_t)(j & 1), abort_flag, p.timeout_ns, p.err,
-                      kDevErrTimeoutSoftmax);
+                      kDevErrTimeoutSoftmax, wtag(kBarSFull + t, j));
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
       if (!ok) break;
       tc_fence_after();
@@ -503,7 +517,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(kBarPReady + t));
     }
     if (ok) {
-      ok = wait_phase(bar(kBarODone + t), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutSoftmax);
+      ok = wait_phase(bar(kBarODone + t), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutSoftmax,
+                      wtag(kBarODone + t, n_kv));
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {

@@ -184,6 +184,7 @@ FM_API const char *fm_last_error(void);
 /* ABI version of this header: (major << 16) | minor. */
 FM_API int fm_version(void);
 
+
 #ifdef __cplusplus
 }
 #endif

@@ -189,3 +189,4 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     finally:
         fm._lib = saved
         importlib.invalidate_caches()
+
