@@ -7,8 +7,8 @@ pointers and the current CUDA stream, and turns error codes into exceptions.
 PyTorch provides device memory and streams and nothing else.
 
 Functions with the ABI's names (same arguments, torch tensors in place of pointers):
-``fm_bounds_workspace_size``, ``fm_bounds``, ``fm_attn_chunk``, ``fm_finalize``,
-``fm_sync_status``, ``fm_last_error``, ``fm_version``.
+``fm_bounds_workspace_size``, ``fm_bounds``, ``fm_bounds_noalloc``, ``fm_attn_chunk``,
+``fm_finalize``, ``fm_sync_status``, ``fm_last_error``, ``fm_version``.
 
 ``FixedMAttention`` owns the buffers of one problem shape and runs the whole path
 (bounds, one ``fm_attn_chunk`` per KV chunk, finalize); ``attention()`` is the
@@ -34,7 +34,8 @@ FM_BLOCK_Q = 128
 ERROR_NAMES = {0: "FM_OK", 1: "FM_ERR_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_DTYPE", 4: "FM_ERR_UNSUPPORTED",
                5: "FM_ERR_BOUNDS_MISMATCH", 6: "FM_ERR_CUDA", 7: "FM_ERR_TIMEOUT"}
 ABI_SYMBOLS = ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
-               "fm_last_error", "fm_version")
+               "fm_last_error", "fm_version", "fm_bounds_noalloc")
+FM_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
 class FMError(RuntimeError):
@@ -83,12 +84,13 @@ def load(path: str | None = None):
     lib.fm_bounds.argtypes = [P, P, P, P, P, P, ctypes.c_size_t, P]
     lib.fm_attn_chunk.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_int, P]
     lib.fm_finalize.argtypes = [P, P, P, P]
+    lib.fm_bounds_noalloc.argtypes = [P, P, P, P, P, P]
     lib.fm_sync_status.argtypes = [P]
     lib.fm_last_error.restype = ctypes.c_char_p
     lib.fm_last_error.argtypes = []
     lib.fm_version.argtypes = []
     for name in ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
-                 "fm_version"):
+                 "fm_version", "fm_bounds_noalloc"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -175,6 +177,14 @@ def fm_bounds(q, k_full, v_full, opt: fm_opts, bounds: Bounds, workspace: torch.
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     return _check(load().fm_bounds(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), ctypes.byref(opt),
                                    ctypes.byref(bounds.out), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fm_bounds_noalloc(q, k_full, v_full, opt: fm_opts, bounds: Bounds, stream=None):
+    """fm_bounds without a workspace: the library's static device scratch is used instead
+    (for callers that cannot allocate; see include/fm.h)."""
+    tq, tk, tv = tensor(q), tensor(k_full), tensor(v_full)
+    return _check(load().fm_bounds_noalloc(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), ctypes.byref(opt),
+                                           ctypes.byref(bounds.out), _stream(stream)))
 
 
 def fm_attn_chunk(q, k_chunk, v_chunk, bounds: Bounds, opt: fm_opts, acc_o, acc_sum, acc_max,

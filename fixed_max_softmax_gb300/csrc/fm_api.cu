@@ -357,3 +357,50 @@ int fm_sync_status(fm_stream_t stream) {
 
 }  // extern "C"
 
+// ---------------------------------------------------------------------------------
+// fm_bounds_noalloc: fm_bounds with its scratch in a file-scope device array, for callers
+// that cannot allocate.  The array is per GPU and lives as long as the process; host code
+// only ever sees a stand-in for its name, so its device address is looked up once per
+// device, with that device current, and that address is what the kernels receive.
+namespace fm {
+namespace {
+
+__device__ __align__(256) unsigned char g_bounds_scratch[FM_NOALLOC_SCRATCH_BYTES];
+
+int bounds_scratch_address(void **addr) {
+  static void *ptrs[kMaxDevices] = {};
+  static cudaError_t errs[kMaxDevices] = {};
+  static std::once_flag once[kMaxDevices];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "fm_bounds_noalloc: no current device");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FM_ERR_UNSUPPORTED, "fm_bounds_noalloc: device index %d", dev);
+  std::call_once(once[dev], [dev] {
+    void *p = nullptr;
+    errs[dev] = cudaGetSymbolAddress(&p, g_bounds_scratch);
+    if (errs[dev] == cudaSuccess) ptrs[dev] = p;
+  });
+  if (errs[dev] != cudaSuccess) return cuda_fail(errs[dev], "fm_bounds_noalloc: cudaGetSymbolAddress");
+  *addr = ptrs[dev];
+  return FM_OK;
+}
+
+}  // namespace
+}  // namespace fm
+
+extern "C" int fm_bounds_noalloc(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_full,
+                                 const fm_opts *opts, fm_bounds_out *out, fm_stream_t stream) {
+  t_err.clear();
+  if (k_full && k_full->B >= 0 && k_full->H >= 0 && k_full->S >= 0 && k_full->D >= 0) {
+    const size_t need = bounds_workspace_bytes(k_full->B, k_full->H, k_full->S, k_full->D);
+    if (need > FM_NOALLOC_SCRATCH_BYTES)
+      return fail(FM_ERR_UNSUPPORTED,
+                  "fm_bounds_noalloc: this problem needs %zu bytes of scratch; the library's static scratch "
+                  "holds %zu (use fm_bounds with a workspace)",
+                  need, (size_t)FM_NOALLOC_SCRATCH_BYTES);
+  }
+  void *scratch = nullptr;
+  int rc = bounds_scratch_address(&scratch);
+  if (rc != FM_OK) return rc;
+  return fm_bounds(q, k_full, v_full, opts, out, scratch, FM_NOALLOC_SCRATCH_BYTES, stream);
+}

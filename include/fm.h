@@ -184,6 +184,29 @@ FM_API const char *fm_last_error(void);
 /* ABI version of this header: (major << 16) | minor. */
 FM_API int fm_version(void);
 
+/* Upper bound of the scratch fm_bounds_noalloc can use: 4 MiB.  That covers, at D = 128,
+ * about 120 heads of 75,600 keys (fm_bounds_workspace_size gives the exact need). */
+#define FM_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
+/* fm_bounds_noalloc -- fm_bounds for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call: it exists for callers whose device memory
+ * is planned in full before they run (an inference engine that reserves its arena up
+ * front and forbids allocation afterwards, a plug-in inside another framework's memory
+ * pool) and for latency-critical streams that must not pay cudaMalloc's implicit device
+ * synchronisation.  Same arguments and results as fm_bounds, minus the workspace: the
+ * scratch lives in a file-scope device array of FM_NOALLOC_SCRATCH_BYTES inside libfm,
+ * which every GPU that loads the library holds until the process exits.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library routine.
+ *   - The first call on each device looks up the array's device address with that device
+ *     current (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents; nothing in
+ *     it needs to start at zero, since every slot the kernels read is written earlier in
+ *     the same call.  Calls that overlap on the GPU (other streams, other threads) race
+ *     on it: serialise them.
+ * Errors: those of fm_bounds, plus FM_ERR_UNSUPPORTED when the problem needs more scratch
+ * than FM_NOALLOC_SCRATCH_BYTES (nothing is enqueued then). */
+FM_API int fm_bounds_noalloc(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_full,
+                             const fm_opts *opts, fm_bounds_out *out, fm_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -190,3 +190,15 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
         fm._lib = saved
         importlib.invalidate_caches()
 
+
+def test_noalloc_refuses_oversized_problems_on_the_host(lib):
+    t = fake(1, 200, 75600, 128)
+    out = fm.fm_bounds_out()
+    rc = lib.fm_bounds_noalloc(ctypes.byref(t), ctypes.byref(t), ctypes.byref(t), ctypes.byref(fm.opts()),
+                               ctypes.byref(out), None)
+    assert rc == fm.FM_ERR_UNSUPPORTED and "scratch" in fm.fm_last_error()
+    # invalid dtype is still reported as such by the shared validation
+    t16 = fake(1, 2, 100, 128, fm.FM_F16)
+    rc = lib.fm_bounds_noalloc(ctypes.byref(t16), ctypes.byref(t16), ctypes.byref(t16), ctypes.byref(fm.opts()),
+                               ctypes.byref(out), None)
+    assert rc in (fm.FM_ERR_DTYPE, fm.FM_ERR_CUDA)
