@@ -45,7 +45,7 @@ namespace {
 constexpr int kBQ = 128;   // rows per Q tile = TMEM lanes
 constexpr int kBK = 128;   // keys per KV tile
 constexpr int kHD = 128;   // head dimension
-constexpr int kStages = 4; // K/V ring: K_j in stage (2j)%4, V_j in stage (2j+1)%4
+constexpr int kStages = 5; // K/V ring: K_j in stage (2j)%5, V_j in stage (2j+1)%5
 constexpr int kTileBytes = kBK * kHD * 2;     // 32 KiB
 constexpr int kPanelBytes = 128 * 64 * 2;     // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr int kThreads = 384;
@@ -215,7 +215,44 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
 }
+// The same load without waiting: the registers are valid only after tmem_ld_wait(r).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+      "%13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, "
+      "[%32];"
+      : FM_R8(0), FM_R8(8), FM_R8(16), FM_R8(24)
+      : "r"(taddr)
+      : "memory");
+}
 #undef FM_R8
+#define FM_W8(i) "+r"(r[i + 0]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), \
+                 "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+// Wait for this thread's TMEM loads.  `r` (the destination of the last one) passes through
+// the instruction, so the compiler cannot schedule a use of it before the wait.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : FM_W8(0), FM_W8(8), FM_W8(16), FM_W8(24) : : "memory");
+}
+#undef FM_W8
+// Two fp32 lanes in one 64-bit register (Blackwell's packed fp32x2 arithmetic).
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
@@ -262,35 +299,84 @@ struct TcParams {
   unsigned long long timeout_ns;
 };
 
-// Fixed-m softmax of one 128x128 S tile for this thread's row; P overwrites S.
+// p = 2^(alpha*s - bias) for 32 scores of one full chunk, two at a time with fp32x2 FMA and
+// adds; the row sum goes to two pair accumulators, P to 16 bf16x2 words.
+__device__ __forceinline__ void exp_chunk_full(const uint32_t (&s)[32], uint64_t a2, uint64_t nb2, uint64_t &acc0,
+                                               uint64_t &acc1, uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    float z0, z1;
+    f2_unpack(f2_fma(f2_pack(s[2 * e], s[2 * e + 1]), a2, nb2), z0, z1);
+    const float p0 = ex2(z0), p1 = ex2(z1);
+    const uint64_t pp = f2_pack(__float_as_uint(p0), __float_as_uint(p1));
+    if (e & 1) acc1 = f2_add(acc1, pp); else acc0 = f2_add(acc0, pp);
+    pk[e] = pack_bf16(p0, p1);
+  }
+}
+
+// The same for the chunk holding the ragged end of the keys: columns >= nvalid give 0.
+__device__ __forceinline__ void exp_chunk_masked(const uint32_t (&s)[32], int col0, int nvalid, float alpha,
+                                                 float nbias, float (&l)[4], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const int col = col0 + 2 * e;
+    const float p0 = col < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e]), alpha, nbias)) : 0.f;
+    const float p1 = col + 1 < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e + 1]), alpha, nbias)) : 0.f;
+    l[e & 3] += p0;
+    l[(e + 2) & 3] += p1;
+    pk[e] = pack_bf16(p0, p1);
+  }
+}
+
+// Fixed-m softmax of one 128x128 S tile for this thread's row; P overwrites S.  The four
+// 32-column TMEM loads are double-buffered: chunk c+1 is in flight while chunk c is
+// exponentiated.
 __device__ __forceinline__ void softmax_fixed_tile(uint32_t tS, int nvalid, float alpha, float nbias,
                                                    float (&l)[4]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t s[32];
-    tmem_ld32(tS + c * 32, s);
-    uint32_t pk[16];
-    if (nvalid >= kBK) {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), alpha, nbias));
-        const float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), alpha, nbias));
-        l[e & 3] += p0;
-        l[(e + 2) & 3] += p1;
-        pk[e] = pack_bf16(p0, p1);
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int col = c * 32 + 2 * e;
-        const float p0 = col < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e]), alpha, nbias)) : 0.f;
-        const float p1 = col + 1 < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e + 1]), alpha, nbias)) : 0.f;
-        l[e & 3] += p0;
-        l[(e + 2) & 3] += p1;
-        pk[e] = pack_bf16(p0, p1);
-      }
-    }
-    tmem_st16(tS + c * 16, pk);  // P columns [16c, 16c+16) lie in S columns already read
+  uint32_t sa[32], sb[32];
+  uint32_t pk[16];
+  tmem_ld32_async(tS, sa);
+  tmem_ld_wait(sa);
+  if (nvalid >= kBK) {
+    const uint64_t a2 = f2_pack(__float_as_uint(alpha), __float_as_uint(alpha));
+    const uint64_t nb2 = f2_pack(__float_as_uint(nbias), __float_as_uint(nbias));
+    uint64_t acc0 = 0, acc1 = 0;  // +0.0f pairs
+    tmem_ld32_async(tS + 32, sb);
+    exp_chunk_full(sa, a2, nb2, acc0, acc1, pk);
+    tmem_st16(tS + 0, pk);  // P columns [16c, 16c+16) lie in S columns already read
+    tmem_ld_wait(sb);
+    tmem_ld32_async(tS + 64, sa);
+    exp_chunk_full(sb, a2, nb2, acc0, acc1, pk);
+    tmem_st16(tS + 16, pk);
+    tmem_ld_wait(sa);
+    tmem_ld32_async(tS + 96, sb);
+    exp_chunk_full(sa, a2, nb2, acc0, acc1, pk);
+    tmem_st16(tS + 32, pk);
+    tmem_ld_wait(sb);
+    exp_chunk_full(sb, a2, nb2, acc0, acc1, pk);
+    tmem_st16(tS + 48, pk);
+    float x0, x1, y0, y1;
+    f2_unpack(acc0, x0, x1);
+    f2_unpack(acc1, y0, y1);
+    l[0] += x0;
+    l[1] += x1;
+    l[2] += y0;
+    l[3] += y1;
+  } else {
+    tmem_ld32_async(tS + 32, sb);
+    exp_chunk_masked(sa, 0, nvalid, alpha, nbias, l, pk);
+    tmem_st16(tS + 0, pk);
+    tmem_ld_wait(sb);
+    tmem_ld32_async(tS + 64, sa);
+    exp_chunk_masked(sb, 32, nvalid, alpha, nbias, l, pk);
+    tmem_st16(tS + 16, pk);
+    tmem_ld_wait(sa);
+    tmem_ld32_async(tS + 96, sb);
+    exp_chunk_masked(sa, 64, nvalid, alpha, nbias, l, pk);
+    tmem_st16(tS + 32, pk);
+    tmem_ld_wait(sb);
+    exp_chunk_masked(sb, 96, nvalid, alpha, nbias, l, pk);
+    tmem_st16(tS + 48, pk);
   }
 }
 
