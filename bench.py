@@ -46,6 +46,23 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(t_ms: float, device=None) -> float:
+    """The slowest rank's time (all ranks get it); the local time when not distributed."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return t_ms
+    tt = torch.tensor([t_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def whole_job_tflops(world: int, flops_per_rank_step: float, steps: int, t_ms: float) -> float:
+    """Units processed by all ranks (each an independent replica) over the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (t_ms * 1e-3) / 1e12
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
 
@@ -214,12 +231,9 @@ def run_ours(args, rank, world, local_rank):
     fm.fm_sync_status(stream)
     t_ms = start.elapsed_time(end)
     chunk_ms = [chunk_events[i].elapsed_time(chunk_events[i + 1]) for i in range(0, len(chunk_events), 2)]
-    if dist is not None:
-        tt = torch.tensor([t_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms = float(tt.item())
+    t_ms = max_over_ranks(t_ms, dev)
     ms_per_step = t_ms / args.steps
-    value = world * step_flops * args.steps / (t_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, step_flops, args.steps, t_ms)
 
     # ---- end to end through the public API with host buffers (pinned), copies timed
     e2e = None
@@ -247,12 +261,8 @@ def run_ours(args, rank, world, local_rank):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         fm.fm_sync_status(stream)
-        te = e0.elapsed_time(e1)
-        if dist is not None:
-            tt = torch.tensor([te], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            te = float(tt.item())
-        e2e = {"value": world * step_flops * args.e2e_steps / (te * 1e-3) / 1e12, "unit": "TFLOP/s",
+        te = max_over_ranks(e0.elapsed_time(e1), dev)
+        e2e = {"value": whole_job_tflops(world, step_flops, args.e2e_steps, te), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(3 * q.numel() * q.element_size()),
                "d2h_bytes_per_step": int(fa.out.numel() * fa.out.element_size()),
                "ms_per_step": te / args.e2e_steps, "steps": args.e2e_steps}

@@ -8,7 +8,7 @@ PyTorch provides device memory and streams and nothing else.
 
 Functions with the ABI's names (same arguments, torch tensors in place of pointers):
 ``fm_bounds_workspace_size``, ``fm_bounds``, ``fm_bounds_noalloc``, ``fm_attn_chunk``,
-``fm_finalize``, ``fm_sync_status``, ``fm_last_error``, ``fm_version``.
+``fm_finalize``, ``fm_finalize_lse``, ``fm_sync_status``, ``fm_last_error``, ``fm_version``.
 
 ``FixedMAttention`` owns the buffers of one problem shape and runs the whole path
 (bounds, one ``fm_attn_chunk`` per KV chunk, finalize); ``attention()`` is the
@@ -34,7 +34,7 @@ FM_BLOCK_Q = 128
 ERROR_NAMES = {0: "FM_OK", 1: "FM_ERR_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_DTYPE", 4: "FM_ERR_UNSUPPORTED",
                5: "FM_ERR_BOUNDS_MISMATCH", 6: "FM_ERR_CUDA", 7: "FM_ERR_TIMEOUT"}
 ABI_SYMBOLS = ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
-               "fm_last_error", "fm_version", "fm_bounds_noalloc")
+               "fm_last_error", "fm_version", "fm_bounds_noalloc", "fm_finalize_lse")
 FM_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -52,17 +52,18 @@ class fm_tensor(ctypes.Structure):
 
 class fm_opts(ctypes.Structure):
     _fields_ = [("softmax_scale", ctypes.c_float), ("centering", ctypes.c_int32),
-                ("force_online", ctypes.c_int32)]
+                ("force_online", ctypes.c_int32), ("per_row", ctypes.c_int32)]
 
 
 class fm_bounds_out(ctypes.Structure):
     _fields_ = [("m", ctypes.c_void_p), ("flag", ctypes.c_void_p), ("qmax_sq", ctypes.c_void_p),
                 ("kmax_sq", ctypes.c_void_p), ("kbar", ctypes.c_void_p), ("qkbar", ctypes.c_void_p),
-                ("vmax_sq", ctypes.c_void_p),
+                ("shift", ctypes.c_void_p), ("vmax_sq", ctypes.c_void_p),
                 ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("Sq", ctypes.c_int64), ("D", ctypes.c_int64),
                 ("n_qblocks", ctypes.c_int64), ("N_total", ctypes.c_int64),
                 ("C", ctypes.c_int32), ("W", ctypes.c_int32), ("gate", ctypes.c_int32),
-                ("centered", ctypes.c_int32), ("alpha", ctypes.c_float), ("dtype", ctypes.c_int32),
+                ("centered", ctypes.c_int32), ("per_row", ctypes.c_int32), ("alpha", ctypes.c_float),
+                ("dtype", ctypes.c_int32),
                 ("kv_seen", ctypes.c_int64), ("online_lock", ctypes.c_int32), ("magic", ctypes.c_uint32)]
 
 
@@ -85,12 +86,13 @@ def load(path: str | None = None):
     lib.fm_attn_chunk.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_int, P]
     lib.fm_finalize.argtypes = [P, P, P, P]
     lib.fm_bounds_noalloc.argtypes = [P, P, P, P, P, P]
+    lib.fm_finalize_lse.argtypes = [P, P, P, P, P, P]
     lib.fm_sync_status.argtypes = [P]
     lib.fm_last_error.restype = ctypes.c_char_p
     lib.fm_last_error.argtypes = []
     lib.fm_version.argtypes = []
     for name in ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
-                 "fm_version", "fm_bounds_noalloc"):
+                 "fm_version", "fm_bounds_noalloc", "fm_finalize_lse"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -116,8 +118,9 @@ def tensor(t: torch.Tensor) -> fm_tensor:
     return d
 
 
-def opts(softmax_scale: float = 0.0, centering: bool = False, force_online: bool = False) -> fm_opts:
-    return fm_opts(float(softmax_scale), int(bool(centering)), int(bool(force_online)))
+def opts(softmax_scale: float = 0.0, centering: bool = False, force_online: bool = False,
+         per_row: bool = False) -> fm_opts:
+    return fm_opts(float(softmax_scale), int(bool(centering)), int(bool(force_online)), int(bool(per_row)))
 
 
 def _stream(stream):
@@ -164,12 +167,14 @@ class Bounds:
         self.kmax_sq = torch.zeros(B, H, dtype=torch.float32, **kw)
         self.kbar = torch.zeros(B, H, D, dtype=torch.float32, **kw)
         self.qkbar = torch.zeros(B, H, max(Sq, 1), dtype=torch.float32, **kw)
+        self.shift = torch.zeros(B, H, max(Sq, 1), dtype=torch.float32, **kw)
         self.vmax_sq = torch.zeros(1, dtype=torch.float32, **kw)
         self.out = fm_bounds_out()
         self.out.m, self.out.flag = self.m.data_ptr(), self.flag.data_ptr()
         self.out.qmax_sq, self.out.kmax_sq = self.qmax_sq.data_ptr(), self.kmax_sq.data_ptr()
         self.out.kbar, self.out.qkbar, self.out.vmax_sq = (self.kbar.data_ptr(), self.qkbar.data_ptr(),
                                                            self.vmax_sq.data_ptr())
+        self.out.shift = self.shift.data_ptr()
 
 
 def fm_bounds(q, k_full, v_full, opt: fm_opts, bounds: Bounds, workspace: torch.Tensor | None, stream=None):
@@ -200,6 +205,12 @@ def fm_finalize(acc_o, acc_sum, o_out, stream=None):
     return _check(load().fm_finalize(_ptr(acc_o), _ptr(acc_sum), ctypes.byref(to), _stream(stream)))
 
 
+def fm_finalize_lse(acc_o, acc_sum, acc_max, o_out, lse, stream=None):
+    to = tensor(o_out)
+    return _check(load().fm_finalize_lse(_ptr(acc_o), _ptr(acc_sum), _ptr(acc_max), ctypes.byref(to), _ptr(lse),
+                                         _stream(stream)))
+
+
 def fm_sync_status(stream=None):
     return _check(load().fm_sync_status(_stream(stream)))
 
@@ -209,13 +220,14 @@ class FixedMAttention:
 
     forward(q, k, v, chunks) runs fm_bounds over all of K/V, one fm_attn_chunk per
     (start, length) slice of the key sequence (the ring's steps, sequentially), and
-    fm_finalize into `out` (fp32 or the input dtype).
+    fm_finalize into `out` (fp32 or the input dtype); with_lse=True finalizes with
+    fm_finalize_lse and also fills `lse` [B, H, Sq] (natural log).
     """
 
     def __init__(self, B, H, Sq, N, D, device="cuda", centering=False, softmax_scale=0.0,
-                 force_online=False, out_dtype=torch.float32):
+                 force_online=False, out_dtype=torch.float32, per_row=False):
         self.shape = (B, H, Sq, N, D)
-        self.opt = opts(softmax_scale, centering, force_online)
+        self.opt = opts(softmax_scale, centering, force_online, per_row)
         self.bounds = Bounds(B, H, Sq, D, device)
         nbytes = fm_bounds_workspace_size(B, H, N, D)
         self.workspace = torch.empty(max(nbytes, 16) // 4 + 4, dtype=torch.float32, device=device)
@@ -223,23 +235,30 @@ class FixedMAttention:
         self.acc_sum = torch.empty(B, H, Sq, dtype=torch.float32, device=device)
         self.acc_max = torch.empty(B, H, Sq, dtype=torch.float32, device=device)
         self.out = torch.empty(B, H, Sq, D, dtype=out_dtype, device=device)
+        self.lse = None
 
-    def forward(self, q, k, v, chunks=None, stream=None):
+    def forward(self, q, k, v, chunks=None, stream=None, with_lse=False):
         N = k.shape[2]
         chunks = [(0, N)] if chunks is None else chunks
         fm_bounds(q, k, v, self.opt, self.bounds, self.workspace, stream)
         for i, (s, n) in enumerate(chunks):
             fm_attn_chunk(q, k[:, :, s:s + n], v[:, :, s:s + n], self.bounds, self.opt, self.acc_o,
                           self.acc_sum, self.acc_max, i > 0, stream)
-        fm_finalize(self.acc_o, self.acc_sum, self.out, stream)
+        if with_lse:
+            if self.lse is None:
+                self.lse = torch.empty(self.acc_sum.shape, dtype=torch.float32, device=self.acc_sum.device)
+            fm_finalize_lse(self.acc_o, self.acc_sum, self.acc_max, self.out, self.lse, stream)
+        else:
+            fm_finalize(self.acc_o, self.acc_sum, self.out, stream)
         return self.out
 
     __call__ = forward
 
 
 def attention(q, k, v, chunks=None, centering=False, softmax_scale=0.0, force_online=False,
-              out_dtype=torch.float32, stream=None):
+              out_dtype=torch.float32, stream=None, per_row=False):
     """One-call fixed-m attention forward: returns o [B, H, Sq, D]."""
     B, H, Sq, D = q.shape
-    fa = FixedMAttention(B, H, Sq, k.shape[2], D, q.device, centering, softmax_scale, force_online, out_dtype)
+    fa = FixedMAttention(B, H, Sq, k.shape[2], D, q.device, centering, softmax_scale, force_online, out_dtype,
+                         per_row)
     return fa.forward(q, k, v, chunks, stream).clone()

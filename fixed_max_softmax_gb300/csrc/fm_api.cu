@@ -171,14 +171,17 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
     return rc;
   if ((rc = check_qkv(vq, vk, vv))) return rc;
   if (!out) return fail(FM_ERR_ARG, "out is NULL");
-  if (opts && opts->centering != 0 && opts->centering != 1) return fail(FM_ERR_ARG, "centering must be 0 or 1");
+  if (opts && ((opts->centering != 0 && opts->centering != 1) || (opts->per_row != 0 && opts->per_row != 1)))
+    return fail(FM_ERR_ARG, "centering and per_row must be 0 or 1");
   const int centering = opts ? opts->centering : 0;
+  const int per_row = opts ? opts->per_row : 0;
   double alpha;
   if ((rc = make_alpha(opts, vq.D, &alpha))) return rc;
   const int64_t B = vq.B, H = vq.H, Sq = vq.S, D = vq.D, N = vk.S;
   const int64_t nqb = ceil_div(Sq, FM_BLOCK_Q);
   // every non-empty device array must be given (torch hands out NULL for empty ones)
-  if ((B * H * nqb > 0 && (!out->m || !out->flag || !out->qmax_sq)) || (B * H * Sq > 0 && !out->qkbar) ||
+  if ((B * H * nqb > 0 && (!out->m || !out->flag || !out->qmax_sq)) ||
+      (B * H * Sq > 0 && (!out->qkbar || !out->shift)) ||
       (B * H > 0 && (!out->kmax_sq || !out->kbar || !out->vmax_sq)))
     return fail(FM_ERR_ARG, "fm_bounds_out: every device array pointer must be set");
   const size_t need = bounds_workspace_bytes(B, H, N, D);
@@ -203,6 +206,7 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
   out->W = W;
   out->gate = gate;
   out->centered = centering;
+  out->per_row = per_row;
   out->alpha = (float)alpha;
   out->dtype = vq.dtype;
   out->kv_seen = 0;
@@ -217,6 +221,7 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
   a.k = vk;
   a.v = vv;
   a.centering = centering;
+  a.per_row = per_row;
   a.alpha = alpha;
   a.C = C;
   a.gate = gate;
@@ -227,6 +232,7 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
   a.kmax_sq = out->kmax_sq;
   a.kbar = out->kbar;
   a.qkbar = out->qkbar;
+  a.shift = out->shift;
   a.vmax_sq = out->vmax_sq;
   a.ws = workspace;
   a.ws_bytes = workspace_bytes;
@@ -284,6 +290,7 @@ int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor 
     return fail(FM_ERR_BOUNDS_MISMATCH, "accumulate=1 before any accumulate=0 chunk for these bounds");
   const int64_t rows = vq.B * vq.H * vq.S;
   if (rows > 0 && (!acc_o || !acc_sum || !acc_max)) return fail(FM_ERR_ARG, "accumulator pointer is NULL");
+  if (rows > 0 && (!bounds->flag || !bounds->shift)) return fail(FM_ERR_ARG, "bounds flag/shift pointer is NULL");
   if (reinterpret_cast<uintptr_t>(acc_o) % 16 || reinterpret_cast<uintptr_t>(acc_sum) % 4 ||
       reinterpret_cast<uintptr_t>(acc_max) % 4)
     return fail(FM_ERR_ARG, "acc_o must be 16-byte aligned, acc_sum/acc_max 4-byte aligned");
@@ -298,9 +305,8 @@ int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor 
   a.force_online = force_online;
   a.accumulate = accumulate;
   a.nqb = nqb;
-  a.m = bounds->m;
   a.flag = bounds->flag;
-  a.qkbar = bounds->qkbar;
+  a.shift = bounds->shift;
   a.acc_o = acc_o;
   a.acc_sum = acc_sum;
   a.acc_max = acc_max;
@@ -334,6 +340,20 @@ int fm_finalize(const float *acc_o, const float *acc_sum, const fm_tensor *o_out
   if (reinterpret_cast<uintptr_t>(acc_o) % 16) return fail(FM_ERR_ARG, "acc_o must be 16-byte aligned");
   cudaError_t e = launch_finalize(acc_o, acc_sum, vo, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fm_finalize launch");
+  return FM_OK;
+}
+
+int fm_finalize_lse(const float *acc_o, const float *acc_sum, const float *acc_max, const fm_tensor *o_out,
+                    float *lse, fm_stream_t stream) {
+  t_err.clear();
+  View vo;
+  int rc;
+  if ((rc = to_view(o_out, "o_out", &vo))) return rc;
+  const int64_t rows = vo.B * vo.H * vo.S;
+  if (rows > 0 && (!acc_o || !acc_sum || !acc_max || !lse)) return fail(FM_ERR_ARG, "a pointer is NULL");
+  if (reinterpret_cast<uintptr_t>(acc_o) % 16) return fail(FM_ERR_ARG, "acc_o must be 16-byte aligned");
+  cudaError_t e = launch_finalize_lse(acc_o, acc_sum, acc_max, vo, lse, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fm_finalize_lse launch");
   return FM_OK;
 }
 

@@ -17,6 +17,7 @@
 //              shuffles; per-block maxima -> qmax_sq (Q) and the workspace (K, V);
 //              qkbar per row
 //   4. finish  per head: key max, global V max, U, m, flag
+//   5. shift   per row: b_i = m_i + alpha*q_i.kbar (m_i per row or per Q-block)
 // Bytes: Q + K + V once each, plus K once more for the mean when centering.
 #include <cuda_bf16.h>
 #include <math.h>
@@ -140,7 +141,7 @@ __global__ void kmean_kernel(const float *part, int64_t H, int64_t P, int D, int
 template <typename T, int EPL, bool CONTIG>
 __global__ void __launch_bounds__(kThreads)
     norms_kernel(View q, View k, View v, int64_t nqb, int64_t nkb, int centering, float alpha,
-                 const float *kbar, float *qmax_sq, float *qkbar, float *kblk, float *vblk) {
+                 const float *kbar, float *qmax_sq, float *qkbar, float *qsq, float *kblk, float *vblk) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t b = blockIdx.z, h = blockIdx.y, bx = blockIdx.x;
   const int64_t bh = b * q.H + h;
@@ -167,7 +168,10 @@ __global__ void __launch_bounds__(kThreads)
       ss = warp_sum(ss);
       dk = warp_sum(dk);
       best = fmaxf(best, ss);
-      if (lane == 0) qkbar[bh * q.S + r] = alpha * dk;
+      if (lane == 0) {
+        qkbar[bh * q.S + r] = alpha * dk;
+        qsq[bh * q.S + r] = ss;  // per-row |q|^2, turned into the row's shift by shift_kernel
+      }
     }
   } else if (bx < nqb + nkb) {
     // K rows: |k - kbar|^2 (kbar = 0 when not centering)
@@ -239,6 +243,25 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// 5. Row shifts: b_i = m_i + alpha*q_i.kbar, with m_i = ceil(alpha*|q_i|*sqrt(kmax)) - C
+// (per row) or the row's Q-block m.  `shift` holds |q_i|^2 on entry (from norms_kernel).
+__global__ void __launch_bounds__(kThreads)
+    shift_kernel(int64_t H, int64_t Sq, int64_t nqb, int per_row, double alpha, int C, const float *kmax_sq,
+                 const int32_t *m, const float *qkbar, float *shift) {
+  const int64_t bh = blockIdx.z * H + blockIdx.y;
+  const int64_t r = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+  if (r >= Sq) return;
+  const int64_t i = bh * Sq + r;
+  int32_t mi;
+  if (per_row) {
+    const double U = alpha * sqrt((double)shift[i]) * sqrt((double)kmax_sq[bh]);
+    mi = (int32_t)ceil(U) - C;
+  } else {
+    mi = m[bh * nqb + r / kQRows];
+  }
+  shift[i] = (float)mi + qkbar[i];
+}
+
 template <typename T, int EPL, bool CONTIG>
 cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st) {
   const int64_t B = a.q.B, H = a.q.H, N = a.k.S;
@@ -257,10 +280,14 @@ cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st
   const int64_t nx = a.nqb + 2 * w.nkb;
   if (nx > 0) {
     norms_kernel<T, EPL, CONTIG><<<dim3((unsigned)nx, (unsigned)H, (unsigned)B), kThreads, 0, st>>>(
-        a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, kblk, vblk);
+        a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk);
   }
   finish_kernel<<<dim3((unsigned)H, (unsigned)B), kThreads, 0, st>>>(
       H, a.nqb, w.nkb, B * H, kblk, vblk, a.alpha, a.C, a.gate, a.qmax_sq, a.kmax_sq, a.vmax_sq, a.m, a.flag);
+  if (a.q.S > 0) {
+    shift_kernel<<<dim3((unsigned)ceil_div(a.q.S, kThreads), (unsigned)H, (unsigned)B), kThreads, 0, st>>>(
+        H, a.q.S, a.nqb, a.per_row, a.alpha, a.C, a.kmax_sq, a.m, a.qkbar, a.shift);
+  }
   return cudaGetLastError();
 }
 

@@ -4,10 +4,10 @@
 // fp32 arithmetic, so no TF32 or bf16 rounding of the operands), D = 64, strides that
 // TMA cannot describe, and empty chunks.  Same semantics as the tensor-core kernel:
 //   eligible Q-block  (flag = 1, not forced online): pure-add fixed-m accumulation,
-//       p_ij = 2^(alpha*s_ij - b_i), b_i = m + qkbar_i
+//       p_ij = 2^(alpha*s_ij - b_i), b_i = the row's shift from fm_bounds (m + alpha*q_i.kbar)
 //       ("Kernel reference: ring_attention_const_max_fwd", sections "A static bound makes
 //       the ring reduction pure addition" and "Accumulate, then normalize once";
-//       PR #477 Summary for m and the exp2 form; "Virtual K-centering" for qkbar)
+//       PR #477 Summary for m and the exp2 form; "Virtual K-centering" for the centering term)
 //   other Q-blocks: online softmax with a running row max r_i kept in acc_max and
 //       rescaling of the partial sums when it grows (PR #478 "Cross-Ring Safety
 //       Fallback": standard online-softmax accumulation across the chunks).
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kRows *(D / kDimsPerThread))
   const bool row_ok = row < a.q.S;
   const int64_t qb = (int64_t)blockIdx.x * kRows / FM_BLOCK_Q;  // the CTA lies in one Q-block
   const bool fixed = !a.force_online && a.flag[bh * a.nqb + qb] != 0;
-  const float bias = fixed ? ((float)a.m[bh * a.nqb + qb] + (row_ok ? a.qkbar[bh * a.q.S + row] : 0.f)) : 0.f;
+  const float bias = (fixed && row_ok) ? a.shift[bh * a.q.S + row] : 0.f;
 
   float qv[kDimsPerThread], ov[kDimsPerThread];
   const T *qp = reinterpret_cast<const T *>(a.q.ptr) + b * a.q.sB + h * a.q.sH + (row_ok ? row : 0) * a.q.sS;

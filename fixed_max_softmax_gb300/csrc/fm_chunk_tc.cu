@@ -7,7 +7,7 @@
 //                         registers, bf16 P written back over S in TMEM (tcgen05.st)
 //   O += P V              tcgen05.mma with A = P read from TMEM, B = V from shared memory
 //   epilogue              O and the row sums are added into (or initialise) acc_o/acc_sum
-// For an eligible Q-block the shift b_i = m + qkbar_i is fixed before the chunk starts,
+// For an eligible Q-block the shift b_i (m + alpha*q_i.kbar, from fm_bounds) is fixed before the chunk starts,
 // so there is no row max, no rescale of O and the cross-chunk merge is a pure add
 // ("Kernel reference: ring_attention_const_max_fwd", sections "Dropping the online max
 // buys a better layout", "A static bound makes the ring reduction pure addition",
@@ -291,9 +291,8 @@ struct TcParams {
   int Nc, H, n_kv;
   float alpha;
   int force_online, accumulate;
-  const int32_t *m;
   const uint8_t *flag;
-  const float *qkbar;
+  const float *shift;
   float *acc_o, *acc_sum, *acc_max;
   unsigned int *err;
   unsigned long long timeout_ns;
@@ -582,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t bh = (int64_t)b * p.H + h;
     const bool fixed = !tile_ok || (!p.force_online && p.flag[bh * p.nqb + qb] != 0);
     float bias = 0.f;
-    if (fixed && tile_ok) bias = (float)p.m[bh * p.nqb + qb] + (row_ok ? p.qkbar[bh * p.Sq + row] : 0.f);
+    if (fixed && row_ok) bias = p.shift[bh * p.Sq + row];
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)(t * 128);
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(t * 128);
@@ -728,9 +727,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   p.alpha = a.alpha;
   p.force_online = a.force_online;
   p.accumulate = a.accumulate;
-  p.m = a.m;
   p.flag = a.flag;
-  p.qkbar = a.qkbar;
+  p.shift = a.shift;
   p.acc_o = a.acc_o;
   p.acc_sum = a.acc_sum;
   p.acc_max = a.acc_max;

@@ -12,10 +12,11 @@
 namespace fm {
 namespace {
 
-template <bool BF16, bool VEC>
+template <bool BF16, bool VEC, bool LSE>
 __global__ void __launch_bounds__(256) finalize_kernel(const float *__restrict__ acc_o,
-                                                       const float *__restrict__ acc_sum, View o,
-                                                       int64_t n_quads) {
+                                                       const float *__restrict__ acc_sum,
+                                                       const float *__restrict__ acc_max, float *__restrict__ lse,
+                                                       View o, int64_t n_quads) {
   const int64_t D = o.D;
   const int64_t qpr = D / 4;  // quads per row
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_quads;
@@ -25,7 +26,12 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float *__restrict__
     const int64_t s = r % o.S;
     const int64_t bh = r / o.S;
     const int64_t h = bh % o.H, b = bh / o.H;
-    const float inv = 1.0f / fmaxf(acc_sum[r], FM_SUM_CLAMP);
+    const float sum = acc_sum[r];
+    const float inv = 1.0f / fmaxf(sum, FM_SUM_CLAMP);
+    // natural-log LSE of the scaled scores: acc_sum * 2^acc_max = sum_j 2^(alpha*q.k_j)
+    if constexpr (LSE) {
+      if (d0 == 0) lse[r] = 0.69314718055994531f * (acc_max[r] + log2f(sum));
+    }
     const float4 a = *reinterpret_cast<const float4 *>(acc_o + r * D + d0);
     const float x[4] = {a.x * inv, a.y * inv, a.z * inv, a.w * inv};
     const int64_t off = b * o.sB + h * o.sH + s * o.sS + d0 * o.sD;
@@ -54,9 +60,9 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float *__restrict__
   }
 }
 
-}  // namespace
-
-cudaError_t launch_finalize(const float *acc_o, const float *acc_sum, const View &o, cudaStream_t st) {
+template <bool LSE>
+cudaError_t launch_typed(const float *acc_o, const float *acc_sum, const float *acc_max, const View &o,
+                         float *lse, cudaStream_t st) {
   const int64_t n_quads = o.B * o.H * o.S * (o.D / 4);
   if (n_quads == 0) return cudaSuccess;
   const size_t es = o.dtype == FM_F32 ? 4 : 2;
@@ -68,13 +74,24 @@ cudaError_t launch_finalize(const float *acc_o, const float *acc_sum, const View
   const int64_t cap = (int64_t)sms * 16;
   if (blocks > cap) blocks = cap;
   if (o.dtype == FM_BF16) {
-    if (vec) finalize_kernel<true, true><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, o, n_quads);
-    else finalize_kernel<true, false><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, o, n_quads);
+    if (vec) finalize_kernel<true, true, LSE><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, acc_max, lse, o, n_quads);
+    else finalize_kernel<true, false, LSE><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, acc_max, lse, o, n_quads);
   } else {
-    if (vec) finalize_kernel<false, true><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, o, n_quads);
-    else finalize_kernel<false, false><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, o, n_quads);
+    if (vec) finalize_kernel<false, true, LSE><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, acc_max, lse, o, n_quads);
+    else finalize_kernel<false, false, LSE><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, acc_max, lse, o, n_quads);
   }
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_finalize(const float *acc_o, const float *acc_sum, const View &o, cudaStream_t st) {
+  return launch_typed<false>(acc_o, acc_sum, nullptr, o, nullptr, st);
+}
+
+cudaError_t launch_finalize_lse(const float *acc_o, const float *acc_sum, const float *acc_max, const View &o,
+                                float *lse, cudaStream_t st) {
+  return launch_typed<true>(acc_o, acc_sum, acc_max, o, lse, st);
 }
 
 }  // namespace fm

@@ -35,12 +35,13 @@ struct View {
 struct BoundsArgs {
   View q, k, v;
   int centering;
+  int per_row;    // one shift per query row instead of per Q-block
   double alpha;   // softmax_scale * log2(e), fp64 for the bound
   int C, gate;
   int64_t nqb;    // ceil(Sq / 128)
   int32_t *m;
   uint8_t *flag;
-  float *qmax_sq, *kmax_sq, *kbar, *qkbar, *vmax_sq;
+  float *qmax_sq, *kmax_sq, *kbar, *qkbar, *shift, *vmax_sq;
   void *ws;
   size_t ws_bytes;
 };
@@ -54,9 +55,8 @@ struct ChunkArgs {
   int force_online;
   int accumulate;
   int64_t nqb;
-  const int32_t *m;
-  const uint8_t *flag;
-  const float *qkbar;      // [B,H,Sq] (zeros when not centering)
+  const uint8_t *flag;     // [B,H,nqb]
+  const float *shift;      // [B,H,Sq] the fixed-m shift of each row
   float *acc_o, *acc_sum, *acc_max;
   unsigned int *err;       // device error word
   unsigned long long timeout_ns;
@@ -73,6 +73,9 @@ cudaError_t launch_chunk_empty_init(const ChunkArgs &a, cudaStream_t st);
 // ---- finalize (fm_finalize.cu) ---------------------------------------------
 cudaError_t launch_finalize(const float *acc_o, const float *acc_sum, const View &o,
                             cudaStream_t st);
+// The same plus lse = ln2 * (acc_max + log2(acc_sum)) per row.
+cudaError_t launch_finalize_lse(const float *acc_o, const float *acc_sum, const float *acc_max,
+                                const View &o, float *lse, cudaStream_t st);
 
 // ---- helpers shared by host code -------------------------------------------
 int current_device_sm_count();

@@ -84,6 +84,10 @@ typedef struct {
   float softmax_scale;  /* <= 0 selects 1/sqrt(D) ([NKI] Interface table) */
   int32_t centering;    /* 1: virtual K-centering ([PR477] "Virtual K-centering") */
   int32_t force_online; /* 1: every Q-block takes the online-softmax fallback */
+  int32_t per_row;      /* 1: each query row gets its own shift m_i = ceil(U_i) - C, with
+                           U_i = alpha*|q_i|*max|k| ([NKI] "Best practices": give each query
+                           row its own bound); 0: one m per 128-row Q-block ([PR477]).
+                           Eligibility stays per Q-block in both cases. */
 } fm_opts;
 
 /* Bounds of one attention call ([PR477] Summary, "Dynamic eligibility bounding").
@@ -95,8 +99,11 @@ typedef struct {
  *   kmax_sq f32   [B, H]       max_j ||k_j - kbar||^2 (centered) or ||k_j||^2
  *   kbar    f32   [B, H, D]    mean key over all real keys ([PR478] Summary); 0 if
  *                              not centering
- *   qkbar   f32   [B, H, Sq]   alpha * q_i . kbar, the per-row centering term applied
- *                              in registers by the chunk kernels; 0 if not centering
+ *   qkbar   f32   [B, H, Sq]   alpha * q_i . kbar, the per-row centering term; 0 if not
+ *                              centering
+ *   shift   f32   [B, H, Sq]   the row's whole base-2 shift b_i = m_i + qkbar_i, with m_i
+ *                              the row's own ceil(U_i) - C (opts.per_row) or its Q-block's
+ *                              m; the chunk kernels subtract it in registers
  *   vmax_sq f32   [1]          max over all of V of v^2 (v_ok = vmax_sq <= 256^2)
  * with alpha = softmax_scale * log2(e) (base-2 logits, [PR477]'s exp2 formulation)
  * and U = alpha * sqrt(qmax_sq) * sqrt(kmax_sq), the Cauchy-Schwarz bound on the
@@ -108,12 +115,14 @@ typedef struct {
   float *kmax_sq;
   float *kbar;
   float *qkbar;
+  float *shift;
   float *vmax_sq;
   /* filled by fm_bounds */
   int64_t B, H, Sq, D, n_qblocks;
   int64_t N_total;   /* total KV length over every chunk of the call */
   int32_t C, W, gate; /* C(N) = 127 - ceil(log2 N) - 8, W = C + 125, gate = floor(W/2) */
   int32_t centered;  /* the opts.centering the bounds were measured with */
+  int32_t per_row;   /* the opts.per_row they were built with */
   float alpha;
   int32_t dtype;
   /* updated by fm_attn_chunk (host-side bookkeeping of the chunk sequence) */
@@ -143,7 +152,7 @@ FM_API int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tenso
 /* fm_attn_chunk -- fold one KV chunk into the unnormalised fp32 accumulators
  * ([NKI] "A static bound makes the ring reduction pure addition", "Accumulate, then
  * normalize once").  For an eligible Q-block (flag = 1, force_online = 0) each row i
- * adds p_ij = 2^(alpha*q_i.k_j - m - qkbar_i) to acc_sum and p_ij*v_j to acc_o: pure
+ * adds p_ij = 2^(alpha*q_i.k_j - shift_i) to acc_sum and p_ij*v_j to acc_o: pure
  * addition across chunks.  Other Q-blocks take the online-softmax fallback ([PR478]
  * "Cross-Ring Safety Fallback"): a running row max kept in acc_max, with rescaling.
  *   q        [B, H, Sq, D]   the same queries given to fm_bounds
@@ -151,8 +160,8 @@ FM_API int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tenso
  *   v_chunk  [B, H, Nc, D]
  *   bounds   from fm_bounds for this call; kv_seen/online_lock are updated
  *   acc_o    f32 [B, H, Sq, D] contiguous;  acc_sum, acc_max f32 [B, H, Sq] contiguous.
- *            acc_max holds each row's current base-2 shift (m + qkbar_i on fixed-m
- *            rows, the running max on fallback rows), so acc_sum * 2^acc_max is the
+ *            acc_max holds each row's current base-2 shift (shift_i on fixed-m rows,
+ *            the running max on fallback rows), so acc_sum * 2^acc_max is the
  *            row's sum of 2^z.
  *   accumulate  0: overwrite the accumulators (first chunk); 1: add into them
  * Errors: FM_ERR_BOUNDS_MISMATCH when bounds->magic is wrong, the bounds' shape is
@@ -171,6 +180,17 @@ FM_API int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_
  * Errors: FM_ERR_ARG, FM_ERR_DTYPE, FM_ERR_CUDA. */
 FM_API int fm_finalize(const float *acc_o, const float *acc_sum, const fm_tensor *o_out,
                 fm_stream_t stream);
+
+/* fm_finalize_lse -- fm_finalize that also writes each row's log-sum-exp of the scaled
+ * scores, lse_i = ln(sum_j exp(softmax_scale * q_i.k_j)), for training and for merging
+ * partial results ([NKI] Interface: with training the kernel also returns
+ * lse = c_i + log(sum_exp)).  Since acc_max holds each row's base-2 shift on both paths,
+ * lse_i = ln(2) * (acc_max_i + log2(acc_sum_i)); a row that saw no key gets -inf.
+ *   acc_max f32 [B, H, Sq] contiguous (as left by fm_attn_chunk)
+ *   lse     f32 [B, H, Sq] contiguous, written
+ * Errors: those of fm_finalize. */
+FM_API int fm_finalize_lse(const float *acc_o, const float *acc_sum, const float *acc_max,
+                           const fm_tensor *o_out, float *lse, fm_stream_t stream);
 
 /* fm_sync_status -- synchronise `stream`, then report and clear this GPU's device
  * error word: FM_ERR_TIMEOUT if a kernel gave up on a pipeline wait (its outputs are

@@ -11,7 +11,8 @@ Sources and the reading of each step are in the C file's header:
 * ``attention``  -- plain softmax attention (the exact result fixed-m reaches, by the
   shift invariance of softmax in "Kernel reference: ring_attention_const_max_fwd",
   section "What you should know before reading").
-* ``constants`` / ``bounds`` -- C(N), W, gate, U, m and the eligibility flag from
+* ``constants`` / ``bounds`` -- C(N), W, gate, U, m (per Q-block or per row), the row
+  shift and the eligibility flag from
   "feat(attention): fixed-m splash attention kernel with dynamic bounds and safety
   fallbacks", Summary ("Dynamic eligibility bounding", "Virtual K-centering").
 * ``fixed_m_emulate_f32`` -- fp32 fixed-m sum with an arbitrary shift and
@@ -73,7 +74,7 @@ def _load():
         lib.fmo_attention.argtypes = [P, P, P, i64, i64, i64, i64, ctypes.c_double, P, P, ctypes.c_int]
         lib.fmo_bounds.restype = None
         lib.fmo_bounds.argtypes = [P, P, P, i64, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int,
-                                   ctypes.c_int, i64, P, P, P, P, P, P, P, P, P]
+                                   ctypes.c_int, i64, P, P, P, P, P, P, P, P, P, ctypes.c_int, P, P, P]
         lib.fmo_fixed_m_emulate_f32.restype = None
         lib.fmo_fixed_m_emulate_f32.argtypes = [P, P, P, i64, i64, i64, ctypes.c_double, P, P, P, P,
                                                 P, P]
@@ -141,7 +142,7 @@ def attention(q, k, v, scale: float | None = None, threads: int = 0, return_lse:
 
 
 def bounds(q, k, v, scale: float | None = None, centering: bool = False, dtype_safe: bool = True,
-           vmax: int = VMAX_DEFAULT, bq: int = BQ_DEFAULT) -> dict:
+           vmax: int = VMAX_DEFAULT, bq: int = BQ_DEFAULT, per_row: bool = False) -> dict:
     """Bounds of one fixed-m call in fp64 (norms, kbar, U, m, flag, C, W, gate).
 
     q: [B, H, Sq, D] (or [G, Sq, D]); k, v: [B, H, N, D] -- N is the TOTAL KV length
@@ -163,10 +164,14 @@ def bounds(q, k, v, scale: float | None = None, centering: bool = False, dtype_s
     m = np.zeros((G, nqb), dtype=np.int32)
     flag = np.zeros((G, nqb), dtype=np.uint8)
     qkbar = np.zeros((G, Sq))
+    U_row = np.zeros((G, Sq))
+    m_row = np.zeros((G, Sq), dtype=np.int32)
+    shift = np.zeros((G, Sq))
     consts = np.zeros((4,), dtype=np.int32)
     _load().fmo_bounds(_ptr(qa), _ptr(ka), _ptr(va), G, Sq, N, D, bq, float(scale), int(bool(centering)),
                        int(bool(dtype_safe)), int(vmax), _ptr(qmax_sq), _ptr(kbar), _ptr(kmax_sq),
-                       _ptr(vmax_sq), _ptr(U), _ptr(m), _ptr(flag), _ptr(qkbar), _ptr(consts))
+                       _ptr(vmax_sq), _ptr(U), _ptr(m), _ptr(flag), _ptr(qkbar), _ptr(consts), int(bool(per_row)),
+                       _ptr(U_row), _ptr(m_row), _ptr(shift))
     lead = tuple(q4[:-2]) if len(q4) == 4 else (G,)
     # distance of U to the nearest integer and to the gate: where fp32 device sums can
     # legitimately round across an integer (the tie band of the parity tests)
@@ -180,6 +185,10 @@ def bounds(q, k, v, scale: float | None = None, centering: bool = False, dtype_s
         "m": m.reshape(lead + (nqb,)),
         "flag": flag.reshape(lead + (nqb,)),
         "qkbar": qkbar.reshape(lead + (Sq,)),
+        "U_row": U_row.reshape(lead + (Sq,)),
+        "m_row": m_row.reshape(lead + (Sq,)),
+        "shift": shift.reshape(lead + (Sq,)),
+        "margin_row": np.minimum(np.abs(U_row - np.round(U_row)), np.abs(U_row - consts[2])).reshape(lead + (Sq,)),
         "margin": margin.reshape(lead + (nqb,)),
         "C": int(consts[0]),
         "W": int(consts[1]),

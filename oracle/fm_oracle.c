@@ -145,12 +145,15 @@ void fmo_attention(const double *q, const double *k, const double *v, int64_t G,
  *   m       [G, nqb]  ceil(U) - C
  *   flag    [G, nqb]  v_ok && U <= gate
  *   qkbar   [G, Sq] or NULL: alpha * q_i . kbar (the per-row centering term)
- *   consts  [4]       C, W, gate, v_ok                                            */
+ *   consts  [4]       C, W, gate, v_ok
+ *   U_row, m_row [G, Sq] or NULL: the per-row bound alpha*|q_i|*sqrt(kmax_sq) and its shift
+ *   shift   [G, Sq] or NULL: m (per_row ? m_row : the row's Q-block m) + qkbar          */
 void fmo_bounds(const double *q, const double *k, const double *v, int64_t G, int64_t Sq,
                 int64_t N, int64_t D, int64_t bq, double scale, int centering,
                 int dtype_safe, int64_t vmax, double *qmax_sq, double *kbar,
                 double *kmax_sq, double *vmax_sq, double *U, int32_t *m, uint8_t *flag,
-                double *qkbar, int32_t *consts) {
+                double *qkbar, int32_t *consts, int per_row, double *U_row, int32_t *m_row,
+                double *shift) {
   const double alpha = scale * FMO_LOG2E;
   int C, W, gate;
   fmo_constants(N, vmax, &C, &W, &gate);
@@ -201,12 +204,23 @@ void fmo_bounds(const double *q, const double *k, const double *v, int64_t G, in
       m[g * nqb + b] = (int32_t)ceil(u) - C;
       flag[g * nqb + b] = (uint8_t)(v_ok && (u <= (double)gate));
     }
-    if (qkbar) {
-      for (int64_t i = 0; i < Sq; i++) {
-        double dot = 0.0;
-        for (int64_t d = 0; d < D; d++) dot += qg[i * D + d] * kb[d];
-        qkbar[g * Sq + i] = alpha * dot;
+    for (int64_t i = 0; i < Sq; i++) {
+      double dot = 0.0, ss = 0.0;
+      for (int64_t d = 0; d < D; d++) {
+        dot += qg[i * D + d] * kb[d];
+        ss += qg[i * D + d] * qg[i * D + d];
       }
+      /* per-row bound of "Kernel reference: ring_attention_const_max_fwd", sections
+       * "Picking a max that is safe without measuring it" and "Best practices" (give each
+       * query row its own bound), with the shift of PR #477: m_i = ceil(U_i) - C */
+      double ur = alpha * sqrt(ss) * sqrt(km);
+      int32_t mr = (int32_t)ceil(ur) - C;
+      if (U_row) U_row[g * Sq + i] = ur;
+      if (m_row) m_row[g * Sq + i] = mr;
+      if (qkbar) qkbar[g * Sq + i] = alpha * dot;
+      /* the full base-2 shift of row i: its m (per row, or its Q-block's) plus the
+       * centering term alpha*q_i.kbar ("Virtual K-centering") */
+      if (shift) shift[g * Sq + i] = (double)(per_row ? mr : m[g * nqb + i / bq]) + alpha * dot;
     }
   }
   consts[0] = C;

@@ -42,7 +42,7 @@ def test_exports_nothing_else():
 def test_struct_layouts_match_header():
     # sizes the C compiler gives the header's structs (x86-64 and aarch64 LP64 agree)
     assert ctypes.sizeof(fm.fm_tensor) == 8 + 4 + 4 + 4 * 8 + 4 * 8
-    assert ctypes.sizeof(fm.fm_opts) == 12
+    assert ctypes.sizeof(fm.fm_opts) == 16
     assert fm.fm_bounds_out.magic.offset + 4 == ctypes.sizeof(fm.fm_bounds_out)
 
 
@@ -68,7 +68,7 @@ def call_bounds(lib, q, k, v, opt=None, out=None, ws=FAKE, ws_bytes=1 << 30):
     opt = opt or fm.opts()
     if out is None:
         out = fm.fm_bounds_out()
-        for f in ("m", "flag", "qmax_sq", "kmax_sq", "kbar", "qkbar", "vmax_sq"):
+        for f in ("m", "flag", "qmax_sq", "kmax_sq", "kbar", "qkbar", "shift", "vmax_sq"):
             setattr(out, f, FAKE)
     return lib.fm_bounds(ctypes.byref(q), ctypes.byref(k), ctypes.byref(v), ctypes.byref(opt), ctypes.byref(out),
                          ws, ws_bytes, None)
@@ -90,14 +90,14 @@ def test_bounds_shape_and_support_errors(lib):
     assert call_bounds(lib, q, fake(1, 2, 300, 128, fm.FM_F32), v) == fm.FM_ERR_DTYPE  # mixed types
     assert call_bounds(lib, q, k, v, ws_bytes=16) == fm.FM_ERR_ARG                   # workspace too small
     bad = fm.fm_bounds_out()
-    for f in ("flag", "qmax_sq", "kmax_sq", "kbar", "qkbar", "vmax_sq"):
+    for f in ("flag", "qmax_sq", "kmax_sq", "kbar", "qkbar", "shift", "vmax_sq"):
         setattr(bad, f, FAKE)
     assert call_bounds(lib, q, k, v, out=bad) == fm.FM_ERR_ARG
 
 
 def good_bounds(B=1, H=2, Sq=256, D=128, N=300, centered=0, alpha=None):
     b = fm.fm_bounds_out()
-    for f in ("m", "flag", "qmax_sq", "kmax_sq", "kbar", "qkbar", "vmax_sq"):
+    for f in ("m", "flag", "qmax_sq", "kmax_sq", "kbar", "qkbar", "shift", "vmax_sq"):
         setattr(b, f, FAKE)
     b.B, b.H, b.Sq, b.D = B, H, Sq, D
     b.n_qblocks = (Sq + 127) // 128
@@ -152,8 +152,10 @@ def test_chunk_kv_accounting(lib):
 
 def test_chunk_flag_values(lib):
     assert call_chunk(lib, good_bounds(), accumulate=2) == fm.FM_ERR_ARG
-    o = fm.fm_opts(0.0, 2, 0)
+    o = fm.fm_opts(0.0, 2, 0, 0)
     assert call_chunk(lib, good_bounds(), opt=o) == fm.FM_ERR_ARG
+    q, k = fake(1, 2, 256, 128), fake(1, 2, 300, 128)
+    assert call_bounds(lib, q, k, k, opt=fm.fm_opts(0.0, 0, 0, 3)) == fm.FM_ERR_ARG
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device error path")

@@ -33,11 +33,12 @@ def dev():
     return torch.device("cuda:0")
 
 
-def run(q, k, v, chunks=None, centering=False, force_online=False, out_dtype=torch.float32):
+def run(q, k, v, chunks=None, centering=False, force_online=False, out_dtype=torch.float32, with_lse=False,
+        per_row=False):
     B, H, Sq, D = q.shape
     fa = fm.FixedMAttention(B, H, Sq, k.shape[2], D, q.device, centering=centering, force_online=force_online,
-                            out_dtype=out_dtype)
-    o = fa.forward(q, k, v, chunks)
+                            out_dtype=out_dtype, per_row=per_row)
+    o = fa.forward(q, k, v, chunks, with_lse=with_lse)
     fm.fm_sync_status()
     return fa, o
 
@@ -68,6 +69,16 @@ def check_bounds(fa, ob, heads=None, check_vmax=True):
         # v^2 of a bf16 value is exact in fp32; of an fp32 value it takes one rounding
         g = float(fa.bounds.vmax_sq.item())
         assert abs(g - ob["vmax_sq"]) <= 2.0 ** -23 * ob["vmax_sq"], (g, ob["vmax_sq"])
+    # the row shift b_i = m_i + qkbar_i: exact integer part outside the tie band, plus qkbar
+    sh = sel(fa.bounds.shift.cpu().numpy())[..., : ob["shift"].shape[-1]].astype(np.float64)
+    if fa.bounds.out.per_row:
+        safe_rows = ob["margin_row"] > 1e-4 * np.maximum(1.0, ob["U_row"])
+    else:
+        Sq = ob["shift"].shape[-1]
+        safe_rows = np.repeat(safe, 128, axis=-1)[..., :Sq]
+    d = np.abs(sh - ob["shift"])
+    assert np.all(d[safe_rows] <= 1e-4 * np.maximum(1.0, np.abs(ob["shift"][safe_rows]))), float(d[safe_rows].max())
+    assert np.all(d <= 1.0 + 1e-4 * np.maximum(1.0, np.abs(ob["shift"])))
     b = fa.bounds.out
     assert (b.C, b.W, b.gate) == (ob["C"], ob["W"], ob["gate"])
     assert b.magic == fm.FM_BOUNDS_MAGIC
@@ -160,6 +171,41 @@ def test_schedule_invariance_bitwise(dev):
         assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("name,centering", [("wan", True), ("mix", False), ("adversarial", True)])
+def test_per_row_shift_parity(dev, name, centering):
+    """Per-row bounds: shifts match the oracle's per-row m_i + qkbar_i, outputs match the
+    oracle, and per-row and per-block runs agree within the tolerance."""
+    q, k, v = workloads.make_inputs(name, device="cpu", heads=[0, 5, 33], Sq=390, N=700)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    fa, o = run(qd, kd, vd, [(0, 350), (350, 350)], centering=centering, per_row=True)
+    check_bounds(fa, oracle.bounds(q, k, v, centering=centering, per_row=True))
+    ref = oracle.attention(q, k, v)
+    assert maxerr(o, ref) <= TOL_BF16
+    _, o_blk = run(qd, kd, vd, [(0, 350), (350, 350)], centering=centering, per_row=False)
+    assert maxerr(o, o_blk) <= TOL_BF16
+
+
+TOL_LSE = 1e-4  # fp32 S and sums, ex2.approx: about 1e-5 absolute on |lse| < 100
+
+
+@pytest.mark.parametrize("force_online", [False, True])
+def test_lse_matches_oracle(dev, force_online):
+    """LSE (natural log of the scaled scores' exp-sum) from acc_max and acc_sum, both paths."""
+    for name, centering, dt in (("wan", True, torch.bfloat16), ("mix", False, torch.bfloat16),
+                                ("tiny", False, torch.float32)):
+        q, k, v = workloads.make_inputs(name, device="cpu", heads=range(3), Sq=300, N=333)
+        q, k, v = q.to(dt), k.to(dt), v.to(dt)
+        fa, o = run(q.to(dev), k.to(dev), v.to(dev), [(0, 200), (200, 133)], centering=centering,
+                    force_online=force_online, with_lse=True)
+        ref, ref_lse = oracle.attention(q, k, v, return_lse=True)
+        assert maxerr(fa.lse, ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse)))), name
+        assert maxerr(o, ref) <= (TOL_F32 if dt == torch.float32 else TOL_BF16)
+    # an empty key set gives -inf
+    z = torch.zeros(1, 1, 5, 128, dtype=torch.bfloat16, device=dev)
+    fa, _ = run(z, z[:, :, :0], z[:, :, :0], [(0, 0)], with_lse=True)
+    assert torch.all(torch.isneginf(fa.lse))
+
+
 # ------------------------------------------------------------------ full-size workloads (sampled rows)
 
 def sampled(q, k, v, o, heads, rows):
@@ -199,6 +245,12 @@ def test_wan_full_size(dev):
     # rows: first Q-block pair, one block in the middle, the ragged 80-row tail
     rows = list(range(0, 256)) + list(range(37760, 37888)) + list(range(75520, 75600))
     assert sampled(q, k, v, o, [0, 17], rows) <= TOL_BF16
+    # the LSE of the same rows, from the accumulators of this call
+    lse = torch.empty_like(fa.acc_sum)
+    fm.fm_finalize_lse(fa.acc_o, fa.acc_sum, fa.acc_max, fa.out, lse)
+    _, ref_lse = oracle.attention(q[0, [0, 17]][:, rows].cpu(), k[0, [0, 17]].cpu(), v[0, [0, 17]].cpu(),
+                                  return_lse=True)
+    assert maxerr(lse[0, [0, 17]][:, rows], ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse))))
     _, o2 = run(q, k, v, workloads.chunk_bounds(w), centering=True, force_online=True)
     assert maxerr(o2[0, [0, 17]][:, rows], o[0, [0, 17]][:, rows]) <= TOL_BF16
 

@@ -264,6 +264,35 @@ def test_invariant_on_generated_eligible_tiles():
                 assert zz.min() >= -125 and zz.max() <= b["C"], (name, h, qb)
 
 
+def test_per_row_shift_keeps_every_row_in_the_window():
+    """Per-row bounds (the page's recommended granularity): each row's own shift keeps all
+    its exponents in [-125, C] (brute force), is never above its block's, and for the row
+    that attains its bound the top exponent sits in (C-1, C]."""
+    import workloads
+    for name, cen in (("mix", False), ("mix", True), ("wan", True), ("adversarial", True)):
+        q, k, v = workloads.make_inputs(name, heads=[0, 3, 30], Sq=300, N=700)
+        b = oracle.bounds(q, k, v, centering=cen, per_row=True)
+        blk = oracle.bounds(q, k, v, centering=cen, per_row=False)
+        qa, ka = q.double().numpy(), k.double().numpy()
+        for h in range(3):
+            z = b["alpha"] * qa[0, h] @ (ka[0, h] - b["kbar"][0, h]).T
+            e = z - b["shift"][0, h][:, None] + b["qkbar"][0, h][:, None]  # z - m_i (centering term apart)
+            zc = b["alpha"] * qa[0, h] @ ka[0, h].T - b["shift"][0, h][:, None]  # the kernels' exponent
+            assert np.allclose(e, zc, atol=1e-9)
+            for qb in range(b["flag"].shape[2]):
+                if not b["flag"][0, h, qb]:
+                    continue
+                ee = e[qb * 128:(qb + 1) * 128]
+                assert ee.min() >= -125 and ee.max() <= b["C"], (name, h, qb)
+            assert np.all(b["m_row"][0, h] <= np.repeat(blk["m"][0, h], 128)[:300])
+            assert np.all(b["shift"][0, h] <= blk["shift"][0, h] + 1e-12)
+    # a row parallel to the longest key attains its own bound: top exponent in (C-1, C]
+    q, k, scale, alpha = _aligned_case(40.5, N=4096)
+    b = oracle.bounds(q[None], k[None], np.ones((1, 4096, 8)), scale=scale, centering=True, per_row=True)
+    top = (alpha * q[0] @ k.T).max() - b["shift"][0, 0]
+    assert b["C"] - 1 < top <= b["C"]
+
+
 # ---------------------------------------------------------------- adversarial verdicts (T4, T5, T7)
 
 def test_adversarial_gate_rejects_231():

@@ -58,7 +58,7 @@ def assert_same(ref, got):
     # (the tolerance the parity tests use for them is kept as the bar)
     assert torch.equal(ref.m, got.m)
     assert torch.equal(ref.flag, got.flag)
-    for name in ("qmax_sq", "kmax_sq", "kbar", "qkbar", "vmax_sq"):
+    for name in ("qmax_sq", "kmax_sq", "kbar", "qkbar", "shift", "vmax_sq"):
         a, b = getattr(ref, name).cpu().numpy(), getattr(got, name).cpu().numpy()
         np.testing.assert_allclose(b, a, rtol=2e-5, atol=2e-6, err_msg=name)
     for f in ("B", "H", "Sq", "D", "n_qblocks", "N_total", "C", "W", "gate", "centered", "alpha", "magic"):
