@@ -30,6 +30,22 @@ sys.path.insert(0, ROOT)
 METRIC = "fixed-m attn fwd TFLOP/s (bf16, S=75,600, H=40, D=128) and % of BF16 tensor peak"
 WORKLOAD = "wan"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+# DRAM bytes (read + write) per launch of the chunk kernel from one ncu capture (see
+# profiles/fm_chunk_tc_wan_h8.md): 8 heads, averaged over the init and the accumulate
+# launch, scaled x5 to 40 heads (every term of the traffic grows with the head count).
+# Valid only for the kernel source it was measured on: the bench reports null otherwise.
+CHUNK_TRAFFIC = {"source_sha256_16": "e8f96f31f17e9359", "bytes_per_launch": 5 * (601.047e6 + 912.607e6) / 2}
+
+
+def chunk_traffic():
+    import hashlib
+
+    src = os.path.join(ROOT, "fixed_max_softmax_gb300", "csrc", "fm_chunk_tc.cu")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    return CHUNK_TRAFFIC["bytes_per_launch"] if h == CHUNK_TRAFFIC["source_sha256_16"] else None
 
 
 def load_peaks():
@@ -209,7 +225,7 @@ def run_ours(args, rank, world, local_rank):
                 ev[-1].record(stream)
         fm.fm_finalize(fa.acc_o, fa.acc_sum, fa.out, stream)
 
-    launches_per_step = 4 + len(chunks) + 1  # bounds: ksum, kmean, norms, finish; chunks; finalize
+    launches_per_step = 5 + len(chunks) + 1  # bounds: ksum, kmean, norms, finish, shift; chunks; finalize
     for _ in range(args.warmup):
         step()
     fm.fm_sync_status(stream)
@@ -235,48 +251,55 @@ def run_ours(args, rank, world, local_rank):
     ms_per_step = t_ms / args.steps
     value = whole_job_tflops(world, step_flops, args.steps, t_ms)
 
-    # ---- end to end through the public API with host buffers (pinned), copies timed
+    # ---- end to end through the public API with host buffers (pinned), copies timed:
+    # every step uploads its Q/K/V from pinned host memory and reads its output back; the
+    # package's HostPipeline overlaps step i+1's upload and step i-1's read-back with step
+    # i's kernels
     e2e = None
     if args.e2e_steps > 0:
         qh = q.cpu().pin_memory()
         kh = k.cpu().pin_memory()
         vh = v.cpu().pin_memory()
-        oh = torch.empty(fa.out.shape, dtype=fa.out.dtype).pin_memory()
-        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-
-        def e2e_step():
-            qd.copy_(qh, non_blocking=True)
-            kd.copy_(kh, non_blocking=True)
-            vd.copy_(vh, non_blocking=True)
-            fa.forward(qd, kd, vd, chunks, stream)
-            oh.copy_(fa.out, non_blocking=True)
-
-        e2e_step()
-        torch.cuda.synchronize(dev)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier()
-        e0.record(stream)
-        for _ in range(args.e2e_steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
+        outs = [torch.empty(fa.out.shape, dtype=fa.out.dtype).pin_memory() for _ in range(2)]
+        hp = fm.HostPipeline(fa, q.dtype, dev)
+        hp.run([(qh, kh, vh, outs[0])], chunks)  # warm-up
         fm.fm_sync_status(stream)
-        te = max_over_ranks(e0.elapsed_time(e1), dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        hp.run([(qh, kh, vh, outs[i % 2]) for i in range(args.e2e_steps)], chunks)
+        torch.cuda.synchronize(dev)
+        te = max_over_ranks((time.perf_counter() - t0) * 1e3, dev)
+        fm.fm_sync_status(stream)
         e2e = {"value": whole_job_tflops(world, step_flops, args.e2e_steps, te), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(3 * q.numel() * q.element_size()),
                "d2h_bytes_per_step": int(fa.out.numel() * fa.out.element_size()),
-               "ms_per_step": te / args.e2e_steps, "steps": args.e2e_steps}
+               "ms_per_step": te / args.e2e_steps, "steps": args.e2e_steps,
+               "timing": "host wall clock between device synchronisations",
+               "overlap": "upload of step i+1 and read-back of step i-1 run during step i (HostPipeline)"}
 
     if rank != 0:
         return
     peaks, peak_src = load_peaks()
     chunk_flops = [w.flops(heads=w.B * H, keys=n) for _, n in chunks]
+    # algorithmic bytes of a chunk launch: Q, this chunk's K and V, the accumulators written
+    # (and read back on every chunk after the first), averaged over the step's launches
+    rows = w.B * H * w.Sq
+    algo = []
+    for i, (_, n) in enumerate(chunks):
+        io = q.element_size() * (rows * w.D + 2 * w.B * H * n * w.D)
+        acc = 4 * rows * (w.D + 2)
+        algo.append(io + acc * (2 if i > 0 else 1))
+    algo_bytes = statistics.mean(algo)
     per_launch_flops = statistics.mean(chunk_flops)
     chunk_avg_ms = statistics.mean(chunk_ms)
     achieved = per_launch_flops / (chunk_avg_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
+    traffic = args.traffic if args.traffic is not None else (chunk_traffic() if H == w.H else None)
     roofline = {"bound": "tensor", "kernel": "fm_chunk_tc_kernel", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": args.traffic,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                "traffic_unit": "bytes per launch (dram read + write)",
+                "algorithmic_bytes_per_launch": algo_bytes,
                 "peak_kind": f"bf16 sustained ({peak_src})",
                 "frac_of_burst_peak": achieved / peaks["bf16_tflops"], "launch_ms": chunk_avg_ms}
     cpu = None
@@ -311,7 +334,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=6)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=256, help="query rows per reference step")

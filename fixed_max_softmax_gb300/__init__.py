@@ -8,7 +8,8 @@ PyTorch provides device memory and streams and nothing else.
 
 Functions with the ABI's names (same arguments, torch tensors in place of pointers):
 ``fm_bounds_workspace_size``, ``fm_bounds``, ``fm_bounds_noalloc``, ``fm_attn_chunk``,
-``fm_finalize``, ``fm_finalize_lse``, ``fm_sync_status``, ``fm_last_error``, ``fm_version``.
+``fm_finalize``, ``fm_finalize_lse``, ``fm_sync_status``, ``fm_probe_wait_timeout``,
+``fm_last_error``, ``fm_version``.
 
 ``FixedMAttention`` owns the buffers of one problem shape and runs the whole path
 (bounds, one ``fm_attn_chunk`` per KV chunk, finalize); ``attention()`` is the
@@ -34,7 +35,7 @@ FM_BLOCK_Q = 128
 ERROR_NAMES = {0: "FM_OK", 1: "FM_ERR_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_DTYPE", 4: "FM_ERR_UNSUPPORTED",
                5: "FM_ERR_BOUNDS_MISMATCH", 6: "FM_ERR_CUDA", 7: "FM_ERR_TIMEOUT"}
 ABI_SYMBOLS = ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
-               "fm_last_error", "fm_version", "fm_bounds_noalloc", "fm_finalize_lse")
+               "fm_last_error", "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout")
 FM_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -87,12 +88,13 @@ def load(path: str | None = None):
     lib.fm_finalize.argtypes = [P, P, P, P]
     lib.fm_bounds_noalloc.argtypes = [P, P, P, P, P, P]
     lib.fm_finalize_lse.argtypes = [P, P, P, P, P, P]
+    lib.fm_probe_wait_timeout.argtypes = [ctypes.c_uint, P]
     lib.fm_sync_status.argtypes = [P]
     lib.fm_last_error.restype = ctypes.c_char_p
     lib.fm_last_error.argtypes = []
     lib.fm_version.argtypes = []
     for name in ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
-                 "fm_version", "fm_bounds_noalloc", "fm_finalize_lse"):
+                 "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -215,6 +217,10 @@ def fm_sync_status(stream=None):
     return _check(load().fm_sync_status(_stream(stream)))
 
 
+def fm_probe_wait_timeout(timeout_ms: int, stream=None):
+    return _check(load().fm_probe_wait_timeout(int(timeout_ms), _stream(stream)))
+
+
 class FixedMAttention:
     """Buffers and the call sequence of one fixed-m attention forward of a fixed shape.
 
@@ -262,3 +268,64 @@ def attention(q, k, v, chunks=None, centering=False, softmax_scale=0.0, force_on
     fa = FixedMAttention(B, H, Sq, k.shape[2], D, q.device, centering, softmax_scale, force_online, out_dtype,
                          per_row)
     return fa.forward(q, k, v, chunks, stream).clone()
+
+
+class HostPipeline:
+    """Fixed-m attention over a stream of batches that live in (pinned) host memory.
+
+    Batch i+1's inputs are copied to the device on one stream while batch i computes on
+    another, and batch i-1's output is read back on a third: every batch still makes the
+    full host -> device -> host round trip, but the copies hide behind the kernels.  Two
+    device copies of the inputs and of the output alternate between batches; the bounds
+    and accumulators of `fa` are reused in order on the compute stream.
+    """
+
+    def __init__(self, fa: FixedMAttention, in_dtype, device="cuda"):
+        B, H, Sq, N, D = fa.shape
+        self.fa = fa
+        self.device = torch.device(device)
+        self.q = [torch.empty(B, H, Sq, D, dtype=in_dtype, device=device) for _ in range(2)]
+        self.k = [torch.empty(B, H, N, D, dtype=in_dtype, device=device) for _ in range(2)]
+        self.v = [torch.empty(B, H, N, D, dtype=in_dtype, device=device) for _ in range(2)]
+        self.o = [torch.empty_like(fa.out) for _ in range(2)]
+        self.s_h2d = torch.cuda.Stream(device=device)
+        self.s_d2h = torch.cuda.Stream(device=device)
+        self.s_comp = torch.cuda.Stream(device=device)
+
+    def run(self, batches, chunks=None):
+        """batches: iterable of (q_host, k_host, v_host, o_host); o_host is filled.  Returns
+        when every output is back in host memory."""
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        computed = [None, None]  # compute of the batch that last used each slot has finished
+        read_back = [None, None]  # its output has left the slot
+        for i, (qh, kh, vh, oh) in enumerate(batches):
+            s = i % 2
+            with torch.cuda.stream(self.s_h2d):
+                if computed[s] is not None:
+                    self.s_h2d.wait_event(computed[s])
+                self.q[s].copy_(qh, non_blocking=True)
+                self.k[s].copy_(kh, non_blocking=True)
+                self.v[s].copy_(vh, non_blocking=True)
+                uploaded = ev()
+                uploaded.record(self.s_h2d)
+            fa = self.fa
+            with torch.cuda.stream(self.s_comp):
+                self.s_comp.wait_event(uploaded)
+                if read_back[s] is not None:
+                    self.s_comp.wait_event(read_back[s])
+                N = self.k[s].shape[2]
+                cs = [(0, N)] if chunks is None else chunks
+                fm_bounds(self.q[s], self.k[s], self.v[s], fa.opt, fa.bounds, fa.workspace, self.s_comp)
+                for j, (st, n) in enumerate(cs):
+                    fm_attn_chunk(self.q[s], self.k[s][:, :, st:st + n], self.v[s][:, :, st:st + n], fa.bounds,
+                                  fa.opt, fa.acc_o, fa.acc_sum, fa.acc_max, j > 0, self.s_comp)
+                fm_finalize(fa.acc_o, fa.acc_sum, self.o[s], self.s_comp)
+                computed[s] = ev()
+                computed[s].record(self.s_comp)
+            with torch.cuda.stream(self.s_d2h):
+                self.s_d2h.wait_event(computed[s])
+                oh.copy_(self.o[s], non_blocking=True)
+                read_back[s] = ev()
+                read_back[s].record(self.s_d2h)
+        for st in (self.s_h2d, self.s_comp, self.s_d2h):
+            st.synchronize()

@@ -357,6 +357,17 @@ int fm_finalize_lse(const float *acc_o, const float *acc_sum, const float *acc_m
   return FM_OK;
 }
 
+int fm_probe_wait_timeout(unsigned int timeout_ms, fm_stream_t stream) {
+  t_err.clear();
+  if (timeout_ms < 1 || timeout_ms > 10000) return fail(FM_ERR_ARG, "timeout_ms must be in [1, 10000]");
+  unsigned int *err = dev_error_ptr();
+  if (!err) return fail(FM_ERR_CUDA, "cannot resolve the device error word (no CUDA device?)");
+  cudaError_t e = launch_wait_probe(err, (unsigned long long)timeout_ms * 1000000ull,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fm_probe_wait_timeout launch");
+  return FM_OK;
+}
+
 int fm_sync_status(fm_stream_t stream) {
   t_err.clear();
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

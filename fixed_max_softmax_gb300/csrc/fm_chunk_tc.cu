@@ -660,6 +660,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The failure path of the bounded waits, on its own: one thread waits on an mbarrier
+// phase that nothing completes, gives up after `timeout_ns` and records the failure in the
+// error word exactly as the chunk kernel's waits do.
+__global__ void wait_probe_kernel(unsigned int *err, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar_storage;
+  const uint32_t bar = smem_u32(&bar_storage);
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) wait_phase(bar, 0, nullptr, timeout_ns, err, kDevErrTimeoutProbe, 0);
+}
+
 // ---------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -736,6 +750,11 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   p.timeout_ns = a.timeout_ns;
   dim3 grid((unsigned)((a.nqb + 1) / 2), (unsigned)a.q.H, (unsigned)a.q.B);
   fm_chunk_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_probe(unsigned int *err, unsigned long long timeout_ns, cudaStream_t st) {
+  wait_probe_kernel<<<1, 32, 0, st>>>(err, timeout_ns);
   return cudaGetLastError();
 }
 

@@ -16,6 +16,7 @@ enum : unsigned int {
   kDevErrTimeoutMma = 2,
   kDevErrTimeoutSoftmax = 3,
   kDevErrTimeoutDrain = 4,
+  kDevErrTimeoutProbe = 5,
 };
 
 // Default limit of a pipeline wait inside a kernel.  One CTA of the chunk kernel runs
@@ -67,6 +68,8 @@ cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st);
 // cudaErrorNotSupported, launching nothing, when the tensor maps cannot be encoded.
 bool chunk_tc_supported(const ChunkArgs &a);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
+// One bounded wait that can never complete (the failure-detection probe).
+cudaError_t launch_wait_probe(unsigned int *err, unsigned long long timeout_ns, cudaStream_t st);
 // Empty chunk (Nc == 0) with accumulate == 0: write the empty state.
 cudaError_t launch_chunk_empty_init(const ChunkArgs &a, cudaStream_t st);
 

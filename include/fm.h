@@ -197,6 +197,14 @@ FM_API int fm_finalize_lse(const float *acc_o, const float *acc_sum, const float
  * then invalid), FM_ERR_CUDA on an asynchronous CUDA error, else FM_OK. */
 FM_API int fm_sync_status(fm_stream_t stream);
 
+/* fm_probe_wait_timeout -- exercise the failure path of the kernels' bounded waits: one
+ * thread waits on a barrier phase that nothing completes and gives up after timeout_ms
+ * (1..10000), recording the failure in the device error word, so that the next
+ * fm_sync_status returns FM_ERR_TIMEOUT (role 5) and clears it.  Nothing faults and the
+ * context stays usable.  No counterpart in the pages: it tests the library's own failure
+ * detection.  Errors: FM_ERR_ARG, FM_ERR_CUDA. */
+FM_API int fm_probe_wait_timeout(unsigned int timeout_ms, fm_stream_t stream);
+
 /* Message of the last failing call on this thread ("" if none).  Valid until the
  * thread's next fm_* call. */
 FM_API const char *fm_last_error(void);

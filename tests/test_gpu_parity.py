@@ -206,6 +206,35 @@ def test_lse_matches_oracle(dev, force_online):
     assert torch.all(torch.isneginf(fa.lse))
 
 
+def test_bounded_wait_reports_timeout_and_context_survives(dev):
+    """Failure detection without a fault: a wait on a barrier nothing completes gives up
+    after 50 ms, fm_sync_status reports FM_ERR_TIMEOUT once, and work continues."""
+    fm.fm_probe_wait_timeout(50)
+    with pytest.raises(fm.FMError) as e:
+        fm.fm_sync_status()
+    assert e.value.code == fm.FM_ERR_TIMEOUT and "role 5" in str(e.value)
+    fm.fm_sync_status()  # cleared
+    q, k, v = workloads.make_inputs("wan", device="cpu", heads=[0], Sq=130, N=140)
+    _, o = run(q.to(dev), k.to(dev), v.to(dev), centering=True)
+    assert maxerr(o, oracle.attention(q, k, v)) <= TOL_BF16
+
+
+def test_host_pipeline_matches_device_path(dev):
+    """HostPipeline (overlapped upload / compute / read-back) gives the device path's bits."""
+    Sq, N = 700, 900
+    batches, refs = [], []
+    for i in range(3):
+        q, k, v = workloads.make_inputs("mix", device="cpu", heads=range(2 + i % 2, 4 + i % 2), Sq=Sq, N=N)
+        _, o = run(q.to(dev), k.to(dev), v.to(dev), [(0, 450), (450, 450)], centering=True)
+        refs.append(o.cpu())
+        batches.append((q.pin_memory(), k.pin_memory(), v.pin_memory(), torch.empty(o.shape).pin_memory()))
+    fa = fm.FixedMAttention(1, 2, Sq, N, 128, dev, centering=True)
+    fm.HostPipeline(fa, torch.bfloat16, dev).run(batches, [(0, 450), (450, 450)])
+    fm.fm_sync_status()
+    for (_, _, _, oh), ref in zip(batches, refs):
+        assert torch.equal(oh, ref)
+
+
 # ------------------------------------------------------------------ full-size workloads (sampled rows)
 
 def sampled(q, k, v, o, heads, rows):
