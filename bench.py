@@ -2,8 +2,8 @@
 
 One step = the whole hot path on one batch of synthetic input:
     fm_bounds (norms, key mean, m, flags over all 75,600 keys)
-    fm_attn_chunk x 2 (two KV chunks of 37,800, the ring's steps run sequentially)
-    fm_finalize
+    fm_attn_chunk (first KV chunk of 37,800 keys, the ring's first step)
+    fm_attn_chunk_final (second chunk, folded and normalised into o in the same pass)
 at B=1, H=40, S_q=S_k=75,600, D=128, bf16, virtual K-centering on.
 TFLOP/s = 4*H*S_q*S_k*D / t (the two contractions), t from CUDA events on the launch stream.
 
@@ -218,14 +218,17 @@ def run_ours(args, rank, world, local_rank):
             if ev is not None:
                 ev.append(torch.cuda.Event(enable_timing=True))
                 ev[-1].record(stream)
-            fm.fm_attn_chunk(q, k[:, :, s:s + n], v[:, :, s:s + n], fa.bounds, fa.opt, fa.acc_o, fa.acc_sum,
-                             fa.acc_max, i > 0, stream)
+            if i == len(chunks) - 1:  # last chunk: fold and normalise in one pass
+                fm.fm_attn_chunk_final(q, k[:, :, s:s + n], v[:, :, s:s + n], fa.bounds, fa.opt, fa.acc_o,
+                                       fa.acc_sum, fa.acc_max, i > 0, fa.out, None, stream)
+            else:
+                fm.fm_attn_chunk(q, k[:, :, s:s + n], v[:, :, s:s + n], fa.bounds, fa.opt, fa.acc_o, fa.acc_sum,
+                                 fa.acc_max, i > 0, stream)
             if ev is not None:
                 ev.append(torch.cuda.Event(enable_timing=True))
                 ev[-1].record(stream)
-        fm.fm_finalize(fa.acc_o, fa.acc_sum, fa.out, stream)
 
-    launches_per_step = 5 + len(chunks) + 1  # bounds: ksum, kmean, norms, finish, shift; chunks; finalize
+    launches_per_step = 5 + len(chunks)  # bounds: ksum, kmean, norms, finish, shift; chunks (normalise fused)
     for _ in range(args.warmup):
         step()
     fm.fm_sync_status(stream)
@@ -289,7 +292,10 @@ def run_ours(args, rank, world, local_rank):
     for i, (_, n) in enumerate(chunks):
         io = q.element_size() * (rows * w.D + 2 * w.B * H * n * w.D)
         acc = 4 * rows * (w.D + 2)
-        algo.append(io + acc * (2 if i > 0 else 1))
+        if i == len(chunks) - 1 and i > 0:  # fused normalise: acc read, o (bf16) written, acc_o not
+            algo.append(io + acc + 4 * rows * 2 + fa.out.element_size() * rows * w.D)
+        else:
+            algo.append(io + acc * (2 if i > 0 else 1))
     algo_bytes = statistics.mean(algo)
     per_launch_flops = statistics.mean(chunk_flops)
     chunk_avg_ms = statistics.mean(chunk_ms)

@@ -8,7 +8,8 @@ PyTorch provides device memory and streams and nothing else.
 
 Functions with the ABI's names (same arguments, torch tensors in place of pointers):
 ``fm_bounds_workspace_size``, ``fm_bounds``, ``fm_bounds_noalloc``, ``fm_attn_chunk``,
-``fm_finalize``, ``fm_finalize_lse``, ``fm_sync_status``, ``fm_probe_wait_timeout``,
+``fm_attn_chunk_final``, ``fm_finalize``, ``fm_finalize_lse``, ``fm_sync_status``,
+``fm_probe_wait_timeout``,
 ``fm_last_error``, ``fm_version``.
 
 ``FixedMAttention`` owns the buffers of one problem shape and runs the whole path
@@ -35,7 +36,8 @@ FM_BLOCK_Q = 128
 ERROR_NAMES = {0: "FM_OK", 1: "FM_ERR_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_DTYPE", 4: "FM_ERR_UNSUPPORTED",
                5: "FM_ERR_BOUNDS_MISMATCH", 6: "FM_ERR_CUDA", 7: "FM_ERR_TIMEOUT"}
 ABI_SYMBOLS = ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
-               "fm_last_error", "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout")
+               "fm_last_error", "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout",
+               "fm_attn_chunk_final")
 FM_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -89,12 +91,14 @@ def load(path: str | None = None):
     lib.fm_bounds_noalloc.argtypes = [P, P, P, P, P, P]
     lib.fm_finalize_lse.argtypes = [P, P, P, P, P, P]
     lib.fm_probe_wait_timeout.argtypes = [ctypes.c_uint, P]
+    lib.fm_attn_chunk_final.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_int, P, P, P]
     lib.fm_sync_status.argtypes = [P]
     lib.fm_last_error.restype = ctypes.c_char_p
     lib.fm_last_error.argtypes = []
     lib.fm_version.argtypes = []
     for name in ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
-                 "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout"):
+                 "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout",
+               "fm_attn_chunk_final"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -202,6 +206,15 @@ def fm_attn_chunk(q, k_chunk, v_chunk, bounds: Bounds, opt: fm_opts, acc_o, acc_
                                        _ptr(acc_max), int(bool(accumulate)), _stream(stream)))
 
 
+def fm_attn_chunk_final(q, k_chunk, v_chunk, bounds: Bounds, opt: fm_opts, acc_o, acc_sum, acc_max,
+                        accumulate: bool, o_out, lse=None, stream=None):
+    tq, tk, tv, to = tensor(q), tensor(k_chunk), tensor(v_chunk), tensor(o_out)
+    return _check(load().fm_attn_chunk_final(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv),
+                                             ctypes.byref(bounds.out), ctypes.byref(opt), _ptr(acc_o),
+                                             _ptr(acc_sum), _ptr(acc_max), int(bool(accumulate)), ctypes.byref(to),
+                                             _ptr(lse), _stream(stream)))
+
+
 def fm_finalize(acc_o, acc_sum, o_out, stream=None):
     to = tensor(o_out)
     return _check(load().fm_finalize(_ptr(acc_o), _ptr(acc_sum), ctypes.byref(to), _stream(stream)))
@@ -225,9 +238,10 @@ class FixedMAttention:
     """Buffers and the call sequence of one fixed-m attention forward of a fixed shape.
 
     forward(q, k, v, chunks) runs fm_bounds over all of K/V, one fm_attn_chunk per
-    (start, length) slice of the key sequence (the ring's steps, sequentially), and
-    fm_finalize into `out` (fp32 or the input dtype); with_lse=True finalizes with
-    fm_finalize_lse and also fills `lse` [B, H, Sq] (natural log).
+    (start, length) slice of the key sequence (the ring's steps, sequentially) and writes
+    `out` (fp32 or the input dtype): by default the last chunk goes through
+    fm_attn_chunk_final (fold and normalise in one pass); fused_final=False uses a separate
+    fm_finalize.  with_lse=True also fills `lse` [B, H, Sq] (natural log).
     """
 
     def __init__(self, B, H, Sq, N, D, device="cuda", centering=False, softmax_scale=0.0,
@@ -243,16 +257,21 @@ class FixedMAttention:
         self.out = torch.empty(B, H, Sq, D, dtype=out_dtype, device=device)
         self.lse = None
 
-    def forward(self, q, k, v, chunks=None, stream=None, with_lse=False):
+    def forward(self, q, k, v, chunks=None, stream=None, with_lse=False, fused_final=True):
         N = k.shape[2]
         chunks = [(0, N)] if chunks is None else chunks
         fm_bounds(q, k, v, self.opt, self.bounds, self.workspace, stream)
+        if with_lse and self.lse is None:
+            self.lse = torch.empty(self.acc_sum.shape, dtype=torch.float32, device=self.acc_sum.device)
+        lse = self.lse if with_lse else None
         for i, (s, n) in enumerate(chunks):
-            fm_attn_chunk(q, k[:, :, s:s + n], v[:, :, s:s + n], self.bounds, self.opt, self.acc_o,
-                          self.acc_sum, self.acc_max, i > 0, stream)
+            kc, vc = k[:, :, s:s + n], v[:, :, s:s + n]
+            if fused_final and i == len(chunks) - 1:
+                fm_attn_chunk_final(q, kc, vc, self.bounds, self.opt, self.acc_o, self.acc_sum, self.acc_max, i > 0,
+                                    self.out, lse, stream)
+                return self.out
+            fm_attn_chunk(q, kc, vc, self.bounds, self.opt, self.acc_o, self.acc_sum, self.acc_max, i > 0, stream)
         if with_lse:
-            if self.lse is None:
-                self.lse = torch.empty(self.acc_sum.shape, dtype=torch.float32, device=self.acc_sum.device)
             fm_finalize_lse(self.acc_o, self.acc_sum, self.acc_max, self.out, self.lse, stream)
         else:
             fm_finalize(self.acc_o, self.acc_sum, self.out, stream)
@@ -317,9 +336,10 @@ class HostPipeline:
                 cs = [(0, N)] if chunks is None else chunks
                 fm_bounds(self.q[s], self.k[s], self.v[s], fa.opt, fa.bounds, fa.workspace, self.s_comp)
                 for j, (st, n) in enumerate(cs):
-                    fm_attn_chunk(self.q[s], self.k[s][:, :, st:st + n], self.v[s][:, :, st:st + n], fa.bounds,
-                                  fa.opt, fa.acc_o, fa.acc_sum, fa.acc_max, j > 0, self.s_comp)
-                fm_finalize(fa.acc_o, fa.acc_sum, self.o[s], self.s_comp)
+                    call = fm_attn_chunk_final if j == len(cs) - 1 else fm_attn_chunk
+                    extra = (self.o[s],) if j == len(cs) - 1 else ()
+                    call(self.q[s], self.k[s][:, :, st:st + n], self.v[s][:, :, st:st + n], fa.bounds, fa.opt,
+                         fa.acc_o, fa.acc_sum, fa.acc_max, j > 0, *extra, stream=self.s_comp)
                 computed[s] = ev()
                 computed[s].record(self.s_comp)
             with torch.cuda.stream(self.s_d2h):

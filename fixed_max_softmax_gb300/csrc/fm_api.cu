@@ -242,9 +242,13 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
   return FM_OK;
 }
 
-int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk, fm_bounds_out *bounds,
-                  const fm_opts *opts, float *acc_o, float *acc_sum, float *acc_max, int accumulate,
-                  fm_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// fm_attn_chunk, and with o_out given fm_attn_chunk_final.
+int attn_chunk_impl(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk, fm_bounds_out *bounds,
+                    const fm_opts *opts, float *acc_o, float *acc_sum, float *acc_max, int accumulate,
+                    const fm_tensor *o_out, float *lse, fm_stream_t stream) {
   t_err.clear();
   View vq, vk, vv;
   int rc;
@@ -295,6 +299,12 @@ int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor 
       reinterpret_cast<uintptr_t>(acc_max) % 4)
     return fail(FM_ERR_ARG, "acc_o must be 16-byte aligned, acc_sum/acc_max 4-byte aligned");
 
+  View vo;
+  if (o_out) {
+    if ((rc = to_view(o_out, "o_out", &vo))) return rc;
+    if (vo.B != vq.B || vo.H != vq.H || vo.S != vq.S || vo.D != vq.D)
+      return fail(FM_ERR_SHAPE, "o_out must have q's shape [B, H, Sq, D]");
+  }
   unsigned int *err = dev_error_ptr();
   if (!err) return fail(FM_ERR_CUDA, "cannot resolve the device error word (no CUDA device?)");
   ChunkArgs a;
@@ -314,20 +324,54 @@ int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor 
   a.timeout_ns = wait_timeout_ns();
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
+  bool finalize_separately = o_out != nullptr;
   if (rows > 0) {
     if (vk.S == 0) {
       if (!accumulate) e = launch_chunk_empty_init(a, st);
     } else if (chunk_tc_supported(a)) {
+      if (o_out && chunk_tc_final_supported(a, vo)) {  // the kernel normalises and writes o itself
+        a.out = &vo;
+        a.lse = lse;
+        finalize_separately = false;
+      }
       e = launch_chunk_tc(a, st);
-      if (e == cudaErrorNotSupported) e = launch_chunk_simt(a, st);
+      if (e == cudaErrorNotSupported) {
+        finalize_separately = o_out != nullptr;
+        a.out = nullptr;
+        e = launch_chunk_simt(a, st);
+      }
     } else {
       e = launch_chunk_simt(a, st);
     }
   }
   if (e != cudaSuccess) return cuda_fail(e, "fm_attn_chunk launch");
+  if (finalize_separately && rows > 0) {
+    e = lse ? launch_finalize_lse(acc_o, acc_sum, acc_max, vo, lse, st) : launch_finalize(acc_o, acc_sum, vo, st);
+    if (e != cudaSuccess) return cuda_fail(e, "fm_attn_chunk_final finalize launch");
+  }
   bounds->kv_seen = seen;
   bounds->online_lock = force_online;
   return FM_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk, fm_bounds_out *bounds,
+                  const fm_opts *opts, float *acc_o, float *acc_sum, float *acc_max, int accumulate,
+                  fm_stream_t stream) {
+  return attn_chunk_impl(q, k_chunk, v_chunk, bounds, opts, acc_o, acc_sum, acc_max, accumulate, nullptr, nullptr,
+                         stream);
+}
+
+int fm_attn_chunk_final(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk,
+                        fm_bounds_out *bounds, const fm_opts *opts, float *acc_o, float *acc_sum, float *acc_max,
+                        int accumulate, const fm_tensor *o_out, float *lse, fm_stream_t stream) {
+  if (!o_out) {
+    t_err.clear();
+    return fail(FM_ERR_ARG, "o_out is NULL");
+  }
+  return attn_chunk_impl(q, k_chunk, v_chunk, bounds, opts, acc_o, acc_sum, acc_max, accumulate, o_out, lse, stream);
 }
 
 int fm_finalize(const float *acc_o, const float *acc_sum, const fm_tensor *o_out, fm_stream_t stream) {

@@ -296,6 +296,11 @@ struct TcParams {
   float *acc_o, *acc_sum, *acc_max;
   unsigned int *err;
   unsigned long long timeout_ns;
+  // fused normalise of the last chunk: out != nullptr selects it
+  void *out;
+  int out_bf16;
+  int64_t osB, osH, osS;
+  float *lse;
 };
 
 // p = 2^(alpha*s - bias) for 32 scores of one full chunk, two at a time with fp32x2 FMA and
@@ -617,6 +622,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         cprev = (R == -INFINITY) ? 0.f : exp2f(R - nr);
         cnew = (run == -INFINITY) ? 0.f : exp2f(run - nr);
       }
+      // the row's sum and shift after this chunk
+      float sum_new = lsum;
+      if (row_ok && p.accumulate) sum_new = fixed ? p.acc_sum[rflat] + lsum : fmaf(p.acc_sum[rflat], cprev, lsum * cnew);
+      const float shift_new = fixed ? bias : nr;
+      const bool final_out = p.out != nullptr;
+      // with the normalise fused in, o = acc / max(sum, 1e-37) goes straight to `out`
+      // ("Kernel reference: ring_attention_const_max_fwd": the last ring step folds and
+      // normalises); acc_o itself is then not written back
+      const float inv = final_out ? 1.0f / fmaxf(sum_new, FM_SUM_CLAMP) : 1.0f;
+      const int64_t hh = bh % p.H, bb = bh / p.H;
+      const int64_t ooff = bb * p.osB + hh * p.osH + row * p.osS;
+      const float4 *src = reinterpret_cast<const float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
       float4 *dst = reinterpret_cast<float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -628,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float4 x = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
                                    __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
             if (p.accumulate) {
-              const float4 y = dst[c * 8 + q4];
+              const float4 y = src[c * 8 + q4];
               if (fixed) {
                 x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
               } else {
@@ -636,18 +653,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 x.z = fmaf(y.z, cprev, x.z * cnew); x.w = fmaf(y.w, cprev, x.w * cnew);
               }
             }
-            dst[c * 8 + q4] = x;
+            if (!final_out) {
+              dst[c * 8 + q4] = x;
+            } else if (p.out_bf16) {
+              uint2 u;
+              u.x = pack_bf16(x.x * inv, x.y * inv);
+              u.y = pack_bf16(x.z * inv, x.w * inv);
+              *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + ooff + c * 32 + q4 * 4) = u;
+            } else {
+              *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + ooff + c * 32 + q4 * 4) =
+                  make_float4(x.x * inv, x.y * inv, x.z * inv, x.w * inv);
+            }
           }
         }
       }
       if (row_ok) {
-        if (fixed) {
-          p.acc_sum[rflat] = p.accumulate ? p.acc_sum[rflat] + lsum : lsum;
-          p.acc_max[rflat] = bias;
-        } else {
-          p.acc_sum[rflat] = p.accumulate ? fmaf(p.acc_sum[rflat], cprev, lsum * cnew) : lsum;
-          p.acc_max[rflat] = nr;
-        }
+        p.acc_sum[rflat] = sum_new;
+        p.acc_max[rflat] = shift_new;
+        if (final_out && p.lse) p.lse[rflat] = 0.69314718055994531f * (shift_new + log2f(sum_new));
       }
     }
   }
@@ -724,6 +747,14 @@ bool chunk_tc_supported(const ChunkArgs &a) {
          a.k.S <= (int64_t)1 << 30 && a.q.S <= (int64_t)1 << 30;
 }
 
+bool chunk_tc_final_supported(const ChunkArgs &a, const View &o) {
+  const int64_t es = o.dtype == FM_F32 ? 4 : 2;
+  const int64_t vec = 4 * es;  // bytes of one vector store (4 elements)
+  return o.D == kHD && o.sD == 1 && reinterpret_cast<uintptr_t>(o.ptr) % 16 == 0 &&
+         (o.sS * es) % vec == 0 && (o.sH * es) % vec == 0 && (o.sB * es) % vec == 0 && o.B == a.q.B &&
+         o.H == a.q.H && o.S == a.q.S;
+}
+
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   // a layout the driver's tensor-map encoder refuses is reported so the caller can use
@@ -748,6 +779,17 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   p.acc_max = a.acc_max;
   p.err = a.err;
   p.timeout_ns = a.timeout_ns;
+  p.out = nullptr;
+  p.out_bf16 = 0;
+  p.osB = p.osH = p.osS = 0;
+  p.lse = a.lse;
+  if (a.out) {
+    p.out = const_cast<void *>(a.out->ptr);
+    p.out_bf16 = a.out->dtype == FM_BF16;
+    p.osB = a.out->sB;
+    p.osH = a.out->sH;
+    p.osS = a.out->sS;
+  }
   dim3 grid((unsigned)((a.nqb + 1) / 2), (unsigned)a.q.H, (unsigned)a.q.B);
   fm_chunk_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
   return cudaGetLastError();

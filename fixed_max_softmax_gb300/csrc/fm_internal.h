@@ -61,6 +61,10 @@ struct ChunkArgs {
   float *acc_o, *acc_sum, *acc_max;
   unsigned int *err;       // device error word
   unsigned long long timeout_ns;
+  // last chunk with the normalise fused in (tensor-core path only): o = acc / sum is
+  // written to `out` (and lse, when given) instead of acc_o being written back
+  const View *out = nullptr;
+  float *lse = nullptr;
 };
 // SIMT path: fp32 inputs (exact fp32 arithmetic), any D in {64,128}, any strides.
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st);
@@ -68,6 +72,8 @@ cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st);
 // cudaErrorNotSupported, launching nothing, when the tensor maps cannot be encoded.
 bool chunk_tc_supported(const ChunkArgs &a);
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st);
+// Can the tensor-core kernel write `o` itself (unit D stride, 16-byte aligned rows)?
+bool chunk_tc_final_supported(const ChunkArgs &a, const View &o);
 // One bounded wait that can never complete (the failure-detection probe).
 cudaError_t launch_wait_probe(unsigned int *err, unsigned long long timeout_ns, cudaStream_t st);
 // Empty chunk (Nc == 0) with accumulate == 0: write the empty state.

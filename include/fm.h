@@ -16,6 +16,7 @@
  *     fm_bounds(q, k_full, v_full)                       once
  *     fm_attn_chunk(q, k_c, v_c, accumulate = c > 0)     once per chunk c
  *     fm_finalize(acc_o, acc_sum -> o)                   once
+ * or, fusing the last two: fm_attn_chunk_final(..., o) for the last chunk.
  *
  * Conventions shared by every call:
  *   - Tensors are described by fm_tensor: a logical [B, H, S, D] array with element
@@ -172,6 +173,21 @@ FM_API int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tenso
 FM_API int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk,
                   fm_bounds_out *bounds, const fm_opts *opts, float *acc_o, float *acc_sum,
                   float *acc_max, int accumulate, fm_stream_t stream);
+
+/* fm_attn_chunk_final -- fold the LAST KV chunk and normalise in the same pass ([NKI]
+ * "The ring loop": the last step folds and normalises, so the output write hides behind
+ * attention instead of running as a separate tail).  Same arguments and checks as
+ * fm_attn_chunk, plus
+ *   o_out  [B, H, Sq, D] FM_F32 or FM_BF16 (any strides): o = acc / max(acc_sum, 1e-37)
+ *   lse    f32 [B, H, Sq] contiguous, or NULL: as written by fm_finalize_lse
+ * acc_sum and acc_max are updated as by fm_attn_chunk; acc_o is NOT (its contents are
+ * unspecified afterwards).  The result equals fm_attn_chunk followed by fm_finalize (or
+ * fm_finalize_lse); the tensor-core kernel does both in one launch where the layout of
+ * o_out allows 16-byte stores, otherwise the two steps run back to back. */
+FM_API int fm_attn_chunk_final(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk,
+                               fm_bounds_out *bounds, const fm_opts *opts, float *acc_o, float *acc_sum,
+                               float *acc_max, int accumulate, const fm_tensor *o_out, float *lse,
+                               fm_stream_t stream);
 
 /* fm_finalize -- o = acc_o / max(acc_sum, 1e-37) ([NKI] "Accumulate, then normalize
  * once": one divide, sum floored near the smallest fp32 normal).

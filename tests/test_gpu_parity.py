@@ -206,6 +206,38 @@ def test_lse_matches_oracle(dev, force_online):
     assert torch.all(torch.isneginf(fa.lse))
 
 
+@pytest.mark.parametrize("force_online", [False, True])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_fused_final_chunk_equals_chunk_plus_finalize(dev, force_online, out_dtype):
+    """fm_attn_chunk_final (fold + normalise in one pass) gives the same bits as
+    fm_attn_chunk followed by fm_finalize_lse, and matches the oracle."""
+    q, k, v = workloads.make_inputs("mix", device="cpu", heads=range(3), Sq=333, N=600)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    chunks = [(0, 256), (256, 344)]
+    outs = []
+    for fused in (True, False):
+        fa = fm.FixedMAttention(1, 3, 333, 600, 128, dev, centering=False, force_online=force_online,
+                                out_dtype=out_dtype)
+        o = fa.forward(qd, kd, vd, chunks, with_lse=True, fused_final=fused).clone()
+        fm.fm_sync_status()
+        outs.append((o, fa.lse.clone(), fa.acc_sum.clone(), fa.acc_max.clone()))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+    ref, ref_lse = oracle.attention(q, k, v, return_lse=True)
+    assert maxerr(outs[0][0], ref) <= TOL_BF16
+    assert maxerr(outs[0][1], ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse))))
+    # an output layout the kernel cannot store to directly (D not contiguous) takes the
+    # chunk + finalize route inside the same call
+    fa = fm.FixedMAttention(1, 3, 333, 600, 128, dev, centering=False, force_online=force_online)
+    o_t = torch.empty(1, 3, 128, 333, dtype=out_dtype, device=dev).transpose(2, 3)
+    fm.fm_bounds(qd, kd, vd, fa.opt, fa.bounds, fa.workspace)
+    fm.fm_attn_chunk(qd, kd[:, :, :256], vd[:, :, :256], fa.bounds, fa.opt, fa.acc_o, fa.acc_sum, fa.acc_max, False)
+    fm.fm_attn_chunk_final(qd, kd[:, :, 256:], vd[:, :, 256:], fa.bounds, fa.opt, fa.acc_o, fa.acc_sum, fa.acc_max,
+                           True, o_t)
+    fm.fm_sync_status()
+    assert torch.equal(o_t, outs[0][0])
+
+
 def test_bounded_wait_reports_timeout_and_context_survives(dev):
     """Failure detection without a fault: a wait on a barrier nothing completes gives up
     after 50 ms, fm_sync_status reports FM_ERR_TIMEOUT once, and work continues."""
