@@ -31,10 +31,10 @@ METRIC = "fixed-m attn fwd TFLOP/s (bf16, S=75,600, H=40, D=128) and % of BF16 t
 WORKLOAD = "wan"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 # DRAM bytes (read + write) per launch of the chunk kernel from one ncu capture (see
-# profiles/fm_chunk_tc_wan_h8.md): 8 heads, averaged over the init and the accumulate
+# profiles/fm_chunk_tc_wan_h8.md): 8 heads, averaged over the first-chunk and the final-chunk
 # launch, scaled x5 to 40 heads (every term of the traffic grows with the head count).
 # Valid only for the kernel source it was measured on: the bench reports null otherwise.
-CHUNK_TRAFFIC = {"source_sha256_16": "e8f96f31f17e9359", "bytes_per_launch": 5 * (601.047e6 + 912.607e6) / 2}
+CHUNK_TRAFFIC = {"source_sha256_16": "ae89d921050ee96c", "bytes_per_launch": 5 * (598.423e6 + 827.504e6) / 2}
 
 
 def chunk_traffic():
@@ -197,11 +197,13 @@ def run_ours(args, rank, world, local_rank):
     fm.load()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = workloads.WORKLOADS[WORKLOAD]
+    w = workloads.WORKLOADS[args.workload]
     chunks = workloads.chunk_bounds(w)
     H = w.H if args.heads is None else args.heads
-    q, k, v = workloads.make_inputs(WORKLOAD, device=dev, heads=range(H))
-    fa = fm.FixedMAttention(w.B, H, w.Sq, w.N, w.D, dev, centering=True, out_dtype=torch.bfloat16)
+    centering = w.centering[0] if args.centering == "auto" else args.centering == "on"
+    q, k, v = workloads.make_inputs(w.name, device=dev, heads=range(H))
+    fa = fm.FixedMAttention(w.B, H, w.Sq, w.N, w.D, dev, centering=centering, force_online=args.force_online,
+                            out_dtype=q.dtype)
     stream = torch.cuda.current_stream(dev)
     step_flops = w.flops(heads=w.B * H)
     dist = None
@@ -301,7 +303,8 @@ def run_ours(args, rank, world, local_rank):
     chunk_avg_ms = statistics.mean(chunk_ms)
     achieved = per_launch_flops / (chunk_avg_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
-    traffic = args.traffic if args.traffic is not None else (chunk_traffic() if H == w.H else None)
+    traffic = args.traffic if args.traffic is not None else (
+        chunk_traffic() if (H == w.H and w.name == WORKLOAD and not args.force_online) else None)
     roofline = {"bound": "tensor", "kernel": "fm_chunk_tc_kernel", "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "traffic_unit": "bytes per launch (dram read + write)",
@@ -309,18 +312,21 @@ def run_ours(args, rank, world, local_rank):
                 "peak_kind": f"bf16 sustained ({peak_src})",
                 "frac_of_burst_peak": achieved / peaks["bf16_tflops"], "launch_ms": chunk_avg_ms}
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and w.name == WORKLOAD:
         cv, info = cpu_oracle_sample(args.cpu_seconds)
         cpu = {"value": cv, "unit": "TFLOP/s", "cores": info["threads"], "kind": "oracle",
                "sample": f"1 head x {info['rows']} query rows x all {w.N} keys, fp64, "
                          f"{info['seconds']:.1f} s"}
     clocks = clk.summary()
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": METRIC if w.name == WORKLOAD else f"fixed-m attn fwd TFLOP/s ({w.name})",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{w.name}: B={w.B} H={H} S_q=S_k={w.Sq} D={w.D} bf16, "
-                               f"{len(chunks)} KV chunks of {chunks[0][1]}, virtual K-centering",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name}: B={w.B} H={H} S_q=S_k={w.Sq} D={w.D} {w.dtype}, "
+                               f"{len(chunks)} KV chunks of {chunks[0][1]}, "
+                               f"virtual K-centering {'on' if centering else 'off'}"
+                               + (", every tile forced onto the online fallback" if args.force_online else ""),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (774 MB per tensor), no flush",
                    "fixed_m_tile_fraction": eligible},
@@ -345,6 +351,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=256, help="query rows per reference step")
     ap.add_argument("--heads", type=int, default=None, help="first N heads only (profiling a smaller case)")
+    ap.add_argument("--workload", default=WORKLOAD, help="wan (default, the headline), h40_s4096, mix, adversarial")
+    ap.add_argument("--centering", choices=["auto", "on", "off"], default="auto")
+    ap.add_argument("--force-online", action="store_true", help="run every tile on the online fallback")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per chunk launch from an ncu capture of the current kernel")
     args = ap.parse_args()

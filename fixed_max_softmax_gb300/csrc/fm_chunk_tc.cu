@@ -233,6 +233,11 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32
 __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" : FM_W8(0), FM_W8(8), FM_W8(16), FM_W8(24) : : "memory");
 }
+// Ties `r` (the destination of an earlier load covered by a tmem_ld_wait just before)
+// to this point, so that no use of it is scheduled above that wait.
+__device__ __forceinline__ void tmem_reg_tie(uint32_t (&r)[32]) {
+  asm volatile("" : FM_W8(0), FM_W8(8), FM_W8(16), FM_W8(24) : : "memory");
+}
 #undef FM_W8
 // Two fp32 lanes in one 64-bit register (Blackwell's packed fp32x2 arithmetic).
 __device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
@@ -384,55 +389,86 @@ __device__ __forceinline__ void softmax_fixed_tile(uint32_t tS, int nvalid, floa
   }
 }
 
-// Online softmax of one S tile: running max `run` (base-2 units), lazy rescale of O.
+__device__ __forceinline__ float max32(const uint32_t (&s)[32], int col0, int nvalid, float mx) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (col0 + e < nvalid) mx = fmaxf(mx, __uint_as_float(s[e]));
+  return mx;
+}
+
+// Online softmax of one S tile, in one pass over TMEM: all 128 scores of the row are loaded
+// at once; the tile max updates the running max `run` (base-2 units) lazily (only when it
+// grows by more than 2^8, or on the first tile); p = 2^(alpha*s - run) goes back over S as
+// bf16 P; the row sum is rescaled before the new terms are added, and O in TMEM after P is
+// out.  The rescale decision is per row but tcgen05.ld/st are warp-collective, so the warp
+// rescales when any of its rows needs it and the other rows use a scale of 1.
 __device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, int nvalid, float alpha,
                                                     bool have_o, float &run, float (&l)[4]) {
+  uint32_t s0[32], s1[32], s2[32], s3[32];
+  tmem_ld32_async(tS, s0);
+  tmem_ld32_async(tS + 32, s1);
+  tmem_ld32_async(tS + 64, s2);
+  tmem_ld32_async(tS + 96, s3);
+  tmem_ld_wait(s0);  // waits for all four
+  tmem_reg_tie(s1);
+  tmem_reg_tie(s2);
+  tmem_reg_tie(s3);
   float mx = -INFINITY;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t s[32];
-    tmem_ld32(tS + c * 32, s);
-#pragma unroll
-    for (int e = 0; e < 32; ++e)
-      if (c * 32 + e < nvalid) mx = fmaxf(mx, __uint_as_float(s[e]));
-  }
+  mx = max32(s0, 0, nvalid, mx);
+  mx = max32(s1, 32, nvalid, mx);
+  mx = max32(s2, 64, nvalid, mx);
+  mx = max32(s3, 96, nvalid, mx);
   const float zmax = mx * alpha;
-  // The decision is per row, but tcgen05.ld/st are warp-collective: the warp rescales
-  // when any of its rows needs it, and rows that do not keep their max (scale 1).
   const bool need = run == -INFINITY || zmax > run + kLazyRescale;
-  if (__any_sync(0xffffffffu, need)) {
+  const bool any = __any_sync(0xffffffffu, need);
+  float sc = 1.0f;
+  if (any) {
     const float nr = need ? fmaxf(run, zmax) : run;
-    if (have_o) {  // O holds earlier tiles (j > 0): every row's run is finite then
-      const float sc = need ? ex2(run - nr) : 1.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) l[i] *= sc;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * sc);
-        tmem_st32(tO + c * 32, o);
-      }
-    }
+    if (have_o && need) sc = ex2(run - nr);  // O holds earlier tiles only when j > 0
     run = nr;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) l[i] *= sc;
   }
   const float nb = -run;
+  uint32_t pk[16];
+  if (nvalid >= kBK) {
+    const uint64_t a2 = f2_pack(__float_as_uint(alpha), __float_as_uint(alpha));
+    const uint64_t nb2 = f2_pack(__float_as_uint(nb), __float_as_uint(nb));
+    uint64_t acc0 = 0, acc1 = 0;
+    exp_chunk_full(s0, a2, nb2, acc0, acc1, pk);
+    tmem_st16(tS + 0, pk);
+    exp_chunk_full(s1, a2, nb2, acc0, acc1, pk);
+    tmem_st16(tS + 16, pk);
+    exp_chunk_full(s2, a2, nb2, acc0, acc1, pk);
+    tmem_st16(tS + 32, pk);
+    exp_chunk_full(s3, a2, nb2, acc0, acc1, pk);
+    tmem_st16(tS + 48, pk);
+    float x0, x1, y0, y1;
+    f2_unpack(acc0, x0, x1);
+    f2_unpack(acc1, y0, y1);
+    l[0] += x0;
+    l[1] += x1;
+    l[2] += y0;
+    l[3] += y1;
+  } else {
+    exp_chunk_masked(s0, 0, nvalid, alpha, nb, l, pk);
+    tmem_st16(tS + 0, pk);
+    exp_chunk_masked(s1, 32, nvalid, alpha, nb, l, pk);
+    tmem_st16(tS + 16, pk);
+    exp_chunk_masked(s2, 64, nvalid, alpha, nb, l, pk);
+    tmem_st16(tS + 32, pk);
+    exp_chunk_masked(s3, 96, nvalid, alpha, nb, l, pk);
+    tmem_st16(tS + 48, pk);
+  }
+  if (any && have_o) {
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t s[32];
-    tmem_ld32(tS + c * 32, s);
-    uint32_t pk[16];
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tO + c * 32, o);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) {
-      const int col = c * 32 + 2 * e;
-      const float p0 = col < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e]), alpha, nb)) : 0.f;
-      const float p1 = col + 1 < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e + 1]), alpha, nb)) : 0.f;
-      l[e & 3] += p0;
-      l[(e + 2) & 3] += p1;
-      pk[e] = pack_bf16(p0, p1);
+      for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * sc);
+      tmem_st32(tO + c * 32, o);
     }
-    tmem_st16(tS + c * 16, pk);
   }
 }
 
