@@ -7,6 +7,8 @@ the online-fallback path within the same tolerance of each other.  Small cases a
 compared element by element; the full-size workloads on sampled (head, row) sets that
 include every ragged tail.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -236,6 +238,52 @@ def test_fused_final_chunk_equals_chunk_plus_finalize(dev, force_online, out_dty
                            True, o_t)
     fm.fm_sync_status()
     assert torch.equal(o_t, outs[0][0])
+
+
+def test_long_key_sequence_and_batches(dev):
+    """2^20 keys (C(N) = 99, gate = 112) folded in 3 uneven chunks, and B = 2."""
+    N = 1 << 20
+    q, k, v = workloads.make_inputs("wan", device=dev, heads=[0], Sq=200, N=N)
+    chunks = [(0, 300001), (300001, 500000), (800001, N - 800001)]
+    fa, o = run(q, k, v, chunks, centering=True)
+    assert (fa.bounds.out.C, fa.bounds.out.gate) == oracle.constants(N)[0:3:2]
+    ref = oracle.attention(q.cpu(), k.cpu(), v.cpu())
+    assert maxerr(o, ref) <= TOL_BF16
+    # two batches with different recipes
+    q1, k1, v1 = workloads.make_inputs("mix", device="cpu", heads=range(3), Sq=1000, N=1500)
+    q2, k2, v2 = workloads.make_inputs("wan", device="cpu", heads=range(3), Sq=1000, N=1500)
+    q, k, v = torch.cat([q1, q2]), torch.cat([k1, k2]), torch.cat([v1, v2])
+    fa, o = run(q.to(dev), k.to(dev), v.to(dev), [(0, 700), (700, 800)], centering=True)
+    check_bounds(fa, oracle.bounds(q, k, v, centering=True))
+    assert maxerr(o, oracle.attention(q, k, v)) <= TOL_BF16
+
+
+def test_device_flags_follow_the_gate_edge(dev):
+    """Queries whose bound sits just under / over the gate: the device flags match the
+    oracle's decision exactly (both values are far from the tie band)."""
+    N, D = 4096, 128
+    C, W, gate = oracle.constants(N)
+    g = torch.Generator().manual_seed(11)
+    k = torch.randn(1, 1, N, D, generator=g)
+    v = torch.randn(1, 1, N, D, generator=g)
+    q = torch.randn(1, 1, 4 * 128, D, generator=g)
+    kb = k.bfloat16().double()
+    kmax = (kb - kb.mean(dim=2, keepdim=True)).norm(dim=-1).max().item()
+    alpha = math.log2(math.e) / math.sqrt(D)
+    # one loud row per Q-block, its bound set to gate - 1.5, gate - 0.5, gate + 0.5, gate + 1.5
+    # (bf16 rounding of the query moves U by about 0.2)
+    for blk, u in enumerate((gate - 1.5, gate - 0.5, gate + 0.5, gate + 1.5)):
+        qr = q[0, 0, blk * 128]
+        q[0, 0, blk * 128] = qr / qr.norm() * (u / (alpha * kmax))
+    qb, kbf, vb = q.bfloat16(), k.bfloat16(), v.bfloat16()
+    fa, o = run(qb.to(dev), kbf.to(dev), vb.to(dev), [(0, 2000), (2000, 2096)], centering=True)
+    ob = oracle.bounds(qb, kbf, vb, centering=True)
+    check_bounds(fa, ob)
+    # the oracle's verdict on the rounded values rules, outside the tie band
+    safe = ob["margin"][0, 0] > 1e-4 * np.maximum(1.0, ob["U"][0, 0])
+    assert np.array_equal(fa.bounds.flag.cpu().numpy()[0, 0][safe], ob["flag"][0, 0][safe])
+    assert list(ob["flag"][0, 0]) == [1, 1, 0, 0], ob["U"][0, 0]
+    assert maxerr(o, oracle.attention(qb, kbf, vb)) <= TOL_BF16
 
 
 def test_bounded_wait_reports_timeout_and_context_survives(dev):
