@@ -8,7 +8,8 @@ PyTorch provides device memory and streams and nothing else.
 
 Functions with the ABI's names (same arguments, torch tensors in place of pointers):
 ``fm_bounds_workspace_size``, ``fm_bounds``, ``fm_bounds_noalloc``, ``fm_attn_chunk``,
-``fm_attn_chunk_final``, ``fm_finalize``, ``fm_finalize_lse``, ``fm_sync_status``,
+``fm_attn_chunk_final``, ``fm_attn_chunks``, ``fm_finalize``, ``fm_finalize_lse``,
+``fm_sync_status``,
 ``fm_probe_wait_timeout``,
 ``fm_last_error``, ``fm_version``.
 
@@ -37,7 +38,8 @@ ERROR_NAMES = {0: "FM_OK", 1: "FM_ERR_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_DTYPE"
                5: "FM_ERR_BOUNDS_MISMATCH", 6: "FM_ERR_CUDA", 7: "FM_ERR_TIMEOUT"}
 ABI_SYMBOLS = ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
                "fm_last_error", "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout",
-               "fm_attn_chunk_final")
+               "fm_attn_chunk_final", "fm_attn_chunks")
+FM_MAX_CHUNKS = 8
 FM_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -92,13 +94,14 @@ def load(path: str | None = None):
     lib.fm_finalize_lse.argtypes = [P, P, P, P, P, P]
     lib.fm_probe_wait_timeout.argtypes = [ctypes.c_uint, P]
     lib.fm_attn_chunk_final.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_int, P, P, P]
+    lib.fm_attn_chunks.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, P, ctypes.c_int, P, P, P]
     lib.fm_sync_status.argtypes = [P]
     lib.fm_last_error.restype = ctypes.c_char_p
     lib.fm_last_error.argtypes = []
     lib.fm_version.argtypes = []
     for name in ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
                  "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout",
-               "fm_attn_chunk_final"):
+                 "fm_attn_chunk_final", "fm_attn_chunks"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -215,6 +218,19 @@ def fm_attn_chunk_final(q, k_chunk, v_chunk, bounds: Bounds, opt: fm_opts, acc_o
                                              _ptr(lse), _stream(stream)))
 
 
+def fm_attn_chunks(q, k_chunks, v_chunks, bounds: Bounds, opt: fm_opts, acc_o, acc_sum, acc_max,
+                   accumulate: bool, o_out=None, lse=None, stream=None):
+    """Fold a list of consecutive KV chunks in one pass (and normalise into o_out if given)."""
+    n = len(k_chunks)
+    ks = (fm_tensor * n)(*[tensor(t) for t in k_chunks])
+    vs = (fm_tensor * n)(*[tensor(t) for t in v_chunks])
+    to = tensor(o_out) if o_out is not None else None
+    return _check(load().fm_attn_chunks(ctypes.byref(tensor(q)), ks, vs, n, ctypes.byref(bounds.out),
+                                        ctypes.byref(opt), _ptr(acc_o), _ptr(acc_sum), _ptr(acc_max),
+                                        int(bool(accumulate)), None if to is None else ctypes.byref(to), _ptr(lse),
+                                        _stream(stream)))
+
+
 def fm_finalize(acc_o, acc_sum, o_out, stream=None):
     to = tensor(o_out)
     return _check(load().fm_finalize(_ptr(acc_o), _ptr(acc_sum), ctypes.byref(to), _stream(stream)))
@@ -241,7 +257,9 @@ class FixedMAttention:
     (start, length) slice of the key sequence (the ring's steps, sequentially) and writes
     `out` (fp32 or the input dtype): by default the last chunk goes through
     fm_attn_chunk_final (fold and normalise in one pass); fused_final=False uses a separate
-    fm_finalize.  with_lse=True also fills `lse` [B, H, Sq] (natural log).
+    fm_finalize.  one_launch=True folds all chunks with fm_attn_chunks instead (one launch per
+    FM_MAX_CHUNKS chunks, accumulators on chip across them).  with_lse=True also fills
+    `lse` [B, H, Sq] (natural log).
     """
 
     def __init__(self, B, H, Sq, N, D, device="cuda", centering=False, softmax_scale=0.0,
@@ -257,13 +275,21 @@ class FixedMAttention:
         self.out = torch.empty(B, H, Sq, D, dtype=out_dtype, device=device)
         self.lse = None
 
-    def forward(self, q, k, v, chunks=None, stream=None, with_lse=False, fused_final=True):
+    def forward(self, q, k, v, chunks=None, stream=None, with_lse=False, fused_final=True, one_launch=False):
         N = k.shape[2]
         chunks = [(0, N)] if chunks is None else chunks
         fm_bounds(q, k, v, self.opt, self.bounds, self.workspace, stream)
         if with_lse and self.lse is None:
             self.lse = torch.empty(self.acc_sum.shape, dtype=torch.float32, device=self.acc_sum.device)
         lse = self.lse if with_lse else None
+        if one_launch:  # every chunk (up to FM_MAX_CHUNKS per call) and the normalise in one pass
+            for g0 in range(0, len(chunks), FM_MAX_CHUNKS):
+                grp = chunks[g0:g0 + FM_MAX_CHUNKS]
+                last = g0 + FM_MAX_CHUNKS >= len(chunks)
+                fm_attn_chunks(q, [k[:, :, s:s + n] for s, n in grp], [v[:, :, s:s + n] for s, n in grp],
+                               self.bounds, self.opt, self.acc_o, self.acc_sum, self.acc_max, g0 > 0,
+                               self.out if last else None, lse if last else None, stream)
+            return self.out
         for i, (s, n) in enumerate(chunks):
             kc, vc = k[:, :, s:s + n], v[:, :, s:s + n]
             if fused_final and i == len(chunks) - 1:

@@ -245,17 +245,27 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
 }  // extern "C"
 
 namespace {
-// fm_attn_chunk, and with o_out given fm_attn_chunk_final.
-int attn_chunk_impl(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk, fm_bounds_out *bounds,
-                    const fm_opts *opts, float *acc_o, float *acc_sum, float *acc_max, int accumulate,
-                    const fm_tensor *o_out, float *lse, fm_stream_t stream) {
+// fm_attn_chunks: n consecutive chunks folded in order; with o_out given, the normalise of
+// fm_attn_chunk_final follows the last one.  fm_attn_chunk and fm_attn_chunk_final are
+// the n = 1 cases.
+int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_tensor *v_chunks, int n_chunks,
+                     fm_bounds_out *bounds, const fm_opts *opts, float *acc_o, float *acc_sum, float *acc_max,
+                     int accumulate, const fm_tensor *o_out, float *lse, fm_stream_t stream) {
   t_err.clear();
-  View vq, vk, vv;
+  View vq;
   int rc;
-  if ((rc = to_view(q, "q", &vq)) || (rc = to_view(k_chunk, "k_chunk", &vk)) ||
-      (rc = to_view(v_chunk, "v_chunk", &vv)))
-    return rc;
-  if ((rc = check_qkv(vq, vk, vv))) return rc;
+  if ((rc = to_view(q, "q", &vq))) return rc;
+  if (n_chunks < 1 || n_chunks > FM_MAX_CHUNKS)
+    return fail(FM_ERR_ARG, "n_chunks = %d outside [1, %d]", n_chunks, FM_MAX_CHUNKS);
+  if (!k_chunks || !v_chunks) return fail(FM_ERR_ARG, "k_chunks / v_chunks is NULL");
+  View vk[FM_MAX_CHUNKS], vv[FM_MAX_CHUNKS];
+  int64_t keys = 0;
+  for (int c = 0; c < n_chunks; ++c) {
+    if ((rc = to_view(&k_chunks[c], "k_chunk", &vk[c])) || (rc = to_view(&v_chunks[c], "v_chunk", &vv[c])))
+      return rc;
+    if ((rc = check_qkv(vq, vk[c], vv[c]))) return rc;
+    keys += vk[c].S;
+  }
   if (!bounds) return fail(FM_ERR_ARG, "bounds is NULL");
   if (accumulate != 0 && accumulate != 1) return fail(FM_ERR_ARG, "accumulate must be 0 or 1");
   if (opts && ((opts->centering != 0 && opts->centering != 1) || (opts->force_online != 0 && opts->force_online != 1)))
@@ -284,7 +294,7 @@ int attn_chunk_impl(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tenso
   if ((rc = make_alpha(opts, vq.D, &alpha))) return rc;
   if ((float)alpha != bounds->alpha)
     return fail(FM_ERR_BOUNDS_MISMATCH, "softmax scale differs from the one the bounds were computed with");
-  const int64_t seen = accumulate ? bounds->kv_seen + vk.S : vk.S;
+  const int64_t seen = accumulate ? bounds->kv_seen + keys : keys;
   if (seen > bounds->N_total)
     return fail(FM_ERR_BOUNDS_MISMATCH, "%lld keys folded in exceed the %lld keys the bounds cover",
                 (long long)seen, (long long)bounds->N_total);
@@ -309,11 +319,8 @@ int attn_chunk_impl(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tenso
   if (!err) return fail(FM_ERR_CUDA, "cannot resolve the device error word (no CUDA device?)");
   ChunkArgs a;
   a.q = vq;
-  a.k = vk;
-  a.v = vv;
   a.alpha = (float)alpha;
   a.force_online = force_online;
-  a.accumulate = accumulate;
   a.nqb = nqb;
   a.flag = bounds->flag;
   a.shift = bounds->shift;
@@ -326,22 +333,51 @@ int attn_chunk_impl(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tenso
   cudaError_t e = cudaSuccess;
   bool finalize_separately = o_out != nullptr;
   if (rows > 0) {
-    if (vk.S == 0) {
-      if (!accumulate) e = launch_chunk_empty_init(a, st);
-    } else if (chunk_tc_supported(a)) {
-      if (o_out && chunk_tc_final_supported(a, vo)) {  // the kernel normalises and writes o itself
-        a.out = &vo;
-        a.lse = lse;
-        finalize_separately = false;
+    // chunks without keys add nothing; only the accumulators' first initialisation matters
+    View ks[FM_MAX_CHUNKS], vs[FM_MAX_CHUNKS];
+    int n = 0;
+    for (int c = 0; c < n_chunks; ++c)
+      if (vk[c].S > 0) {
+        ks[n] = vk[c];
+        vs[n] = vv[c];
+        ++n;
       }
-      e = launch_chunk_tc(a, st);
-      if (e == cudaErrorNotSupported) {
-        finalize_separately = o_out != nullptr;
-        a.out = nullptr;
-        e = launch_chunk_simt(a, st);
+    a.accumulate = accumulate;
+    if (n == 0) {
+      if (!accumulate) {
+        a.k = vk[0];
+        a.v = vv[0];
+        e = launch_chunk_empty_init(a, st);
       }
     } else {
-      e = launch_chunk_simt(a, st);
+      a.k = ks[0];
+      a.v = vs[0];
+      a.n_chunks = n;
+      a.ks = ks;
+      a.vs = vs;
+      if (chunk_tc_supported(a)) {
+        if (o_out && chunk_tc_final_supported(a, vo)) {  // the kernel normalises and writes o itself
+          a.out = &vo;
+          a.lse = lse;
+          finalize_separately = false;
+        }
+        e = launch_chunk_tc(a, st);
+        if (e == cudaErrorNotSupported) {  // tensor maps refused: the CUDA-core kernel, chunk by chunk
+          finalize_separately = o_out != nullptr;
+          e = cudaSuccess;
+        } else {
+          n = 0;  // done
+        }
+      }
+      a.out = nullptr;
+      a.lse = nullptr;
+      a.n_chunks = 0;
+      for (int c = 0; c < n && e == cudaSuccess; ++c) {
+        a.k = ks[c];
+        a.v = vs[c];
+        a.accumulate = c == 0 ? accumulate : 1;
+        e = launch_chunk_simt(a, st);
+      }
     }
   }
   if (e != cudaSuccess) return cuda_fail(e, "fm_attn_chunk launch");
@@ -360,8 +396,15 @@ extern "C" {
 int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk, fm_bounds_out *bounds,
                   const fm_opts *opts, float *acc_o, float *acc_sum, float *acc_max, int accumulate,
                   fm_stream_t stream) {
-  return attn_chunk_impl(q, k_chunk, v_chunk, bounds, opts, acc_o, acc_sum, acc_max, accumulate, nullptr, nullptr,
-                         stream);
+  return attn_chunks_impl(q, k_chunk, v_chunk, 1, bounds, opts, acc_o, acc_sum, acc_max, accumulate, nullptr,
+                          nullptr, stream);
+}
+
+int fm_attn_chunks(const fm_tensor *q, const fm_tensor *k_chunks, const fm_tensor *v_chunks, int n_chunks,
+                   fm_bounds_out *bounds, const fm_opts *opts, float *acc_o, float *acc_sum, float *acc_max,
+                   int accumulate, const fm_tensor *o_out, float *lse, fm_stream_t stream) {
+  return attn_chunks_impl(q, k_chunks, v_chunks, n_chunks, bounds, opts, acc_o, acc_sum, acc_max, accumulate, o_out,
+                          lse, stream);
 }
 
 int fm_attn_chunk_final(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk,
@@ -371,7 +414,8 @@ int fm_attn_chunk_final(const fm_tensor *q, const fm_tensor *k_chunk, const fm_t
     t_err.clear();
     return fail(FM_ERR_ARG, "o_out is NULL");
   }
-  return attn_chunk_impl(q, k_chunk, v_chunk, bounds, opts, acc_o, acc_sum, acc_max, accumulate, o_out, lse, stream);
+  return attn_chunks_impl(q, k_chunk, v_chunk, 1, bounds, opts, acc_o, acc_sum, acc_max, accumulate, o_out, lse,
+                          stream);
 }
 
 int fm_finalize(const float *acc_o, const float *acc_sum, const fm_tensor *o_out, fm_stream_t stream) {

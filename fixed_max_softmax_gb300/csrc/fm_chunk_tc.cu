@@ -19,7 +19,9 @@
 // and merge with the previous chunks through acc_max.
 //
 // CTA = two 128-row Q tiles of one (batch, head) (256 rows) against every KV tile of the
-// chunk; 12 warps:
+// launch: one chunk, or several consecutive chunks (up to 8), whose key tiles are walked in
+// order with each chunk's own tensor maps and ragged end, so that O and the row sums stay
+// on chip across the chunk boundaries.  12 warps:
 //   warp 0      TMA producer: Q tiles once, then K_j, V_j into a 4-stage ring
 //   warp 1      TMEM allocator; lane 0 issues every MMA and commit
 //   warps 4-7   softmax + epilogue of Q tile 0 (TMEM lanes 0-127)
@@ -291,9 +293,21 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+constexpr int kMaxChunks = FM_MAX_CHUNKS;  // consecutive KV chunks one launch can fold
+
+// Tensor maps of Q and of each chunk's K and V (kernel parameter space).
+struct TcMaps {
+  CUtensorMap q;
+  CUtensorMap k[kMaxChunks];
+  CUtensorMap v[kMaxChunks];
+};
+
 struct TcParams {
   int64_t Sq, nqb;
-  int Nc, H, n_kv;
+  int H, n_kv;                      // n_kv: key tiles over all chunks of the launch
+  int n_chunks;
+  int tile0[kMaxChunks + 1];        // first key tile of each chunk (prefix sums)
+  int len[kMaxChunks];              // keys in each chunk
   float alpha;
   int force_online, accumulate;
   const uint8_t *flag;
@@ -473,8 +487,7 @@ __device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, in
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    fm_chunk_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const TcParams p) {
+    fm_chunk_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -516,20 +529,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_expect_tx(bar(kBarQFull), 4 * kPanelBytes);
       for (int t = 0; t < 2; ++t)
         for (int pn = 0; pn < 2; ++pn)
-          tma_load_4d(base + kOffQ + t * kTileBytes + pn * kPanelBytes, &tmQ, bar(kBarQFull), pn * 64,
+          tma_load_4d(base + kOffQ + t * kTileBytes + pn * kPanelBytes, &maps.q, bar(kBarQFull), pn * 64,
                       (int)((qb0 + t) * kBQ), h, b);
       bool ok = true;
+      int c = 0;  // chunk of key tile j
       for (int j = 0; j < n_kv && ok; ++j) {
+        while (j >= p.tile0[c + 1]) ++c;
+        const int jl = j - p.tile0[c];  // tile within its chunk
         for (int w = 0; w < 2 && ok; ++w) {
           const int idx = 2 * j + w, s = idx % kStages, round = idx / kStages;
           ok = wait_phase(bar(kBarKVEmpty + s), (uint32_t)((round & 1) ^ 1), abort_flag, p.timeout_ns, p.err,
                           kDevErrTimeoutProducer, wtag(kBarKVEmpty + s, j));
           if (!ok) break;
           mbar_expect_tx(bar(kBarKVFull + s), kTileBytes);
-          const CUtensorMap *tm = w ? &tmV : &tmK;
+          const CUtensorMap *tm = w ? &maps.v[c] : &maps.k[c];
           for (int pn = 0; pn < 2; ++pn)
             tma_load_4d(base + kOffKV + s * kTileBytes + pn * kPanelBytes, tm, bar(kBarKVFull + s), pn * 64,
-                        j * kBK, h, b);
+                        jl * kBK, h, b);
           last_round[s] = round;
         }
       }
@@ -629,13 +645,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l[4] = {0.f, 0.f, 0.f, 0.f};
     float run = -INFINITY;
     bool ok = true;
+    int c = 0;  // chunk of key tile j
     for (int j = 0; j < n_kv; ++j) {
+      while (j >= p.tile0[c + 1]) ++c;
       ok = wait_phase(bar(kBarSFull + t), (uint32_t)(j & 1), abort_flag, p.timeout_ns, p.err,
                       kDevErrTimeoutSoftmax, wtag(kBarSFull + t, j));
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
       if (!ok) break;
       tc_fence_after();
-      const int nvalid = min(kBK, p.Nc - j * kBK);
+      const int nvalid = min(kBK, p.len[c] - (j - p.tile0[c]) * kBK);  // ragged end of each chunk
       if (fixed) softmax_fixed_tile(tS, nvalid, p.alpha, -bias, l);
       else softmax_online_tile(tS, tO, nvalid, p.alpha, j > 0, run, l);
       tmem_st_wait();
@@ -778,7 +796,15 @@ bool tma_view_ok(const View &t) {
 }  // namespace
 
 bool chunk_tc_supported(const ChunkArgs &a) {
-  return tma_view_ok(a.q) && tma_view_ok(a.k) && tma_view_ok(a.v) &&
+  if (a.n_chunks > kMaxChunks) return false;
+  for (int c = 0; c < a.n_chunks; ++c)
+    if (!tma_view_ok(a.ks[c]) || !tma_view_ok(a.vs[c]) || a.ks[c].S > ((int64_t)1 << 30)) return false;
+  if (a.n_chunks > 0) {
+    int64_t total = 0;
+    for (int c = 0; c < a.n_chunks; ++c) total += a.ks[c].S;
+    if (total > ((int64_t)1 << 30)) return false;
+  }
+  return tma_view_ok(a.q) && (a.n_chunks > 0 || (tma_view_ok(a.k) && tma_view_ok(a.v))) &&
          reinterpret_cast<uintptr_t>(a.acc_o) % 16 == 0 && a.q.B <= 65535 && a.q.H <= 65535 &&
          a.k.S <= (int64_t)1 << 30 && a.q.S <= (int64_t)1 << 30;
 }
@@ -792,19 +818,30 @@ bool chunk_tc_final_supported(const ChunkArgs &a, const View &o) {
 }
 
 cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
-  CUtensorMap mq, mk, mv;
+  const int nc = a.n_chunks > 0 ? a.n_chunks : 1;
+  if (nc > kMaxChunks) return cudaErrorNotSupported;
+  const View *ks = a.n_chunks > 0 ? a.ks : &a.k;
+  const View *vs = a.n_chunks > 0 ? a.vs : &a.v;
+  TcMaps maps;
   // a layout the driver's tensor-map encoder refuses is reported so the caller can use
   // the CUDA-core kernel instead; nothing has been launched then
-  if (!encode_map(&mq, a.q) || !encode_map(&mk, a.k) || !encode_map(&mv, a.v)) return cudaErrorNotSupported;
+  if (!encode_map(&maps.q, a.q)) return cudaErrorNotSupported;
+  for (int c = 0; c < nc; ++c)
+    if (!encode_map(&maps.k[c], ks[c]) || !encode_map(&maps.v[c], vs[c])) return cudaErrorNotSupported;
   cudaError_t e =
       cudaFuncSetAttribute(fm_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   TcParams p;
   p.Sq = a.q.S;
   p.nqb = a.nqb;
-  p.Nc = (int)a.k.S;
   p.H = (int)a.q.H;
-  p.n_kv = (int)((a.k.S + kBK - 1) / kBK);
+  p.n_chunks = nc;
+  p.tile0[0] = 0;
+  for (int c = 0; c < kMaxChunks; ++c) {
+    p.len[c] = c < nc ? (int)ks[c].S : 0;
+    p.tile0[c + 1] = p.tile0[c] + (c < nc ? (int)((ks[c].S + kBK - 1) / kBK) : 0);
+  }
+  p.n_kv = p.tile0[nc];
   p.alpha = a.alpha;
   p.force_online = a.force_online;
   p.accumulate = a.accumulate;
@@ -827,7 +864,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
     p.osS = a.out->sS;
   }
   dim3 grid((unsigned)((a.nqb + 1) / 2), (unsigned)a.q.H, (unsigned)a.q.B);
-  fm_chunk_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
+  fm_chunk_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(maps, p);
   return cudaGetLastError();
 }
 

@@ -65,6 +65,10 @@ struct ChunkArgs {
   // written to `out` (and lse, when given) instead of acc_o being written back
   const View *out = nullptr;
   float *lse = nullptr;
+  // several consecutive chunks in one launch (tensor-core path): n_chunks > 0 selects
+  // ks/vs instead of k/v
+  int n_chunks = 0;
+  const View *ks = nullptr, *vs = nullptr;
 };
 // SIMT path: fp32 inputs (exact fp32 arithmetic), any D in {64,128}, any strides.
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st);

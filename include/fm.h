@@ -189,6 +189,22 @@ FM_API int fm_attn_chunk_final(const fm_tensor *q, const fm_tensor *k_chunk, con
                                float *acc_max, int accumulate, const fm_tensor *o_out, float *lse,
                                fm_stream_t stream);
 
+/* fm_attn_chunks -- fold n_chunks consecutive KV chunks (1..FM_MAX_CHUNKS) in one pass, and
+ * with o_out given normalise after the last one.  The result equals fm_attn_chunk on each
+ * chunk in order (the first with `accumulate`, the rest adding), followed by fm_finalize /
+ * fm_finalize_lse when o_out is given; acc_o is then left unspecified, as with
+ * fm_attn_chunk_final.  On the tensor-core path one launch walks every chunk's key tiles
+ * (each with its own ragged end) and O and the row sums stay on chip across the chunk
+ * boundaries, as the accumulator stays resident for the whole ring in [NKI] ("A static
+ * bound makes the ring reduction pure addition").  k_chunks / v_chunks: arrays of n_chunks
+ * fm_tensor [B, H, Nc, D].  Errors: those of fm_attn_chunk_final, FM_ERR_ARG for n_chunks
+ * outside [1, FM_MAX_CHUNKS]. */
+#define FM_MAX_CHUNKS 8
+FM_API int fm_attn_chunks(const fm_tensor *q, const fm_tensor *k_chunks, const fm_tensor *v_chunks,
+                          int n_chunks, fm_bounds_out *bounds, const fm_opts *opts, float *acc_o,
+                          float *acc_sum, float *acc_max, int accumulate, const fm_tensor *o_out,
+                          float *lse, fm_stream_t stream);
+
 /* fm_finalize -- o = acc_o / max(acc_sum, 1e-37) ([NKI] "Accumulate, then normalize
  * once": one divide, sum floored near the smallest fp32 normal).
  *   acc_o f32 [B, H, Sq, D] and acc_sum f32 [B, H, Sq], contiguous

@@ -142,6 +142,20 @@ def test_token_major_layout_and_bf16_output(dev):
     assert maxerr(o, ref) <= TOL_BF16
 
 
+def test_strided_head_dim_layout(dev):
+    """D not contiguous ([B, H, D, S] storage seen as [B, H, S, D]): the bounds pass takes its
+    scalar-load path and the chunks the CUDA-core kernel; results still match the oracle."""
+    q, k, v = workloads.make_inputs("mix", device="cpu", heads=range(2), Sq=300, N=260)
+    tq = q.transpose(2, 3).contiguous().to(dev).transpose(2, 3)
+    tk = k.transpose(2, 3).contiguous().to(dev).transpose(2, 3)
+    tv = v.transpose(2, 3).contiguous().to(dev).transpose(2, 3)
+    assert tq.stride(3) != 1
+    for cen in (False, True):
+        fa, o = run(tq, tk, tv, [(0, 130), (130, 130)], centering=cen)
+        check_bounds(fa, oracle.bounds(q, k, v, centering=cen))
+        assert maxerr(o, oracle.attention(q, k, v)) <= TOL_BF16
+
+
 def test_empty_and_degenerate_inputs(dev):
     # a single key: output equals its value (up to bf16 P rounding, exact here: p=1 scale)
     q, k, v = workloads.make_inputs("wan", device="cpu", heads=[0], Sq=5, N=1)
@@ -284,6 +298,30 @@ def test_device_flags_follow_the_gate_edge(dev):
     assert np.array_equal(fa.bounds.flag.cpu().numpy()[0, 0][safe], ob["flag"][0, 0][safe])
     assert list(ob["flag"][0, 0]) == [1, 1, 0, 0], ob["U"][0, 0]
     assert maxerr(o, oracle.attention(qb, kbf, vb)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("force_online", [False, True])
+def test_chunks_in_one_launch(dev, force_online):
+    """fm_attn_chunks folds several ragged chunks in one launch (O and sums on chip across
+    them): matches the oracle and the one-call-per-chunk path (different fp32 summation
+    order, so within the tolerance, not bitwise); 11 chunks take two launches."""
+    q, k, v = workloads.make_inputs("mix", device="cpu", heads=range(3), Sq=300, N=1500)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    ref, ref_lse = oracle.attention(q, k, v, return_lse=True)
+    for chunks in ([(0, 200), (200, 1), (201, 0), (201, 1299)],
+                   [(i * 136, 136 if i < 10 else 140) for i in range(11)]):
+        assert sum(n for _, n in chunks) == 1500
+        fa = fm.FixedMAttention(1, 3, 300, 1500, 128, dev, centering=False, force_online=force_online)
+        o1 = fa.forward(qd, kd, vd, chunks, with_lse=True, one_launch=True).clone()
+        lse1 = fa.lse.clone()
+        fm.fm_sync_status()
+        fb = fm.FixedMAttention(1, 3, 300, 1500, 128, dev, centering=False, force_online=force_online)
+        o2 = fb.forward(qd, kd, vd, chunks).clone()
+        fm.fm_sync_status()
+        assert maxerr(o1, ref) <= TOL_BF16
+        assert maxerr(o1, o2) <= TOL_BF16
+        assert maxerr(lse1, ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse))))
+        assert fa.bounds.out.kv_seen == 1500
 
 
 def test_bounded_wait_reports_timeout_and_context_survives(dev):
