@@ -828,9 +828,17 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   if (!encode_map(&maps.q, a.q)) return cudaErrorNotSupported;
   for (int c = 0; c < nc; ++c)
     if (!encode_map(&maps.k[c], ks[c]) || !encode_map(&maps.v[c], vs[c])) return cudaErrorNotSupported;
-  cudaError_t e =
-      cudaFuncSetAttribute(fm_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  // once per device (and so never while a stream is being captured into a graph, as long
+  // as the first call on a device comes before any capture)
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(fm_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
   TcParams p;
   p.Sq = a.q.S;
   p.nqb = a.nqb;

@@ -324,6 +324,33 @@ def test_chunks_in_one_launch(dev, force_online):
         assert fa.bounds.out.kv_seen == 1500
 
 
+@pytest.mark.parametrize("one_launch", [False, True])
+def test_cuda_graph_capture_and_replay(dev, one_launch):
+    """The whole path (bounds, chunks, fused normalise) captured once in a CUDA graph and
+    replayed on new data in the same buffers gives the eager result bit for bit."""
+    Sq, N = 700, 900
+    chunks = [(0, 450), (450, 450)]
+    q, k, v = workloads.make_inputs("mix", device=dev, heads=range(3), Sq=Sq, N=N)
+    q2, k2, v2 = workloads.make_inputs("wan", device=dev, heads=range(3), Sq=Sq, N=N)
+    fa = fm.FixedMAttention(1, 3, Sq, N, 128, dev, centering=True)
+    fa.forward(q, k, v, chunks, one_launch=one_launch)  # first calls on the device happen before capture
+    fm.fm_sync_status()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa.forward(q, k, v, chunks, one_launch=one_launch)
+    q.copy_(q2)
+    k.copy_(k2)
+    v.copy_(v2)
+    g.replay()
+    torch.cuda.synchronize()
+    fm.fm_sync_status()
+    fb = fm.FixedMAttention(1, 3, Sq, N, 128, dev, centering=True)
+    ref = fb.forward(q2, k2, v2, chunks, one_launch=one_launch)
+    fm.fm_sync_status()
+    assert torch.equal(fa.out, ref)
+    assert maxerr(fa.out, oracle.attention(q2.cpu(), k2.cpu(), v2.cpu())) <= TOL_BF16
+
+
 def test_bounded_wait_reports_timeout_and_context_survives(dev):
     """Failure detection without a fault: a wait on a barrier nothing completes gives up
     after 50 ms, fm_sync_status reports FM_ERR_TIMEOUT once, and work continues."""
