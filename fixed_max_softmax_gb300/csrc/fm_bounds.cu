@@ -35,8 +35,10 @@ constexpr int kMaxPartials = 64;    // row ranges per head for the key sum
 
 __host__ __device__ inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Row ranges per head for the key sum: one per 128 rows, so that short sequences still give
+// enough CTAs to keep HBM busy, and at most kMaxPartials.
 inline int64_t num_partials(int64_t N) {
-  int64_t p = ceil_div(N, 1024);
+  int64_t p = ceil_div(N, 128);
   return p < 1 ? 1 : (p > kMaxPartials ? kMaxPartials : p);
 }
 
@@ -108,6 +110,7 @@ __global__ void __launch_bounds__(kThreads) ksum_kernel(View k, int64_t P, float
   float acc[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+#pragma unroll 4
   for (int64_t r = r0 + warp; r < r1; r += kWarps) {
     float x[EPL];
     load_row<T, EPL, CONTIG>(base + r * k.sS, k.sD, lane, x);
@@ -156,7 +159,8 @@ __global__ void __launch_bounds__(kThreads)
     // Q-block: per-row |q|^2 and alpha * q.kbar
     const T *base = reinterpret_cast<const T *>(q.ptr) + b * q.sB + h * q.sH;
     const int64_t r0 = bx * kQRows, r1 = min(q.S, r0 + kQRows);
-    for (int64_t r = r0 + warp; r < r1; r += kWarps) {
+#pragma unroll 4
+  for (int64_t r = r0 + warp; r < r1; r += kWarps) {
       float x[EPL];
       load_row<T, EPL, CONTIG>(base + r * q.sS, q.sD, lane, x);
       float ss = 0.f, dk = 0.f;
@@ -177,7 +181,8 @@ __global__ void __launch_bounds__(kThreads)
     // K rows: |k - kbar|^2 (kbar = 0 when not centering)
     const T *base = reinterpret_cast<const T *>(k.ptr) + b * k.sB + h * k.sH;
     const int64_t r0 = (bx - nqb) * kKVRows, r1 = min(k.S, r0 + kKVRows);
-    for (int64_t r = r0 + warp; r < r1; r += kWarps) {
+#pragma unroll 4
+  for (int64_t r = r0 + warp; r < r1; r += kWarps) {
       float x[EPL];
       load_row<T, EPL, CONTIG>(base + r * k.sS, k.sD, lane, x);
       float ss = 0.f;
@@ -192,7 +197,8 @@ __global__ void __launch_bounds__(kThreads)
     // V rows: max element square
     const T *base = reinterpret_cast<const T *>(v.ptr) + b * v.sB + h * v.sH;
     const int64_t r0 = (bx - nqb - nkb) * kKVRows, r1 = min(v.S, r0 + kKVRows);
-    for (int64_t r = r0 + warp; r < r1; r += kWarps) {
+#pragma unroll 4
+  for (int64_t r = r0 + warp; r < r1; r += kWarps) {
       float x[EPL];
       load_row<T, EPL, CONTIG>(base + r * v.sS, v.sD, lane, x);
 #pragma unroll

@@ -22,7 +22,7 @@
 // launch: one chunk, or several consecutive chunks (up to 8), whose key tiles are walked in
 // order with each chunk's own tensor maps and ragged end, so that O and the row sums stay
 // on chip across the chunk boundaries.  12 warps:
-//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a 4-stage ring
+//   warp 0      TMA producer: Q tiles once, then K_j, V_j into a 5-stage ring
 //   warp 1      TMEM allocator; lane 0 issues every MMA and commit
 //   warps 4-7   softmax + epilogue of Q tile 0 (TMEM lanes 0-127)
 //   warps 8-11  softmax + epilogue of Q tile 1

@@ -245,7 +245,7 @@ FM_API const char *fm_last_error(void);
 FM_API int fm_version(void);
 
 /* Upper bound of the scratch fm_bounds_noalloc can use: 4 MiB.  That covers, at D = 128,
- * about 120 heads of 75,600 keys (fm_bounds_workspace_size gives the exact need). */
+ * up to 119 heads of 75,600 keys (fm_bounds_workspace_size gives the exact need). */
 #define FM_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 
 /* fm_bounds_noalloc -- fm_bounds for callers that cannot allocate device memory.
