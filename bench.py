@@ -33,19 +33,32 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # DRAM bytes (read + write) per launch of the chunk kernel from one ncu capture (see
 # profiles/fm_chunk_tc_wan_h8.md): 8 heads, averaged over the first-chunk and the final-chunk
 # launch, scaled x5 to 40 heads (every term of the traffic grows with the head count).
-# Valid only for the kernel source it was measured on: the bench reports null otherwise.
-CHUNK_TRAFFIC = {"source_sha256_16": "ae89d921050ee96c", "bytes_per_launch": 5 * (598.423e6 + 827.504e6) / 2}
+# Valid only for the kernel code it was measured on (comments aside): the bench reports null
+# otherwise.
+CHUNK_TRAFFIC = {"code_sha256_16": "ae89d921050ee96c", "bytes_per_launch": 5 * (598.423e6 + 827.504e6) / 2}
+
+
+def kernel_code_hash(path: str) -> str:
+    """sha256[:16] of a CUDA source with its // comments and blank lines removed, so that a
+    comment edit keeps a recorded measurement while any change to the code drops it."""
+    import hashlib
+    import re
+
+    lines = []
+    for ln in open(path, encoding="utf-8").read().splitlines():
+        ln = re.sub(r"//.*$", "", ln).rstrip()
+        if ln:
+            lines.append(ln)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
 
 
 def chunk_traffic():
-    import hashlib
-
     src = os.path.join(ROOT, "fixed_max_softmax_gb300", "csrc", "fm_chunk_tc.cu")
     try:
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        h = kernel_code_hash(src)
     except OSError:
         return None
-    return CHUNK_TRAFFIC["bytes_per_launch"] if h == CHUNK_TRAFFIC["source_sha256_16"] else None
+    return CHUNK_TRAFFIC["bytes_per_launch"] if h == CHUNK_TRAFFIC["code_sha256_16"] else None
 
 
 def load_peaks():
