@@ -14,7 +14,9 @@ Sources and the reading of each step are in the C file's header:
 * ``constants`` / ``bounds`` -- C(N), W, gate, U, m (per Q-block or per row), the row
   shift and the eligibility flag from
   "feat(attention): fixed-m splash attention kernel with dynamic bounds and safety
-  fallbacks", Summary ("Dynamic eligibility bounding", "Virtual K-centering").
+  fallbacks", Summary ("Dynamic eligibility bounding", "Virtual K-centering"); with
+  ``sink_keys``, the loudest keys left out of the key max ("Kernel reference:
+  ring_attention_const_max_fwd", section "Adapting this kernel").
 * ``fixed_m_emulate_f32`` -- fp32 fixed-m sum with an arbitrary shift and
   flush-to-zero, to demonstrate the failure modes the gate exists to prevent.
 
@@ -74,7 +76,7 @@ def _load():
         lib.fmo_attention.argtypes = [P, P, P, i64, i64, i64, i64, ctypes.c_double, P, P, ctypes.c_int]
         lib.fmo_bounds.restype = None
         lib.fmo_bounds.argtypes = [P, P, P, i64, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int,
-                                   ctypes.c_int, i64, P, P, P, P, P, P, P, P, P, ctypes.c_int, P, P, P]
+                                   ctypes.c_int, i64, P, P, P, P, P, P, P, P, P, ctypes.c_int, P, P, P, i64, P, P]
         lib.fmo_fixed_m_emulate_f32.restype = None
         lib.fmo_fixed_m_emulate_f32.argtypes = [P, P, P, i64, i64, i64, ctypes.c_double, P, P, P, P,
                                                 P, P]
@@ -142,12 +144,14 @@ def attention(q, k, v, scale: float | None = None, threads: int = 0, return_lse:
 
 
 def bounds(q, k, v, scale: float | None = None, centering: bool = False, dtype_safe: bool = True,
-           vmax: int = VMAX_DEFAULT, bq: int = BQ_DEFAULT, per_row: bool = False) -> dict:
+           vmax: int = VMAX_DEFAULT, bq: int = BQ_DEFAULT, per_row: bool = False, sink_keys: int = 0) -> dict:
     """Bounds of one fixed-m call in fp64 (norms, kbar, U, m, flag, C, W, gate).
 
     q: [B, H, Sq, D] (or [G, Sq, D]); k, v: [B, H, N, D] -- N is the TOTAL KV length
     over every chunk of the call.  Arrays come back with leading dims [B, H] when the
-    inputs were 4-D.
+    inputs were 4-D.  sink_keys > 0 leaves that many loudest keys per head out of the key
+    max ("sink_idx", ascending, padded with 2**31-1; "sink_gap" is the distance of the
+    last sink's squared norm to the first kept one).
     """
     q4 = np.shape(q)
     qa, ka, va = _as3(q), _as3(k), _as3(v)
@@ -168,10 +172,13 @@ def bounds(q, k, v, scale: float | None = None, centering: bool = False, dtype_s
     m_row = np.zeros((G, Sq), dtype=np.int32)
     shift = np.zeros((G, Sq))
     consts = np.zeros((4,), dtype=np.int32)
+    ns = int(sink_keys)
+    sink_idx = np.zeros((G, max(ns, 1)), dtype=np.int32)
+    sink_gap = np.zeros((G,))
     _load().fmo_bounds(_ptr(qa), _ptr(ka), _ptr(va), G, Sq, N, D, bq, float(scale), int(bool(centering)),
                        int(bool(dtype_safe)), int(vmax), _ptr(qmax_sq), _ptr(kbar), _ptr(kmax_sq),
                        _ptr(vmax_sq), _ptr(U), _ptr(m), _ptr(flag), _ptr(qkbar), _ptr(consts), int(bool(per_row)),
-                       _ptr(U_row), _ptr(m_row), _ptr(shift))
+                       _ptr(U_row), _ptr(m_row), _ptr(shift), ns, _ptr(sink_idx), _ptr(sink_gap))
     lead = tuple(q4[:-2]) if len(q4) == 4 else (G,)
     # distance of U to the nearest integer and to the gate: where fp32 device sums can
     # legitimately round across an integer (the tie band of the parity tests)
@@ -196,6 +203,8 @@ def bounds(q, k, v, scale: float | None = None, centering: bool = False, dtype_s
         "v_ok": bool(consts[3]),
         "alpha": float(scale) * float(np.log2(np.e)),
         "N": int(N),
+        "sink_idx": sink_idx[:, :ns].reshape(lead + (ns,)),
+        "sink_gap": sink_gap.reshape(lead),
     }
 
 

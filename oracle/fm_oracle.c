@@ -10,7 +10,7 @@
  *            (AWS Neuron docs), sections "What you should know before reading",
  *            "Picking a max that is safe without measuring it",
  *            "A static bound makes the ring reduction pure addition",
- *            "Accumulate, then normalize once".
+ *            "Accumulate, then normalize once", "Adapting this kernel" (key sinks).
  *   [PR477]  "feat(attention): fixed-m splash attention kernel with dynamic bounds and
  *            safety fallbacks" (maxdiffusion PR #477), Summary: "Dynamic eligibility
  *            bounding" equations for C(N), W(N), gate, m_i, U_i and the invariant;
@@ -28,7 +28,9 @@
  *                      for the OUTPUT is plain attention, with the textbook max
  *                      subtraction, over the full (concatenated) key sequence.
  *   fmo_constants   -- C(N), W(N), gate from [PR477] Summary.
- *   fmo_bounds      -- norms, key mean, U, m, flag, in the pages' order ([PR477]).
+ *   fmo_bounds      -- norms, key mean, U, m, flag, in the pages' order ([PR477]);
+ *                      optionally the key sinks left out of the key max ([NKI]
+ *                      "Adapting this kernel").
  *   fmo_fixed_m_emulate_f32 -- a sequential fp32 emulation of the fixed-m sum with
  *                      an ARBITRARY shift, flushing subnormal terms to zero.  It
  *                      exists only to show what goes wrong with a wrong gate or an
@@ -68,6 +70,12 @@ void fmo_constants(int64_t n_total, int64_t vmax, int *C, int *W, int *gate) {
   *W = w;
   /* floor division, correct for negative w too */
   *gate = (w >= 0) ? (w / 2) : -((-w + 1) / 2);
+}
+
+/* qsort comparator: descending doubles */
+static int fmo_cmp_desc(const void *a, const void *b) {
+  double x = *(const double *)a, y = *(const double *)b;
+  return (x < y) - (x > y);
 }
 
 int fmo_num_threads(void) {
@@ -147,13 +155,16 @@ void fmo_attention(const double *q, const double *k, const double *v, int64_t G,
  *   qkbar   [G, Sq] or NULL: alpha * q_i . kbar (the per-row centering term)
  *   consts  [4]       C, W, gate, v_ok
  *   U_row, m_row [G, Sq] or NULL: the per-row bound alpha*|q_i|*sqrt(kmax_sq) and its shift
- *   shift   [G, Sq] or NULL: m (per_row ? m_row : the row's Q-block m) + qkbar          */
+ *   shift   [G, Sq] or NULL: m (per_row ? m_row : the row's Q-block m) + qkbar
+ *   n_sink  : 0, or the number of loudest keys per problem left out of the key max
+ *   sink_idx [G, n_sink]: those keys' indices, ascending, padded with INT32_MAX
+ *   sink_gap [G] or NULL: n_sink-th largest squared key norm minus the (n_sink+1)-th  */
 void fmo_bounds(const double *q, const double *k, const double *v, int64_t G, int64_t Sq,
                 int64_t N, int64_t D, int64_t bq, double scale, int centering,
                 int dtype_safe, int64_t vmax, double *qmax_sq, double *kbar,
                 double *kmax_sq, double *vmax_sq, double *U, int32_t *m, uint8_t *flag,
                 double *qkbar, int32_t *consts, int per_row, double *U_row, int32_t *m_row,
-                double *shift) {
+                double *shift, int64_t n_sink, int32_t *sink_idx, double *sink_gap) {
   const double alpha = scale * FMO_LOG2E;
   int C, W, gate;
   fmo_constants(N, vmax, &C, &W, &gate);
@@ -181,14 +192,37 @@ void fmo_bounds(const double *q, const double *k, const double *v, int64_t G, in
     }
     /* max key norm, measured on the keys the kernel exponentiates */
     double km = 0.0;
+    double *knorm = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
     for (int64_t j = 0; j < N; j++) {
       double ss = 0.0;
       for (int64_t d = 0; d < D; d++) {
         double x = kg[j * D + d] - kb[d];
         ss += x * x;
       }
+      knorm[j] = ss;
       if (ss > km) km = ss;
     }
+    if (n_sink > 0) {
+      /* key sinks ("Kernel reference: ring_attention_const_max_fwd", section "Adapting this
+       * kernel": leave the few loudest keys out of the max reduction).  tau = the
+       * (n_sink+1)-th largest squared norm, counted with multiplicity (0 with fewer keys);
+       * the sinks are the keys strictly above tau, so at most n_sink of them, and the max
+       * over every other key is tau itself. */
+      double *sorted = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+      memcpy(sorted, knorm, sizeof(double) * (size_t)N);
+      qsort(sorted, (size_t)N, sizeof(double), fmo_cmp_desc);
+      double tau = (N > n_sink) ? sorted[n_sink] : 0.0;
+      int64_t t = 0;
+      for (int64_t j = 0; j < N; j++)
+        if (knorm[j] > tau) sink_idx[g * n_sink + t++] = (int32_t)j;
+      for (; t < n_sink; t++) sink_idx[g * n_sink + t] = INT32_MAX;
+      /* how far the n_sink-th largest norm sits above tau: where fp32 norms could pick
+       * another set (0 when they tie, +inf with no (n_sink+1)-th key) */
+      if (sink_gap) sink_gap[g] = (N > n_sink) ? sorted[n_sink - 1] - tau : INFINITY;
+      free(sorted);
+      km = tau;
+    }
+    free(knorm);
     kmax_sq[g] = km;
     /* per-row query norms -> per-block max */
     for (int64_t b = 0; b < nqb; b++) {

@@ -394,3 +394,100 @@ def test_emulator_closed_forms():
     em = oracle.fixed_m_emulate_f32(qq, k, v, mrow)
     exact = oracle.attention(qq[None], k[None], v[None])[0]
     assert np.max(np.abs(em["o"] - exact)) < 1e-5
+
+
+# ---------------------------------------------------------------- key sinks
+
+INT32_MAX = 2**31 - 1
+
+
+def _planted_keys(norms, D=4):
+    """Key j = norms[j] * (+/-) e_(j mod D): exactly the given norms, mean of small norm."""
+    k = np.zeros((len(norms), D))
+    for j, n in enumerate(norms):
+        k[j, j % D] = n if (j // D) % 2 == 0 else -n
+    return k
+
+
+def test_sinks_closed_form_selection():
+    """Planted norms: the n loudest keys are the sinks, the key max is the next norm down."""
+    norms = [1.0, 2.0, 300.0, 3.0, 100.0, 4.0, 200.0, 5.0]
+    k = _planted_keys(norms)[None]
+    q = np.ones((1, 3, 4))
+    v = np.zeros((1, 8, 4))
+    for n, sinks, kmax in [(1, [2], 200.0), (2, [2, 6], 100.0), (3, [2, 4, 6], 5.0),
+                           (5, [2, 4, 6, 7, 5], 3.0)]:
+        b = oracle.bounds(q, k, v, sink_keys=n)
+        assert list(b["sink_idx"][0]) == sorted(sinks), (n, b["sink_idx"])
+        assert b["kmax_sq"][0] == pytest.approx(kmax ** 2, rel=1e-12)
+        assert b["U"][0, 0] == pytest.approx(b["alpha"] * 2.0 * kmax, rel=1e-12)  # |q| = 2
+    b0 = oracle.bounds(q, k, v)
+    assert b0["kmax_sq"][0] == pytest.approx(300.0 ** 2, rel=1e-12) and b0["sink_idx"].shape == (1, 0)
+
+
+def test_sinks_ties_and_short_sequences():
+    """Keys tied with the first kept one are not sinks (the set is the keys strictly above
+    it); with fewer keys than sinks + 1 every nonzero key is a sink and the bound is 0."""
+    k = _planted_keys([7.0, 1.0, 7.0, 2.0])[None]
+    q, v = np.ones((1, 2, 4)), np.zeros((1, 4, 4))
+    b = oracle.bounds(q, k, v, sink_keys=1)
+    assert list(b["sink_idx"][0]) == [INT32_MAX]
+    assert b["kmax_sq"][0] == pytest.approx(49.0) and b["sink_gap"][0] == pytest.approx(0.0, abs=1e-12)
+    b = oracle.bounds(q, k, v, sink_keys=2)
+    assert list(b["sink_idx"][0]) == [0, 2] and b["kmax_sq"][0] == pytest.approx(4.0)
+    k2 = _planted_keys([3.0, 0.0])[None]
+    b = oracle.bounds(q, k2, np.zeros((1, 2, 4)), sink_keys=4)
+    assert list(b["sink_idx"][0]) == [0, INT32_MAX, INT32_MAX, INT32_MAX]
+    assert b["kmax_sq"][0] == 0.0 and b["U"][0, 0] == 0.0 and b["m"][0, 0] == -b["C"]
+    assert b["sink_gap"][0] == math.inf
+
+
+def test_sinks_use_the_centered_norms():
+    """With centering the loudness of a key is measured as |k - kbar|: keys along the mean
+    are quiet once it is removed."""
+    D, N = 4, 20
+    base = np.array([10.0, 0.0, 0.0, 0.0])
+    k = np.tile(base, (N, 1))
+    k[1] = np.array([11.0, 0.0, 0.0, 0.0])   # loudest raw (121), along the mean: quiet centered
+    k[4] = np.array([10.0, 3.0, 0.0, 0.0])   # 109 raw, loudest once the mean is removed
+    q, v = np.ones((1, 2, D)), np.zeros((1, N, D))
+    raw = oracle.bounds(q, k[None], v, sink_keys=1)
+    cen = oracle.bounds(q, k[None], v, sink_keys=1, centering=True)
+    assert list(raw["sink_idx"][0]) == [1]
+    assert list(cen["sink_idx"][0]) == [4]
+    d = k - k.mean(0)
+    assert cen["kmax_sq"][0] == pytest.approx(np.sort((d * d).sum(1))[-2], rel=1e-12)
+
+
+def test_sink_workload_needs_the_sinks_folded_exactly():
+    """The sinks workload: with its 4 planted sinks left out of the key max every tile is
+    eligible and every kept key stays in [-125, C] (T3), while a sink through the same shift
+    leaves the window and overflows fp32.  Folding the sinks back exactly (an online merge
+    of the kept keys' fixed-m sums with the sink terms) gives plain attention."""
+    import workloads
+    q, k, v = workloads.make_inputs("sinks", heads=[0], Sq=256, N=600)
+    b0 = oracle.bounds(q, k, v)
+    b = oracle.bounds(q, k, v, sink_keys=4)
+    assert not b0["flag"].any() and b["flag"].all()
+    sinks = list(b["sink_idx"][0, 0])
+    assert sinks == workloads.sink_positions(600)
+    qa, ka, va = q[0, 0].double().numpy(), k[0, 0].double().numpy(), v[0, 0].double().numpy()
+    keep = np.setdiff1d(np.arange(600), sinks)
+    z = b["alpha"] * qa @ ka.T
+    shift = b["shift"][0, 0][:, None]
+    e = z - shift
+    assert e[:, keep].min() >= -125 and e[:, keep].max() <= b["C"]
+    assert e[:, sinks].max() > 128  # 2^e is not an fp32 number
+    em_all = oracle.fixed_m_emulate_f32(qa, ka, va, b["shift"][0, 0])
+    assert em_all["n_overflow"].sum() > 0
+    em = oracle.fixed_m_emulate_f32(qa, ka[keep], va[keep], b["shift"][0, 0])
+    assert em["n_overflow"].sum() == 0
+    # online merge of the kept keys' (o, sum) at shift b_i with the sink terms
+    zs = z[:, sinks]
+    new = np.maximum(b["shift"][0, 0], zs.max(1))
+    sc = np.exp2(b["shift"][0, 0] - new)
+    ps = np.exp2(zs - new[:, None])
+    num = em["acc_o"].astype(np.float64) * sc[:, None] + ps @ va[sinks]
+    den = em["acc_sum"].astype(np.float64) * sc + ps.sum(1)
+    exact = oracle.attention(qa[None], ka[None], va[None])[0]
+    assert np.max(np.abs(num / den[:, None] - exact)) < 1e-5
