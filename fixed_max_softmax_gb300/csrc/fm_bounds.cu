@@ -159,8 +159,7 @@ __global__ void __launch_bounds__(kThreads)
     // Q-block: per-row |q|^2 and alpha * q.kbar
     const T *base = reinterpret_cast<const T *>(q.ptr) + b * q.sB + h * q.sH;
     const int64_t r0 = bx * kQRows, r1 = min(q.S, r0 + kQRows);
-#pragma unroll 4
-  for (int64_t r = r0 + warp; r < r1; r += kWarps) {
+    for (int64_t r = r0 + warp; r < r1; r += kWarps) {
       float x[EPL];
       load_row<T, EPL, CONTIG>(base + r * q.sS, q.sD, lane, x);
       float ss = 0.f, dk = 0.f;
@@ -181,8 +180,7 @@ __global__ void __launch_bounds__(kThreads)
     // K rows: |k - kbar|^2 (kbar = 0 when not centering)
     const T *base = reinterpret_cast<const T *>(k.ptr) + b * k.sB + h * k.sH;
     const int64_t r0 = (bx - nqb) * kKVRows, r1 = min(k.S, r0 + kKVRows);
-#pragma unroll 4
-  for (int64_t r = r0 + warp; r < r1; r += kWarps) {
+    for (int64_t r = r0 + warp; r < r1; r += kWarps) {
       float x[EPL];
       load_row<T, EPL, CONTIG>(base + r * k.sS, k.sD, lane, x);
       float ss = 0.f;
@@ -197,8 +195,7 @@ __global__ void __launch_bounds__(kThreads)
     // V rows: max element square
     const T *base = reinterpret_cast<const T *>(v.ptr) + b * v.sB + h * v.sH;
     const int64_t r0 = (bx - nqb - nkb) * kKVRows, r1 = min(v.S, r0 + kKVRows);
-#pragma unroll 4
-  for (int64_t r = r0 + warp; r < r1; r += kWarps) {
+    for (int64_t r = r0 + warp; r < r1; r += kWarps) {
       float x[EPL];
       load_row<T, EPL, CONTIG>(base + r * v.sS, v.sD, lane, x);
 #pragma unroll
