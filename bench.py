@@ -216,7 +216,7 @@ def run_ours(args, rank, world, local_rank):
     centering = w.centering[0] if args.centering == "auto" else args.centering == "on"
     q, k, v = workloads.make_inputs(w.name, device=dev, heads=range(H))
     fa = fm.FixedMAttention(w.B, H, w.Sq, w.N, w.D, dev, centering=centering, force_online=args.force_online,
-                            out_dtype=q.dtype)
+                            out_dtype=q.dtype, sink_keys=args.sink_keys)
     stream = torch.cuda.current_stream(dev)
     step_flops = w.flops(heads=w.B * H)
     dist = None
@@ -243,7 +243,10 @@ def run_ours(args, rank, world, local_rank):
                 ev.append(torch.cuda.Event(enable_timing=True))
                 ev[-1].record(stream)
 
-    launches_per_step = 5 + len(chunks)  # bounds: ksum, kmean, norms, finish, shift; chunks (normalise fused)
+    # bounds: ksum, kmean (centering only), norms, finish, shift; one launch per chunk with the normalise
+    # fused into the last; with key sinks the bounds add their selection and the step ends with
+    # the sinks' fold and a separate normalise
+    launches_per_step = (5 if centering else 3) + len(chunks) + (3 if args.sink_keys else 0)
     for _ in range(args.warmup):
         step()
     fm.fm_sync_status(stream)
@@ -363,7 +366,8 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": f"{w.name}: B={w.B} H={H} S_q=S_k={w.Sq} D={w.D} {w.dtype}, "
                                f"{len(chunks)} KV chunks of {chunks[0][1]}, "
                                f"virtual K-centering {'on' if centering else 'off'}"
-                               + (", every tile forced onto the online fallback" if args.force_online else ""),
+                               + (", every tile forced onto the online fallback" if args.force_online else "")
+                               + (f", {args.sink_keys} key sinks per head" if args.sink_keys else ""),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (774 MB per tensor), no flush",
                    "fixed_m_tile_fraction": eligible},
@@ -389,9 +393,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=256, help="query rows per reference step")
     ap.add_argument("--heads", type=int, default=None, help="first N heads only (profiling a smaller case)")
-    ap.add_argument("--workload", default=WORKLOAD, help="wan (default, the headline), h40_s4096, mix, adversarial")
+    ap.add_argument("--workload", default=WORKLOAD, help="wan (default, the headline), h40_s4096, mix, adversarial, sinks")
     ap.add_argument("--centering", choices=["auto", "on", "off"], default="auto")
     ap.add_argument("--force-online", action="store_true", help="run every tile on the online fallback")
+    ap.add_argument("--sink-keys", type=int, default=0, help="leave this many loudest keys per head out of the key max")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per chunk launch from an ncu capture of the current kernel")
     args = ap.parse_args()

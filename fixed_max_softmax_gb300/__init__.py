@@ -8,8 +8,8 @@ PyTorch provides device memory and streams and nothing else.
 
 Functions with the ABI's names (same arguments, torch tensors in place of pointers):
 ``fm_bounds_workspace_size``, ``fm_bounds``, ``fm_bounds_noalloc``, ``fm_attn_chunk``,
-``fm_attn_chunk_final``, ``fm_attn_chunks``, ``fm_finalize``, ``fm_finalize_lse``,
-``fm_sync_status``,
+``fm_attn_chunk_final``, ``fm_attn_chunks``, ``fm_fold_sinks``, ``fm_finalize``,
+``fm_finalize_lse``, ``fm_sync_status``,
 ``fm_probe_wait_timeout``,
 ``fm_last_error``, ``fm_version``.
 
@@ -38,8 +38,9 @@ ERROR_NAMES = {0: "FM_OK", 1: "FM_ERR_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_DTYPE"
                5: "FM_ERR_BOUNDS_MISMATCH", 6: "FM_ERR_CUDA", 7: "FM_ERR_TIMEOUT"}
 ABI_SYMBOLS = ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
                "fm_last_error", "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout",
-               "fm_attn_chunk_final", "fm_attn_chunks")
+               "fm_attn_chunk_final", "fm_attn_chunks", "fm_fold_sinks")
 FM_MAX_CHUNKS = 8
+FM_MAX_SINKS = 8
 FM_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 
@@ -57,19 +58,21 @@ class fm_tensor(ctypes.Structure):
 
 class fm_opts(ctypes.Structure):
     _fields_ = [("softmax_scale", ctypes.c_float), ("centering", ctypes.c_int32),
-                ("force_online", ctypes.c_int32), ("per_row", ctypes.c_int32)]
+                ("force_online", ctypes.c_int32), ("per_row", ctypes.c_int32), ("sink_keys", ctypes.c_int32)]
 
 
 class fm_bounds_out(ctypes.Structure):
     _fields_ = [("m", ctypes.c_void_p), ("flag", ctypes.c_void_p), ("qmax_sq", ctypes.c_void_p),
                 ("kmax_sq", ctypes.c_void_p), ("kbar", ctypes.c_void_p), ("qkbar", ctypes.c_void_p),
                 ("shift", ctypes.c_void_p), ("vmax_sq", ctypes.c_void_p),
+                ("sink_idx", ctypes.c_void_p), ("sink_k", ctypes.c_void_p), ("sink_v", ctypes.c_void_p),
                 ("B", ctypes.c_int64), ("H", ctypes.c_int64), ("Sq", ctypes.c_int64), ("D", ctypes.c_int64),
                 ("n_qblocks", ctypes.c_int64), ("N_total", ctypes.c_int64),
                 ("C", ctypes.c_int32), ("W", ctypes.c_int32), ("gate", ctypes.c_int32),
-                ("centered", ctypes.c_int32), ("per_row", ctypes.c_int32), ("alpha", ctypes.c_float),
-                ("dtype", ctypes.c_int32),
-                ("kv_seen", ctypes.c_int64), ("online_lock", ctypes.c_int32), ("magic", ctypes.c_uint32)]
+                ("centered", ctypes.c_int32), ("per_row", ctypes.c_int32), ("n_sink", ctypes.c_int32),
+                ("alpha", ctypes.c_float), ("dtype", ctypes.c_int32),
+                ("kv_seen", ctypes.c_int64), ("online_lock", ctypes.c_int32), ("sinks_folded", ctypes.c_int32),
+                ("magic", ctypes.c_uint32)]
 
 
 _lib = None
@@ -95,13 +98,14 @@ def load(path: str | None = None):
     lib.fm_probe_wait_timeout.argtypes = [ctypes.c_uint, P]
     lib.fm_attn_chunk_final.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_int, P, P, P]
     lib.fm_attn_chunks.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, P, ctypes.c_int, P, P, P]
+    lib.fm_fold_sinks.argtypes = [P, P, P, P, P, P, P]
     lib.fm_sync_status.argtypes = [P]
     lib.fm_last_error.restype = ctypes.c_char_p
     lib.fm_last_error.argtypes = []
     lib.fm_version.argtypes = []
     for name in ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
                  "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout",
-                 "fm_attn_chunk_final", "fm_attn_chunks"):
+                 "fm_attn_chunk_final", "fm_attn_chunks", "fm_fold_sinks"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -128,8 +132,9 @@ def tensor(t: torch.Tensor) -> fm_tensor:
 
 
 def opts(softmax_scale: float = 0.0, centering: bool = False, force_online: bool = False,
-         per_row: bool = False) -> fm_opts:
-    return fm_opts(float(softmax_scale), int(bool(centering)), int(bool(force_online)), int(bool(per_row)))
+         per_row: bool = False, sink_keys: int = 0) -> fm_opts:
+    return fm_opts(float(softmax_scale), int(bool(centering)), int(bool(force_online)), int(bool(per_row)),
+                   int(sink_keys))
 
 
 def _stream(stream):
@@ -178,12 +183,17 @@ class Bounds:
         self.qkbar = torch.zeros(B, H, max(Sq, 1), dtype=torch.float32, **kw)
         self.shift = torch.zeros(B, H, max(Sq, 1), dtype=torch.float32, **kw)
         self.vmax_sq = torch.zeros(1, dtype=torch.float32, **kw)
+        self.sink_idx = torch.zeros(B, H, FM_MAX_SINKS, dtype=torch.int32, **kw)
+        self.sink_k = torch.zeros(B, H, FM_MAX_SINKS, D, dtype=torch.float32, **kw)
+        self.sink_v = torch.zeros(B, H, FM_MAX_SINKS, D, dtype=torch.float32, **kw)
         self.out = fm_bounds_out()
         self.out.m, self.out.flag = self.m.data_ptr(), self.flag.data_ptr()
         self.out.qmax_sq, self.out.kmax_sq = self.qmax_sq.data_ptr(), self.kmax_sq.data_ptr()
         self.out.kbar, self.out.qkbar, self.out.vmax_sq = (self.kbar.data_ptr(), self.qkbar.data_ptr(),
                                                            self.vmax_sq.data_ptr())
         self.out.shift = self.shift.data_ptr()
+        self.out.sink_idx, self.out.sink_k, self.out.sink_v = (self.sink_idx.data_ptr(), self.sink_k.data_ptr(),
+                                                               self.sink_v.data_ptr())
 
 
 def fm_bounds(q, k_full, v_full, opt: fm_opts, bounds: Bounds, workspace: torch.Tensor | None, stream=None):
@@ -231,6 +241,14 @@ def fm_attn_chunks(q, k_chunks, v_chunks, bounds: Bounds, opt: fm_opts, acc_o, a
                                         _stream(stream)))
 
 
+def fm_fold_sinks(q, bounds: Bounds, opt: fm_opts, acc_o, acc_sum, acc_max, stream=None):
+    """Merge the key sinks set aside by fm_bounds back into the accumulators (after the last
+    chunk, before fm_finalize); a no-op without sinks."""
+    tq = tensor(q)
+    return _check(load().fm_fold_sinks(ctypes.byref(tq), ctypes.byref(bounds.out), ctypes.byref(opt), _ptr(acc_o),
+                                       _ptr(acc_sum), _ptr(acc_max), _stream(stream)))
+
+
 def fm_finalize(acc_o, acc_sum, o_out, stream=None):
     to = tensor(o_out)
     return _check(load().fm_finalize(_ptr(acc_o), _ptr(acc_sum), ctypes.byref(to), _stream(stream)))
@@ -259,13 +277,14 @@ class FixedMAttention:
     fm_attn_chunk_final (fold and normalise in one pass); fused_final=False uses a separate
     fm_finalize.  one_launch=True folds all chunks with fm_attn_chunks instead (one launch per
     FM_MAX_CHUNKS chunks, accumulators on chip across them).  with_lse=True also fills
-    `lse` [B, H, Sq] (natural log).
+    `lse` [B, H, Sq] (natural log).  sink_keys > 0 leaves that many of each head's loudest
+    keys out of the key max; they are folded back exactly before the normalise.
     """
 
     def __init__(self, B, H, Sq, N, D, device="cuda", centering=False, softmax_scale=0.0,
-                 force_online=False, out_dtype=torch.float32, per_row=False):
+                 force_online=False, out_dtype=torch.float32, per_row=False, sink_keys=0):
         self.shape = (B, H, Sq, N, D)
-        self.opt = opts(softmax_scale, centering, force_online, per_row)
+        self.opt = opts(softmax_scale, centering, force_online, per_row, sink_keys)
         self.bounds = Bounds(B, H, Sq, D, device)
         nbytes = fm_bounds_workspace_size(B, H, N, D)
         self.workspace = torch.empty(max(nbytes, 16) // 4 + 4, dtype=torch.float32, device=device)
@@ -297,6 +316,7 @@ class FixedMAttention:
                                     self.out, lse, stream)
                 return self.out
             fm_attn_chunk(q, kc, vc, self.bounds, self.opt, self.acc_o, self.acc_sum, self.acc_max, i > 0, stream)
+        fm_fold_sinks(q, self.bounds, self.opt, self.acc_o, self.acc_sum, self.acc_max, stream)
         if with_lse:
             fm_finalize_lse(self.acc_o, self.acc_sum, self.acc_max, self.out, self.lse, stream)
         else:
@@ -307,11 +327,11 @@ class FixedMAttention:
 
 
 def attention(q, k, v, chunks=None, centering=False, softmax_scale=0.0, force_online=False,
-              out_dtype=torch.float32, stream=None, per_row=False):
+              out_dtype=torch.float32, stream=None, per_row=False, sink_keys=0):
     """One-call fixed-m attention forward: returns o [B, H, Sq, D]."""
     B, H, Sq, D = q.shape
     fa = FixedMAttention(B, H, Sq, k.shape[2], D, q.device, centering, softmax_scale, force_online, out_dtype,
-                         per_row)
+                         per_row, sink_keys)
     return fa.forward(q, k, v, chunks, stream).clone()
 
 

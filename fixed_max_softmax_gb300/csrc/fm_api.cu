@@ -150,7 +150,7 @@ using namespace fm;
 
 extern "C" {
 
-int fm_version(void) { return (1 << 16) | 0; }
+int fm_version(void) { return (1 << 16) | 1; }
 
 const char *fm_last_error(void) { return t_err.c_str(); }
 
@@ -175,9 +175,16 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
     return fail(FM_ERR_ARG, "centering and per_row must be 0 or 1");
   const int centering = opts ? opts->centering : 0;
   const int per_row = opts ? opts->per_row : 0;
+  const int n_sink = opts ? opts->sink_keys : 0;
+  if (n_sink < 0 || n_sink > FM_MAX_SINKS) return fail(FM_ERR_ARG, "sink_keys = %d outside [0, %d]", n_sink, FM_MAX_SINKS);
   double alpha;
   if ((rc = make_alpha(opts, vq.D, &alpha))) return rc;
   const int64_t B = vq.B, H = vq.H, Sq = vq.S, D = vq.D, N = vk.S;
+  if (n_sink > 0 && B * H > 0 && (!out->sink_idx || !out->sink_k || !out->sink_v))
+    return fail(FM_ERR_ARG, "fm_bounds_out: sink_idx, sink_k and sink_v must be set when sink_keys > 0");
+  // the chunk kernels find a sink by its global key index in 32-bit arithmetic
+  if (n_sink > 0 && N > (int64_t)INT32_MAX - 256)
+    return fail(FM_ERR_UNSUPPORTED, "key sinks need N_total <= 2^31 - 256 (got %lld)", (long long)N);
   const int64_t nqb = ceil_div(Sq, FM_BLOCK_Q);
   // every non-empty device array must be given (torch hands out NULL for empty ones)
   if ((B * H * nqb > 0 && (!out->m || !out->flag || !out->qmax_sq)) ||
@@ -207,6 +214,8 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
   out->gate = gate;
   out->centered = centering;
   out->per_row = per_row;
+  out->n_sink = n_sink;
+  out->sinks_folded = 0;
   out->alpha = (float)alpha;
   out->dtype = vq.dtype;
   out->kv_seen = 0;
@@ -234,6 +243,10 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
   a.qkbar = out->qkbar;
   a.shift = out->shift;
   a.vmax_sq = out->vmax_sq;
+  a.n_sink = n_sink;
+  a.sink_idx = out->sink_idx;
+  a.sink_k = out->sink_k;
+  a.sink_v = out->sink_v;
   a.ws = workspace;
   a.ws_bytes = workspace_bytes;
   cudaError_t e = launch_bounds(a, reinterpret_cast<cudaStream_t>(stream));
@@ -302,6 +315,16 @@ int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_ten
     return fail(FM_ERR_BOUNDS_MISMATCH, "force_online must stay the same across the chunks of one call");
   if (accumulate && bounds->online_lock < 0)
     return fail(FM_ERR_BOUNDS_MISMATCH, "accumulate=1 before any accumulate=0 chunk for these bounds");
+  const int n_sink = opts ? opts->sink_keys : 0;
+  if (n_sink != bounds->n_sink)
+    return fail(FM_ERR_BOUNDS_MISMATCH,
+                "bounds were built with sink_keys=%d, the call has sink_keys=%d: the chunks must skip exactly the "
+                "keys left out of the key max",
+                bounds->n_sink, n_sink);
+  if (accumulate && bounds->sinks_folded)
+    return fail(FM_ERR_BOUNDS_MISMATCH,
+                "the key sinks were already folded in: no chunk may be added after fm_fold_sinks");
+  if (n_sink > 0 && vq.B * vq.H > 0 && !bounds->sink_idx) return fail(FM_ERR_ARG, "bounds sink_idx is NULL");
   const int64_t rows = vq.B * vq.H * vq.S;
   if (rows > 0 && (!acc_o || !acc_sum || !acc_max)) return fail(FM_ERR_ARG, "accumulator pointer is NULL");
   if (rows > 0 && (!bounds->flag || !bounds->shift)) return fail(FM_ERR_ARG, "bounds flag/shift pointer is NULL");
@@ -329,6 +352,10 @@ int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_ten
   a.acc_max = acc_max;
   a.err = err;
   a.timeout_ns = wait_timeout_ns();
+  // key sinks: the chunks skip them by global key index; the first chunk of this call
+  // starts where the keys folded so far end
+  a.sinks = n_sink > 0 ? bounds->sink_idx : nullptr;
+  a.key0 = accumulate ? bounds->kv_seen : 0;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   bool finalize_separately = o_out != nullptr;
@@ -356,7 +383,8 @@ int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_ten
       a.ks = ks;
       a.vs = vs;
       if (chunk_tc_supported(a)) {
-        if (o_out && chunk_tc_final_supported(a, vo)) {  // the kernel normalises and writes o itself
+        // the kernel normalises and writes o itself, unless key sinks must be folded first
+        if (o_out && n_sink == 0 && chunk_tc_final_supported(a, vo)) {
           a.out = &vo;
           a.lse = lse;
           finalize_separately = false;
@@ -377,16 +405,23 @@ int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_ten
         a.v = vs[c];
         a.accumulate = c == 0 ? accumulate : 1;
         e = launch_chunk_simt(a, st);
+        a.key0 += ks[c].S;
       }
     }
   }
   if (e != cudaSuccess) return cuda_fail(e, "fm_attn_chunk launch");
+  if (o_out && n_sink > 0 && rows > 0) {  // the last chunk is in: merge the sinks back, then normalise
+    e = launch_fold_sinks(vq, (float)alpha, bounds->sink_idx, bounds->sink_k, bounds->sink_v, acc_o, acc_sum,
+                          acc_max, st);
+    if (e != cudaSuccess) return cuda_fail(e, "key-sink fold launch");
+  }
   if (finalize_separately && rows > 0) {
     e = lse ? launch_finalize_lse(acc_o, acc_sum, acc_max, vo, lse, st) : launch_finalize(acc_o, acc_sum, vo, st);
     if (e != cudaSuccess) return cuda_fail(e, "fm_attn_chunk_final finalize launch");
   }
   bounds->kv_seen = seen;
   bounds->online_lock = force_online;
+  bounds->sinks_folded = (o_out && n_sink > 0) ? 1 : 0;
   return FM_OK;
 }
 }  // namespace
@@ -442,6 +477,40 @@ int fm_finalize_lse(const float *acc_o, const float *acc_sum, const float *acc_m
   if (reinterpret_cast<uintptr_t>(acc_o) % 16) return fail(FM_ERR_ARG, "acc_o must be 16-byte aligned");
   cudaError_t e = launch_finalize_lse(acc_o, acc_sum, acc_max, vo, lse, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "fm_finalize_lse launch");
+  return FM_OK;
+}
+
+int fm_fold_sinks(const fm_tensor *q, fm_bounds_out *bounds, const fm_opts *opts, float *acc_o, float *acc_sum,
+                  float *acc_max, fm_stream_t stream) {
+  t_err.clear();
+  View vq;
+  int rc;
+  if ((rc = to_view(q, "q", &vq))) return rc;
+  if (!bounds) return fail(FM_ERR_ARG, "bounds is NULL");
+  if (bounds->magic != FM_BOUNDS_MAGIC)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "bounds were not produced by fm_bounds (magic 0x%08x)", bounds->magic);
+  if (bounds->B != vq.B || bounds->H != vq.H || bounds->Sq != vq.S || bounds->D != vq.D || bounds->dtype != vq.dtype)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "bounds do not belong to these queries");
+  const int n_sink = opts ? opts->sink_keys : 0;
+  if (n_sink != bounds->n_sink)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "bounds were built with sink_keys=%d, the call has sink_keys=%d",
+                bounds->n_sink, n_sink);
+  double alpha;
+  if ((rc = make_alpha(opts, vq.D, &alpha))) return rc;
+  if ((float)alpha != bounds->alpha)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "softmax scale differs from the one the bounds were computed with");
+  if (bounds->online_lock < 0) return fail(FM_ERR_BOUNDS_MISMATCH, "no chunk has been folded in yet");
+  if (bounds->sinks_folded) return fail(FM_ERR_BOUNDS_MISMATCH, "the key sinks were already folded in");
+  if (n_sink == 0) return FM_OK;
+  const int64_t rows = vq.B * vq.H * vq.S;
+  if (rows > 0 && (!acc_o || !acc_sum || !acc_max)) return fail(FM_ERR_ARG, "accumulator pointer is NULL");
+  if (rows > 0 && (!bounds->sink_idx || !bounds->sink_k || !bounds->sink_v))
+    return fail(FM_ERR_ARG, "bounds sink arrays are NULL");
+  if (reinterpret_cast<uintptr_t>(acc_o) % 16) return fail(FM_ERR_ARG, "acc_o must be 16-byte aligned");
+  cudaError_t e = launch_fold_sinks(vq, (float)alpha, bounds->sink_idx, bounds->sink_k, bounds->sink_v, acc_o,
+                                    acc_sum, acc_max, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fm_fold_sinks launch");
+  bounds->sinks_folded = 1;
   return FM_OK;
 }
 

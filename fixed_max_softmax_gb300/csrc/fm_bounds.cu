@@ -15,11 +15,15 @@
 //   2. kmean   (centering only) ordered sum of the P partials / N          -> kbar
 //   3. main    one grid over Q-blocks, K row-blocks and V row-blocks: row norms via warp
 //              shuffles; per-block maxima -> qmax_sq (Q) and the workspace (K, V);
-//              qkbar per row
+//              qkbar per row; with key sinks, each K block's n_sink + 1 loudest keys
+//   3b. sinks  (key sinks only) per head: the n_sink + 1 loudest keys over the blocks'
+//              candidates; the sinks and the max over the other keys ("Kernel reference:
+//              ring_attention_const_max_fwd", section "Adapting this kernel")
 //   4. finish  per head: key max, global V max, U, m, flag
 //   5. shift   per row: b_i = m_i + alpha*q_i.kbar (m_i per row or per Q-block)
 // Bytes: Q + K + V once each, plus K once more for the mean when centering.
 #include <cuda_bf16.h>
+#include <limits.h>
 #include <math.h>
 
 #include "fm_internal.h"
@@ -42,9 +46,16 @@ inline int64_t num_partials(int64_t N) {
   return p < 1 ? 1 : (p > kMaxPartials ? kMaxPartials : p);
 }
 
+// A key-sink candidate: squared norm and global key index (v = -1: no candidate).
+struct SinkCand {
+  float v;
+  int32_t idx;
+};
+constexpr int kCandPerBlock = FM_MAX_SINKS + 1;  // each K block keeps its top n_sink + 1
+
 struct WsLayout {
   int64_t P, nkb, nvb;
-  size_t off_part, off_kb, off_vb, total;
+  size_t off_part, off_kb, off_vb, off_cand, total;
 };
 
 WsLayout ws_layout(int64_t B, int64_t H, int64_t N, int64_t D) {
@@ -55,7 +66,9 @@ WsLayout ws_layout(int64_t B, int64_t H, int64_t N, int64_t D) {
   w.off_part = 0;
   w.off_kb = w.off_part + sizeof(float) * (size_t)(B * H * w.P * D);
   w.off_vb = w.off_kb + sizeof(float) * (size_t)(B * H * w.nkb);
-  w.total = w.off_vb + sizeof(float) * (size_t)(B * H * w.nvb);
+  w.off_cand = w.off_vb + sizeof(float) * (size_t)(B * H * w.nvb);
+  w.off_cand = (w.off_cand + 15) & ~(size_t)15;
+  w.total = w.off_cand + sizeof(SinkCand) * (size_t)(B * H * w.nkb * kCandPerBlock);
   w.total = (w.total + 255) & ~(size_t)255;
   return w;
 }
@@ -97,6 +110,26 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+// Key-sink order: louder first, the lower index first among equal norms.
+__device__ __forceinline__ bool sink_before(float v, int32_t i, float bv, int32_t bi) {
+  return v > bv || (v == bv && i < bi);
+}
+// (v, i) comes after the previous pick (pv, pi) in that order.
+__device__ __forceinline__ bool sink_after(float v, int32_t i, float pv, int32_t pi) {
+  return v < pv || (v == pv && i > pi);
+}
+__device__ __forceinline__ void warp_best_sink(float &bv, int32_t &bi) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (sink_before(ov, oi, bv, bi)) {
+      bv = ov;
+      bi = oi;
+    }
+  }
 }
 
 // 1. Partial key sums: CTA (p, h, b) sums rows [p*len, (p+1)*len) of head (b, h).
@@ -144,12 +177,14 @@ __global__ void kmean_kernel(const float *part, int64_t H, int64_t P, int D, int
 template <typename T, int EPL, bool CONTIG>
 __global__ void __launch_bounds__(kThreads)
     norms_kernel(View q, View k, View v, int64_t nqb, int64_t nkb, int centering, float alpha,
-                 const float *kbar, float *qmax_sq, float *qkbar, float *qsq, float *kblk, float *vblk) {
+                 const float *kbar, float *qmax_sq, float *qkbar, float *qsq, float *kblk, float *vblk,
+                 int n_sink, SinkCand *cand) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t b = blockIdx.z, h = blockIdx.y, bx = blockIdx.x;
   const int64_t bh = b * q.H + h;
   const int D = 32 * EPL;
   __shared__ float wmax[kWarps];
+  __shared__ float knorm[kKVRows];  // key blocks with sinks: each row's squared norm
   float kb[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) kb[e] = centering ? kbar[bh * D + lane * EPL + e] : 0.f;
@@ -189,7 +224,9 @@ __global__ void __launch_bounds__(kThreads)
         float c = x[e] - kb[e];
         ss = fmaf(c, c, ss);
       }
-      best = fmaxf(best, warp_sum(ss));
+      ss = warp_sum(ss);
+      best = fmaxf(best, ss);
+      if (n_sink > 0 && lane == 0) knorm[r - r0] = ss;
     }
   } else {
     // V rows: max element square
@@ -213,13 +250,128 @@ __global__ void __launch_bounds__(kThreads)
     else if (bx < nqb + nkb) kblk[bh * nkb + (bx - nqb)] = mx;
     else vblk[bh * nkb + (bx - nqb - nkb)] = mx;
   }
+  if (n_sink > 0 && bx >= nqb && bx < nqb + nkb && warp == 0) {
+    // this block's n_sink + 1 loudest keys, in sink order (its rows' norms are in knorm,
+    // written before the barrier above)
+    const int64_t r0 = (bx - nqb) * kKVRows;
+    const int cnt = (int)min((int64_t)kKVRows, k.S - r0);
+    SinkCand *out = cand + (bh * nkb + (bx - nqb)) * kCandPerBlock;
+    float pv = INFINITY;
+    int32_t pi = -1;
+    for (int t = 0; t <= n_sink; ++t) {
+      float bv = -1.f;
+      int32_t bi = INT_MAX;
+      for (int e = lane; e < cnt; e += 32) {
+        const float v = knorm[e];
+        const int32_t i = (int32_t)(r0 + e);
+        if (sink_after(v, i, pv, pi) && sink_before(v, i, bv, bi)) {
+          bv = v;
+          bi = i;
+        }
+      }
+      warp_best_sink(bv, bi);
+      if (lane == 0) out[t] = SinkCand{bv, bi};
+      pv = bv;
+      pi = bi;
+    }
+  }
+}
+
+// 3b. Key sinks of head (b, h): the n_sink + 1 loudest keys over the blocks' candidates.
+// tau = the (n_sink+1)-th norm (0 if there is none); the sinks are the picks strictly above
+// tau, so the largest norm of every other key is tau.  Writes sink_idx (ascending, INT32_MAX
+// pads), kmax_sq = tau, and the sinks' raw key and value rows.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    sink_select_kernel(View k, View v, int64_t nkb, int n_sink, const SinkCand *cand, int32_t *sink_idx,
+                       float *sink_k, float *sink_v, float *kmax_sq) {
+  const int64_t b = blockIdx.y, h = blockIdx.x;
+  const int64_t bh = b * k.H + h;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const SinkCand *c = cand + bh * nkb * kCandPerBlock;
+  const int64_t M = nkb * (n_sink + 1);
+  __shared__ float wv[kWarps];
+  __shared__ int32_t wi[kWarps];
+  __shared__ float pick_v[FM_MAX_SINKS + 1];
+  __shared__ int32_t pick_i[FM_MAX_SINKS + 1];
+  __shared__ int32_t list[FM_MAX_SINKS];
+  float pv = INFINITY;
+  int32_t pi = -1;
+  for (int t = 0; t <= n_sink; ++t) {
+    float bv = -1.f;
+    int32_t bi = INT_MAX;
+    for (int64_t e = threadIdx.x; e < M; e += kThreads) {
+      const SinkCand x = c[(e / (n_sink + 1)) * kCandPerBlock + e % (n_sink + 1)];
+      if (x.v >= 0.f && sink_after(x.v, x.idx, pv, pi) && sink_before(x.v, x.idx, bv, bi)) {
+        bv = x.v;
+        bi = x.idx;
+      }
+    }
+    warp_best_sink(bv, bi);
+    if (lane == 0) {
+      wv[warp] = bv;
+      wi[warp] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float fv = wv[0];
+      int32_t fi = wi[0];
+      for (int w = 1; w < kWarps; ++w)
+        if (sink_before(wv[w], wi[w], fv, fi)) {
+          fv = wv[w];
+          fi = wi[w];
+        }
+      pick_v[t] = fv;
+      pick_i[t] = fi;
+    }
+    __syncthreads();
+    pv = pick_v[t];
+    pi = pick_i[t];
+  }
+  if (threadIdx.x == 0) {
+    const float tau = pick_v[n_sink] >= 0.f ? pick_v[n_sink] : 0.f;
+    int n = 0;
+    for (int t = 0; t < n_sink; ++t)
+      if (pick_v[t] >= 0.f && pick_v[t] > tau) list[n++] = pick_i[t];
+    for (int i = 1; i < n; ++i)  // ascending key order
+      for (int j = i; j > 0 && list[j - 1] > list[j]; --j) {
+        const int32_t x = list[j];
+        list[j] = list[j - 1];
+        list[j - 1] = x;
+      }
+    for (int t = n; t < FM_MAX_SINKS; ++t) list[t] = INT_MAX;
+    for (int t = 0; t < FM_MAX_SINKS; ++t) sink_idx[bh * FM_MAX_SINKS + t] = list[t];
+    kmax_sq[bh] = tau;
+  }
+  __syncthreads();
+  const int D = (int)k.D;
+  const T *kp = reinterpret_cast<const T *>(k.ptr) + b * k.sB + h * k.sH;
+  const T *vp = reinterpret_cast<const T *>(v.ptr) + b * v.sB + h * v.sH;
+  for (int e = threadIdx.x; e < FM_MAX_SINKS * D; e += kThreads) {
+    const int slot = e / D, d = e % D;
+    const int32_t idx = list[slot];
+    float kx = 0.f, vx = 0.f;
+    if (idx != INT_MAX) {
+      const T a = kp[(int64_t)idx * k.sS + (int64_t)d * k.sD];
+      const T w = vp[(int64_t)idx * v.sS + (int64_t)d * v.sD];
+      if constexpr (sizeof(T) == 2) {
+        kx = __bfloat162float(a);
+        vx = __bfloat162float(w);
+      } else {
+        kx = (float)a;
+        vx = (float)w;
+      }
+    }
+    sink_k[(bh * FM_MAX_SINKS + slot) * D + d] = kx;
+    sink_v[(bh * FM_MAX_SINKS + slot) * D + d] = vx;
+  }
 }
 
 // 4. Per head: key max, global V max, then U, m, flag for every Q-block.
 __global__ void __launch_bounds__(kThreads)
     finish_kernel(int64_t H, int64_t nqb, int64_t nkb, int64_t n_heads_total, const float *kblk,
                   const float *vblk, double alpha, int C, int gate, const float *qmax_sq,
-                  float *kmax_sq, float *vmax_sq, int32_t *m, uint8_t *flag) {
+                  float *kmax_sq, float *vmax_sq, int32_t *m, uint8_t *flag, int kmax_given) {
   const int64_t bh = blockIdx.y * H + blockIdx.x;
   __shared__ float red[2][kWarps];
   float km = 0.f, vm = 0.f;
@@ -233,6 +385,8 @@ __global__ void __launch_bounds__(kThreads)
   km = 0.f; vm = 0.f;
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) { km = fmaxf(km, red[0][w]); vm = fmaxf(vm, red[1][w]); }
+  if (kmax_given) km = kmax_sq[bh];  // the key sinks' pass left the max over the other keys
+  __syncthreads();
   if (threadIdx.x == 0) {
     kmax_sq[bh] = km;
     if (bh == 0) vmax_sq[0] = vm;
@@ -272,6 +426,7 @@ cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st
   float *part = reinterpret_cast<float *>(ws + w.off_part);
   float *kblk = reinterpret_cast<float *>(ws + w.off_kb);
   float *vblk = reinterpret_cast<float *>(ws + w.off_vb);
+  SinkCand *cand = reinterpret_cast<SinkCand *>(ws + w.off_cand);
   const int D = (int)a.q.D;
   if (a.centering && N > 0) {
     ksum_kernel<T, EPL, CONTIG><<<dim3((unsigned)w.P, (unsigned)H, (unsigned)B), kThreads, 0, st>>>(a.k, w.P, part);
@@ -283,10 +438,16 @@ cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st
   const int64_t nx = a.nqb + 2 * w.nkb;
   if (nx > 0) {
     norms_kernel<T, EPL, CONTIG><<<dim3((unsigned)nx, (unsigned)H, (unsigned)B), kThreads, 0, st>>>(
-        a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk);
+        a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk,
+        a.n_sink, cand);
+  }
+  if (a.n_sink > 0) {
+    sink_select_kernel<T><<<dim3((unsigned)H, (unsigned)B), kThreads, 0, st>>>(
+        a.k, a.v, w.nkb, a.n_sink, cand, a.sink_idx, a.sink_k, a.sink_v, a.kmax_sq);
   }
   finish_kernel<<<dim3((unsigned)H, (unsigned)B), kThreads, 0, st>>>(
-      H, a.nqb, w.nkb, B * H, kblk, vblk, a.alpha, a.C, a.gate, a.qmax_sq, a.kmax_sq, a.vmax_sq, a.m, a.flag);
+      H, a.nqb, w.nkb, B * H, kblk, vblk, a.alpha, a.C, a.gate, a.qmax_sq, a.kmax_sq, a.vmax_sq, a.m, a.flag,
+      a.n_sink > 0);
   if (a.q.S > 0) {
     shift_kernel<<<dim3((unsigned)ceil_div(a.q.S, kThreads), (unsigned)H, (unsigned)B), kThreads, 0, st>>>(
         H, a.q.S, a.nqb, a.per_row, a.alpha, a.C, a.kmax_sq, a.m, a.qkbar, a.shift);

@@ -13,7 +13,9 @@
 //       Fallback": standard online-softmax accumulation across the chunks).
 // One CTA = 64 query rows of one (batch, head); each row is split over D/32 threads that
 // each own 32 dimensions of q and of the output; 32-key tiles of K and V are staged in
-// shared memory as fp32.
+// shared memory as fp32.  Key sinks (the loudest keys the bounds pass set aside, "Kernel
+// reference: ring_attention_const_max_fwd", section "Adapting this kernel") add nothing
+// here: a per-tile bit mask drops them along with the keys past the chunk's end.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -38,6 +40,7 @@ __global__ void __launch_bounds__(kRows *(D / kDimsPerThread))
   constexpr int NT = kRows * TPR;
   __shared__ float Ks[kKeys][D];
   __shared__ float Vs[kKeys][D];
+  __shared__ unsigned keep_bits;  // bit j: key j of the tile counts (in range, not a sink)
 
   const int tid = threadIdx.x;
   const int lr = tid / TPR;  // local row
@@ -76,7 +79,20 @@ __global__ void __launch_bounds__(kRows *(D / kDimsPerThread))
       Ks[j][d] = kx;
       Vs[j][d] = vx;
     }
+    if (tid == 0) {
+      unsigned kb = nvalid >= kKeys ? 0xffffffffu : ((1u << nvalid) - 1u);
+      if (a.sinks) {
+        const int64_t g0 = a.key0 + j0;
+        const int32_t *sk = a.sinks + bh * FM_MAX_SINKS;
+        for (int t = 0; t < FM_MAX_SINKS; ++t) {
+          const int64_t g = sk[t];
+          if (g >= g0 && g < g0 + nvalid) kb &= ~(1u << (int)(g - g0));
+        }
+      }
+      keep_bits = kb;
+    }
     __syncthreads();
+    const unsigned keep = keep_bits;
     float s[kKeys];
 #pragma unroll
     for (int j = 0; j < kKeys; ++j) {
@@ -92,7 +108,7 @@ __global__ void __launch_bounds__(kRows *(D / kDimsPerThread))
       float mx = -INFINITY;
 #pragma unroll
       for (int j = 0; j < kKeys; ++j)
-        if (j < nvalid) mx = fmaxf(mx, s[j] * a.alpha);
+        if ((keep >> j) & 1u) mx = fmaxf(mx, s[j] * a.alpha);
       if (mx > run) {
         const float sc = exp2f(run - mx);  // 0 when run = -inf
         l *= sc;
@@ -104,7 +120,7 @@ __global__ void __launch_bounds__(kRows *(D / kDimsPerThread))
     }
 #pragma unroll
     for (int j = 0; j < kKeys; ++j) {
-      const float p = (j < nvalid) ? exp2f(fmaf(s[j], a.alpha, -shift)) : 0.f;
+      const float p = ((keep >> j) & 1u) ? exp2f(fmaf(s[j], a.alpha, -shift)) : 0.f;
       l += p;
 #pragma unroll
       for (int d = 0; d < kDimsPerThread; ++d) ov[d] = fmaf(p, Vs[j][part * kDimsPerThread + d], ov[d]);

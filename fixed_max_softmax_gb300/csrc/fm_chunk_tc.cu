@@ -35,6 +35,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+#include <limits.h>
 #include <math.h>
 
 #include <mutex>
@@ -68,7 +69,8 @@ constexpr int kBarDrain = kBarODone + 2;
 constexpr int kNumBars = kBarDrain + 1;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
-constexpr int kSmemUsed = kOffAbort + 8;
+constexpr int kOffSinks = kOffAbort + 8;  // the head's key sinks (FM_MAX_SINKS int32)
+constexpr int kSmemUsed = kOffSinks + 4 * FM_MAX_SINKS;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5 = 1),
@@ -320,6 +322,10 @@ struct TcParams {
   int out_bf16;
   int64_t osB, osH, osS;
   float *lse;
+  // key sinks to skip: [B,H,FM_MAX_SINKS] ascending global key indices (INT_MAX pads), or
+  // nullptr; key0[c] is the global index of chunk c's first key
+  const int32_t *sinks;
+  int key0[kMaxChunks];
 };
 
 // p = 2^(alpha*s - bias) for 32 scores of one full chunk, two at a time with fp32x2 FMA and
@@ -335,6 +341,56 @@ __device__ __forceinline__ void exp_chunk_full(const uint32_t (&s)[32], uint64_t
     if (e & 1) acc1 = f2_add(acc1, pp); else acc0 = f2_add(acc0, pp);
     pk[e] = pack_bf16(p0, p1);
   }
+}
+
+// The smallest key sink of the head's list (at shared-memory address `ssk`: ascending
+// int32, INT_MAX pads) above `g`, or INT_MAX.
+__device__ __forceinline__ int sink_after_key(uint32_t ssk, int g) {
+  int n = INT_MAX;
+#pragma unroll
+  for (int t = 0; t < FM_MAX_SINKS; ++t) {
+    int x;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x) : "r"(ssk + 4u * t) : "memory");
+    if (x > g) n = min(n, x);
+  }
+  return n;
+}
+
+// Which of a tile's 128 key columns count: the first nvalid (the rest lie past the chunk's
+// end) minus the key sinks whose global index falls in the tile.  `next_sink` is the
+// smallest sink index not yet passed (INT_MAX when there is none).
+__device__ __forceinline__ uint32_t first_bits(int n) {
+  return n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+}
+// Write -inf over the scores of those columns in TMEM, so that the softmax that follows
+// gives them p = 2^-inf = 0 (and leaves them out of the online row max) with no masks of
+// its own.  Only for the rare tiles that have such columns; warp-uniform, like every
+// tcgen05.ld/st (all rows of a tile share its key columns).
+__device__ __noinline__ void mask_tile(uint32_t tS, int nvalid, int g0, uint32_t ssk, int &next_sink) {
+  uint32_t k0 = first_bits(nvalid), k1 = first_bits(nvalid - 32), k2 = first_bits(nvalid - 64),
+           k3 = first_bits(nvalid - 96);
+  while (next_sink < g0 + nvalid) {
+    const int col = next_sink - g0;
+    const uint32_t bit = ~(1u << (col & 31));
+    const int w = col >> 5;
+    k0 &= w == 0 ? bit : 0xffffffffu;
+    k1 &= w == 1 ? bit : 0xffffffffu;
+    k2 &= w == 2 ? bit : 0xffffffffu;
+    k3 &= w == 3 ? bit : 0xffffffffu;
+    next_sink = sink_after_key(ssk, next_sink);
+  }
+  const uint32_t keep[4] = {k0, k1, k2, k3};
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    if (keep[c] == 0xffffffffu) continue;
+    uint32_t sc[32];
+    tmem_ld32(tS + 32 * c, sc);
+#pragma unroll
+    for (int e = 0; e < 32; ++e)
+      if (!((keep[c] >> e) & 1u)) sc[e] = 0xff800000u;  // -inf
+    tmem_st32(tS + 32 * c, sc);
+  }
+  tmem_st_wait();
 }
 
 // The same for the chunk holding the ragged end of the keys: columns >= nvalid give 0.
@@ -353,54 +409,36 @@ __device__ __forceinline__ void exp_chunk_masked(const uint32_t (&s)[32], int co
 
 // Fixed-m softmax of one 128x128 S tile for this thread's row; P overwrites S.  The four
 // 32-column TMEM loads are double-buffered: chunk c+1 is in flight while chunk c is
-// exponentiated.
-__device__ __forceinline__ void softmax_fixed_tile(uint32_t tS, int nvalid, float alpha, float nbias,
-                                                   float (&l)[4]) {
+// exponentiated.  Key columns to leave out hold -inf (mask_tile) and give p = 0.
+__device__ __forceinline__ void softmax_fixed_tile(uint32_t tS, float alpha, float nbias, float (&l)[4]) {
   uint32_t sa[32], sb[32];
   uint32_t pk[16];
   tmem_ld32_async(tS, sa);
   tmem_ld_wait(sa);
-  if (nvalid >= kBK) {
-    const uint64_t a2 = f2_pack(__float_as_uint(alpha), __float_as_uint(alpha));
-    const uint64_t nb2 = f2_pack(__float_as_uint(nbias), __float_as_uint(nbias));
-    uint64_t acc0 = 0, acc1 = 0;  // +0.0f pairs
-    tmem_ld32_async(tS + 32, sb);
-    exp_chunk_full(sa, a2, nb2, acc0, acc1, pk);
-    tmem_st16(tS + 0, pk);  // P columns [16c, 16c+16) lie in S columns already read
-    tmem_ld_wait(sb);
-    tmem_ld32_async(tS + 64, sa);
-    exp_chunk_full(sb, a2, nb2, acc0, acc1, pk);
-    tmem_st16(tS + 16, pk);
-    tmem_ld_wait(sa);
-    tmem_ld32_async(tS + 96, sb);
-    exp_chunk_full(sa, a2, nb2, acc0, acc1, pk);
-    tmem_st16(tS + 32, pk);
-    tmem_ld_wait(sb);
-    exp_chunk_full(sb, a2, nb2, acc0, acc1, pk);
-    tmem_st16(tS + 48, pk);
-    float x0, x1, y0, y1;
-    f2_unpack(acc0, x0, x1);
-    f2_unpack(acc1, y0, y1);
-    l[0] += x0;
-    l[1] += x1;
-    l[2] += y0;
-    l[3] += y1;
-  } else {
-    tmem_ld32_async(tS + 32, sb);
-    exp_chunk_masked(sa, 0, nvalid, alpha, nbias, l, pk);
-    tmem_st16(tS + 0, pk);
-    tmem_ld_wait(sb);
-    tmem_ld32_async(tS + 64, sa);
-    exp_chunk_masked(sb, 32, nvalid, alpha, nbias, l, pk);
-    tmem_st16(tS + 16, pk);
-    tmem_ld_wait(sa);
-    tmem_ld32_async(tS + 96, sb);
-    exp_chunk_masked(sa, 64, nvalid, alpha, nbias, l, pk);
-    tmem_st16(tS + 32, pk);
-    tmem_ld_wait(sb);
-    exp_chunk_masked(sb, 96, nvalid, alpha, nbias, l, pk);
-    tmem_st16(tS + 48, pk);
-  }
+  const uint64_t a2 = f2_pack(__float_as_uint(alpha), __float_as_uint(alpha));
+  const uint64_t nb2 = f2_pack(__float_as_uint(nbias), __float_as_uint(nbias));
+  uint64_t acc0 = 0, acc1 = 0;  // +0.0f pairs
+  tmem_ld32_async(tS + 32, sb);
+  exp_chunk_full(sa, a2, nb2, acc0, acc1, pk);
+  tmem_st16(tS + 0, pk);  // P columns [16c, 16c+16) lie in S columns already read
+  tmem_ld_wait(sb);
+  tmem_ld32_async(tS + 64, sa);
+  exp_chunk_full(sb, a2, nb2, acc0, acc1, pk);
+  tmem_st16(tS + 16, pk);
+  tmem_ld_wait(sa);
+  tmem_ld32_async(tS + 96, sb);
+  exp_chunk_full(sa, a2, nb2, acc0, acc1, pk);
+  tmem_st16(tS + 32, pk);
+  tmem_ld_wait(sb);
+  exp_chunk_full(sb, a2, nb2, acc0, acc1, pk);
+  tmem_st16(tS + 48, pk);
+  float x0, x1, y0, y1;
+  f2_unpack(acc0, x0, x1);
+  f2_unpack(acc1, y0, y1);
+  l[0] += x0;
+  l[1] += x1;
+  l[2] += y0;
+  l[3] += y1;
 }
 
 __device__ __forceinline__ float max32(const uint32_t (&s)[32], int col0, int nvalid, float mx) {
@@ -415,7 +453,8 @@ __device__ __forceinline__ float max32(const uint32_t (&s)[32], int col0, int nv
 // grows by more than 2^8, or on the first tile); p = 2^(alpha*s - run) goes back over S as
 // bf16 P; the row sum is rescaled before the new terms are added, and O in TMEM after P is
 // out.  The rescale decision is per row but tcgen05.ld/st are warp-collective, so the warp
-// rescales when any of its rows needs it and the other rows use a scale of 1.
+// rescales when any of its rows needs it and the other rows use a scale of 1.  Key sinks
+// hold -inf (mask_tile) and give p = 0 like the columns past nvalid.
 __device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, int nvalid, float alpha,
                                                     bool have_o, float &run, float (&l)[4]) {
   uint32_t s0[32], s1[32], s2[32], s3[32];
@@ -438,12 +477,13 @@ __device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, in
   float sc = 1.0f;
   if (any) {
     const float nr = need ? fmaxf(run, zmax) : run;
-    if (have_o && need) sc = ex2(run - nr);  // O holds earlier tiles only when j > 0
+    // O holds earlier tiles only when j > 0, and nothing but zeros while run is -inf
+    if (have_o && need) sc = run == -INFINITY ? 0.f : ex2(run - nr);
     run = nr;
 #pragma unroll
     for (int i = 0; i < 4; ++i) l[i] *= sc;
   }
-  const float nb = -run;
+  const float nb = run == -INFINITY ? 0.f : -run;  // every key so far left out: p = 2^-inf = 0
   uint32_t pk[16];
   if (nvalid >= kBK) {
     const uint64_t a2 = f2_pack(__float_as_uint(alpha), __float_as_uint(alpha));
@@ -513,6 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(kBarDrain), 1);
     fence_mbar_init();
+    int32_t *ssk = reinterpret_cast<int32_t *>(gbase + kOffSinks);
+    for (int t = 0; t < FM_MAX_SINKS; ++t)
+      ssk[t] = p.sinks ? p.sinks[((int64_t)b * p.H + h) * FM_MAX_SINKS + t] : INT_MAX;
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
@@ -637,13 +680,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_ok = tile_ok && row < p.Sq;
     const int64_t bh = (int64_t)b * p.H + h;
     const bool fixed = !tile_ok || (!p.force_online && p.flag[bh * p.nqb + qb] != 0);
-    float bias = 0.f;
-    if (fixed && row_ok) bias = p.shift[bh * p.Sq + row];
+    // the row's shift: fixed-m rows subtract b_i from fm_bounds; online rows their running
+    // max (one register serves both, the kernel is at its register limit)
+    float shv = -INFINITY;
+    if (fixed) shv = row_ok ? p.shift[bh * p.Sq + row] : 0.f;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)(t * 128);
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(t * 128);
     float l[4] = {0.f, 0.f, 0.f, 0.f};
-    float run = -INFINITY;
+    // key sinks of this head (ascending global key indices, INT_MAX pads): columns to drop
+    int next_sink = sink_after_key(base + kOffSinks, INT_MIN);
     bool ok = true;
     int c = 0;  // chunk of key tile j
     for (int j = 0; j < n_kv; ++j) {
@@ -653,9 +699,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
       if (!ok) break;
       tc_fence_after();
-      const int nvalid = min(kBK, p.len[c] - (j - p.tile0[c]) * kBK);  // ragged end of each chunk
-      if (fixed) softmax_fixed_tile(tS, nvalid, p.alpha, -bias, l);
-      else softmax_online_tile(tS, tO, nvalid, p.alpha, j > 0, run, l);
+      const int jl = (j - p.tile0[c]) * kBK;  // first key of the tile within its chunk
+      const int nvalid = min(kBK, p.len[c] - jl);  // ragged end of each chunk
+      const int g0 = p.key0[c] + jl;               // global index of the tile's first key
+      if (next_sink < g0) next_sink = sink_after_key(base + kOffSinks, g0 - 1);  // sinks before this tile
+      // -inf over the key sinks in this tile, and (fixed-m rows) over the columns past the
+      // chunk's end; the online rows mask those columns themselves
+      if (next_sink < g0 + nvalid || (fixed && nvalid < kBK)) mask_tile(tS, nvalid, g0, base + kOffSinks, next_sink);
+      if (fixed) softmax_fixed_tile(tS, p.alpha, -shv, l);
+      else softmax_online_tile(tS, tO, nvalid, p.alpha, j > 0, shv, l);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(kBarPReady + t));
@@ -669,17 +721,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const float lsum = (l[0] + l[1]) + (l[2] + l[3]);
       const int64_t rflat = bh * p.Sq + row;
-      float cprev = 0.f, cnew = 1.f, nr = run;
+      float cprev = 0.f, cnew = 1.f, nr = shv;
       if (!fixed && row_ok && p.accumulate) {
         const float R = p.acc_max[rflat];
-        nr = fmaxf(R, run);
+        nr = fmaxf(R, shv);
         cprev = (R == -INFINITY) ? 0.f : exp2f(R - nr);
-        cnew = (run == -INFINITY) ? 0.f : exp2f(run - nr);
+        cnew = (shv == -INFINITY) ? 0.f : exp2f(shv - nr);
       }
       // the row's sum and shift after this chunk
       float sum_new = lsum;
       if (row_ok && p.accumulate) sum_new = fixed ? p.acc_sum[rflat] + lsum : fmaf(p.acc_sum[rflat], cprev, lsum * cnew);
-      const float shift_new = fixed ? bias : nr;
+      const float shift_new = nr;  // b_i on fixed-m rows
       const bool final_out = p.out != nullptr;
       // with the normalise fused in, o = acc / max(sum, 1e-37) goes straight to `out`
       // ("Kernel reference: ring_attention_const_max_fwd": the last ring step folds and
@@ -850,6 +902,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
     p.tile0[c + 1] = p.tile0[c] + (c < nc ? (int)((ks[c].S + kBK - 1) / kBK) : 0);
   }
   p.n_kv = p.tile0[nc];
+  p.sinks = a.sinks;
+  int64_t g = a.sinks ? a.key0 : 0;  // without sinks the global offsets are not needed
+  for (int c = 0; c < kMaxChunks; ++c) {
+    p.key0[c] = (int)g;
+    if (c < nc) g += ks[c].S;
+  }
   p.alpha = a.alpha;
   p.force_online = a.force_online;
   p.accumulate = a.accumulate;

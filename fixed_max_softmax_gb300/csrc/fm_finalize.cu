@@ -5,7 +5,13 @@
 // floored near the smallest fp32 normal so an all-underflow row divides by the floor).
 // HBM-bound elementwise pass: each thread handles four consecutive output elements of
 // a row (one 16-byte load of acc_o), grid-stride over the whole tensor.
+//
+// Also here: the fold of the key sinks, the few loudest keys of a head that the bounds
+// pass left out of the key max and the chunks left out of their sums ("Kernel reference:
+// ring_attention_const_max_fwd", section "Adapting this kernel").  One online-softmax
+// merge per row, in fp32, before the divide.
 #include <cuda_bf16.h>
+#include <limits.h>
 
 #include "fm_internal.h"
 
@@ -60,6 +66,89 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float *__restrict__
   }
 }
 
+constexpr int kFoldWarps = 8;
+constexpr int kFoldRowsPerWarp = 8;
+constexpr int kFoldRows = kFoldWarps * kFoldRowsPerWarp;  // rows per CTA
+
+// One warp per row; lane owns EPL = D/32 consecutive dimensions.  The head's sinks (raw
+// key and value rows) are staged in shared memory once per CTA.
+template <typename T, int EPL>
+__global__ void __launch_bounds__(kFoldWarps * 32)
+    fold_sinks_kernel(View q, float alpha, const int32_t *__restrict__ sink_idx, const float *__restrict__ sink_k,
+                      const float *__restrict__ sink_v, float *__restrict__ acc_o, float *__restrict__ acc_sum,
+                      float *__restrict__ acc_max) {
+  constexpr int D = 32 * EPL;
+  __shared__ float sk[FM_MAX_SINKS][D];
+  __shared__ float sv[FM_MAX_SINKS][D];
+  const int64_t b = blockIdx.z, h = blockIdx.y;
+  const int64_t bh = b * q.H + h;
+  int ns = 0;
+  while (ns < FM_MAX_SINKS && sink_idx[bh * FM_MAX_SINKS + ns] != INT_MAX) ++ns;  // ascending, padded
+  if (ns == 0) return;  // no sink in this head: nothing to merge
+  for (int e = threadIdx.x; e < ns * D; e += blockDim.x) {
+    sk[e / D][e % D] = sink_k[(bh * FM_MAX_SINKS) * D + e];
+    sv[e / D][e % D] = sink_v[(bh * FM_MAX_SINKS) * D + e];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const T *qb = reinterpret_cast<const T *>(q.ptr) + b * q.sB + h * q.sH;
+  for (int k = 0; k < kFoldRowsPerWarp; ++k) {
+    const int64_t row = (int64_t)blockIdx.x * kFoldRows + warp * kFoldRowsPerWarp + k;
+    if (row >= q.S) break;
+    float qx[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const T t = qb[row * q.sS + (int64_t)(lane * EPL + e) * q.sD];
+      if constexpr (sizeof(T) == 2) qx[e] = __bfloat162float(t); else qx[e] = (float)t;
+    }
+    float z[FM_MAX_SINKS];
+    const int64_t r = bh * q.S + row;
+    const float r_old = acc_max[r];
+    float r_new = r_old;
+#pragma unroll
+    for (int s = 0; s < FM_MAX_SINKS; ++s) {
+      if (s < ns) {
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dot = fmaf(qx[e], sk[s][lane * EPL + e], dot);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        z[s] = alpha * dot;  // raw base-2 logit, the units of acc_max
+        r_new = fmaxf(r_new, z[s]);
+      }
+    }
+    const float c = r_old == -INFINITY ? 0.f : exp2f(r_old - r_new);
+    float4 *ao = reinterpret_cast<float4 *>(acc_o + r * D) + lane * EPL / 4;
+    float o[EPL];
+    if constexpr (EPL == 4) {
+      const float4 a = *ao;
+      o[0] = a.x * c; o[1] = a.y * c; o[2] = a.z * c; o[3] = a.w * c;
+    } else {
+      const float2 a = *reinterpret_cast<const float2 *>(acc_o + r * D + lane * EPL);
+      o[0] = a.x * c; o[1] = a.y * c;
+    }
+    float psum = 0.f;
+#pragma unroll
+    for (int s = 0; s < FM_MAX_SINKS; ++s) {
+      if (s < ns) {
+        const float p = exp2f(z[s] - r_new);
+        psum += p;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[e] = fmaf(p, sv[s][lane * EPL + e], o[e]);
+      }
+    }
+    if constexpr (EPL == 4) {
+      *ao = make_float4(o[0], o[1], o[2], o[3]);
+    } else {
+      *reinterpret_cast<float2 *>(acc_o + r * D + lane * EPL) = make_float2(o[0], o[1]);
+    }
+    if (lane == 0) {
+      acc_sum[r] = fmaf(acc_sum[r], c, psum);
+      acc_max[r] = r_new;
+    }
+  }
+}
+
 template <bool LSE>
 cudaError_t launch_typed(const float *acc_o, const float *acc_sum, const float *acc_max, const View &o,
                          float *lse, cudaStream_t st) {
@@ -92,6 +181,25 @@ cudaError_t launch_finalize(const float *acc_o, const float *acc_sum, const View
 cudaError_t launch_finalize_lse(const float *acc_o, const float *acc_sum, const float *acc_max, const View &o,
                                 float *lse, cudaStream_t st) {
   return launch_typed<true>(acc_o, acc_sum, acc_max, o, lse, st);
+}
+
+cudaError_t launch_fold_sinks(const View &q, float alpha, const int32_t *sink_idx, const float *sink_k,
+                              const float *sink_v, float *acc_o, float *acc_sum, float *acc_max, cudaStream_t st) {
+  if (q.B * q.H * q.S == 0) return cudaSuccess;
+  const dim3 grid((unsigned)((q.S + kFoldRows - 1) / kFoldRows), (unsigned)q.H, (unsigned)q.B);
+  const unsigned threads = kFoldWarps * 32;
+  if (q.dtype == FM_BF16) {
+    if (q.D == 128)
+      fold_sinks_kernel<__nv_bfloat16, 4><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum, acc_max);
+    else
+      fold_sinks_kernel<__nv_bfloat16, 2><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum, acc_max);
+  } else {
+    if (q.D == 128)
+      fold_sinks_kernel<float, 4><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum, acc_max);
+    else
+      fold_sinks_kernel<float, 2><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum, acc_max);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace fm

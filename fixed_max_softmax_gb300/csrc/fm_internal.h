@@ -43,6 +43,11 @@ struct BoundsArgs {
   int32_t *m;
   uint8_t *flag;
   float *qmax_sq, *kmax_sq, *kbar, *qkbar, *shift, *vmax_sq;
+  // key sinks: n_sink > 0 leaves that many of each head's loudest keys out of the key max
+  int n_sink = 0;
+  int32_t *sink_idx = nullptr;  // [B,H,FM_MAX_SINKS] ascending global key index, INT32_MAX pads
+  float *sink_k = nullptr;      // [B,H,FM_MAX_SINKS,D] raw key rows of the sinks
+  float *sink_v = nullptr;      // [B,H,FM_MAX_SINKS,D] their value rows
   void *ws;
   size_t ws_bytes;
 };
@@ -69,6 +74,10 @@ struct ChunkArgs {
   // ks/vs instead of k/v
   int n_chunks = 0;
   const View *ks = nullptr, *vs = nullptr;
+  // key sinks to skip: [B,H,FM_MAX_SINKS] ascending global key indices (INT32_MAX pads),
+  // or nullptr; key0 is the global index of the first chunk's first key
+  const int32_t *sinks = nullptr;
+  int64_t key0 = 0;
 };
 // SIMT path: fp32 inputs (exact fp32 arithmetic), any D in {64,128}, any strides.
 cudaError_t launch_chunk_simt(const ChunkArgs &a, cudaStream_t st);
@@ -89,6 +98,11 @@ cudaError_t launch_finalize(const float *acc_o, const float *acc_sum, const View
 // The same plus lse = ln2 * (acc_max + log2(acc_sum)) per row.
 cudaError_t launch_finalize_lse(const float *acc_o, const float *acc_sum, const float *acc_max,
                                 const View &o, float *lse, cudaStream_t st);
+
+// Key sinks merged back into the accumulators after the last chunk (online merge per row).
+cudaError_t launch_fold_sinks(const View &q, float alpha, const int32_t *sink_idx, const float *sink_k,
+                              const float *sink_v, float *acc_o, float *acc_sum, float *acc_max,
+                              cudaStream_t st);
 
 // ---- helpers shared by host code -------------------------------------------
 int current_device_sm_count();

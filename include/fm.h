@@ -17,6 +17,10 @@
  *     fm_attn_chunk(q, k_c, v_c, accumulate = c > 0)     once per chunk c
  *     fm_finalize(acc_o, acc_sum -> o)                   once
  * or, fusing the last two: fm_attn_chunk_final(..., o) for the last chunk.
+ * With key sinks (opts.sink_keys > 0) the loudest keys of each head are left out of the
+ * key max and out of the chunks' fixed-m sums, and fm_fold_sinks merges them back exactly
+ * after the last chunk (fm_attn_chunk_final and fm_attn_chunks with o_out do this
+ * themselves).
  *
  * Conventions shared by every call:
  *   - Tensors are described by fm_tensor: a logical [B, H, S, D] array with element
@@ -70,6 +74,7 @@ enum {
 #define FM_BLOCK_Q 128              /* rows per Q-block: the granularity of m and flag */
 #define FM_VMAX 256                 /* the V bound of [PR477]'s commit message */
 #define FM_SUM_CLAMP 1e-37f         /* [NKI] "Accumulate, then normalize once" */
+#define FM_MAX_SINKS 8              /* most key sinks per head (opts.sink_keys) */
 
 /* A logical [B, H, S, D] tensor: element (b,h,s,d) lives at
  * ptr + (b*stride[0] + h*stride[1] + s*stride[2] + d*stride[3]) * elemsize. */
@@ -89,6 +94,15 @@ typedef struct {
                            U_i = alpha*|q_i|*max|k| ([NKI] "Best practices": give each query
                            row its own bound); 0: one m per 128-row Q-block ([PR477]).
                            Eligibility stays per Q-block in both cases. */
+  int32_t sink_keys;    /* 0..FM_MAX_SINKS: leave up to this many of each head's loudest
+                           keys out of the key max ([NKI] "Adapting this kernel": attention
+                           sinks inflate max|k| for every row, and excluding those few keys
+                           from the max reduction recovers the bound).  The sinks are the
+                           keys whose norm (|k - kbar| with centering) is strictly above the
+                           (sink_keys+1)-th largest, so ties at that norm stay ordinary keys;
+                           kmax_sq becomes that norm squared.  The chunks skip the sinks and
+                           fm_fold_sinks merges them back exactly, so the output is still
+                           plain attention over every key. */
 } fm_opts;
 
 /* Bounds of one attention call ([PR477] Summary, "Dynamic eligibility bounding").
@@ -106,6 +120,10 @@ typedef struct {
  *                              the row's own ceil(U_i) - C (opts.per_row) or its Q-block's
  *                              m; the chunk kernels subtract it in registers
  *   vmax_sq f32   [1]          max over all of V of v^2 (v_ok = vmax_sq <= 256^2)
+ *   sink_idx int32 [B, H, FM_MAX_SINKS]  global key indices of the head's sinks, ascending,
+ *                              padded with INT32_MAX (only with opts.sink_keys > 0)
+ *   sink_k, sink_v f32 [B, H, FM_MAX_SINKS, D]  the sinks' raw key and value rows (zero in
+ *                              padding slots), kept for fm_fold_sinks (sink_keys > 0 only)
  * with alpha = softmax_scale * log2(e) (base-2 logits, [PR477]'s exp2 formulation)
  * and U = alpha * sqrt(qmax_sq) * sqrt(kmax_sq), the Cauchy-Schwarz bound on the
  * base-2 logit ([NKI] "Picking a max that is safe without measuring it"). */
@@ -118,22 +136,28 @@ typedef struct {
   float *qkbar;
   float *shift;
   float *vmax_sq;
+  int32_t *sink_idx; /* required when opts.sink_keys > 0, else ignored (may be NULL) */
+  float *sink_k;
+  float *sink_v;
   /* filled by fm_bounds */
   int64_t B, H, Sq, D, n_qblocks;
   int64_t N_total;   /* total KV length over every chunk of the call */
   int32_t C, W, gate; /* C(N) = 127 - ceil(log2 N) - 8, W = C + 125, gate = floor(W/2) */
   int32_t centered;  /* the opts.centering the bounds were measured with */
   int32_t per_row;   /* the opts.per_row they were built with */
+  int32_t n_sink;    /* the opts.sink_keys they were built with */
   float alpha;
   int32_t dtype;
   /* updated by fm_attn_chunk (host-side bookkeeping of the chunk sequence) */
   int64_t kv_seen;
   int32_t online_lock;
+  int32_t sinks_folded; /* set by fm_fold_sinks; no chunk may follow it */
   uint32_t magic; /* FM_BOUNDS_MAGIC once fm_bounds has succeeded */
 } fm_bounds_out;
 
 /* Scratch bytes fm_bounds needs for k_full of shape [B, H, N_total, D] (partial
- * key sums for the mean, per-block key and value maxima).  Returns FM_OK. */
+ * key sums for the mean, per-block key and value maxima, per-block key-sink candidates).
+ * Returns FM_OK. */
 FM_API int fm_bounds_workspace_size(int64_t B, int64_t H, int64_t N_total, int64_t D, size_t *bytes);
 
 /* fm_bounds -- norms, key mean, m and the per-tile flag ([PR477] Summary; the
@@ -141,11 +165,13 @@ FM_API int fm_bounds_workspace_size(int64_t B, int64_t H, int64_t N_total, int64
  *   q      [B, H, Sq, D]  queries (all rows of the call)
  *   k_full [B, H, N, D]   ALL keys of the call (every chunk), N = N_total
  *   v_full [B, H, N, D]   all values
- *   opts   softmax_scale and centering (force_online is ignored here)
+ *   opts   softmax_scale, centering, per_row, sink_keys (force_online is ignored here)
  *   out    caller-filled pointers; every other field is written
  *   workspace, workspace_bytes  device scratch of at least fm_bounds_workspace_size
- * Device results are deterministic (fixed-order reductions).  Errors: FM_ERR_ARG,
- * FM_ERR_SHAPE, FM_ERR_DTYPE, FM_ERR_UNSUPPORTED, FM_ERR_CUDA. */
+ * Device results are deterministic (fixed-order reductions; key-sink ties broken by the
+ * lower index).  Errors: FM_ERR_ARG (also sink_keys outside [0, FM_MAX_SINKS] or a missing
+ * sink array), FM_ERR_SHAPE, FM_ERR_DTYPE, FM_ERR_UNSUPPORTED (also sinks with N_total
+ * above 2^31 - 256), FM_ERR_CUDA. */
 FM_API int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_full,
               const fm_opts *opts, fm_bounds_out *out, void *workspace, size_t workspace_bytes,
               fm_stream_t stream);
@@ -165,11 +191,15 @@ FM_API int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tenso
  *            the running max on fallback rows), so acc_sum * 2^acc_max is the
  *            row's sum of 2^z.
  *   accumulate  0: overwrite the accumulators (first chunk); 1: add into them
+ * Key sinks (bounds->n_sink > 0): a key whose global index is in bounds->sink_idx adds
+ * nothing here.  The global index of a chunk's first key is the number of keys folded
+ * before it (bounds->kv_seen), so the chunks must come in the key order fm_bounds saw.
  * Errors: FM_ERR_BOUNDS_MISMATCH when bounds->magic is wrong, the bounds' shape is
  * not [B, H, ceil(Sq/128)], bounds->centered != opts->centering (raw-key bounds must
  * never pair with centered logits: [PR477] "matched pair"), the softmax scale
- * differs, more keys arrive than bounds->N_total, or force_online changes within a
- * call; plus the errors of fm_bounds. */
+ * differs, more keys arrive than bounds->N_total, force_online changes within a call,
+ * opts->sink_keys differs from bounds->n_sink, or the sinks were already folded in
+ * (accumulate = 1 after fm_fold_sinks); plus the errors of fm_bounds. */
 FM_API int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk,
                   fm_bounds_out *bounds, const fm_opts *opts, float *acc_o, float *acc_sum,
                   float *acc_max, int accumulate, fm_stream_t stream);
@@ -183,7 +213,8 @@ FM_API int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_
  * acc_sum and acc_max are updated as by fm_attn_chunk; acc_o is NOT (its contents are
  * unspecified afterwards).  The result equals fm_attn_chunk followed by fm_finalize (or
  * fm_finalize_lse); the tensor-core kernel does both in one launch where the layout of
- * o_out allows 16-byte stores, otherwise the two steps run back to back. */
+ * o_out allows 16-byte stores, otherwise the two steps run back to back.  With key sinks
+ * the steps are fm_attn_chunk, fm_fold_sinks and fm_finalize(_lse), back to back. */
 FM_API int fm_attn_chunk_final(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk,
                                fm_bounds_out *bounds, const fm_opts *opts, float *acc_o, float *acc_sum,
                                float *acc_max, int accumulate, const fm_tensor *o_out, float *lse,
@@ -224,6 +255,22 @@ FM_API int fm_finalize(const float *acc_o, const float *acc_sum, const fm_tensor
 FM_API int fm_finalize_lse(const float *acc_o, const float *acc_sum, const float *acc_max,
                            const fm_tensor *o_out, float *lse, fm_stream_t stream);
 
+/* fm_fold_sinks -- merge the key sinks that fm_bounds set aside back into the accumulators,
+ * exactly, after the last chunk and before fm_finalize(_lse) ([NKI] "Adapting this kernel"
+ * leaves the loudest keys out of the max reduction; this is how their terms still count).
+ * For each row i, with z_s = alpha * q_i.k_s the raw base-2 logit of sink s (from
+ * bounds->sink_k) and r_i = acc_max_i the row's current shift:
+ *   r' = max(r_i, max_s z_s),  c = 2^(r_i - r'),
+ *   acc_o_i = c * acc_o_i + sum_s 2^(z_s - r') v_s,  acc_sum_i = c * acc_sum_i + sum_s 2^(z_s - r'),
+ *   acc_max_i = r'
+ * (an online-softmax merge in fp32), so that acc_sum * 2^acc_max stays the row's sum of 2^z
+ * and fm_finalize_lse stays valid.  A no-op when bounds->n_sink == 0.
+ *   q, opts  as given to the chunks;  acc_o / acc_sum / acc_max  as left by the last chunk
+ * Errors: FM_ERR_BOUNDS_MISMATCH (bounds not matching q or opts, no chunk folded yet, or the
+ * sinks already folded), FM_ERR_ARG, FM_ERR_CUDA. */
+FM_API int fm_fold_sinks(const fm_tensor *q, fm_bounds_out *bounds, const fm_opts *opts, float *acc_o,
+                         float *acc_sum, float *acc_max, fm_stream_t stream);
+
 /* fm_sync_status -- synchronise `stream`, then report and clear this GPU's device
  * error word: FM_ERR_TIMEOUT if a kernel gave up on a pipeline wait (its outputs are
  * then invalid), FM_ERR_CUDA on an asynchronous CUDA error, else FM_OK. */
@@ -245,7 +292,7 @@ FM_API const char *fm_last_error(void);
 FM_API int fm_version(void);
 
 /* Upper bound of the scratch fm_bounds_noalloc can use: 4 MiB.  That covers, at D = 128,
- * up to 119 heads of 75,600 keys (fm_bounds_workspace_size gives the exact need). */
+ * up to 74 heads of 75,600 keys (fm_bounds_workspace_size gives the exact need). */
 #define FM_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
 
 /* fm_bounds_noalloc -- fm_bounds for callers that cannot allocate device memory.

@@ -39,11 +39,32 @@ def test_exports_nothing_else():
     assert names == header_symbols()
 
 
-def test_struct_layouts_match_header():
-    # sizes the C compiler gives the header's structs (x86-64 and aarch64 LP64 agree)
-    assert ctypes.sizeof(fm.fm_tensor) == 8 + 4 + 4 + 4 * 8 + 4 * 8
-    assert ctypes.sizeof(fm.fm_opts) == 16
-    assert fm.fm_bounds_out.magic.offset + 4 == ctypes.sizeof(fm.fm_bounds_out)
+def test_struct_layouts_match_header(tmp_path):
+    """The ctypes mirrors of fm_tensor, fm_opts and fm_bounds_out have the size and field
+    offsets the C compiler gives the header's structs."""
+    import subprocess
+    structs = {"fm_tensor": fm.fm_tensor, "fm_opts": fm.fm_opts, "fm_bounds_out": fm.fm_bounds_out}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "fm.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'  printf("{name} size %zu\\n", sizeof({name}));')
+        for f, _ in cls._fields_:
+            lines.append(f'  printf("{name} {f} %zu\\n", offsetof({name}, {f}));')
+    lines += ["  return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    seen = 0
+    for ln in out:
+        if not ln.strip():
+            continue
+        name, field, val = ln.split()
+        cls = structs[name]
+        got = ctypes.sizeof(cls) if field == "size" else getattr(cls, field).offset
+        assert got == int(val), (name, field, got, val)
+        seen += 1
+    assert seen == sum(len(c._fields_) + 1 for c in structs.values())
 
 
 def test_version_and_workspace(lib):
@@ -204,3 +225,44 @@ def test_noalloc_refuses_oversized_problems_on_the_host(lib):
     rc = lib.fm_bounds_noalloc(ctypes.byref(t16), ctypes.byref(t16), ctypes.byref(t16), ctypes.byref(fm.opts()),
                                ctypes.byref(out), None)
     assert rc in (fm.FM_ERR_DTYPE, fm.FM_ERR_CUDA)
+
+
+def test_key_sink_validation(lib):
+    q, k = fake(1, 2, 256, 128), fake(1, 2, 300, 128)
+    # sink_keys outside [0, FM_MAX_SINKS]
+    assert call_bounds(lib, q, k, k, opt=fm.opts(sink_keys=fm.FM_MAX_SINKS + 1)) == fm.FM_ERR_ARG
+    assert call_bounds(lib, q, k, k, opt=fm.opts(sink_keys=-1)) == fm.FM_ERR_ARG
+    # sinks asked for without the arrays to hold them
+    assert call_bounds(lib, q, k, k, opt=fm.opts(sink_keys=2)) == fm.FM_ERR_ARG
+    assert "sink" in fm.fm_last_error()
+    # the chunks must skip exactly the keys the bounds left out of the key max
+    b = good_bounds()
+    assert call_chunk(lib, b, opt=fm.opts(sink_keys=2)) == fm.FM_ERR_BOUNDS_MISMATCH
+    b.n_sink = 2
+    assert call_chunk(lib, b) == fm.FM_ERR_BOUNDS_MISMATCH
+    # nothing may follow the fold of the sinks
+    b = good_bounds()
+    b.n_sink, b.online_lock, b.kv_seen, b.sinks_folded = 2, 0, 100, 1
+    b.sink_idx = b.sink_k = b.sink_v = FAKE
+    assert call_chunk(lib, b, nc=100, accumulate=1, opt=fm.opts(sink_keys=2)) == fm.FM_ERR_BOUNDS_MISMATCH
+    assert "fold" in fm.fm_last_error()
+
+
+def test_fold_sinks_validation(lib):
+    q = fake(1, 2, 256, 128)
+
+    def fold(b, opt=None):
+        return lib.fm_fold_sinks(ctypes.byref(q), ctypes.byref(b), ctypes.byref(opt or fm.opts(sink_keys=2)), FAKE,
+                                 FAKE, FAKE, None)
+    b = good_bounds()
+    b.n_sink = 2
+    b.sink_idx = b.sink_k = b.sink_v = FAKE
+    assert fold(b) == fm.FM_ERR_BOUNDS_MISMATCH          # no chunk folded yet
+    b.online_lock = 0
+    assert fold(b, fm.opts(sink_keys=1)) == fm.FM_ERR_BOUNDS_MISMATCH  # other sink count
+    b.sinks_folded = 1
+    assert fold(b) == fm.FM_ERR_BOUNDS_MISMATCH          # folded twice
+    b2 = good_bounds()
+    b2.online_lock = 0
+    assert lib.fm_fold_sinks(ctypes.byref(q), ctypes.byref(b2), ctypes.byref(fm.opts()), FAKE, FAKE, FAKE,
+                             None) == fm.FM_OK           # no sinks: nothing to do, nothing enqueued

@@ -36,10 +36,10 @@ def dev():
 
 
 def run(q, k, v, chunks=None, centering=False, force_online=False, out_dtype=torch.float32, with_lse=False,
-        per_row=False):
+        per_row=False, sink_keys=0):
     B, H, Sq, D = q.shape
     fa = fm.FixedMAttention(B, H, Sq, k.shape[2], D, q.device, centering=centering, force_online=force_online,
-                            out_dtype=out_dtype, per_row=per_row)
+                            out_dtype=out_dtype, per_row=per_row, sink_keys=sink_keys)
     o = fa.forward(q, k, v, chunks, with_lse=with_lse)
     fm.fm_sync_status()
     return fa, o
@@ -460,3 +460,118 @@ def test_adversarial_full(dev):
     assert sampled(q, k, v, o, [0, 25], rows) <= TOL_BF16
     _, o2 = run(q, k, v, None, centering=True, force_online=True)
     assert maxerr(o2[0, [0, 25]][:, rows], o[0, [0, 25]][:, rows]) <= TOL_BF16
+
+
+# ------------------------------------------------------------------ key sinks
+
+def check_sinks(fa, ob, heads=None):
+    """Device sink lists equal the oracle's wherever the n-th and (n+1)-th loudest keys are
+    apart by more than fp32 norms can blur (elsewhere the two sets may differ in near-ties,
+    which changes no output: every key is still counted once).  Returns the heads compared."""
+    n = ob["sink_idx"].shape[-1]
+    got = fa.bounds.sink_idx.cpu().numpy()
+    if heads is not None:
+        got = got[:, heads]
+    got = got.reshape(-1, fm.FM_MAX_SINKS)
+    ref = ob["sink_idx"].reshape(-1, n)
+    gap = ob["sink_gap"].reshape(-1)
+    tau = ob["kmax_sq"].reshape(-1)
+    compared = 0
+    for g in range(ref.shape[0]):
+        assert np.all(got[g, n:] == 2**31 - 1)
+        if gap[g] > 1e-4 * max(1.0, tau[g]):
+            assert np.array_equal(got[g, :n], ref[g]), (g, got[g], ref[g])
+            compared += 1
+    return compared
+
+
+@pytest.mark.parametrize("centering", [False, True])
+@pytest.mark.parametrize("force_online", [False, True])
+@pytest.mark.parametrize("chunks", [[(0, 300), (300, 400)], [(0, 353), (353, 347)], [(0, 700)]])
+def test_key_sinks_element_by_element(dev, chunks, force_online, centering):
+    """The sinks workload (4 loud keys at 0, 1, N/2+3, N-1 in heads 0-19): with the 4 sinks
+    left out of the key max every tile is eligible, the chunks skip the sinks (two in one tile,
+    one at a chunk start or mid-chunk, one in a ragged tail) and the fold merges them back:
+    the output is plain attention over every key."""
+    q, k, v = workloads.make_inputs("sinks", device="cpu", heads=[0, 1, 25], Sq=300, N=700)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    fa, o = run(qd, kd, vd, chunks, centering=centering, force_online=force_online, sink_keys=4, with_lse=True)
+    ob = oracle.bounds(q, k, v, centering=centering, sink_keys=4)
+    check_bounds(fa, ob)
+    assert check_sinks(fa, ob) >= 2  # the two sink heads at least
+    assert list(fa.bounds.sink_idx[0, 0, :4].cpu().numpy()) == workloads.sink_positions(700)
+    if not force_online:
+        assert bool(fa.bounds.flag.all())
+    ref, ref_lse = oracle.attention(q, k, v, return_lse=True)
+    assert maxerr(o, ref) <= TOL_BF16
+    assert maxerr(fa.lse, ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse))))
+    # without sinks the sink heads fall back to online softmax everywhere; same output
+    fb, o_plain = run(qd, kd, vd, chunks, centering=centering, force_online=force_online)
+    if not centering and not force_online:
+        assert not fb.bounds.flag[0, :2].any()
+    assert maxerr(o, o_plain) <= TOL_BF16
+
+
+@pytest.mark.parametrize("sink_keys", [1, 2, 8])
+def test_key_sink_counts_and_paths(dev, sink_keys):
+    """Fewer sinks than loud keys (the rest stay in, their heads still fall back), more sinks
+    than loud keys (ordinary keys become sinks too), on the fused-final, separate-finalize
+    (explicit fm_fold_sinks) and one-launch paths, which agree bit for bit where they share
+    the arithmetic."""
+    q, k, v = workloads.make_inputs("sinks", device="cpu", heads=[0, 30], Sq=260, N=900)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    chunks = [(0, 450), (450, 450)]
+    ref = oracle.attention(q, k, v)
+    ob = oracle.bounds(q, k, v, sink_keys=sink_keys)
+    outs = {}
+    for mode in ("fused", "separate", "one_launch"):
+        fa = fm.FixedMAttention(1, 2, 260, 900, 128, dev, sink_keys=sink_keys)
+        o = fa.forward(qd, kd, vd, chunks, fused_final=mode == "fused", one_launch=mode == "one_launch").clone()
+        fm.fm_sync_status()
+        check_bounds(fa, ob)
+        check_sinks(fa, ob)
+        assert np.array_equal(fa.bounds.flag.cpu().numpy(), ob["flag"])
+        assert maxerr(o, ref) <= TOL_BF16, mode
+        assert fa.bounds.out.sinks_folded == 1
+        outs[mode] = o
+    assert torch.equal(outs["fused"], outs["separate"])
+    assert maxerr(outs["one_launch"], outs["fused"]) <= TOL_BF16
+
+
+def test_key_sinks_cuda_core_path_and_edges(dev):
+    """fp32 inputs (CUDA-core kernel, exact fp32) with sinks; a key set made only of sinks
+    (every key left out of the chunks, the fold alone gives the output); no chunk may follow
+    the fold."""
+    q, k, v = workloads.make_inputs("sinks", device="cpu", heads=[0, 1], Sq=200, N=300)
+    q32, k32, v32 = q.float(), k.float(), v.float()
+    fa, o = run(q32.to(dev), k32.to(dev), v32.to(dev), [(0, 150), (150, 150)], sink_keys=4)
+    ob = oracle.bounds(q32, k32, v32, sink_keys=4)
+    check_bounds(fa, ob)
+    check_sinks(fa, ob)
+    assert maxerr(o, oracle.attention(q32, k32, v32)) <= TOL_F32
+    # three keys, four sinks: all three are sinks, tau = 0, m = -C
+    qs, ks, vs = q[:, :, :130], k[:, :, 5:8], v[:, :, 5:8]
+    fa, o = run(qs.to(dev), ks.to(dev), vs.to(dev), [(0, 2), (2, 1)], sink_keys=4)
+    assert list(fa.bounds.sink_idx[0, 0].cpu().numpy()[:3]) == [0, 1, 2]
+    assert float(fa.bounds.kmax_sq.max().item()) == 0.0
+    assert maxerr(o, oracle.attention(qs, ks, vs)) <= TOL_BF16
+    with pytest.raises(fm.FMError) as e:
+        fm.fm_attn_chunk(qs.to(dev), ks.to(dev), vs.to(dev), fa.bounds, fa.opt, fa.acc_o, fa.acc_sum, fa.acc_max, True)
+    assert e.value.code == fm.FM_ERR_BOUNDS_MISMATCH
+
+
+def test_sinks_full(dev):
+    """The sinks workload at full size (H=40, S=4096, 4 chunks of 1024): 4 sinks make every
+    tile eligible; sampled rows match the oracle and the run without sinks."""
+    w = workloads.WORKLOADS["sinks"]
+    q, k, v = workloads.make_inputs("sinks", device=dev)
+    fa, o = run(q, k, v, workloads.chunk_bounds(w), sink_keys=4)
+    ob = oracle.bounds(q.cpu(), k.cpu(), v.cpu(), sink_keys=4)
+    check_bounds(fa, ob)
+    assert check_sinks(fa, ob) >= w.extra["sink_heads"]
+    assert bool(fa.bounds.flag.all())
+    rows = list(range(0, 128)) + list(range(2000, 2100)) + list(range(3968, 4096))
+    assert sampled(q, k, v, o, [0, 19, 39], rows) <= TOL_BF16
+    fb, o2 = run(q, k, v, workloads.chunk_bounds(w))
+    assert not fb.bounds.flag[0, :w.extra["sink_heads"]].any()
+    assert maxerr(o2[0, [0, 39]][:, rows], o[0, [0, 39]][:, rows]) <= TOL_BF16
