@@ -245,8 +245,8 @@ def run_ours(args, rank, world, local_rank):
 
     # bounds: ksum, kmean (centering only), norms, finish, shift; one launch per chunk with the normalise
     # fused into the last; with key sinks the bounds add their selection and the step ends with
-    # the sinks' fold and a separate normalise
-    launches_per_step = (5 if centering else 3) + len(chunks) + (3 if args.sink_keys else 0)
+    # one pass that folds the sinks back and normalises
+    launches_per_step = (5 if centering else 3) + len(chunks) + (2 if args.sink_keys else 0)
     for _ in range(args.warmup):
         step()
     fm.fm_sync_status(stream)

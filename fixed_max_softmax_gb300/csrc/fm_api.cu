@@ -410,10 +410,11 @@ int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_ten
     }
   }
   if (e != cudaSuccess) return cuda_fail(e, "fm_attn_chunk launch");
-  if (o_out && n_sink > 0 && rows > 0) {  // the last chunk is in: merge the sinks back, then normalise
-    e = launch_fold_sinks(vq, (float)alpha, bounds->sink_idx, bounds->sink_k, bounds->sink_v, acc_o, acc_sum,
-                          acc_max, st);
+  if (o_out && n_sink > 0 && rows > 0) {  // the last chunk is in: merge the sinks back and normalise
+    e = launch_fold_sinks_final(vq, (float)alpha, bounds->sink_idx, bounds->sink_k, bounds->sink_v, acc_o, acc_sum,
+                                acc_max, vo, lse, st);
     if (e != cudaSuccess) return cuda_fail(e, "key-sink fold launch");
+    finalize_separately = false;
   }
   if (finalize_separately && rows > 0) {
     e = lse ? launch_finalize_lse(acc_o, acc_sum, acc_max, vo, lse, st) : launch_finalize(acc_o, acc_sum, vo, st);

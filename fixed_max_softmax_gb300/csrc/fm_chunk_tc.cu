@@ -343,16 +343,13 @@ __device__ __forceinline__ void exp_chunk_full(const uint32_t (&s)[32], uint64_t
   }
 }
 
-// The smallest key sink of the head's list (at shared-memory address `ssk`: ascending
-// int32, INT_MAX pads) above `g`, or INT_MAX.
-__device__ __forceinline__ int sink_after_key(uint32_t ssk, int g) {
+// The smallest key sink of the head's list (in shared memory: ascending int32, INT_MAX
+// pads) above `g`, or INT_MAX.
+__device__ __forceinline__ int sink_after_key(const int32_t *ssk, int g) {
   int n = INT_MAX;
 #pragma unroll
-  for (int t = 0; t < FM_MAX_SINKS; ++t) {
-    int x;
-    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(x) : "r"(ssk + 4u * t) : "memory");
-    if (x > g) n = min(n, x);
-  }
+  for (int t = 0; t < FM_MAX_SINKS; ++t)
+    if (ssk[t] > g) n = min(n, ssk[t]);
   return n;
 }
 
@@ -366,7 +363,7 @@ __device__ __forceinline__ uint32_t first_bits(int n) {
 // gives them p = 2^-inf = 0 (and leaves them out of the online row max) with no masks of
 // its own.  Only for the rare tiles that have such columns; warp-uniform, like every
 // tcgen05.ld/st (all rows of a tile share its key columns).
-__device__ __noinline__ void mask_tile(uint32_t tS, int nvalid, int g0, uint32_t ssk, int &next_sink) {
+__device__ __noinline__ void mask_tile(uint32_t tS, int nvalid, int g0, const int32_t *ssk, int &next_sink) {
   uint32_t k0 = first_bits(nvalid), k1 = first_bits(nvalid - 32), k2 = first_bits(nvalid - 64),
            k3 = first_bits(nvalid - 96);
   while (next_sink < g0 + nvalid) {
@@ -689,7 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(t * 128);
     float l[4] = {0.f, 0.f, 0.f, 0.f};
     // key sinks of this head (ascending global key indices, INT_MAX pads): columns to drop
-    int next_sink = sink_after_key(base + kOffSinks, INT_MIN);
+    int next_sink = sink_after_key(reinterpret_cast<const int32_t *>(gbase + kOffSinks), INT_MIN);
     bool ok = true;
     int c = 0;  // chunk of key tile j
     for (int j = 0; j < n_kv; ++j) {
@@ -702,10 +699,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int jl = (j - p.tile0[c]) * kBK;  // first key of the tile within its chunk
       const int nvalid = min(kBK, p.len[c] - jl);  // ragged end of each chunk
       const int g0 = p.key0[c] + jl;               // global index of the tile's first key
-      if (next_sink < g0) next_sink = sink_after_key(base + kOffSinks, g0 - 1);  // sinks before this tile
+      if (next_sink < g0)  // sinks before this tile
+        next_sink = sink_after_key(reinterpret_cast<const int32_t *>(gbase + kOffSinks), g0 - 1);
       // -inf over the key sinks in this tile, and (fixed-m rows) over the columns past the
       // chunk's end; the online rows mask those columns themselves
-      if (next_sink < g0 + nvalid || (fixed && nvalid < kBK)) mask_tile(tS, nvalid, g0, base + kOffSinks, next_sink);
+      if (next_sink < g0 + nvalid || (fixed && nvalid < kBK))
+        mask_tile(tS, nvalid, g0, reinterpret_cast<const int32_t *>(gbase + kOffSinks), next_sink);
       if (fixed) softmax_fixed_tile(tS, p.alpha, -shv, l);
       else softmax_online_tile(tS, tO, nvalid, p.alpha, j > 0, shv, l);
       tmem_st_wait();

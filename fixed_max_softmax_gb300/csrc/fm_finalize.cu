@@ -71,12 +71,18 @@ constexpr int kFoldRowsPerWarp = 8;
 constexpr int kFoldRows = kFoldWarps * kFoldRowsPerWarp;  // rows per CTA
 
 // One warp per row; lane owns EPL = D/32 consecutive dimensions.  The head's sinks (raw
-// key and value rows) are staged in shared memory once per CTA.
-template <typename T, int EPL>
+// key and value rows) are staged in shared memory once per CTA.  FINAL: the normalise
+// follows in the same pass (o = acc / max(sum, 1e-37), and lse when given) and acc_o is
+// not written back; acc_sum and acc_max are updated either way.
+struct FoldOut {
+  View o;
+  float *lse;
+};
+template <typename T, int EPL, bool FINAL>
 __global__ void __launch_bounds__(kFoldWarps * 32)
     fold_sinks_kernel(View q, float alpha, const int32_t *__restrict__ sink_idx, const float *__restrict__ sink_k,
                       const float *__restrict__ sink_v, float *__restrict__ acc_o, float *__restrict__ acc_sum,
-                      float *__restrict__ acc_max) {
+                      float *__restrict__ acc_max, FoldOut fo) {
   constexpr int D = 32 * EPL;
   __shared__ float sk[FM_MAX_SINKS][D];
   __shared__ float sv[FM_MAX_SINKS][D];
@@ -84,7 +90,7 @@ __global__ void __launch_bounds__(kFoldWarps * 32)
   const int64_t bh = b * q.H + h;
   int ns = 0;
   while (ns < FM_MAX_SINKS && sink_idx[bh * FM_MAX_SINKS + ns] != INT_MAX) ++ns;  // ascending, padded
-  if (ns == 0) return;  // no sink in this head: nothing to merge
+  if (!FINAL && ns == 0) return;  // no sink in this head: nothing to merge
   for (int e = threadIdx.x; e < ns * D; e += blockDim.x) {
     sk[e / D][e % D] = sink_k[(bh * FM_MAX_SINKS) * D + e];
     sv[e / D][e % D] = sink_v[(bh * FM_MAX_SINKS) * D + e];
@@ -137,13 +143,27 @@ __global__ void __launch_bounds__(kFoldWarps * 32)
         for (int e = 0; e < EPL; ++e) o[e] = fmaf(p, sv[s][lane * EPL + e], o[e]);
       }
     }
-    if constexpr (EPL == 4) {
+    const float sum_new = fmaf(acc_sum[r], c, psum);
+    if constexpr (FINAL) {
+      const float inv = 1.0f / fmaxf(sum_new, FM_SUM_CLAMP);
+      const int64_t off = b * fo.o.sB + h * fo.o.sH + row * fo.o.sS;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) {
+        const int64_t at = off + (int64_t)(lane * EPL + e) * fo.o.sD;
+        if (fo.o.dtype == FM_BF16)
+          reinterpret_cast<__nv_bfloat16 *>(const_cast<void *>(fo.o.ptr))[at] = __float2bfloat16_rn(o[e] * inv);
+        else
+          reinterpret_cast<float *>(const_cast<void *>(fo.o.ptr))[at] = o[e] * inv;
+      }
+      if (fo.lse && lane == 0) fo.lse[r] = 0.69314718055994531f * (r_new + log2f(sum_new));
+    } else if constexpr (EPL == 4) {
       *ao = make_float4(o[0], o[1], o[2], o[3]);
     } else {
       *reinterpret_cast<float2 *>(acc_o + r * D + lane * EPL) = make_float2(o[0], o[1]);
     }
+    __syncwarp();  // every lane has read acc_sum before lane 0 replaces it
     if (lane == 0) {
-      acc_sum[r] = fmaf(acc_sum[r], c, psum);
+      acc_sum[r] = sum_new;
       acc_max[r] = r_new;
     }
   }
@@ -183,23 +203,39 @@ cudaError_t launch_finalize_lse(const float *acc_o, const float *acc_sum, const 
   return launch_typed<true>(acc_o, acc_sum, acc_max, o, lse, st);
 }
 
-cudaError_t launch_fold_sinks(const View &q, float alpha, const int32_t *sink_idx, const float *sink_k,
-                              const float *sink_v, float *acc_o, float *acc_sum, float *acc_max, cudaStream_t st) {
+template <bool FINAL>
+cudaError_t launch_fold(const View &q, float alpha, const int32_t *sink_idx, const float *sink_k, const float *sink_v,
+                        float *acc_o, float *acc_sum, float *acc_max, const FoldOut &fo, cudaStream_t st) {
   if (q.B * q.H * q.S == 0) return cudaSuccess;
   const dim3 grid((unsigned)((q.S + kFoldRows - 1) / kFoldRows), (unsigned)q.H, (unsigned)q.B);
   const unsigned threads = kFoldWarps * 32;
   if (q.dtype == FM_BF16) {
     if (q.D == 128)
-      fold_sinks_kernel<__nv_bfloat16, 4><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum, acc_max);
+      fold_sinks_kernel<__nv_bfloat16, 4, FINAL><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o,
+                                                                            acc_sum, acc_max, fo);
     else
-      fold_sinks_kernel<__nv_bfloat16, 2><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum, acc_max);
+      fold_sinks_kernel<__nv_bfloat16, 2, FINAL><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o,
+                                                                            acc_sum, acc_max, fo);
   } else {
     if (q.D == 128)
-      fold_sinks_kernel<float, 4><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum, acc_max);
+      fold_sinks_kernel<float, 4, FINAL><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum,
+                                                                    acc_max, fo);
     else
-      fold_sinks_kernel<float, 2><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum, acc_max);
+      fold_sinks_kernel<float, 2, FINAL><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum,
+                                                                    acc_max, fo);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_fold_sinks(const View &q, float alpha, const int32_t *sink_idx, const float *sink_k,
+                              const float *sink_v, float *acc_o, float *acc_sum, float *acc_max, cudaStream_t st) {
+  return launch_fold<false>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum, acc_max, FoldOut{View{}, nullptr}, st);
+}
+
+cudaError_t launch_fold_sinks_final(const View &q, float alpha, const int32_t *sink_idx, const float *sink_k,
+                                    const float *sink_v, float *acc_o, float *acc_sum, float *acc_max, const View &o,
+                                    float *lse, cudaStream_t st) {
+  return launch_fold<true>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum, acc_max, FoldOut{o, lse}, st);
 }
 
 }  // namespace fm

@@ -103,6 +103,10 @@ cudaError_t launch_finalize_lse(const float *acc_o, const float *acc_sum, const 
 cudaError_t launch_fold_sinks(const View &q, float alpha, const int32_t *sink_idx, const float *sink_k,
                               const float *sink_v, float *acc_o, float *acc_sum, float *acc_max,
                               cudaStream_t st);
+// The same with the normalise in the same pass: o (and lse when given) written, acc_o not.
+cudaError_t launch_fold_sinks_final(const View &q, float alpha, const int32_t *sink_idx, const float *sink_k,
+                                    const float *sink_v, float *acc_o, float *acc_sum, float *acc_max, const View &o,
+                                    float *lse, cudaStream_t st);
 
 // ---- helpers shared by host code -------------------------------------------
 int current_device_sm_count();

@@ -214,7 +214,8 @@ FM_API int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_
  * unspecified afterwards).  The result equals fm_attn_chunk followed by fm_finalize (or
  * fm_finalize_lse); the tensor-core kernel does both in one launch where the layout of
  * o_out allows 16-byte stores, otherwise the two steps run back to back.  With key sinks
- * the steps are fm_attn_chunk, fm_fold_sinks and fm_finalize(_lse), back to back. */
+ * the chunk is folded as by fm_attn_chunk, then one pass merges the sinks back and
+ * normalises (the result of fm_fold_sinks followed by fm_finalize(_lse)). */
 FM_API int fm_attn_chunk_final(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk,
                                fm_bounds_out *bounds, const fm_opts *opts, float *acc_o, float *acc_sum,
                                float *acc_max, int accumulate, const fm_tensor *o_out, float *lse,

@@ -24,11 +24,11 @@ pages' adversarial examples; no dataset or trained weights are involved):
                                              (mean exactly zero), query row 0 has the norm
                                              that puts its bound at 231.01, other rows
                                              N(0,1); heads 20-39: N(0,1); centering on
-  sinks        B=1 H=40 S=4096   D=128 bf16  q,k,v = N(0,1) * D^(-1/4) as h40_s4096; in heads
+  sinks        B=1 H=40 S=16384  D=128 bf16  q,k,v = N(0,1) * D^(-1/4) as h40_s4096; in heads
                                              0-19 the keys at positions 0, 1, N/2+3 and N-1
                                              are scaled x100 (massive-activation key sinks,
                                              a norm spread in the pages' 100-1000x range);
-                                             4 chunks of 1024; centering off
+                                             4 chunks of 4096; centering off
 """
 from __future__ import annotations
 
@@ -77,7 +77,7 @@ WORKLOADS = {
     "adversarial": Workload("adversarial", 1, 40, 4096, 4096, 128, "bf16", (4096,), (True,), 5,
                             "heads 0-19: +/- unit key pairs, row 0 bound 231.01; heads 20-39 N(0,1)",
                             {"target_bound": 231.01, "adv_heads": 20}),
-    "sinks": Workload("sinks", 1, 40, 4096, 4096, 128, "bf16", (1024,) * 4, (False, True), 6,
+    "sinks": Workload("sinks", 1, 40, 16384, 16384, 128, "bf16", (4096,) * 4, (False, True), 6,
                       "N(0,1)*D^-1/4; heads 0-19: keys 0, 1, N/2+3, N-1 scaled x100",
                       {"sink_heads": 20, "sink_scale": 100.0}),
 }
