@@ -575,3 +575,19 @@ def test_sinks_full(dev):
     fb, o2 = run(q, k, v, workloads.chunk_bounds(w))
     assert not fb.bounds.flag[0, :w.extra["sink_heads"]].any()
     assert maxerr(o2[0, [0, 39]][:, rows], o[0, [0, 39]][:, rows]) <= TOL_BF16
+
+
+def test_key_sinks_with_per_row_centering_and_batches(dev):
+    """Key sinks combined with per-row shifts, centering and B = 2 (each batch entry and head
+    picks its own sinks); LSE included."""
+    q1, k1, v1 = workloads.make_inputs("sinks", device="cpu", heads=[0, 30], Sq=300, N=500)
+    q2, k2, v2 = workloads.make_inputs("sinks", device="cpu", heads=[5, 6], Sq=300, N=500)
+    q, k, v = torch.cat([q1, q2]), torch.cat([k1, k2]), torch.cat([v1, v2])
+    fa, o = run(q.to(dev), k.to(dev), v.to(dev), [(0, 260), (260, 240)], centering=True, per_row=True,
+                sink_keys=3, with_lse=True)
+    ob = oracle.bounds(q, k, v, centering=True, per_row=True, sink_keys=3)
+    check_bounds(fa, ob)
+    check_sinks(fa, ob)
+    ref, ref_lse = oracle.attention(q, k, v, return_lse=True)
+    assert maxerr(o, ref) <= TOL_BF16
+    assert maxerr(fa.lse, ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse))))
