@@ -591,3 +591,26 @@ def test_key_sinks_with_per_row_centering_and_batches(dev):
     ref, ref_lse = oracle.attention(q, k, v, return_lse=True)
     assert maxerr(o, ref) <= TOL_BF16
     assert maxerr(fa.lse, ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse))))
+
+
+@pytest.mark.parametrize("one_launch", [False, True])
+def test_head_and_batch_placement_bitwise(dev, one_launch):
+    """Scheduling changes that leave each (batch, head) problem's arithmetic alone give the same
+    bits (the bit-invariance pattern of PR444's heads_per_tile): heads in reverse order, and
+    the heads laid out as batch entries instead, so that a different CTA of the grid computes
+    each problem."""
+    q, k, v = workloads.make_inputs("mix", device=dev, heads=range(4), Sq=333, N=700)
+    chunks = [(0, 300), (300, 400)]
+
+    def go(qq, kk, vv):
+        fa = fm.FixedMAttention(qq.shape[0], qq.shape[1], 333, 700, 128, dev, centering=False)
+        o = fa.forward(qq, kk, vv, chunks, with_lse=True, one_launch=one_launch).clone()
+        fm.fm_sync_status()
+        return o, fa.lse.clone(), fa.bounds.m.clone(), fa.bounds.shift.clone()
+
+    base = go(q, k, v)
+    rev = go(q.flip(1).contiguous(), k.flip(1).contiguous(), v.flip(1).contiguous())
+    bat = go(q.transpose(0, 1).contiguous(), k.transpose(0, 1).contiguous(), v.transpose(0, 1).contiguous())
+    for a, r, bb in zip(base, rev, bat):
+        assert torch.equal(a, r.flip(1))
+        assert torch.equal(a, bb.transpose(0, 1))
