@@ -390,20 +390,6 @@ __device__ __noinline__ void mask_tile(uint32_t tS, int nvalid, int g0, const in
   tmem_st_wait();
 }
 
-// The same for the chunk holding the ragged end of the keys: columns >= nvalid give 0.
-__device__ __forceinline__ void exp_chunk_masked(const uint32_t (&s)[32], int col0, int nvalid, float alpha,
-                                                 float nbias, float (&l)[4], uint32_t (&pk)[16]) {
-#pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const int col = col0 + 2 * e;
-    const float p0 = col < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e]), alpha, nbias)) : 0.f;
-    const float p1 = col + 1 < nvalid ? ex2(fmaf(__uint_as_float(s[2 * e + 1]), alpha, nbias)) : 0.f;
-    l[e & 3] += p0;
-    l[(e + 2) & 3] += p1;
-    pk[e] = pack_bf16(p0, p1);
-  }
-}
-
 // Fixed-m softmax of one 128x128 S tile for this thread's row; P overwrites S.  The four
 // 32-column TMEM loads are double-buffered: chunk c+1 is in flight while chunk c is
 // exponentiated.  Key columns to leave out hold -inf (mask_tile) and give p = 0.
@@ -438,36 +424,46 @@ __device__ __forceinline__ void softmax_fixed_tile(uint32_t tS, float alpha, flo
   l[3] += y1;
 }
 
-__device__ __forceinline__ float max32(const uint32_t (&s)[32], int col0, int nvalid, float mx) {
+// The max of 64 scores in four independent chains (one chain would put every max
+// operation on the tile's critical path).
+__device__ __forceinline__ float max64(const uint32_t (&a)[32], const uint32_t (&b)[32], float mx) {
+  float m0 = mx, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < 32; ++e)
-    if (col0 + e < nvalid) mx = fmaxf(mx, __uint_as_float(s[e]));
-  return mx;
+  for (int e = 0; e < 32; e += 2) {
+    m0 = fmaxf(m0, __uint_as_float(a[e]));
+    m1 = fmaxf(m1, __uint_as_float(a[e + 1]));
+    m2 = fmaxf(m2, __uint_as_float(b[e]));
+    m3 = fmaxf(m3, __uint_as_float(b[e + 1]));
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
 }
 
-// Online softmax of one S tile, in one pass over TMEM: all 128 scores of the row are loaded
-// at once; the tile max updates the running max `run` (base-2 units) lazily (only when it
-// grows by more than 2^8, or on the first tile); p = 2^(alpha*s - run) goes back over S as
-// bf16 P; the row sum is rescaled before the new terms are added, and O in TMEM after P is
-// out.  The rescale decision is per row but tcgen05.ld/st are warp-collective, so the warp
-// rescales when any of its rows needs it and the other rows use a scale of 1.  Key sinks
-// hold -inf (mask_tile) and give p = 0 like the columns past nvalid.
-__device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, int nvalid, float alpha,
-                                                    bool have_o, float &run, float (&l)[4]) {
-  uint32_t s0[32], s1[32], s2[32], s3[32];
-  tmem_ld32_async(tS, s0);
-  tmem_ld32_async(tS + 32, s1);
-  tmem_ld32_async(tS + 64, s2);
-  tmem_ld32_async(tS + 96, s3);
-  tmem_ld_wait(s0);  // waits for all four
-  tmem_reg_tie(s1);
-  tmem_reg_tie(s2);
-  tmem_reg_tie(s3);
-  float mx = -INFINITY;
-  mx = max32(s0, 0, nvalid, mx);
-  mx = max32(s1, 32, nvalid, mx);
-  mx = max32(s2, 64, nvalid, mx);
-  mx = max32(s3, 96, nvalid, mx);
+// Online softmax of one S tile for this thread's row, in two passes over TMEM: the first
+// takes the row max of the 128 scores (two column halves, 64 registers), the second
+// exponentiates exactly like the fixed-m tile (double-buffered 32-column loads) with the
+// running max as the shift.  The tile max updates the running max `run` (base-2 units)
+// lazily: only when it grows by more than 2^8, or on the first tile.  The row sum is
+// rescaled before the new terms are added, and O in TMEM after P is out.  The rescale
+// decision is per row but tcgen05.ld/st are warp-collective, so the warp rescales when any
+// of its rows needs it and the other rows use a scale of 1.  Columns to leave out (past the
+// chunk's end, key sinks) hold -inf (mask_tile): they drop out of the max and give p = 0;
+// while every key so far was left out, run stays -inf and the shift used is 0.
+__device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, float alpha, bool have_o, float &run,
+                                                    float (&l)[4]) {
+  float mx;
+  {
+    uint32_t sa[32], sb[32];
+    tmem_ld32_async(tS, sa);
+    tmem_ld32_async(tS + 32, sb);
+    tmem_ld_wait(sa);
+    tmem_reg_tie(sb);
+    mx = max64(sa, sb, -INFINITY);
+    tmem_ld32_async(tS + 64, sa);
+    tmem_ld32_async(tS + 96, sb);
+    tmem_ld_wait(sa);
+    tmem_reg_tie(sb);
+    mx = max64(sa, sb, mx);
+  }
   const float zmax = mx * alpha;
   const bool need = run == -INFINITY || zmax > run + kLazyRescale;
   const bool any = __any_sync(0xffffffffu, need);
@@ -480,37 +476,7 @@ __device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, in
 #pragma unroll
     for (int i = 0; i < 4; ++i) l[i] *= sc;
   }
-  const float nb = run == -INFINITY ? 0.f : -run;  // every key so far left out: p = 2^-inf = 0
-  uint32_t pk[16];
-  if (nvalid >= kBK) {
-    const uint64_t a2 = f2_pack(__float_as_uint(alpha), __float_as_uint(alpha));
-    const uint64_t nb2 = f2_pack(__float_as_uint(nb), __float_as_uint(nb));
-    uint64_t acc0 = 0, acc1 = 0;
-    exp_chunk_full(s0, a2, nb2, acc0, acc1, pk);
-    tmem_st16(tS + 0, pk);
-    exp_chunk_full(s1, a2, nb2, acc0, acc1, pk);
-    tmem_st16(tS + 16, pk);
-    exp_chunk_full(s2, a2, nb2, acc0, acc1, pk);
-    tmem_st16(tS + 32, pk);
-    exp_chunk_full(s3, a2, nb2, acc0, acc1, pk);
-    tmem_st16(tS + 48, pk);
-    float x0, x1, y0, y1;
-    f2_unpack(acc0, x0, x1);
-    f2_unpack(acc1, y0, y1);
-    l[0] += x0;
-    l[1] += x1;
-    l[2] += y0;
-    l[3] += y1;
-  } else {
-    exp_chunk_masked(s0, 0, nvalid, alpha, nb, l, pk);
-    tmem_st16(tS + 0, pk);
-    exp_chunk_masked(s1, 32, nvalid, alpha, nb, l, pk);
-    tmem_st16(tS + 16, pk);
-    exp_chunk_masked(s2, 64, nvalid, alpha, nb, l, pk);
-    tmem_st16(tS + 32, pk);
-    exp_chunk_masked(s3, 96, nvalid, alpha, nb, l, pk);
-    tmem_st16(tS + 48, pk);
-  }
+  softmax_fixed_tile(tS, alpha, run == -INFINITY ? 0.f : -run, l);
   if (any && have_o) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -701,12 +667,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int g0 = p.key0[c] + jl;               // global index of the tile's first key
       if (next_sink < g0)  // sinks before this tile
         next_sink = sink_after_key(reinterpret_cast<const int32_t *>(gbase + kOffSinks), g0 - 1);
-      // -inf over the key sinks in this tile, and (fixed-m rows) over the columns past the
-      // chunk's end; the online rows mask those columns themselves
-      if (next_sink < g0 + nvalid || (fixed && nvalid < kBK))
+      // -inf over the key sinks in this tile and over the columns past the chunk's end
+      if (next_sink < g0 + nvalid || nvalid < kBK)
         mask_tile(tS, nvalid, g0, reinterpret_cast<const int32_t *>(gbase + kOffSinks), next_sink);
       if (fixed) softmax_fixed_tile(tS, p.alpha, -shv, l);
-      else softmax_online_tile(tS, tO, nvalid, p.alpha, j > 0, shv, l);
+      else softmax_online_tile(tS, tO, p.alpha, j > 0, shv, l);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(kBarPReady + t));
