@@ -35,7 +35,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # launch, scaled x5 to 40 heads (every term of the traffic grows with the head count).
 # Valid only for the kernel code it was measured on (comments aside): the bench reports null
 # otherwise.
-CHUNK_TRAFFIC = {"code_sha256_16": "457d5a5ecfeb81fa", "bytes_per_launch": 5 * (604.860e6 + 837.735e6) / 2}
+CHUNK_TRAFFIC = {"code_sha256_16": "747bb2211448602d", "bytes_per_launch": 5 * (602.278e6 + 833.299e6) / 2}
 
 
 def kernel_code_hash(path: str) -> str:
