@@ -17,6 +17,10 @@
 // softmax warps keep a running row max, rescale O in TMEM when the max grows by more
 // than 2^8 (lazy rescale: exact, since the final shift is whatever the running max is),
 // and merge with the previous chunks through acc_max.
+// Key columns that must not count -- past a chunk's ragged end, or key sinks that the
+// bounds pass left out of the key max ("Kernel reference: ring_attention_const_max_fwd",
+// section "Adapting this kernel") -- get -inf written over their scores in TMEM before the
+// softmax reads them, so they give p = 0 with no masks in the per-element code.
 //
 // CTA = two 128-row Q tiles of one (batch, head) (256 rows) against every KV tile of the
 // launch: one chunk, or several consecutive chunks (up to 8), whose key tiles are walked in
