@@ -614,3 +614,26 @@ def test_head_and_batch_placement_bitwise(dev, one_launch):
     for a, r, bb in zip(base, rev, bat):
         assert torch.equal(a, r.flip(1))
         assert torch.equal(a, bb.transpose(0, 1))
+
+
+def test_key_sink_positions_and_ties_on_the_device(dev):
+    """Sinks at the edges of the bounds pass's 256-key blocks and of the 128-key tiles
+    (positions 127, 128, 255, 256, 512 of 513 keys), split across chunks at 256; and a tie:
+    two identical loudest keys with sink_keys = 1 give no sink at all (only keys strictly
+    louder than the first kept one are sinks), on the device as in the oracle."""
+    q, k, v = workloads.make_inputs("h40_s4096", device="cpu", heads=[0, 1], Sq=140, N=513)
+    pos = [127, 128, 255, 256, 512]
+    k[:, 0, pos] *= 60.0
+    k[:, 1, 300] = k[:, 1, 40] * 80.0   # head 1: two identical loud keys
+    k[:, 1, 40] = k[:, 1, 300]
+    ob = oracle.bounds(q, k, v, sink_keys=5)
+    fa, o = run(q.to(dev), k.to(dev), v.to(dev), [(0, 256), (256, 257)], sink_keys=5)
+    check_bounds(fa, ob)
+    assert list(fa.bounds.sink_idx[0, 0, :5].cpu().numpy()) == pos
+    assert maxerr(o, oracle.attention(q, k, v)) <= TOL_BF16
+    ob1 = oracle.bounds(q, k, v, sink_keys=1)
+    fb, o1 = run(q.to(dev), k.to(dev), v.to(dev), [(0, 513)], sink_keys=1)
+    assert list(ob1["sink_idx"][0, 1]) == [2**31 - 1]
+    assert int(fb.bounds.sink_idx[0, 1, 0].item()) == 2**31 - 1
+    assert float(fb.bounds.kmax_sq[0, 1].item()) == pytest.approx(float(ob1["kmax_sq"][0, 1]), rel=2e-5)
+    assert maxerr(o1, oracle.attention(q, k, v)) <= TOL_BF16
