@@ -637,3 +637,22 @@ def test_key_sink_positions_and_ties_on_the_device(dev):
     assert int(fb.bounds.sink_idx[0, 1, 0].item()) == 2**31 - 1
     assert float(fb.bounds.kmax_sq[0, 1].item()) == pytest.approx(float(ob1["kmax_sq"][0, 1]), rel=2e-5)
     assert maxerr(o1, oracle.attention(q, k, v)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("force_online", [False, True])
+def test_ring_order_of_chunks(dev, force_online):
+    """The ring hands each device the KV chunks in a rotated order.  The fixed-m merge is a pure
+    add, and the online one a max-rescaled add, so folding the chunks in any order gives the same
+    result up to fp32 summation order (within the bf16 tolerance, and close to each other)."""
+    q, k, v = workloads.make_inputs("mix", device="cpu", heads=range(2), Sq=300, N=900)
+    qd = q.to(dev)
+    parts = [(0, 300), (300, 300), (600, 300)]
+    ref = oracle.attention(q, k, v)
+    outs = []
+    for order in ([0, 1, 2], [1, 2, 0], [2, 0, 1]):
+        kk = torch.cat([k[:, :, s:s + n] for s, n in (parts[i] for i in order)], dim=2).to(dev)
+        vv = torch.cat([v[:, :, s:s + n] for s, n in (parts[i] for i in order)], dim=2).to(dev)
+        _, o = run(qd, kk, vv, parts, force_online=force_online)
+        assert maxerr(o, ref) <= TOL_BF16
+        outs.append(o.clone())
+    assert maxerr(outs[0], outs[1]) <= 1e-3 and maxerr(outs[0], outs[2]) <= 1e-3
