@@ -143,7 +143,7 @@ class ClockSampler:
                 "samples": len(sms)}
 
 
-def cpu_oracle_sample(target_s: float = 12.0, max_rows: int = 4096):
+def cpu_oracle_sample(target_s: float = 12.0, max_rows: int = 24576):
     """Time the fp64 CPU oracle on 1 head x R query rows x all 75,600 keys of the workload.
 
     R grows until one timed call takes about target_s seconds.  Returns (TFLOP/s, dict)."""
