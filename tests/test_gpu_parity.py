@@ -656,3 +656,31 @@ def test_ring_order_of_chunks(dev, force_online):
         assert maxerr(o, ref) <= TOL_BF16
         outs.append(o.clone())
     assert maxerr(outs[0], outs[1]) <= 1e-3 and maxerr(outs[0], outs[2]) <= 1e-3
+
+
+def test_cuda_graph_capture_with_key_sinks(dev):
+    """The key-sink path (selection in the bounds pass, masked chunks, the fold with the
+    normalise) has no host synchronisation either: captured once and replayed on new data it
+    gives the eager bits."""
+    Sq, N = 400, 900
+    chunks = [(0, 450), (450, 450)]
+    q, k, v = workloads.make_inputs("sinks", device=dev, heads=[0, 1, 30], Sq=Sq, N=N)
+    q2, k2, v2 = workloads.make_inputs("sinks", device=dev, heads=[2, 3, 31], Sq=Sq, N=N)
+    fa = fm.FixedMAttention(1, 3, Sq, N, 128, dev, sink_keys=4)
+    fa.forward(q, k, v, chunks, with_lse=True)
+    fm.fm_sync_status()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa.forward(q, k, v, chunks, with_lse=True)
+    q.copy_(q2)
+    k.copy_(k2)
+    v.copy_(v2)
+    g.replay()
+    torch.cuda.synchronize()
+    fm.fm_sync_status()
+    fb = fm.FixedMAttention(1, 3, Sq, N, 128, dev, sink_keys=4)
+    ref = fb.forward(q2, k2, v2, chunks, with_lse=True)
+    fm.fm_sync_status()
+    assert torch.equal(fa.out, ref) and torch.equal(fa.lse, fb.lse)
+    assert torch.equal(fa.bounds.sink_idx, fb.bounds.sink_idx)
+    assert maxerr(fa.out, oracle.attention(q2.cpu(), k2.cpu(), v2.cpu())) <= TOL_BF16
