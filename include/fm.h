@@ -111,7 +111,8 @@ typedef struct {
  *   m       int32 [B, H, nqb]  per-(head, Q-block) shift m = ceil(U) - C(N)
  *   flag    uint8 [B, H, nqb]  1 = eligible for fixed-m: v_ok && U <= gate
  *   qmax_sq f32   [B, H, nqb]  max over the block's rows of ||q_i||^2
- *   kmax_sq f32   [B, H]       max_j ||k_j - kbar||^2 (centered) or ||k_j||^2
+ *   kmax_sq f32   [B, H]       max_j ||k_j - kbar||^2 (centered) or ||k_j||^2, over the
+ *                              keys that are not sinks
  *   kbar    f32   [B, H, D]    mean key over all real keys ([PR478] Summary); 0 if
  *                              not centering
  *   qkbar   f32   [B, H, Sq]   alpha * q_i . kbar, the per-row centering term; 0 if not
