@@ -558,6 +558,17 @@ def test_key_sinks_cuda_core_path_and_edges(dev):
     with pytest.raises(fm.FMError) as e:
         fm.fm_attn_chunk(qs.to(dev), ks.to(dev), vs.to(dev), fa.bounds, fa.opt, fa.acc_o, fa.acc_sum, fa.acc_max, True)
     assert e.value.code == fm.FM_ERR_BOUNDS_MISMATCH
+    # D = 64 (fp32, CUDA-core kernel) with per-row shifts and sinks
+    qt, kt, vt = workloads.make_inputs("tiny", device="cpu")
+    kt[0, 0, [3, 200]] *= 30.0
+    fa, o = run(qt.to(dev), kt.to(dev), vt.to(dev), [(0, 100), (100, 156)], per_row=True, sink_keys=2)
+    check_bounds(fa, oracle.bounds(qt, kt, vt, per_row=True, sink_keys=2))
+    assert list(fa.bounds.sink_idx[0, 0, :2].cpu().numpy()) == [3, 200]
+    assert maxerr(o, oracle.attention(qt, kt, vt)) <= TOL_F32
+    # no keys at all: no sinks, an empty key set gives 0
+    z = torch.zeros(1, 1, 130, 128, dtype=torch.bfloat16, device=dev)
+    fa, o = run(z, z[:, :, :0], z[:, :, :0], [(0, 0)], sink_keys=3)
+    assert torch.all(fa.bounds.sink_idx == 2**31 - 1) and torch.all(o == 0)
 
 
 def test_sinks_full(dev):
