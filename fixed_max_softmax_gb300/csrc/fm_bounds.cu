@@ -135,6 +135,8 @@ __device__ __forceinline__ void warp_best_sink(float &bv, int32_t &bi) {
 // 1. Partial key sums: CTA (p, h, b) sums rows [p*len, (p+1)*len) of head (b, h).
 template <typename T, int EPL, bool CONTIG>
 __global__ void __launch_bounds__(kThreads) ksum_kernel(View k, int64_t P, float *part) {
+  pdl_wait();  // inputs written by the kernels before this one
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t b = blockIdx.z, h = blockIdx.y, p = blockIdx.x;
   const int64_t len = ceil_div(k.S, P);
@@ -165,6 +167,8 @@ __global__ void __launch_bounds__(kThreads) ksum_kernel(View k, int64_t P, float
 
 // 2. Key mean: ordered sum of the P partials of head (b, h), divided by N.
 __global__ void kmean_kernel(const float *part, int64_t H, int64_t P, int D, int64_t N, float *kbar) {
+  pdl_wait();  // inputs written by the kernels before this one
+  pdl_trigger();
   const int64_t bh = blockIdx.y * H + blockIdx.x;
   const int d = threadIdx.x;
   if (d >= D) return;
@@ -179,6 +183,8 @@ __global__ void __launch_bounds__(kThreads)
     norms_kernel(View q, View k, View v, int64_t nqb, int64_t nkb, int centering, float alpha,
                  const float *kbar, float *qmax_sq, float *qkbar, float *qsq, float *kblk, float *vblk,
                  int n_sink, SinkCand *cand) {
+  pdl_wait();  // inputs written by the kernels before this one
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t b = blockIdx.z, h = blockIdx.y, bx = blockIdx.x;
   const int64_t bh = b * q.H + h;
@@ -285,6 +291,8 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
     sink_select_kernel(View k, View v, int64_t nkb, int n_sink, const SinkCand *cand, int32_t *sink_idx,
                        float *sink_k, float *sink_v, float *kmax_sq) {
+  pdl_wait();  // inputs written by the kernels before this one
+  pdl_trigger();
   const int64_t b = blockIdx.y, h = blockIdx.x;
   const int64_t bh = b * k.H + h;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -372,6 +380,8 @@ __global__ void __launch_bounds__(kThreads)
     finish_kernel(int64_t H, int64_t nqb, int64_t nkb, int64_t n_heads_total, const float *kblk,
                   const float *vblk, double alpha, int C, int gate, const float *qmax_sq,
                   float *kmax_sq, float *vmax_sq, int32_t *m, uint8_t *flag, int kmax_given) {
+  pdl_wait();  // inputs written by the kernels before this one
+  pdl_trigger();
   const int64_t bh = blockIdx.y * H + blockIdx.x;
   __shared__ float red[2][kWarps];
   float km = 0.f, vm = 0.f;
@@ -405,6 +415,8 @@ __global__ void __launch_bounds__(kThreads)
 __global__ void __launch_bounds__(kThreads)
     shift_kernel(int64_t H, int64_t Sq, int64_t nqb, int per_row, double alpha, int C, const float *kmax_sq,
                  const int32_t *m, const float *qkbar, float *shift) {
+  pdl_wait();  // inputs written by the kernels before this one
+  pdl_trigger();
   const int64_t bh = blockIdx.z * H + blockIdx.y;
   const int64_t r = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   if (r >= Sq) return;
@@ -428,29 +440,35 @@ cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st
   float *vblk = reinterpret_cast<float *>(ws + w.off_vb);
   SinkCand *cand = reinterpret_cast<SinkCand *>(ws + w.off_cand);
   const int D = (int)a.q.D;
+  const dim3 heads((unsigned)H, (unsigned)B);
+  cudaError_t e = cudaSuccess;
   if (a.centering && N > 0) {
-    ksum_kernel<T, EPL, CONTIG><<<dim3((unsigned)w.P, (unsigned)H, (unsigned)B), kThreads, 0, st>>>(a.k, w.P, part);
-    kmean_kernel<<<dim3((unsigned)H, (unsigned)B), 128, 0, st>>>(part, H, w.P, D, N, a.kbar);
+    e = launch_pdl(ksum_kernel<T, EPL, CONTIG>, dim3((unsigned)w.P, (unsigned)H, (unsigned)B), dim3(kThreads), 0, st,
+                   a.k, w.P, part);
+    if (e == cudaSuccess) e = launch_pdl(kmean_kernel, heads, dim3(128), 0, st, part, H, w.P, D, N, a.kbar);
   } else {
-    cudaError_t e = cudaMemsetAsync(a.kbar, 0, sizeof(float) * (size_t)(B * H * D), st);
-    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(a.kbar, 0, sizeof(float) * (size_t)(B * H * D), st);
   }
+  if (e != cudaSuccess) return e;
   const int64_t nx = a.nqb + 2 * w.nkb;
   if (nx > 0) {
-    norms_kernel<T, EPL, CONTIG><<<dim3((unsigned)nx, (unsigned)H, (unsigned)B), kThreads, 0, st>>>(
-        a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk,
-        a.n_sink, cand);
+    e = launch_pdl(norms_kernel<T, EPL, CONTIG>, dim3((unsigned)nx, (unsigned)H, (unsigned)B), dim3(kThreads), 0, st,
+                   a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk,
+                   vblk, a.n_sink, cand);
+    if (e != cudaSuccess) return e;
   }
   if (a.n_sink > 0) {
-    sink_select_kernel<T><<<dim3((unsigned)H, (unsigned)B), kThreads, 0, st>>>(
-        a.k, a.v, w.nkb, a.n_sink, cand, a.sink_idx, a.sink_k, a.sink_v, a.kmax_sq);
+    e = launch_pdl(sink_select_kernel<T>, heads, dim3(kThreads), 0, st, a.k, a.v, w.nkb, a.n_sink, cand, a.sink_idx,
+                   a.sink_k, a.sink_v, a.kmax_sq);
+    if (e != cudaSuccess) return e;
   }
-  finish_kernel<<<dim3((unsigned)H, (unsigned)B), kThreads, 0, st>>>(
-      H, a.nqb, w.nkb, B * H, kblk, vblk, a.alpha, a.C, a.gate, a.qmax_sq, a.kmax_sq, a.vmax_sq, a.m, a.flag,
-      a.n_sink > 0);
+  e = launch_pdl(finish_kernel, heads, dim3(kThreads), 0, st, H, a.nqb, w.nkb, B * H, kblk, vblk, a.alpha, a.C, a.gate,
+                 a.qmax_sq, a.kmax_sq, a.vmax_sq, a.m, a.flag, (int)(a.n_sink > 0));
+  if (e != cudaSuccess) return e;
   if (a.q.S > 0) {
-    shift_kernel<<<dim3((unsigned)ceil_div(a.q.S, kThreads), (unsigned)H, (unsigned)B), kThreads, 0, st>>>(
-        H, a.q.S, a.nqb, a.per_row, a.alpha, a.C, a.kmax_sq, a.m, a.qkbar, a.shift);
+    e = launch_pdl(shift_kernel, dim3((unsigned)ceil_div(a.q.S, kThreads), (unsigned)H, (unsigned)B), dim3(kThreads),
+                   0, st, H, a.q.S, a.nqb, a.per_row, a.alpha, a.C, a.kmax_sq, a.m, a.qkbar, a.shift);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }

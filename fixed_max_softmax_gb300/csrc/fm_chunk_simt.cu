@@ -36,6 +36,8 @@ __device__ __forceinline__ float ld_elem(const T *p) {
 template <typename T, int D>
 __global__ void __launch_bounds__(kRows *(D / kDimsPerThread))
     chunk_simt_kernel(const ChunkArgs a) {
+  pdl_wait();  // bounds and accumulators written by the kernels before this one
+  pdl_trigger();
   constexpr int TPR = D / kDimsPerThread;  // threads per row (2 or 4)
   constexpr int NT = kRows * TPR;
   __shared__ float Ks[kKeys][D];
@@ -174,8 +176,7 @@ cudaError_t launch_typed(const ChunkArgs &a, cudaStream_t st) {
   constexpr int TPR = D / kDimsPerThread;
   dim3 grid((unsigned)((a.q.S + kRows - 1) / kRows), (unsigned)a.q.H, (unsigned)a.q.B);
   if (grid.x == 0) return cudaSuccess;
-  chunk_simt_kernel<T, D><<<grid, kRows * TPR, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(chunk_simt_kernel<T, D>, grid, dim3(kRows * TPR), 0, st, a);
 }
 
 }  // namespace

@@ -495,6 +495,8 @@ __device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, fl
 
 __global__ void __launch_bounds__(kThreads, 1)
     fm_chunk_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
+  pdl_wait();  // bounds and accumulators written by the kernels before this one
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -898,8 +900,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
     p.osS = a.out->sS;
   }
   dim3 grid((unsigned)((a.nqb + 1) / 2), (unsigned)a.q.H, (unsigned)a.q.B);
-  fm_chunk_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(maps, p);
-  return cudaGetLastError();
+  return launch_pdl(fm_chunk_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, maps, p);
 }
 
 cudaError_t launch_wait_probe(unsigned int *err, unsigned long long timeout_ns, cudaStream_t st) {

@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(256) finalize_kernel(const float *__restrict__
                                                        const float *__restrict__ acc_sum,
                                                        const float *__restrict__ acc_max, float *__restrict__ lse,
                                                        View o, int64_t n_quads) {
+  pdl_wait();  // the accumulators written by the kernels before this one
+  pdl_trigger();
   const int64_t D = o.D;
   const int64_t qpr = D / 4;  // quads per row
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_quads;
@@ -83,6 +85,8 @@ __global__ void __launch_bounds__(kFoldWarps * 32)
     fold_sinks_kernel(View q, float alpha, const int32_t *__restrict__ sink_idx, const float *__restrict__ sink_k,
                       const float *__restrict__ sink_v, float *__restrict__ acc_o, float *__restrict__ acc_sum,
                       float *__restrict__ acc_max, FoldOut fo) {
+  pdl_wait();  // the accumulators written by the kernels before this one
+  pdl_trigger();
   constexpr int D = 32 * EPL;
   __shared__ float sk[FM_MAX_SINKS][D];
   __shared__ float sv[FM_MAX_SINKS][D];
@@ -182,14 +186,19 @@ cudaError_t launch_typed(const float *acc_o, const float *acc_sum, const float *
   int64_t blocks = (n_quads + 255) / 256;
   const int64_t cap = (int64_t)sms * 16;
   if (blocks > cap) blocks = cap;
+  const dim3 grid((unsigned)blocks), threads(256);
+  cudaError_t e;
   if (o.dtype == FM_BF16) {
-    if (vec) finalize_kernel<true, true, LSE><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, acc_max, lse, o, n_quads);
-    else finalize_kernel<true, false, LSE><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, acc_max, lse, o, n_quads);
+    e = vec ? launch_pdl(finalize_kernel<true, true, LSE>, grid, threads, 0, st, acc_o, acc_sum, acc_max, lse, o, n_quads)
+            : launch_pdl(finalize_kernel<true, false, LSE>, grid, threads, 0, st, acc_o, acc_sum, acc_max, lse, o,
+                         n_quads);
   } else {
-    if (vec) finalize_kernel<false, true, LSE><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, acc_max, lse, o, n_quads);
-    else finalize_kernel<false, false, LSE><<<(unsigned)blocks, 256, 0, st>>>(acc_o, acc_sum, acc_max, lse, o, n_quads);
+    e = vec ? launch_pdl(finalize_kernel<false, true, LSE>, grid, threads, 0, st, acc_o, acc_sum, acc_max, lse, o,
+                         n_quads)
+            : launch_pdl(finalize_kernel<false, false, LSE>, grid, threads, 0, st, acc_o, acc_sum, acc_max, lse, o,
+                         n_quads);
   }
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace
@@ -208,23 +217,16 @@ cudaError_t launch_fold(const View &q, float alpha, const int32_t *sink_idx, con
                         float *acc_o, float *acc_sum, float *acc_max, const FoldOut &fo, cudaStream_t st) {
   if (q.B * q.H * q.S == 0) return cudaSuccess;
   const dim3 grid((unsigned)((q.S + kFoldRows - 1) / kFoldRows), (unsigned)q.H, (unsigned)q.B);
-  const unsigned threads = kFoldWarps * 32;
-  if (q.dtype == FM_BF16) {
-    if (q.D == 128)
-      fold_sinks_kernel<__nv_bfloat16, 4, FINAL><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o,
-                                                                            acc_sum, acc_max, fo);
-    else
-      fold_sinks_kernel<__nv_bfloat16, 2, FINAL><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o,
-                                                                            acc_sum, acc_max, fo);
-  } else {
-    if (q.D == 128)
-      fold_sinks_kernel<float, 4, FINAL><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum,
-                                                                    acc_max, fo);
-    else
-      fold_sinks_kernel<float, 2, FINAL><<<grid, threads, 0, st>>>(q, alpha, sink_idx, sink_k, sink_v, acc_o, acc_sum,
-                                                                    acc_max, fo);
-  }
-  return cudaGetLastError();
+  const dim3 threads(kFoldWarps * 32);
+  if (q.dtype == FM_BF16)
+    return q.D == 128 ? launch_pdl(fold_sinks_kernel<__nv_bfloat16, 4, FINAL>, grid, threads, 0, st, q, alpha, sink_idx,
+                                   sink_k, sink_v, acc_o, acc_sum, acc_max, fo)
+                      : launch_pdl(fold_sinks_kernel<__nv_bfloat16, 2, FINAL>, grid, threads, 0, st, q, alpha, sink_idx,
+                                   sink_k, sink_v, acc_o, acc_sum, acc_max, fo);
+  return q.D == 128 ? launch_pdl(fold_sinks_kernel<float, 4, FINAL>, grid, threads, 0, st, q, alpha, sink_idx, sink_k,
+                                 sink_v, acc_o, acc_sum, acc_max, fo)
+                    : launch_pdl(fold_sinks_kernel<float, 2, FINAL>, grid, threads, 0, st, q, alpha, sink_idx, sink_k,
+                                 sink_v, acc_o, acc_sum, acc_max, fo);
 }
 
 cudaError_t launch_fold_sinks(const View &q, float alpha, const int32_t *sink_idx, const float *sink_k,

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/fm.h"
 
 namespace fm {
@@ -110,5 +112,30 @@ cudaError_t launch_fold_sinks_final(const View &q, float alpha, const int32_t *s
 
 // ---- helpers shared by host code -------------------------------------------
 int current_device_sm_count();
+
+// Programmatic dependent launch: the kernel may be scheduled while the kernel before it in
+// the stream is still finishing, so its launch latency and block scheduling overlap that
+// kernel's tail.  Every kernel launched this way runs pdl_wait() before it reads anything
+// an earlier kernel wrote (the wait returns once the previous grid has completed and its
+// memory is visible), and pdl_trigger() to let the next kernel be scheduled.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
 
 }  // namespace fm
