@@ -35,7 +35,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # launch, scaled x5 to 40 heads (every term of the traffic grows with the head count).
 # Valid only for the kernel code it was measured on (comments aside): the bench reports null
 # otherwise.
-CHUNK_TRAFFIC = {"code_sha256_16": "747bb2211448602d", "bytes_per_launch": 5 * (602.278e6 + 833.299e6) / 2}
+CHUNK_TRAFFIC = {"code_sha256_16": "9c5e075705d22a12", "bytes_per_launch": 5 * (604.363e6 + 830.639e6) / 2}
 
 
 def kernel_code_hash(path: str) -> str:
@@ -388,7 +388,7 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-rows", type=int, default=256, help="query rows per reference step")
