@@ -695,3 +695,40 @@ def test_cuda_graph_capture_with_key_sinks(dev):
     assert torch.equal(fa.out, ref) and torch.equal(fa.lse, fb.lse)
     assert torch.equal(fa.bounds.sink_idx, fb.bounds.sink_idx)
     assert maxerr(fa.out, oracle.attention(q2.cpu(), k2.cpu(), v2.cpu())) <= TOL_BF16
+
+
+def test_randomised_shapes_and_options(dev):
+    """Forty seeded random cases against the oracle: batch, heads, query and key lengths
+    (ragged everywhere), chunk splits (empty chunks included), dtype and head dimension, and
+    every option (centering, per-row shifts, key sinks, forced fallback, LSE, one launch)."""
+    rng = np.random.default_rng(1234)
+    for case in range(40):
+        B = int(rng.integers(1, 3))
+        H = int(rng.integers(1, 4))
+        Sq = int(rng.integers(1, 400))
+        N = int(rng.integers(1, 700))
+        D = 128 if rng.random() < 0.8 else 64
+        dt = torch.bfloat16 if (D == 128 and rng.random() < 0.8) else torch.float32
+        g = torch.Generator().manual_seed(case)
+        scale = float(rng.choice([0.3, 1.0, 3.0]))
+        q = (torch.randn(B, H, Sq, D, generator=g) * scale).to(dt)
+        k = (torch.randn(B, H, N, D, generator=g) + float(rng.normal()) * 2.0).to(dt)
+        v = torch.randn(B, H, N, D, generator=g).to(dt)
+        n_chunks = int(rng.integers(1, 5))
+        cuts = np.sort(rng.integers(0, N + 1, size=n_chunks - 1))
+        edges = [0, *cuts.tolist(), N]
+        chunks = [(edges[i], edges[i + 1] - edges[i]) for i in range(n_chunks)]
+        opts = dict(centering=bool(rng.random() < 0.5), per_row=bool(rng.random() < 0.3),
+                    force_online=bool(rng.random() < 0.2), sink_keys=int(rng.choice([0, 0, 1, 3])))
+        fa = fm.FixedMAttention(B, H, Sq, N, D, dev, **opts)
+        one = bool(rng.random() < 0.3)
+        o = fa.forward(q.to(dev), k.to(dev), v.to(dev), chunks, with_lse=True, one_launch=one)
+        fm.fm_sync_status()
+        ref, ref_lse = oracle.attention(q, k, v, return_lse=True)
+        tol = TOL_F32 if dt == torch.float32 else TOL_BF16
+        desc = (case, B, H, Sq, N, D, dt, chunks, opts, one)
+        assert maxerr(o, ref) <= tol, desc
+        assert maxerr(fa.lse, ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse)))), desc
+        ob = oracle.bounds(q, k, v, centering=opts["centering"], per_row=opts["per_row"],
+                           sink_keys=opts["sink_keys"])
+        check_bounds(fa, ob)
