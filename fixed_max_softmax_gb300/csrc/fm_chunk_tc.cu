@@ -711,8 +711,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t ooff = bb * p.osB + hh * p.osH + row * p.osS;
       const float4 *src = reinterpret_cast<const float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
       float4 *dst = reinterpret_cast<float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
+      // the accumulator row comes in 32-column pieces, each loaded while the previous piece is
+      // combined, so that the row pays one memory latency instead of four
+      const bool rd = row_ok && p.accumulate;
+      float4 ya[8], yb[8];
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) ya[q4] = rd ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
+        float4(&ycur)[8] = (c & 1) ? yb : ya;
+        float4(&ynext)[8] = (c & 1) ? ya : yb;
+        if (c < 3) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) ynext[q4] = rd ? src[(c + 1) * 8 + q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         uint32_t o[32];
         tmem_ld32(tO + c * 32, o);
         if (row_ok) {
@@ -721,7 +733,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float4 x = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
                                    __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
             if (p.accumulate) {
-              const float4 y = src[c * 8 + q4];
+              const float4 y = ycur[q4];
               if (fixed) {
                 x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
               } else {
