@@ -266,3 +266,42 @@ def test_fold_sinks_validation(lib):
     b2.online_lock = 0
     assert lib.fm_fold_sinks(ctypes.byref(q), ctypes.byref(b2), ctypes.byref(fm.opts()), FAKE, FAKE, FAKE,
                              None) == fm.FM_OK           # no sinks: nothing to do, nothing enqueued
+
+
+def test_plain_c_program_uses_the_abi(lib, tmp_path):
+    """The boundary is a C ABI: a C program that includes only include/fm.h links against
+    libfm.so and calls it (version, workspace size, a call refused on the host) with no
+    Python in between."""
+    import subprocess
+    src = tmp_path / "use_fm.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "fm.h"
+int main(void) {
+  size_t ws = 0;
+  if (fm_bounds_workspace_size(1, 40, 75600, 128, &ws) != FM_OK || ws == 0) return 1;
+  fm_tensor t;
+  memset(&t, 0, sizeof t);
+  t.ptr = (void *)0x10000;
+  t.dtype = FM_F16;
+  t.B = 1; t.H = 2; t.S = 64; t.D = 128;
+  t.stride[0] = 2 * 64 * 128; t.stride[1] = 64 * 128; t.stride[2] = 128; t.stride[3] = 1;
+  fm_opts o;
+  memset(&o, 0, sizeof o);
+  fm_bounds_out b;
+  memset(&b, 0, sizeof b);
+  int rc = fm_bounds(&t, &t, &t, &o, &b, NULL, 0, NULL);
+  printf("%d %d %zu %s\n", fm_version() >> 16, rc, ws, fm_last_error());
+  return rc == FM_ERR_DTYPE ? 0 : 2;
+}
+''')
+    exe = tmp_path / "use_fm"
+    libdir = os.path.dirname(fm.LIB_PATH)
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe), "-L", libdir,
+                    "-lfm", f"-Wl,-rpath,{libdir}"], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, (r.stdout, r.stderr)
+    major, rc, ws, *msg = r.stdout.split()
+    assert int(major) == 1 and int(rc) == fm.FM_ERR_DTYPE and int(ws) == fm.fm_bounds_workspace_size(1, 40, 75600, 128)
+    assert "fp16" in " ".join(msg)
