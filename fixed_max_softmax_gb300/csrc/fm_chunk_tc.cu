@@ -40,6 +40,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <limits.h>
+#include <string.h>
 #include <math.h>
 
 #include <mutex>
@@ -165,6 +166,30 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm,
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
+}
+
+// O of one Q tile from shared memory into the fp32 accumulator (3-D map over [B*H, Sq, D]):
+// added to it (reduce) or written over it (store).  Rows past Sq are clipped by the map.
+__device__ __forceinline__ void tma_acc_3d(const CUtensorMap *tm, uint32_t src, int c0, int c1, int c2, bool add) {
+  if (add)
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
+                     "l"(reinterpret_cast<uint64_t>(tm)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+  else
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
+                     "l"(reinterpret_cast<uint64_t>(tm)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_and_wait() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// Shared-memory writes of this thread become visible to the bulk-copy (async) proxy.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -303,6 +328,7 @@ constexpr int kMaxChunks = FM_MAX_CHUNKS;  // consecutive KV chunks one launch c
 
 // Tensor maps of Q and of each chunk's K and V (kernel parameter space).
 struct TcMaps {
+  CUtensorMap acc;  // fp32 accumulator [B*H, Sq, D], box 32 x 128 rows (valid when acc_tma)
   CUtensorMap q;
   CUtensorMap k[kMaxChunks];
   CUtensorMap v[kMaxChunks];
@@ -330,6 +356,9 @@ struct TcParams {
   // nullptr; key0[c] is the global index of chunk c's first key
   const int32_t *sinks;
   int key0[kMaxChunks];
+  // the fixed-m epilogue of a chunk that is not the last stages O in shared memory and adds
+  // it into (or stores it over) acc_o with one bulk tensor operation per 32 columns
+  int acc_tma;
 };
 
 // p = 2^(alpha*s - bias) for 32 scores of one full chunk, two at a time with fp32x2 FMA and
@@ -711,6 +740,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t ooff = bb * p.osB + hh * p.osH + row * p.osS;
       const float4 *src = reinterpret_cast<const float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
       float4 *dst = reinterpret_cast<float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
+      // fixed-m tile of a chunk that is not the last: O goes through shared memory and one bulk
+      // tensor operation per 32 columns adds it into acc_o (or stores it there) in the memory
+      // system, so the SM never reads the accumulator.  The staging tile (64 KiB, 128-byte
+      // swizzled boxes of 32 columns) is the Q region for tile 0 -- free once the last S MMA
+      // is done, which the O-done commit covers -- and the first two K/V stages for tile 1,
+      // free once every MMA is done.
+      if (p.acc_tma && fixed && !final_out) {
+        uint8_t *stage = gbase + (t == 0 ? kOffQ : kOffKV);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          uint8_t *line = stage + c * (kBQ * 128) + r * 128;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            *reinterpret_cast<uint4 *>(line + ((q4 ^ (r & 7)) << 4)) =
+                make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+        }
+        fence_proxy_async_smem();
+        named_barrier(1 + t, 128);
+        if (wq == 0 && lane == 0 && tile_ok) {
+          const uint32_t sbase = base + (t == 0 ? kOffQ : kOffKV);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tma_acc_3d(&maps.acc, sbase + c * (kBQ * 128), c * 32, (int)(qb * kBQ), (int)bh, p.accumulate != 0);
+          bulk_commit_and_wait();
+        }
+        if (row_ok) {
+          p.acc_sum[rflat] = sum_new;
+          p.acc_max[rflat] = shift_new;
+        }
+      } else {
       // the accumulator row comes in 32-column pieces, each loaded while the previous piece is
       // combined, so that the row pays one memory latency instead of four
       const bool rd = row_ok && p.accumulate;
@@ -759,6 +820,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.acc_sum[rflat] = sum_new;
         p.acc_max[rflat] = shift_new;
         if (final_out && p.lse) p.lse[rflat] = 0.69314718055994531f * (shift_new + log2f(sum_new));
+      }
       }
     }
   }
@@ -819,6 +881,21 @@ bool encode_map(CUtensorMap *map, const View &t) {
   return r == CUDA_SUCCESS;
 }
 
+// The fp32 accumulator [B, H, Sq, 128] (contiguous) as a 3-D map over [B*H, Sq, 128] with a
+// 32-column x 128-row box, 128-byte swizzle (the staging layout of the epilogue).
+bool encode_acc_map(CUtensorMap *map, float *acc_o, const View &q) {
+  auto enc = get_encode();
+  if (!enc || q.S < 1 || q.B * q.H < 1) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kHD, (cuuint64_t)q.S, (cuuint64_t)(q.B * q.H)};
+  cuuint64_t strides[2] = {(cuuint64_t)kHD * 4, (cuuint64_t)q.S * kHD * 4};
+  cuuint32_t box[3] = {32, (cuuint32_t)kBQ, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, acc_o, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool tma_view_ok(const View &t) {
   if (t.dtype != FM_BF16 || t.D != kHD || t.sD != 1) return false;
   if (reinterpret_cast<uintptr_t>(t.ptr) % 16) return false;
@@ -857,6 +934,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   const View *ks = a.n_chunks > 0 ? a.ks : &a.k;
   const View *vs = a.n_chunks > 0 ? a.vs : &a.v;
   TcMaps maps;
+  memset(&maps, 0, sizeof maps);
   // a layout the driver's tensor-map encoder refuses is reported so the caller can use
   // the CUDA-core kernel instead; nothing has been launched then
   if (!encode_map(&maps.q, a.q)) return cudaErrorNotSupported;
@@ -911,6 +989,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
     p.osH = a.out->sH;
     p.osS = a.out->sS;
   }
+  // non-final chunks add O into acc_o with bulk tensor operations where the map encodes
+  p.acc_tma = (!a.out && encode_acc_map(&maps.acc, a.acc_o, a.q)) ? 1 : 0;
   dim3 grid((unsigned)((a.nqb + 1) / 2), (unsigned)a.q.H, (unsigned)a.q.B);
   return launch_pdl(fm_chunk_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, maps, p);
 }
