@@ -990,7 +990,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
     p.osS = a.out->sS;
   }
   // non-final chunks add O into acc_o with bulk tensor operations where the map encodes
-  p.acc_tma = (!a.out && encode_acc_map(&maps.acc, a.acc_o, a.q)) ? 1 : 0;
+  p.acc_tma = (!a.out && a.q.B * a.q.H <= INT_MAX && encode_acc_map(&maps.acc, a.acc_o, a.q)) ? 1 : 0;
   dim3 grid((unsigned)((a.nqb + 1) / 2), (unsigned)a.q.H, (unsigned)a.q.B);
   return launch_pdl(fm_chunk_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, maps, p);
 }
