@@ -6,7 +6,9 @@
 //   P = 2^(alpha*S - b)   softmax warps: tcgen05.ld of S, FFMA + ex2, row sums in
 //                         registers, bf16 P written back over S in TMEM (tcgen05.st)
 //   O += P V              tcgen05.mma with A = P read from TMEM, B = V from shared memory
-//   epilogue              O and the row sums are added into (or initialise) acc_o/acc_sum
+//   epilogue              O and the row sums are added into (or initialise) acc_o/acc_sum;
+//                         for fixed-m tiles O goes through a swizzled shared-memory tile and a
+//                         TMA reduce-add (store on the first chunk), so the SM never reads acc_o
 // For an eligible Q-block the shift b_i (m + alpha*q_i.kbar, from fm_bounds) is fixed before the chunk starts,
 // so there is no row max, no rescale of O and the cross-chunk merge is a pure add
 // ("Kernel reference: ring_attention_const_max_fwd", sections "Dropping the online max
