@@ -193,6 +193,19 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Named barrier over `count` threads that also returns the AND of their `v`.
+__device__ __forceinline__ bool named_barrier_and(int id, int count, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pin, pout;\n\t"
+      "setp.ne.u32 pin, %1, 0;\n\t"
+      "bar.red.and.pred pout, %2, %3, pin;\n\t"
+      "selp.u32 %0, 1, 0, pout;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -684,6 +697,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // max (one register serves both, the kernel is at its register limit)
     float shv = -INFINITY;
     if (fixed) shv = row_ok ? p.shift[bh * p.Sq + row] : 0.f;
+    // an online row that adds into earlier chunks starts from their shift: as long as this
+    // chunk's scores stay within 2^8 of it, O comes out at the accumulator's own shift and the
+    // merge is a plain add
+    else if (p.accumulate && row_ok) shv = p.acc_max[bh * p.Sq + row];
+    const float shift_prev = shv;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)(t * 128);
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(t * 128);
@@ -724,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t rflat = bh * p.Sq + row;
       float cprev = 0.f, cnew = 1.f, nr = shv;
       if (!fixed && row_ok && p.accumulate) {
-        const float R = p.acc_max[rflat];
+        const float R = shift_prev;  // the previous chunks' shift (acc_max)
         nr = fmaxf(R, shv);
         cprev = (R == -INFINITY) ? 0.f : exp2f(R - nr);
         cnew = (shv == -INFINITY) ? 0.f : exp2f(shv - nr);
@@ -742,13 +760,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t ooff = bb * p.osB + hh * p.osH + row * p.osS;
       const float4 *src = reinterpret_cast<const float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
       float4 *dst = reinterpret_cast<float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
-      // fixed-m tile of a chunk that is not the last: O goes through shared memory and one bulk
-      // tensor operation per 32 columns adds it into acc_o (or stores it there) in the memory
-      // system, so the SM never reads the accumulator.  The staging tile (64 KiB, 128-byte
+      // fixed-m tile of a chunk that is not the last (or any tile of a first chunk, whose O is
+      // simply stored): O goes through shared memory and one bulk tensor operation per 32
+      // columns adds it into acc_o (or stores it there) in the memory system, so the SM never
+      // reads the accumulator.  The staging tile (64 KiB, 128-byte
       // swizzled boxes of 32 columns) is the Q region for tile 0 -- free once the last S MMA
       // is done, which the O-done commit covers -- and the first two K/V stages for tile 1,
       // free once every MMA is done.
-      if (p.acc_tma && fixed && !final_out) {
+      // an online tile whose every row kept the accumulator's shift adds O as plainly as a
+      // fixed-m tile (cprev = cnew = 1)
+      bool plain_add = fixed || !p.accumulate;
+      if (!plain_add && p.acc_tma && !final_out)
+        plain_add = named_barrier_and(1 + t, 128, !row_ok || (shift_prev != -INFINITY && shv == shift_prev));
+      if (p.acc_tma && plain_add && !final_out) {
         uint8_t *stage = gbase + (t == 0 ? kOffQ : kOffKV);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
