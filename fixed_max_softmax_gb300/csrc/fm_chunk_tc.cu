@@ -18,7 +18,9 @@
 // online softmax in the same pipeline (PR #478, "Cross-Ring Safety Fallback"): its
 // softmax warps keep a running row max, rescale O in TMEM when the max grows by more
 // than 2^8 (lazy rescale: exact, since the final shift is whatever the running max is),
-// and merge with the previous chunks through acc_max.
+// and merge with the previous chunks through acc_max.  The running max starts from the
+// previous chunks' shift, so a tile whose rows never move it adds O as plainly as a fixed-m
+// tile.
 // Key columns that must not count -- past a chunk's ragged end, or key sinks that the
 // bounds pass left out of the key max ("Kernel reference: ring_attention_const_max_fwd",
 // section "Adapting this kernel") -- get -inf written over their scores in TMEM before the
