@@ -35,7 +35,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # launch, scaled x5 to 40 heads (every term of the traffic grows with the head count).
 # Valid only for the kernel code it was measured on (comments aside): the bench reports null
 # otherwise.
-CHUNK_TRAFFIC = {"code_sha256_16": "632e19f0770bd1e3", "bytes_per_launch": 5 * (618.256e6 + 825.701e6) / 2}
+CHUNK_TRAFFIC = {"code_sha256_16": "32bf3fdd8738396b", "bytes_per_launch": 5 * (614.435e6 + 835.124e6) / 2}
 
 
 def kernel_code_hash(path: str) -> str:
