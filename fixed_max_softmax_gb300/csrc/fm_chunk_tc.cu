@@ -762,15 +762,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t ooff = bb * p.osB + hh * p.osH + row * p.osS;
       const float4 *src = reinterpret_cast<const float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
       float4 *dst = reinterpret_cast<float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
-      // fixed-m tile of a chunk that is not the last (or any tile of a first chunk, whose O is
-      // simply stored): O goes through shared memory and one bulk tensor operation per 32
-      // columns adds it into acc_o (or stores it there) in the memory system, so the SM never
-      // reads the accumulator.  The staging tile (64 KiB, 128-byte
-      // swizzled boxes of 32 columns) is the Q region for tile 0 -- free once the last S MMA
-      // is done, which the O-done commit covers -- and the first two K/V stages for tile 1,
-      // free once every MMA is done.
-      // an online tile whose every row kept the accumulator's shift adds O as plainly as a
-      // fixed-m tile (cprev = cnew = 1)
+      // A chunk that is not the last, on a tile whose O needs no rescale of the accumulator
+      // (fixed-m; any tile of a first chunk, whose O is simply stored; an online tile whose
+      // every row kept the accumulator's shift, so that cprev = cnew = 1): O goes through
+      // shared memory, and one bulk tensor operation per 32 columns adds it into acc_o (or
+      // stores it there) in the memory system, so the SM never reads the accumulator.  The
+      // staging tile (64 KiB of 128-byte-swizzled 32-column boxes) is the Q region for tile 0,
+      // free once the last S MMA is done, which the O-done commit covers, and the first two
+      // K/V stages for tile 1, free once every MMA is done.
       bool plain_add = fixed || !p.accumulate;
       if (!plain_add && p.acc_tma && !final_out)
         plain_add = named_barrier_and(1 + t, 128, !row_ok || (shift_prev != -INFINITY && shv == shift_prev));
