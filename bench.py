@@ -30,9 +30,10 @@ sys.path.insert(0, ROOT)
 METRIC = "fixed-m attn fwd TFLOP/s (bf16, S=75,600, H=40, D=128) and % of BF16 tensor peak"
 WORKLOAD = "wan"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
-# DRAM bytes (read + write) per launch of the chunk kernel from one ncu capture (see
-# profiles/fm_chunk_tc_wan_h8.md): 8 heads, averaged over the first-chunk and the final-chunk
-# launch, scaled x5 to 40 heads (every term of the traffic grows with the head count).
+# DRAM bytes (read + write) per launch of the chunk kernel from one ncu capture of the Wan
+# step at 8 heads (dram__bytes_read.sum + dram__bytes_write.sum), averaged over the
+# first-chunk and the final-chunk launch, scaled x5 to 40 heads (every term of the traffic
+# grows with the head count).
 # Valid only for the kernel code it was measured on (comments aside): the bench reports null
 # otherwise.
 CHUNK_TRAFFIC = {"code_sha256_16": "32bf3fdd8738396b", "bytes_per_launch": 5 * (614.435e6 + 835.124e6) / 2}

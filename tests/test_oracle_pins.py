@@ -164,7 +164,8 @@ def test_ceil_log2_brute_force():
 # ---------------------------------------------------------------- bounds (closed forms)
 
 def test_bounds_closed_form_norms_and_mean():
-    """Planted norms and an exactly known key mean; U in base-2 logit units (reading R1)."""
+    """Planted norms and an exactly known key mean.  U is in base-2 logit units: it bounds
+    alpha*q.k with alpha = scale*log2(e), the exponent the kernels feed to exp2."""
     D, Sq, N = 16, 300, 64
     r = rng(6)
     c = r.normal(size=(D,))
