@@ -17,6 +17,10 @@ Sources and the reading of each step are in the C file's header:
   fallbacks", Summary ("Dynamic eligibility bounding", "Virtual K-centering"); with
   ``sink_keys``, the loudest keys left out of the key max ("Kernel reference:
   ring_attention_const_max_fwd", section "Adapting this kernel").
+* ``attention_bf16p`` -- the same attention with the numerator's weights rounded to bf16
+  at a given per-row shift: the bf16 reference that "Kernel reference:
+  ring_attention_const_max_fwd", section "Adapting this kernel" (Validation), says to
+  compare a kernel's error distribution against.
 * ``fixed_m_emulate_f32`` -- fp32 fixed-m sum with an arbitrary shift and
   flush-to-zero, to demonstrate the failure modes the gate exists to prevent.
 
@@ -74,6 +78,8 @@ def _load():
         lib.fmo_num_threads.restype = ctypes.c_int
         lib.fmo_attention.restype = None
         lib.fmo_attention.argtypes = [P, P, P, i64, i64, i64, i64, ctypes.c_double, P, P, ctypes.c_int]
+        lib.fmo_attention_bf16p.restype = None
+        lib.fmo_attention_bf16p.argtypes = [P, P, P, i64, i64, i64, i64, ctypes.c_double, P, P, ctypes.c_int]
         lib.fmo_bounds.restype = None
         lib.fmo_bounds.argtypes = [P, P, P, i64, i64, i64, i64, i64, ctypes.c_double, ctypes.c_int,
                                    ctypes.c_int, i64, P, P, P, P, P, P, P, P, P, ctypes.c_int, P, P, P, i64, P, P]
@@ -141,6 +147,31 @@ def attention(q, k, v, scale: float | None = None, threads: int = 0, return_lse:
     if return_lse:
         return o, lse.reshape(shape[:-1])
     return o
+
+
+def attention_bf16p(q, k, v, shift=None, scale: float | None = None, threads: int = 0):
+    """Attention with bf16 P: the "bf16 reference" of "Kernel reference:
+    ring_attention_const_max_fwd", section "Adapting this kernel" (Validation).
+
+    Each numerator weight p_ij = 2^(z_ij - shift_i) (z = scale*log2(e)*q.k, base-2 units)
+    is rounded to bf16's 8-bit significand; the denominator keeps the exact weights; fp64
+    otherwise.  shift: [..., R] per-row base-2 shifts (e.g. bounds(...)["shift"] for the rows
+    evaluated), or None for each row's max.  q: [..., R, D]; k, v: [..., N, D].
+    """
+    qa, ka, va = _as3(q), _as3(k), _as3(v)
+    G, R, D = qa.shape
+    N = ka.shape[1]
+    assert ka.shape == (G, N, D) and va.shape == (G, N, D), (qa.shape, ka.shape, va.shape)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    sh = None
+    if shift is not None:
+        sh = np.ascontiguousarray(_f64(shift).reshape(G, R))
+    o = np.zeros((G, R, D), dtype=np.float64)
+    _load().fmo_attention_bf16p(_ptr(qa), _ptr(ka), _ptr(va), G, R, N, D, float(scale), _ptr(sh), _ptr(o),
+                                int(threads))
+    shape = tuple(np.shape(q)) if not hasattr(q, "shape") else tuple(q.shape)
+    return o.reshape(shape)
 
 
 def bounds(q, k, v, scale: float | None = None, centering: bool = False, dtype_safe: bool = True,

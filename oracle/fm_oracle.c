@@ -31,6 +31,11 @@
  *   fmo_bounds      -- norms, key mean, U, m, flag, in the pages' order ([PR477]);
  *                      optionally the key sinks left out of the key max ([NKI]
  *                      "Adapting this kernel").
+ *   fmo_attention_bf16p -- the same attention with every numerator weight rounded to
+ *                      bf16's 8-bit significand: the "bf16 reference" whose error
+ *                      distribution [NKI] "Adapting this kernel" (Validation) tells you to
+ *                      compare a kernel's against.  The weight's scale is a per-row shift
+ *                      passed in (the fixed-m shift of fmo_bounds, or the row max).
  *   fmo_fixed_m_emulate_f32 -- a sequential fp32 emulation of the fixed-m sum with
  *                      an ARBITRARY shift, flushing subnormal terms to zero.  It
  *                      exists only to show what goes wrong with a wrong gate or an
@@ -133,6 +138,78 @@ void fmo_attention(const double *q, const double *k, const double *v, int64_t G,
       if (lse) lse[gr] = mu + log(denom);
     }
     free(s);
+  }
+}
+
+/* x > 0 rounded to 8 significant bits (bf16's significand: 1 implicit + 7 stored bits),
+ * to nearest with ties to even.  Only the significand is rounded, there is no exponent
+ * limit: the callers pass values in [1, 2). */
+static double fmo_round_sig8(double x) {
+  int e;
+  const double m = frexp(x, &e); /* x = m * 2^e, m in [0.5, 1) */
+  const double t = m * 256.0;    /* [128, 256): the 8 kept bits above the binary point */
+  double r = floor(t);
+  const double d = t - r;
+  if (d > 0.5 || (d == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  return ldexp(r / 256.0, e);
+}
+
+/* Attention with bf16 P: the reference run "in bf16" of [NKI] "Adapting this kernel"
+ * (Validation: run exact attention on the CPU in fp32 and in bf16 and compare both error
+ * distributions with the kernel's).  Reading: what bf16 changes is the probability weights
+ * that multiply V.  Weight j of row i is p_ij = 2^(z_ij - b_i), z_ij = alpha q_i.k_j the
+ * base-2 logit (alpha = scale*log2 e) and b_i the row's shift; it enters the numerator
+ * rounded to 8 significant bits and the denominator unrounded:
+ *   o_i = sum_j bf16(p_ij) v_j / sum_j p_ij.
+ * Rounding commutes with a power of two, so bf16(p) = 2^floor(t) * bf16(2^frac(t)) for
+ * t = z - b: the rounding depends on frac(z - b) alone, and each weight is formed as
+ * 2^(z - mu) times the factor bf16(2^f)/2^f, with mu the row max, so that nothing
+ * overflows whatever b is.  Everything else is fp64.
+ *   q [G, R, D], k, v [G, N, D], shift [G, R] base-2 shifts or NULL for the row max
+ *   o [G, R, D].  N == 0 gives o = 0.                                                    */
+void fmo_attention_bf16p(const double *q, const double *k, const double *v, int64_t G, int64_t R,
+                         int64_t N, int64_t D, double scale, const double *shift, double *o,
+                         int nthreads) {
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#else
+  (void)nthreads;
+#endif
+  const double alpha = scale * FMO_LOG2E;
+  int64_t total = G * R;
+#pragma omp parallel
+  {
+    double *z = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t gr = 0; gr < total; gr++) {
+      int64_t g = gr / R;
+      const double *qi = q + gr * D;
+      const double *kg = k + g * N * D;
+      const double *vg = v + g * N * D;
+      double *oi = o + gr * D;
+      for (int64_t d = 0; d < D; d++) oi[d] = 0.0;
+      if (N == 0) continue;
+      double mu = -INFINITY;
+      for (int64_t j = 0; j < N; j++) {
+        double dot = 0.0;
+        for (int64_t d = 0; d < D; d++) dot += qi[d] * kg[j * D + d];
+        z[j] = alpha * dot;
+        if (z[j] > mu) mu = z[j];
+      }
+      const double b = shift ? shift[gr] : mu;
+      double denom = 0.0;
+      for (int64_t j = 0; j < N; j++) {
+        const double p = exp2(z[j] - mu);
+        const double t = z[j] - b;
+        const double f = t - floor(t);
+        const double e2f = exp2(f);
+        const double w = p * (fmo_round_sig8(e2f) / e2f);
+        denom += p;
+        for (int64_t d = 0; d < D; d++) oi[d] += w * vg[j * D + d];
+      }
+      for (int64_t d = 0; d < D; d++) oi[d] /= denom;
+    }
+    free(z);
   }
 }
 
