@@ -3,7 +3,10 @@
 Bars: m and flag bit-exact outside the tie band (|U - nearest integer| or |U - gate|
 below 1e-4*max(1,U), where fp32 device sums may legitimately round the other way);
 outputs within max-abs 1e-5 for fp32 inputs and 2e-2 for bf16 inputs; the fixed-m and
-the online-fallback path within the same tolerance of each other.  Small cases are
+the online-fallback path within the same tolerance of each other.  Because |o| is about
+2e-2 itself at the pages' sizes, bf16 outputs also meet the scale-aware bars of
+tests/parity.py (max error within 1e-2 of max |o|, every element within the bound bf16 P
+can cause, and an error distribution like the oracle's bf16-P reference).  Small cases are
 compared element by element; the full-size workloads on sampled (head, row) sets that
 include every ragged tail.
 """
@@ -16,6 +19,7 @@ import torch
 import fixed_max_softmax_gb300 as fm
 import oracle
 import workloads
+from tests.parity import Reference
 
 pytestmark = pytest.mark.gpu
 
@@ -50,6 +54,29 @@ def maxerr(a, b):
     b = b.detach().cpu().double().numpy() if hasattr(b, "detach") else np.asarray(b)
     assert a.shape == b.shape, (a.shape, b.shape)
     return float(np.max(np.abs(a - b))) if a.size else 0.0
+
+
+def reference(q, k, v, heads=None, rows=None, centering=False, per_row=False, sink_keys=0):
+    """Oracle reference for the rows under test, of every batch entry and the given heads:
+    exact o, the bf16-P reference at the oracle's own row shift, and the weighted |v|.  The
+    shifts come from bounds over every row and key of those heads."""
+    q, k, v = q.cpu(), k.cpu(), v.cpu()
+    if heads is not None:
+        q, k, v = q[:, heads], k[:, heads], v[:, heads]
+    ob = oracle.bounds(q, k, v, centering=centering, per_row=per_row, sink_keys=sink_keys)
+    shift = ob["shift"]
+    if rows is not None:
+        q, shift = q[:, :, rows], shift[:, :, rows]
+    return Reference(q, k, v, shift)
+
+
+def pick(o, heads=None, rows=None):
+    """The [B, heads, rows, D] part of a device output, matching reference()'s selection."""
+    if heads is not None:
+        o = o[:, heads]
+    if rows is not None:
+        o = o[:, :, rows]
+    return o
 
 
 def check_bounds(fa, ob, heads=None, check_vmax=True):
@@ -114,9 +141,7 @@ def test_bf16_ragged_chunks_element_by_element(dev, shape, centering, force_onli
         q, k, v = torch.cat([q, q2]), torch.cat([k, k2]), torch.cat([v, v2])
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     fa, o = run(qd, kd, vd, chunks, centering=centering, force_online=force_online)
-    ref = oracle.attention(q, k, v)
-    err = maxerr(o, ref)
-    assert err <= TOL_BF16, err
+    reference(q, k, v, centering=centering).check(o, f"{shape} centering={centering} online={force_online}")
     check_bounds(fa, oracle.bounds(q, k, v, centering=centering))
 
 
@@ -261,15 +286,14 @@ def test_long_key_sequence_and_batches(dev):
     chunks = [(0, 300001), (300001, 500000), (800001, N - 800001)]
     fa, o = run(q, k, v, chunks, centering=True)
     assert (fa.bounds.out.C, fa.bounds.out.gate) == oracle.constants(N)[0:3:2]
-    ref = oracle.attention(q.cpu(), k.cpu(), v.cpu())
-    assert maxerr(o, ref) <= TOL_BF16
+    reference(q, k, v, centering=True).check(o, "2^20 keys")
     # two batches with different recipes
     q1, k1, v1 = workloads.make_inputs("mix", device="cpu", heads=range(3), Sq=1000, N=1500)
     q2, k2, v2 = workloads.make_inputs("wan", device="cpu", heads=range(3), Sq=1000, N=1500)
     q, k, v = torch.cat([q1, q2]), torch.cat([k1, k2]), torch.cat([v1, v2])
     fa, o = run(q.to(dev), k.to(dev), v.to(dev), [(0, 700), (700, 800)], centering=True)
     check_bounds(fa, oracle.bounds(q, k, v, centering=True))
-    assert maxerr(o, oracle.attention(q, k, v)) <= TOL_BF16
+    reference(q, k, v, centering=True).check(o, "B = 2")
 
 
 def test_device_flags_follow_the_gate_edge(dev):
@@ -382,24 +406,19 @@ def test_host_pipeline_matches_device_path(dev):
 
 # ------------------------------------------------------------------ full-size workloads (sampled rows)
 
-def sampled(q, k, v, o, heads, rows):
-    qs = q[0, heads][:, rows].cpu()
-    ks, vs = k[0, heads].cpu(), v[0, heads].cpu()
-    ref = oracle.attention(qs, ks, vs)
-    got = o[0, heads][:, rows]
-    return maxerr(got, ref)
-
-
 def test_h40_s4096_full(dev):
     w = workloads.WORKLOADS["h40_s4096"]
     q, k, v = workloads.make_inputs("h40_s4096", device=dev)
     fa, o = run(q, k, v, workloads.chunk_bounds(w), centering=False)
     check_bounds(fa, oracle.bounds(q.cpu(), k.cpu(), v.cpu(), centering=False))
     assert bool(fa.bounds.flag.all())
-    rows = list(range(0, 128)) + list(range(2000, 2100)) + list(range(3968, 4096))
-    assert sampled(q, k, v, o, [0, 39], rows) <= TOL_BF16
+    heads = [0, 13, 26, 39]
+    rows = list(range(0, 128)) + list(range(1000, 1050)) + list(range(2000, 2100)) + list(range(3968, 4096))
+    ref = reference(q, k, v, heads, rows)
+    ref.check(pick(o, heads, rows), "h40_s4096 fixed-m")
     _, o2 = run(q, k, v, workloads.chunk_bounds(w), force_online=True)
-    assert maxerr(o2[0, [0, 39]][:, rows], o[0, [0, 39]][:, rows]) <= TOL_BF16
+    ref.check(pick(o2, heads, rows), "h40_s4096 online")
+    assert maxerr(pick(o2, heads, rows), pick(o, heads, rows)) <= TOL_BF16
 
 
 def test_wan_full_size(dev):
@@ -416,17 +435,23 @@ def test_wan_full_size(dev):
     assert float(fa.bounds.vmax_sq.item()) == vmax
     nqb = fa.bounds.out.n_qblocks
     assert nqb == 591
-    # rows: first Q-block pair, one block in the middle, the ragged 80-row tail
-    rows = list(range(0, 256)) + list(range(37760, 37888)) + list(range(75520, 75600))
-    assert sampled(q, k, v, o, [0, 17], rows) <= TOL_BF16
-    # the LSE of the same rows, from the accumulators of this call
+    # rows: the first Q-block pair, the Q-blocks around row 37,800 (where the key chunks
+    # meet), the last full block and the ragged 80-row tail; eight heads across the range
+    rows = (list(range(0, 256)) + list(range(37632, 37888)) + list(range(75392, 75520))
+            + list(range(75520, 75600)))
+    heads = [0, 5, 11, 17, 22, 28, 33, 39]
+    ref = reference(q, k, v, heads, rows, centering=True)
+    r = ref.check(pick(o, heads, rows), "wan fixed-m")
+    assert r["max_ref"] > 5 * r["max_err"] and r["max_ref"] > 1e-2  # |o| is far above the error
+    # the LSE of two heads' rows, from the accumulators of this call
     lse = torch.empty_like(fa.acc_sum)
     fm.fm_finalize_lse(fa.acc_o, fa.acc_sum, fa.acc_max, fa.out, lse)
     _, ref_lse = oracle.attention(q[0, [0, 17]][:, rows].cpu(), k[0, [0, 17]].cpu(), v[0, [0, 17]].cpu(),
                                   return_lse=True)
     assert maxerr(lse[0, [0, 17]][:, rows], ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse))))
     _, o2 = run(q, k, v, workloads.chunk_bounds(w), centering=True, force_online=True)
-    assert maxerr(o2[0, [0, 17]][:, rows], o[0, [0, 17]][:, rows]) <= TOL_BF16
+    ref.check(pick(o2, heads, rows), "wan online")
+    assert maxerr(pick(o2, heads, rows), pick(o, heads, rows)) <= TOL_BF16
 
 
 @pytest.mark.parametrize("centering", [False, True])
@@ -436,14 +461,14 @@ def test_mix_fallback_full(dev, centering):
     ob = oracle.bounds(q.cpu(), k.cpu(), v.cpu(), centering=centering)
     check_bounds(fa, ob)
     flags = fa.bounds.flag.cpu().numpy()[0]
-    heads_on = [h for h in range(40) if flags[h].all()][:1]
-    heads_off = [h for h in range(40) if not flags[h].any()][:1]
+    heads_on = [h for h in range(40) if flags[h].all()]
+    heads_off = [h for h in range(40) if not flags[h].any()]
     if not centering:
         assert heads_off, "without centering some heads must fall back"
-    rows = list(range(0, 128)) + list(range(16256, 16384))
-    for hs in (heads_on, heads_off):
+    rows = list(range(0, 128)) + list(range(8192, 8320)) + list(range(16256, 16384))
+    for hs in (heads_on[:2], heads_off[:2]):
         if hs:
-            assert sampled(q, k, v, o, hs, rows) <= TOL_BF16, hs
+            reference(q, k, v, hs, rows, centering=centering).check(pick(o, hs, rows), f"mix heads {hs}")
 
 
 def test_adversarial_full(dev):
@@ -456,10 +481,13 @@ def test_adversarial_full(dev):
     adv = w.extra["adv_heads"]
     assert not flags[:adv, 0].any(), "the query with bound 231.01 must be rejected"
     assert flags[:adv, 1:].all() and flags[adv:].all()
-    rows = list(range(0, 256))
-    assert sampled(q, k, v, o, [0, 25], rows) <= TOL_BF16
+    rows = list(range(0, 256)) + list(range(3968, 4096))
+    heads = [0, 7, 19, 25]
+    ref = reference(q, k, v, heads, rows, centering=True)
+    ref.check(pick(o, heads, rows), "adversarial auto")
     _, o2 = run(q, k, v, None, centering=True, force_online=True)
-    assert maxerr(o2[0, [0, 25]][:, rows], o[0, [0, 25]][:, rows]) <= TOL_BF16
+    ref.check(pick(o2, heads, rows), "adversarial online")
+    assert maxerr(pick(o2, heads, rows), pick(o, heads, rows)) <= TOL_BF16
 
 
 # ------------------------------------------------------------------ key sinks
@@ -503,7 +531,7 @@ def test_key_sinks_element_by_element(dev, chunks, force_online, centering):
     if not force_online:
         assert bool(fa.bounds.flag.all())
     ref, ref_lse = oracle.attention(q, k, v, return_lse=True)
-    assert maxerr(o, ref) <= TOL_BF16
+    reference(q, k, v, centering=centering, sink_keys=4).check(o, f"sinks {chunks}")
     assert maxerr(fa.lse, ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse))))
     # without sinks the sink heads fall back to online softmax everywhere; same output
     fb, o_plain = run(qd, kd, vd, chunks, centering=centering, force_online=force_online)
@@ -582,10 +610,16 @@ def test_sinks_full(dev):
     assert check_sinks(fa, ob) >= w.extra["sink_heads"]
     assert bool(fa.bounds.flag.all())
     rows = list(range(0, 128)) + list(range(8190, 8300)) + list(range(16256, 16384))
-    assert sampled(q, k, v, o, [0, 19, 39], rows) <= TOL_BF16
+    heads = [0, 19, 39]
+    ref = reference(q, k, v, heads, rows, sink_keys=4)
+    ref.check(pick(o, heads, rows), "sinks, 4 sink keys")
     fb, o2 = run(q, k, v, workloads.chunk_bounds(w))
     assert not fb.bounds.flag[0, :w.extra["sink_heads"]].any()
-    assert maxerr(o2[0, [0, 39]][:, rows], o[0, [0, 39]][:, rows]) <= TOL_BF16
+    r = ref.check(pick(o2, heads, rows), "sinks, no sink keys")
+    # online rows that continue from the earlier chunks' shift give a later chunk's loud key a
+    # weight of up to 2^8 in bf16: about 1.8e-3 of error here, which must not grow
+    assert r["max_err"] <= 3e-3, r
+    assert maxerr(pick(o2, heads, rows), pick(o, heads, rows)) <= TOL_BF16
 
 
 def test_key_sinks_with_per_row_centering_and_batches(dev):
@@ -728,6 +762,9 @@ def test_randomised_shapes_and_options(dev):
         tol = TOL_F32 if dt == torch.float32 else TOL_BF16
         desc = (case, B, H, Sq, N, D, dt, chunks, opts, one)
         assert maxerr(o, ref) <= tol, desc
+        if dt == torch.bfloat16:
+            reference(q, k, v, centering=opts["centering"], per_row=opts["per_row"],
+                      sink_keys=opts["sink_keys"]).check(o, str(desc))
         assert maxerr(fa.lse, ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse)))), desc
         ob = oracle.bounds(q, k, v, centering=opts["centering"], per_row=opts["per_row"],
                            sink_keys=opts["sink_keys"])
