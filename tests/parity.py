@@ -35,6 +35,24 @@ QUANTILE_FACTOR = 4.0
 FLOOR_REL = 1e-6
 
 
+TOL_F32 = 1e-5  # the benchmark spec, fp32 inputs
+
+
+def f32_bar(q, k, scale=None):
+    """North_star's 1e-5 bar for fp32 inputs, widened in proportion to the logits' bound U
+    above 8.  fp32 rounds a dot product q.k to within about 2^-24 sqrt(D) sum_d |q_d k_d|,
+    and sum_d |q_d k_d| <= |q| |k|, so a base-2 logit carries an error proportional to
+    U = alpha * max|q| * max|k| (the method's own Cauchy-Schwarz bound), which every weight
+    inherits.  At the fp32 workload's inputs U is below 8 and the bar is 1e-5; keys a hundred
+    times louder than the rest widen it accordingly."""
+    q, k = _np(q), _np(k)
+    D = q.shape[-1]
+    alpha = (1.0 / np.sqrt(D) if scale is None else scale) * np.log2(np.e)
+    qn = np.sqrt((q ** 2).sum(-1)).max() if q.size else 0.0
+    kn = np.sqrt((k ** 2).sum(-1)).max() if k.size else 0.0
+    return TOL_F32 * max(1.0, alpha * qn * kn / 8.0)
+
+
 class Reference:
     """Oracle outputs for the rows under test: exact o, the bf16-P reference at the oracle's
     fixed-m shift, and sum_j p |v| / sum_j p (the weighted mean of |v|)."""

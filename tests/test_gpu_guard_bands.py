@@ -18,7 +18,7 @@ import torch
 import fixed_max_softmax_gb300 as fm
 import oracle
 import workloads
-from tests.parity import Reference
+from tests.parity import Reference, f32_bar
 
 pytestmark = pytest.mark.gpu
 
@@ -153,8 +153,9 @@ def test_no_write_outside_any_buffer(dev, Sq, path):
     broken = [name for name, g in guards.items() if not g.intact()]
     assert not broken, f"writes outside {broken} (Sq={Sq}, path={path})"
     got = out.t.float().cpu().numpy()
-    if dtype == torch.float32:
-        assert np.max(np.abs(got - o_ref)) <= 1e-5
+    if dtype == torch.float32:  # 1e-5, widened for the head whose keys are a hundred times louder
+        for h in range(H):
+            assert np.max(np.abs(got[:, h] - o_ref[:, h])) <= f32_bar(q[:, h], k[:, h]), h
     elif out.dtype == torch.bfloat16:  # o itself rounded to bf16: the absolute and relative bars
         err = np.max(np.abs(got - o_ref))
         assert err <= 2e-2 and err <= 1e-2 * np.max(np.abs(o_ref)), err

@@ -443,9 +443,10 @@ def test_wan_full_size(dev):
     ref = reference(q, k, v, heads, rows, centering=True)
     r = ref.check(pick(o, heads, rows), "wan fixed-m")
     assert r["max_ref"] > 5 * r["max_err"] and r["max_ref"] > 1e-2  # |o| is far above the error
-    # the LSE of two heads' rows, from the accumulators of this call
+    # the LSE of two heads' rows, from the accumulators of this call: acc_sum and acc_max are
+    # current after the fused final chunk (acc_o is not, so the o this writes is thrown away)
     lse = torch.empty_like(fa.acc_sum)
-    fm.fm_finalize_lse(fa.acc_o, fa.acc_sum, fa.acc_max, fa.out, lse)
+    fm.fm_finalize_lse(fa.acc_o, fa.acc_sum, fa.acc_max, torch.empty_like(fa.out), lse)
     _, ref_lse = oracle.attention(q[0, [0, 17]][:, rows].cpu(), k[0, [0, 17]].cpu(), v[0, [0, 17]].cpu(),
                                   return_lse=True)
     assert maxerr(lse[0, [0, 17]][:, rows], ref_lse) <= TOL_LSE * max(1.0, float(np.max(np.abs(ref_lse))))

@@ -76,3 +76,12 @@ def test_a_non_finite_element_fails(case):
     bad[0, 3, 5] = np.nan
     with pytest.raises(AssertionError):
         parity.assert_bf16_parity(bad, ref.o, ref.model, ref.abs_v)
+
+
+def test_f32_bar_is_north_stars_at_the_fp32_workload():
+    q, k, _ = workloads.make_inputs("tiny")
+    assert parity.f32_bar(q[0], k[0]) == parity.TOL_F32
+    # a key a hundred times louder widens it in proportion to the bound U
+    k2 = k.clone()
+    k2[0, 0, 3] *= 100.0
+    assert parity.f32_bar(q[0, :1], k2[0, :1]) > 5 * parity.TOL_F32
