@@ -58,7 +58,8 @@ class fm_tensor(ctypes.Structure):
 
 class fm_opts(ctypes.Structure):
     _fields_ = [("softmax_scale", ctypes.c_float), ("centering", ctypes.c_int32),
-                ("force_online", ctypes.c_int32), ("per_row", ctypes.c_int32), ("sink_keys", ctypes.c_int32)]
+                ("force_online", ctypes.c_int32), ("per_row", ctypes.c_int32), ("sink_keys", ctypes.c_int32),
+                ("schedule", ctypes.c_int32)]
 
 
 class fm_bounds_out(ctypes.Structure):
@@ -131,10 +132,15 @@ def tensor(t: torch.Tensor) -> fm_tensor:
     return d
 
 
+FM_SCHEDULE_AUTO, FM_SCHEDULE_GRID, FM_SCHEDULE_PERSISTENT = 0, 1, 2
+SCHEDULES = {"auto": FM_SCHEDULE_AUTO, "grid": FM_SCHEDULE_GRID, "persistent": FM_SCHEDULE_PERSISTENT}
+
+
 def opts(softmax_scale: float = 0.0, centering: bool = False, force_online: bool = False,
-         per_row: bool = False, sink_keys: int = 0) -> fm_opts:
+         per_row: bool = False, sink_keys: int = 0, schedule="auto") -> fm_opts:
+    sched = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
     return fm_opts(float(softmax_scale), int(bool(centering)), int(bool(force_online)), int(bool(per_row)),
-                   int(sink_keys))
+                   int(sink_keys), sched)
 
 
 def _stream(stream):
@@ -278,13 +284,14 @@ class FixedMAttention:
     fm_finalize.  one_launch=True folds all chunks with fm_attn_chunks instead (one launch per
     FM_MAX_CHUNKS chunks, accumulators on chip across them).  with_lse=True also fills
     `lse` [B, H, Sq] (natural log).  sink_keys > 0 leaves that many of each head's loudest
-    keys out of the key max; they are folded back exactly before the normalise.
+    keys out of the key max; they are folded back exactly before the normalise.  schedule:
+    "auto", "grid" or "persistent" (fm_opts.schedule; the same bits either way).
     """
 
     def __init__(self, B, H, Sq, N, D, device="cuda", centering=False, softmax_scale=0.0,
-                 force_online=False, out_dtype=torch.float32, per_row=False, sink_keys=0):
+                 force_online=False, out_dtype=torch.float32, per_row=False, sink_keys=0, schedule="auto"):
         self.shape = (B, H, Sq, N, D)
-        self.opt = opts(softmax_scale, centering, force_online, per_row, sink_keys)
+        self.opt = opts(softmax_scale, centering, force_online, per_row, sink_keys, schedule)
         self.bounds = Bounds(B, H, Sq, D, device)
         nbytes = fm_bounds_workspace_size(B, H, N, D)
         self.workspace = torch.empty(max(nbytes, 16) // 4 + 4, dtype=torch.float32, device=device)

@@ -150,7 +150,7 @@ using namespace fm;
 
 extern "C" {
 
-int fm_version(void) { return (1 << 16) | 1; }
+int fm_version(void) { return (1 << 16) | 2; }
 
 const char *fm_last_error(void) { return t_err.c_str(); }
 
@@ -285,6 +285,9 @@ int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_ten
     return fail(FM_ERR_ARG, "centering and force_online must be 0 or 1");
   const int centering = opts ? opts->centering : 0;
   const int force_online = opts ? opts->force_online : 0;
+  const int schedule = opts ? opts->schedule : FM_SCHEDULE_AUTO;
+  if (schedule < FM_SCHEDULE_AUTO || schedule > FM_SCHEDULE_PERSISTENT)
+    return fail(FM_ERR_ARG, "schedule = %d is not one of FM_SCHEDULE_AUTO, _GRID, _PERSISTENT", schedule);
   // the bounds must belong to this call
   if (bounds->magic != FM_BOUNDS_MAGIC)
     return fail(FM_ERR_BOUNDS_MISMATCH, "bounds were not produced by fm_bounds (magic 0x%08x)", bounds->magic);
@@ -344,6 +347,7 @@ int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_ten
   a.q = vq;
   a.alpha = (float)alpha;
   a.force_online = force_online;
+  a.schedule = schedule;
   a.nqb = nqb;
   a.flag = bounds->flag;
   a.shift = bounds->shift;

@@ -44,6 +44,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <limits.h>
+#include <stdlib.h>
 #include <string.h>
 #include <math.h>
 
@@ -63,6 +64,7 @@ constexpr int kPanelBytes = 128 * 64 * 2;     // 128 rows x 64 bf16 (one 128-byt
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLazyRescale = 8.0f;          // online path: rescale when the max grows by > 2^8
+constexpr int kPersistentMaxTiles = 16;       // launches of at most this many key tiles run persistent
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int kOffQ = 0;
@@ -75,11 +77,12 @@ constexpr int kBarSFull = kBarKVEmpty + kStages;
 constexpr int kBarPReady = kBarSFull + 2;
 constexpr int kBarODone = kBarPReady + 2;
 constexpr int kBarDrain = kBarODone + 2;
-constexpr int kNumBars = kBarDrain + 1;
+constexpr int kBarQEmpty = kBarDrain + 1;  // every S MMA of an item has read Q
+constexpr int kNumBars = kBarQEmpty + 1;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
-constexpr int kOffSinks = kOffAbort + 8;  // the head's key sinks (FM_MAX_SINKS int32)
-constexpr int kSmemUsed = kOffSinks + 4 * FM_MAX_SINKS;
+constexpr int kOffSinks = kOffAbort + 8;  // per softmax group: its item's key sinks (FM_MAX_SINKS int32)
+constexpr int kSmemUsed = kOffSinks + 2 * 4 * FM_MAX_SINKS;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5 = 1),
@@ -183,6 +186,12 @@ __device__ __forceinline__ void tma_acc_3d(const CUtensorMap *tm, uint32_t src, 
     asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
                      "l"(reinterpret_cast<uint64_t>(tm)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
+}
+// acc += v (4 consecutive fp32) as one reduction in the memory system: the same fp32 add
+// as the registers would do, without reading the accumulator through the SM.
+__device__ __forceinline__ void red_add_v4(float *dst, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
 }
 __device__ __forceinline__ void bulk_commit_and_wait() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
@@ -376,6 +385,11 @@ struct TcParams {
   // the fixed-m epilogue of a chunk that is not the last stages O in shared memory and adds
   // it into (or stores it over) acc_o with one bulk tensor operation per 32 columns
   int acc_tma;
+  // persistent schedule: each CTA walks work items (batch, head, Q-tile pair) item =
+  // blockIdx.x, blockIdx.x + gridDim.x, ...; otherwise one item per CTA of a
+  // (pairs, H, B) grid.  n_items = B * H * pairs.
+  int persistent;
+  int64_t n_items, n_pairs;
 };
 
 // p = 2^(alpha*s - bias) for 32 scores of one full chunk, two at a time with fp32x2 FMA and
@@ -550,9 +564,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffAbort);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffTmemSlot);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, h = blockIdx.y;
-  const int64_t qb0 = 2 * (int64_t)blockIdx.x;
   auto bar = [&](int i) -> uint32_t { return base + (uint32_t)(kOffBar + 8 * i); };
+  // this CTA's work items: one, or (persistent) every gridDim.x-th from blockIdx.x on.  Item
+  // -> (b, h, Q-tile pair); consecutive items share a head and so its K/V tiles in L2.
+  const int64_t item0 = p.persistent ? (int64_t)blockIdx.x
+                                     : (int64_t)blockIdx.x + p.n_pairs * ((int64_t)blockIdx.y + (int64_t)p.H * blockIdx.z);
+  const int64_t item_step = p.persistent ? (int64_t)gridDim.x : p.n_items;
+  auto item_bh = [&](int64_t item) -> int64_t { return item / p.n_pairs; };
+  auto item_qb0 = [&](int64_t item) -> int64_t { return 2 * (item % p.n_pairs); };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -567,10 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarODone + t), 1);
     }
     mbar_init(bar(kBarDrain), 1);
+    mbar_init(bar(kBarQEmpty), 1);
     fence_mbar_init();
-    int32_t *ssk = reinterpret_cast<int32_t *>(gbase + kOffSinks);
-    for (int t = 0; t < FM_MAX_SINKS; ++t)
-      ssk[t] = p.sinks ? p.sinks[((int64_t)b * p.H + h) * FM_MAX_SINKS + t] : INT_MAX;
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
@@ -584,32 +601,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       int last_round[kStages];
       for (int s = 0; s < kStages; ++s) last_round[s] = -1;
-      mbar_expect_tx(bar(kBarQFull), 4 * kPanelBytes);
-      for (int t = 0; t < 2; ++t)
-        for (int pn = 0; pn < 2; ++pn)
-          tma_load_4d(base + kOffQ + t * kTileBytes + pn * kPanelBytes, &maps.q, bar(kBarQFull), pn * 64,
-                      (int)((qb0 + t) * kBQ), h, b);
       bool ok = true;
-      int c = 0;  // chunk of key tile j
-      for (int j = 0; j < n_kv && ok; ++j) {
-        while (j >= p.tile0[c + 1]) ++c;
-        const int jl = j - p.tile0[c];  // tile within its chunk
-        for (int w = 0; w < 2 && ok; ++w) {
-          const int idx = 2 * j + w, s = idx % kStages, round = idx / kStages;
-          ok = wait_phase(bar(kBarKVEmpty + s), (uint32_t)((round & 1) ^ 1), abort_flag, p.timeout_ns, p.err,
-                          kDevErrTimeoutProducer, wtag(kBarKVEmpty + s, j));
-          if (!ok) break;
-          mbar_expect_tx(bar(kBarKVFull + s), kTileBytes);
-          const CUtensorMap *tm = w ? &maps.v[c] : &maps.k[c];
+      int64_t q_loads = 0;  // Q tile pairs issued
+      int64_t g = 0;        // key tiles of earlier items (the ring position carries over)
+      for (int64_t item = item0; item < p.n_items && ok; item += item_step, g += n_kv) {
+        const int64_t bh = item_bh(item), qb0 = item_qb0(item);
+        const int h = (int)(bh % p.H), b = (int)(bh / p.H);
+        // Q of the previous item must have been read by all of its S MMAs
+        if (q_loads > 0)
+          ok = wait_phase(bar(kBarQEmpty), (uint32_t)((q_loads - 1) & 1), abort_flag, p.timeout_ns, p.err,
+                          kDevErrTimeoutProducer, wtag(kBarQEmpty, 0));
+        if (!ok) break;
+        mbar_expect_tx(bar(kBarQFull), 4 * kPanelBytes);
+        for (int t = 0; t < 2; ++t)
           for (int pn = 0; pn < 2; ++pn)
-            tma_load_4d(base + kOffKV + s * kTileBytes + pn * kPanelBytes, tm, bar(kBarKVFull + s), pn * 64,
-                        jl * kBK, h, b);
-          last_round[s] = round;
+            tma_load_4d(base + kOffQ + t * kTileBytes + pn * kPanelBytes, &maps.q, bar(kBarQFull), pn * 64,
+                        (int)((qb0 + t) * kBQ), h, b);
+        ++q_loads;
+        int c = 0;  // chunk of key tile j
+        for (int j = 0; j < n_kv && ok; ++j) {
+          while (j >= p.tile0[c + 1]) ++c;
+          const int jl = j - p.tile0[c];  // tile within its chunk
+          for (int w = 0; w < 2 && ok; ++w) {
+            const int64_t idx = 2 * (g + j) + w;
+            const int s = (int)(idx % kStages), round = (int)(idx / kStages);
+            ok = wait_phase(bar(kBarKVEmpty + s), (uint32_t)((round & 1) ^ 1), abort_flag, p.timeout_ns, p.err,
+                            kDevErrTimeoutProducer, wtag(kBarKVEmpty + s, j));
+            if (!ok) break;
+            mbar_expect_tx(bar(kBarKVFull + s), kTileBytes);
+            const CUtensorMap *tm = w ? &maps.v[c] : &maps.k[c];
+            for (int pn = 0; pn < 2; ++pn)
+              tma_load_4d(base + kOffKV + s * kTileBytes + pn * kPanelBytes, tm, bar(kBarKVFull + s), pn * 64,
+                          jl * kBK, h, b);
+            last_round[s] = round;
+          }
         }
       }
       if (!ok) {
         // let every copy already issued land before the CTA can exit
-        wait_phase(bar(kBarQFull), 0, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain, wtag(kBarQFull, 0));
+        if (q_loads > 0)
+          wait_phase(bar(kBarQFull), (uint32_t)((q_loads - 1) & 1), nullptr, p.timeout_ns, p.err,
+                     kDevErrTimeoutDrain, wtag(kBarQFull, 0));
         for (int s = 0; s < kStages; ++s)
           if (last_round[s] >= 0)
             wait_phase(bar(kBarKVFull + s), (uint32_t)(last_round[s] & 1), nullptr, p.timeout_ns, p.err,
@@ -629,53 +661,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto v_desc = [&](int s, int kk) {
         return smem_desc(base + kOffKV + s * kTileBytes + kk * 2048, kPanelBytes, 1024);
       };
-      bool ok = wait_phase(bar(kBarQFull), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma, wtag(kBarQFull, 0));
-      int vs_prev = 0;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int ki = 2 * j, ks = ki % kStages;
-        ok = wait_phase(bar(kBarKVFull + ks), (uint32_t)((ki / kStages) & 1), abort_flag, p.timeout_ns, p.err,
-                        kDevErrTimeoutMma, wtag(kBarKVFull + ks, j));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tS0, q_desc(0, kk), k_desc(ks, kk), kIdescQK, kk > 0);
-        mma_commit(bar(kBarSFull + 0));
-        if (j > 0) {
-          ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((j - 1) & 1), abort_flag, p.timeout_ns, p.err,
-                          kDevErrTimeoutMma, wtag(kBarPReady + 1, j));
+      bool ok = true;
+      int64_t g = 0;
+      int64_t k = 0;  // items done by this CTA
+      for (int64_t item = item0; item < p.n_items && ok; item += item_step, g += n_kv, ++k) {
+        // MMAs of one CTA run in issue order, so S(j) of this item may overwrite the S/P
+        // columns that the previous item's last PV MMAs read; O is overwritten only by PV(0),
+        // issued after the softmax group's P-ready arrival, which follows its epilogue reads.
+        ok = wait_phase(bar(kBarQFull), (uint32_t)(k & 1), abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma,
+                        wtag(kBarQFull, 0));
+        int vs_prev = 0;
+        for (int j = 0; j < n_kv && ok; ++j) {
+          const int64_t gj = g + j;
+          const int64_t ki = 2 * gj;
+          const int ks = (int)(ki % kStages);
+          ok = wait_phase(bar(kBarKVFull + ks), (uint32_t)((ki / kStages) & 1), abort_flag, p.timeout_ns, p.err,
+                          kDevErrTimeoutMma, wtag(kBarKVFull + ks, j));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tO1, tS1 + kk * 8, v_desc(vs_prev, kk), kIdescPV, (j - 1 > 0 || kk > 0));
-          mma_commit(bar(kBarKVEmpty + vs_prev));
-        }
+          for (int kk = 0; kk < 8; ++kk) mma_ss(tS0, q_desc(0, kk), k_desc(ks, kk), kIdescQK, kk > 0);
+          mma_commit(bar(kBarSFull + 0));
+          if (j > 0) {
+            ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((gj - 1) & 1), abort_flag, p.timeout_ns, p.err,
+                            kDevErrTimeoutMma, wtag(kBarPReady + 1, j));
+            if (!ok) break;
+            tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tS1, q_desc(1, kk), k_desc(ks, kk), kIdescQK, kk > 0);
-        mma_commit(bar(kBarSFull + 1));
-        mma_commit(bar(kBarKVEmpty + ks));
-        const int vi = 2 * j + 1, vs = vi % kStages;
-        ok = wait_phase(bar(kBarKVFull + vs), (uint32_t)((vi / kStages) & 1), abort_flag, p.timeout_ns, p.err,
-                        kDevErrTimeoutMma, wtag(kBarKVFull + vs, j)) &&
-             wait_phase(bar(kBarPReady + 0), (uint32_t)(j & 1), abort_flag, p.timeout_ns, p.err,
-                        kDevErrTimeoutMma, wtag(kBarPReady + 0, j));
-        if (!ok) break;
-        tc_fence_after();
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tO1, tS1 + kk * 8, v_desc(vs_prev, kk), kIdescPV, (j - 1 > 0 || kk > 0));
+            mma_commit(bar(kBarKVEmpty + vs_prev));
+          }
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ts(tO0, tS0 + kk * 8, v_desc(vs, kk), kIdescPV, (j > 0 || kk > 0));
-        if (j == n_kv - 1) mma_commit(bar(kBarODone + 0));
-        vs_prev = vs;
-      }
-      if (ok) {
-        ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((n_kv - 1) & 1), abort_flag, p.timeout_ns, p.err,
-                        kDevErrTimeoutMma, wtag(kBarPReady + 1, n_kv));
-        if (ok) {
+          for (int kk = 0; kk < 8; ++kk) mma_ss(tS1, q_desc(1, kk), k_desc(ks, kk), kIdescQK, kk > 0);
+          mma_commit(bar(kBarSFull + 1));
+          mma_commit(bar(kBarKVEmpty + ks));
+          if (j == n_kv - 1) mma_commit(bar(kBarQEmpty));  // the producer may load the next Q
+          const int64_t vi = 2 * gj + 1;
+          const int vs = (int)(vi % kStages);
+          ok = wait_phase(bar(kBarKVFull + vs), (uint32_t)((vi / kStages) & 1), abort_flag, p.timeout_ns, p.err,
+                          kDevErrTimeoutMma, wtag(kBarKVFull + vs, j)) &&
+               wait_phase(bar(kBarPReady + 0), (uint32_t)(gj & 1), abort_flag, p.timeout_ns, p.err,
+                          kDevErrTimeoutMma, wtag(kBarPReady + 0, j));
+          if (!ok) break;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tO1, tS1 + kk * 8, v_desc(vs_prev, kk), kIdescPV, (n_kv - 1 > 0 || kk > 0));
-          mma_commit(bar(kBarKVEmpty + vs_prev));
-          mma_commit(bar(kBarODone + 1));
+          for (int kk = 0; kk < 8; ++kk) mma_ts(tO0, tS0 + kk * 8, v_desc(vs, kk), kIdescPV, (j > 0 || kk > 0));
+          if (j == n_kv - 1) mma_commit(bar(kBarODone + 0));
+          vs_prev = vs;
+        }
+        if (ok) {
+          ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((g + n_kv - 1) & 1), abort_flag, p.timeout_ns, p.err,
+                          kDevErrTimeoutMma, wtag(kBarPReady + 1, n_kv));
+          if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tO1, tS1 + kk * 8, v_desc(vs_prev, kk), kIdescPV, (n_kv - 1 > 0 || kk > 0));
+            mma_commit(bar(kBarKVEmpty + vs_prev));
+            mma_commit(bar(kBarODone + 1));
+          }
         }
       }
       if (!ok) {
@@ -689,56 +734,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = (warp - 4) >> 2;   // Q tile of this group
     const int wq = warp & 3;         // TMEM lane quarter of this warp
     const int r = wq * 32 + lane;    // row within the tile
-    const int64_t qb = qb0 + t;
-    const bool tile_ok = qb < p.nqb;
-    const int64_t row = qb * kBQ + r;
-    const bool row_ok = tile_ok && row < p.Sq;
-    const int64_t bh = (int64_t)b * p.H + h;
-    const bool fixed = !tile_ok || (!p.force_online && p.flag[bh * p.nqb + qb] != 0);
-    // the row's shift: fixed-m rows subtract b_i from fm_bounds; online rows their running
-    // max (one register serves both, the kernel is at its register limit)
-    float shv = -INFINITY;
-    if (fixed) shv = row_ok ? p.shift[bh * p.Sq + row] : 0.f;
-    // an online row that adds into earlier chunks starts from their shift: as long as this
-    // chunk's scores stay within 2^8 of it, O comes out at the accumulator's own shift and the
-    // merge is a plain add
-    else if (p.accumulate && row_ok) shv = p.acc_max[bh * p.Sq + row];
-    const float shift_prev = shv;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)(t * 128);
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(t * 128);
-    float l[4] = {0.f, 0.f, 0.f, 0.f};
-    // key sinks of this head (ascending global key indices, INT_MAX pads): columns to drop
-    int next_sink = sink_after_key(reinterpret_cast<const int32_t *>(gbase + kOffSinks), INT_MIN);
+    int32_t *ssk = reinterpret_cast<int32_t *>(gbase + kOffSinks) + t * FM_MAX_SINKS;
     bool ok = true;
-    int c = 0;  // chunk of key tile j
-    for (int j = 0; j < n_kv; ++j) {
-      while (j >= p.tile0[c + 1]) ++c;
-      ok = wait_phase(bar(kBarSFull + t), (uint32_t)(j & 1), abort_flag, p.timeout_ns, p.err,
-                      kDevErrTimeoutSoftmax, wtag(kBarSFull + t, j));
-      ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
+    int64_t g = 0;
+    int64_t k = 0;
+    for (int64_t item = item0; item < p.n_items && ok; item += item_step, g += n_kv, ++k) {
+      const int64_t bh = item_bh(item);
+      const int64_t qb = item_qb0(item) + t;
+      const bool tile_ok = qb < p.nqb;
+      const int64_t row = qb * kBQ + r;
+      const bool row_ok = tile_ok && row < p.Sq;
+      const bool fixed = !tile_ok || (!p.force_online && p.flag[bh * p.nqb + qb] != 0);
+      // the row's shift: fixed-m rows subtract b_i from fm_bounds; online rows their running
+      // max (one register serves both, the kernel is at its register limit)
+      float shv = -INFINITY;
+      if (fixed) shv = row_ok ? p.shift[bh * p.Sq + row] : 0.f;
+      // an online row that adds into earlier chunks starts from their shift: as long as this
+      // chunk's scores stay within 2^8 of it, O comes out at the accumulator's own shift and the
+      // merge is a plain add
+      else if (p.accumulate && row_ok) shv = p.acc_max[bh * p.Sq + row];
+      const float shift_prev = shv;
+      float l[4] = {0.f, 0.f, 0.f, 0.f};
+      // key sinks of this item's head (ascending global key indices, INT_MAX pads): columns to
+      // drop.  Every thread of the group finished the previous item's tiles (their P-ready
+      // arrivals preceded its O-done) before any thread gets here, so the list can be replaced.
+      // Without sinks the list is never read (next_sink stays INT_MAX).
+      int next_sink = INT_MAX;
+      if (p.sinks) {
+        if (wq == 0 && lane < FM_MAX_SINKS) ssk[lane] = p.sinks[bh * FM_MAX_SINKS + lane];
+        named_barrier(1 + t, 128);
+        next_sink = sink_after_key(ssk, INT_MIN);
+      }
+      int c = 0;  // chunk of key tile j
+      for (int j = 0; j < n_kv; ++j) {
+        while (j >= p.tile0[c + 1]) ++c;
+        ok = wait_phase(bar(kBarSFull + t), (uint32_t)((g + j) & 1), abort_flag, p.timeout_ns, p.err,
+                        kDevErrTimeoutSoftmax, wtag(kBarSFull + t, j));
+        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
+        if (!ok) break;
+        tc_fence_after();
+        const int jl = (j - p.tile0[c]) * kBK;  // first key of the tile within its chunk
+        const int nvalid = min(kBK, p.len[c] - jl);  // ragged end of each chunk
+        const int g0 = p.key0[c] + jl;               // global index of the tile's first key
+        if (next_sink < g0)  // sinks before this tile
+          next_sink = sink_after_key(ssk, g0 - 1);
+        // -inf over the key sinks in this tile and over the columns past the chunk's end
+        if (next_sink < g0 + nvalid || nvalid < kBK) mask_tile(tS, nvalid, g0, ssk, next_sink);
+        if (fixed) softmax_fixed_tile(tS, p.alpha, -shv, l);
+        else softmax_online_tile(tS, tO, p.alpha, j > 0, shv, l);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPReady + t));
+      }
+      if (ok) {
+        ok = wait_phase(bar(kBarODone + t), (uint32_t)(k & 1), abort_flag, p.timeout_ns, p.err,
+                        kDevErrTimeoutSoftmax, wtag(kBarODone + t, n_kv));
+        ok = __all_sync(0xffffffffu, ok);
+      }
       if (!ok) break;
-      tc_fence_after();
-      const int jl = (j - p.tile0[c]) * kBK;  // first key of the tile within its chunk
-      const int nvalid = min(kBK, p.len[c] - jl);  // ragged end of each chunk
-      const int g0 = p.key0[c] + jl;               // global index of the tile's first key
-      if (next_sink < g0)  // sinks before this tile
-        next_sink = sink_after_key(reinterpret_cast<const int32_t *>(gbase + kOffSinks), g0 - 1);
-      // -inf over the key sinks in this tile and over the columns past the chunk's end
-      if (next_sink < g0 + nvalid || nvalid < kBK)
-        mask_tile(tS, nvalid, g0, reinterpret_cast<const int32_t *>(gbase + kOffSinks), next_sink);
-      if (fixed) softmax_fixed_tile(tS, p.alpha, -shv, l);
-      else softmax_online_tile(tS, tO, p.alpha, j > 0, shv, l);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(kBarPReady + t));
-    }
-    if (ok) {
-      ok = wait_phase(bar(kBarODone + t), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutSoftmax,
-                      wtag(kBarODone + t, n_kv));
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
       tc_fence_after();
       const float lsum = (l[0] + l[1]) + (l[2] + l[3]);
       const int64_t rflat = bh * p.Sq + row;
@@ -764,14 +820,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       float4 *dst = reinterpret_cast<float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
       // A chunk that is not the last, on a tile whose O needs no rescale of the accumulator
       // (fixed-m; any tile of a first chunk, whose O is simply stored; an online tile whose
-      // every row kept the accumulator's shift, so that cprev = cnew = 1): O goes through
-      // shared memory, and one bulk tensor operation per 32 columns adds it into acc_o (or
-      // stores it there) in the memory system, so the SM never reads the accumulator.  The
-      // staging tile (64 KiB of 128-byte-swizzled 32-column boxes) is the Q region for tile 0,
-      // free once the last S MMA is done, which the O-done commit covers, and the first two
-      // K/V stages for tile 1, free once every MMA is done.
+      // every row kept the accumulator's shift, so that cprev = cnew = 1), adds O into acc_o
+      // (or stores it there) without reading the accumulator through the SM:
+      //  - one CTA per item: O goes through shared memory, and one bulk tensor operation per
+      //    32 columns does it in the memory system.  The staging tile (64 KiB of
+      //    128-byte-swizzled 32-column boxes) is the Q region for tile 0, free once the last S
+      //    MMA is done, which the O-done commit covers, and the first two K/V stages for tile
+      //    1, free once every MMA is done.
+      //  - persistent: those regions already hold the next item's Q and K/V, so each row adds
+      //    its O from registers with vector reductions (stores on the first chunk).
       bool plain_add = fixed || !p.accumulate;
-      if (!plain_add && p.acc_tma && !final_out)
+      if (!plain_add && (p.acc_tma || p.persistent) && !final_out)
         plain_add = named_barrier_and(1 + t, 128, !row_ok || (shift_prev != -INFINITY && shv == shift_prev));
       if (p.acc_tma && plain_add && !final_out) {
         uint8_t *stage = gbase + (t == 0 ? kOffQ : kOffKV);
@@ -793,6 +852,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 4; ++c)
             tma_acc_3d(&maps.acc, sbase + c * (kBQ * 128), c * 32, (int)(qb * kBQ), (int)bh, p.accumulate != 0);
           bulk_commit_and_wait();
+        }
+        if (row_ok) {
+          p.acc_sum[rflat] = sum_new;
+          p.acc_max[rflat] = shift_new;
+        }
+      } else if (p.persistent && plain_add && !final_out) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          if (row_ok) {
+            float *rowp = p.acc_o + rflat * kHD + c * 32;
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+              if (p.accumulate)
+                red_add_v4(rowp + 4 * q4, o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+              else
+                *reinterpret_cast<uint4 *>(rowp + 4 * q4) = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+            }
+          }
         }
         if (row_ok) {
           p.acc_sum[rflat] = sum_new;
@@ -923,6 +1002,16 @@ bool encode_acc_map(CUtensorMap *map, float *acc_o, const View &q) {
   return r == CUDA_SUCCESS;
 }
 
+// Schedule of a launch (fm_opts.schedule).  AUTO takes the persistent schedule for launches of
+// more than one wave whose items are short (few key tiles), where each CTA's prologue,
+// pipeline fill and epilogue are a large share of its time and can overlap the next item's
+// loads and first MMAs.
+bool use_persistent(int schedule, int64_t n_items, int n_kv, int sms) {
+  if (schedule == FM_SCHEDULE_GRID) return false;
+  if (schedule == FM_SCHEDULE_PERSISTENT) return true;
+  return n_items > sms && n_kv <= kPersistentMaxTiles;
+}
+
 bool tma_view_ok(const View &t) {
   if (t.dtype != FM_BF16 || t.D != kHD || t.sD != 1) return false;
   if (reinterpret_cast<uintptr_t>(t.ptr) % 16) return false;
@@ -1016,9 +1105,16 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
     p.osH = a.out->sH;
     p.osS = a.out->sS;
   }
-  // non-final chunks add O into acc_o with bulk tensor operations where the map encodes
-  p.acc_tma = (!a.out && a.q.B * a.q.H <= INT_MAX && encode_acc_map(&maps.acc, a.acc_o, a.q)) ? 1 : 0;
-  dim3 grid((unsigned)((a.nqb + 1) / 2), (unsigned)a.q.H, (unsigned)a.q.B);
+  p.n_pairs = (a.nqb + 1) / 2;
+  p.n_items = p.n_pairs * a.q.H * a.q.B;
+  const int sms = current_device_sm_count();
+  p.persistent = use_persistent(a.schedule, p.n_items, p.n_kv, sms) ? 1 : 0;
+  // non-final chunks of the one-item-per-CTA schedule add O into acc_o with bulk tensor
+  // operations where the map encodes (the persistent schedule needs that shared memory for the
+  // next item and adds from registers instead)
+  p.acc_tma = (!p.persistent && !a.out && a.q.B * a.q.H <= INT_MAX && encode_acc_map(&maps.acc, a.acc_o, a.q)) ? 1 : 0;
+  const dim3 grid = p.persistent ? dim3((unsigned)(p.n_items < sms ? p.n_items : sms))
+                                 : dim3((unsigned)p.n_pairs, (unsigned)a.q.H, (unsigned)a.q.B);
   return launch_pdl(fm_chunk_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, maps, p);
 }
 

@@ -61,6 +61,7 @@ struct ChunkArgs {
   View q, k, v;            // k, v: this chunk
   float alpha;
   int force_online;
+  int schedule = FM_SCHEDULE_AUTO;  // fm_opts.schedule (tensor-core kernel)
   int accumulate;
   int64_t nqb;
   const uint8_t *flag;     // [B,H,nqb]

@@ -103,7 +103,18 @@ typedef struct {
                            kmax_sq becomes that norm squared.  The chunks skip the sinks and
                            fm_fold_sinks merges them back exactly, so the output is still
                            plain attention over every key. */
+  int32_t schedule;     /* how the tensor-core chunk kernel spreads its work (FM_SCHEDULE_*);
+                           the result is the same bits either way.  Ignored by fm_bounds. */
 } fm_opts;
+
+/* fm_opts.schedule.  A work item is two 128-row Q tiles of one (batch, head) against every key
+ * tile of the call.  GRID launches one CTA per item.  PERSISTENT launches one CTA per SM that
+ * walks the items in turn, loading the next item's Q and K/V tiles and running its first S
+ * MMAs while the softmax warps finish the current item's epilogue (the accumulator add then
+ * comes from registers as vector reductions rather than through shared memory).  AUTO picks
+ * PERSISTENT for launches of more than one wave with at most 16 key tiles per item, where the
+ * per-item prologue and epilogue are a large share of the time, and GRID otherwise. */
+enum { FM_SCHEDULE_AUTO = 0, FM_SCHEDULE_GRID = 1, FM_SCHEDULE_PERSISTENT = 2 };
 
 /* Bounds of one attention call ([PR477] Summary, "Dynamic eligibility bounding").
  * The caller allocates the device arrays and fills the pointers; fm_bounds fills
@@ -290,7 +301,7 @@ FM_API int fm_probe_wait_timeout(unsigned int timeout_ms, fm_stream_t stream);
  * thread's next fm_* call. */
 FM_API const char *fm_last_error(void);
 
-/* ABI version of this header: (major << 16) | minor. */
+/* ABI version of this header: (major << 16) | minor.  1.2 added fm_opts.schedule. */
 FM_API int fm_version(void);
 
 /* Upper bound of the scratch fm_bounds_noalloc can use: 4 MiB.  That covers, at D = 128,

@@ -770,3 +770,40 @@ def test_randomised_shapes_and_options(dev):
         ob = oracle.bounds(q, k, v, centering=opts["centering"], per_row=opts["per_row"],
                            sink_keys=opts["sink_keys"])
         check_bounds(fa, ob)
+
+
+@pytest.mark.parametrize("force_online", [False, True])
+@pytest.mark.parametrize("mode", ["chunks", "fused", "one_launch", "sinks"])
+def test_persistent_schedule_gives_the_grid_bits(dev, mode, force_online):
+    """The persistent schedule (one CTA per SM walking work items, accumulator adds from
+    registers) and the one-CTA-per-item grid (adds through shared memory and bulk tensor
+    reductions) do the same fp32 arithmetic in the same order: identical bits, on more work
+    items (20 heads x 8 Q-tile pairs, the last pair half past Sq) than a GB300 has SMs."""
+    H, Sq, N = 20, 1900, 1500
+    name = "sinks" if mode == "sinks" else "mix"
+    q, k, v = workloads.make_inputs(name, device="cpu", heads=range(H), Sq=Sq, N=N)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    chunks = [(0, 700), (700, 1), (701, 799)]
+    outs = {}
+    for sched in ("grid", "persistent"):
+        fa = fm.FixedMAttention(1, H, Sq, N, 128, dev, centering=mode != "sinks", force_online=force_online,
+                                sink_keys=4 if mode == "sinks" else 0, schedule=sched)
+        o = fa.forward(qd, kd, vd, chunks, with_lse=True, fused_final=mode != "chunks",
+                       one_launch=mode == "one_launch").clone()
+        fm.fm_sync_status()
+        outs[sched] = (o, fa.lse.clone(), fa.acc_sum.clone(), fa.acc_max.clone())
+    for a, b in zip(outs["grid"], outs["persistent"]):
+        assert torch.equal(a, b)
+    heads = [0, 7, 19]
+    rows = list(range(0, 128)) + list(range(1792, 1900))
+    reference(q, k, v, heads, rows, centering=mode != "sinks", sink_keys=4 if mode == "sinks" else 0).check(
+        pick(outs["persistent"][0], heads, rows), f"persistent {mode} online={force_online}")
+
+
+def test_schedule_option_is_validated(dev):
+    q, k, v = workloads.make_inputs("wan", device=dev, heads=[0], Sq=130, N=140)
+    fa = fm.FixedMAttention(1, 1, 130, 140, 128, dev, schedule=3)
+    fm.fm_bounds(q, k, v, fa.opt, fa.bounds, fa.workspace)
+    with pytest.raises(fm.FMError) as e:
+        fm.fm_attn_chunk(q, k, v, fa.bounds, fa.opt, fa.acc_o, fa.acc_sum, fa.acc_max, False)
+    assert e.value.code == fm.FM_ERR_ARG
