@@ -741,7 +741,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int64_t g = 0;
     int64_t k = 0;
-    for (int64_t item = item0; item < p.n_items && ok; item += item_step, g += n_kv, ++k) {
+    // Every thread of the group takes the same named barriers in the same order: a wait that
+    // gave up ends this thread's tile loop, and the group agrees on the outcome at one barrier
+    // that each of its threads reaches, before any other barrier of the item.
+    for (int64_t item = item0; item < p.n_items; item += item_step, g += n_kv, ++k) {
       const int64_t bh = item_bh(item);
       const int64_t qb = item_qb0(item) + t;
       const bool tile_ok = qb < p.nqb;
@@ -794,6 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         kDevErrTimeoutSoftmax, wtag(kBarODone + t, n_kv));
         ok = __all_sync(0xffffffffu, ok);
       }
+      ok = named_barrier_and(1 + t, 128, ok);
       if (!ok) break;
       tc_fence_after();
       const float lsum = (l[0] + l[1]) + (l[2] + l[3]);
