@@ -33,12 +33,14 @@ FM_F32, FM_BF16, FM_F16, FM_F8E4M3, FM_F8E5M2 = 0, 1, 2, 3, 4
 FM_OK, FM_ERR_ARG, FM_ERR_SHAPE, FM_ERR_DTYPE, FM_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
 FM_ERR_BOUNDS_MISMATCH, FM_ERR_CUDA, FM_ERR_TIMEOUT = 5, 6, 7
 FM_BOUNDS_MAGIC = 0x314D4246
+FM_BOUNDS_LOCAL_MAGIC = 0x314C4246
 FM_BLOCK_Q = 128
 ERROR_NAMES = {0: "FM_OK", 1: "FM_ERR_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_DTYPE", 4: "FM_ERR_UNSUPPORTED",
                5: "FM_ERR_BOUNDS_MISMATCH", 6: "FM_ERR_CUDA", 7: "FM_ERR_TIMEOUT"}
 ABI_SYMBOLS = ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
                "fm_last_error", "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout",
-               "fm_attn_chunk_final", "fm_attn_chunks", "fm_fold_sinks")
+               "fm_attn_chunk_final", "fm_attn_chunks", "fm_fold_sinks", "fm_ring_stats_bytes", "fm_ring_key_sums",
+               "fm_bounds_local", "fm_bounds_combine")
 FM_MAX_CHUNKS = 8
 FM_MAX_SINKS = 8
 FM_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -72,7 +74,8 @@ class fm_bounds_out(ctypes.Structure):
                 ("C", ctypes.c_int32), ("W", ctypes.c_int32), ("gate", ctypes.c_int32),
                 ("centered", ctypes.c_int32), ("per_row", ctypes.c_int32), ("n_sink", ctypes.c_int32),
                 ("alpha", ctypes.c_float), ("dtype", ctypes.c_int32),
-                ("kv_seen", ctypes.c_int64), ("online_lock", ctypes.c_int32), ("sinks_folded", ctypes.c_int32),
+                ("kv_seen", ctypes.c_int64), ("next_key_offset", ctypes.c_int64), ("online_lock", ctypes.c_int32),
+                ("sinks_folded", ctypes.c_int32),
                 ("magic", ctypes.c_uint32)]
 
 
@@ -100,13 +103,18 @@ def load(path: str | None = None):
     lib.fm_attn_chunk_final.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_int, P, P, P]
     lib.fm_attn_chunks.argtypes = [P, P, P, ctypes.c_int, P, P, P, P, P, ctypes.c_int, P, P, P]
     lib.fm_fold_sinks.argtypes = [P, P, P, P, P, P, P]
+    lib.fm_ring_stats_bytes.argtypes = [i64, i64, i64, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]
+    lib.fm_ring_key_sums.argtypes = [P, P, P, ctypes.c_size_t, P]
+    lib.fm_bounds_local.argtypes = [P, P, P, i64, i64, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.fm_bounds_combine.argtypes = [P, ctypes.c_int, P, P, P]
     lib.fm_sync_status.argtypes = [P]
     lib.fm_last_error.restype = ctypes.c_char_p
     lib.fm_last_error.argtypes = []
     lib.fm_version.argtypes = []
     for name in ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
                  "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout",
-                 "fm_attn_chunk_final", "fm_attn_chunks", "fm_fold_sinks"):
+                 "fm_attn_chunk_final", "fm_attn_chunks", "fm_fold_sinks", "fm_ring_stats_bytes", "fm_ring_key_sums",
+                 "fm_bounds_local", "fm_bounds_combine"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -217,6 +225,35 @@ def fm_bounds_noalloc(q, k_full, v_full, opt: fm_opts, bounds: Bounds, stream=No
                                            ctypes.byref(bounds.out), _stream(stream)))
 
 
+def fm_ring_stats_bytes(B: int, H: int, D: int, sink_keys: int = 0) -> int:
+    n = ctypes.c_size_t()
+    _check(load().fm_ring_stats_bytes(B, H, D, int(sink_keys), ctypes.byref(n)))
+    return n.value
+
+
+def fm_ring_key_sums(k_shard, ksum, workspace, stream=None):
+    """ksum [B, H, D] f32 <- the sums of this rank's keys (step 1 of the ring bounds)."""
+    tk = tensor(k_shard)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check(load().fm_ring_key_sums(ctypes.byref(tk), _ptr(ksum), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fm_bounds_local(q, k_shard, v_shard, key_offset: int, N_total: int, ksum_total, opt: fm_opts, bounds: Bounds,
+                    stats, workspace, stream=None):
+    """This rank's part of the bounds: bounds' query-side arrays and its statistics block (step 2)."""
+    tq, tk, tv = tensor(q), tensor(k_shard), tensor(v_shard)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    return _check(load().fm_bounds_local(ctypes.byref(tq), ctypes.byref(tk), ctypes.byref(tv), int(key_offset),
+                                         int(N_total), _ptr(ksum_total), ctypes.byref(opt), ctypes.byref(bounds.out),
+                                         _ptr(stats), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def fm_bounds_combine(stats_all, n_ranks: int, opt: fm_opts, bounds: Bounds, stream=None):
+    """Every rank's statistics blocks (rank order) -> the rest of the bounds (step 3)."""
+    return _check(load().fm_bounds_combine(_ptr(stats_all), int(n_ranks), ctypes.byref(opt), ctypes.byref(bounds.out),
+                                           _stream(stream)))
+
+
 def fm_attn_chunk(q, k_chunk, v_chunk, bounds: Bounds, opt: fm_opts, acc_o, acc_sum, acc_max,
                   accumulate: bool, stream=None):
     tq, tk, tv = tensor(q), tensor(k_chunk), tensor(v_chunk)
@@ -312,12 +349,16 @@ class FixedMAttention:
             for g0 in range(0, len(chunks), FM_MAX_CHUNKS):
                 grp = chunks[g0:g0 + FM_MAX_CHUNKS]
                 last = g0 + FM_MAX_CHUNKS >= len(chunks)
+                if any(grp[i][0] + grp[i][1] != grp[i + 1][0] for i in range(len(grp) - 1)):
+                    raise ValueError("one_launch folds consecutive key ranges only")
+                self.bounds.out.next_key_offset = grp[0][0]
                 fm_attn_chunks(q, [k[:, :, s:s + n] for s, n in grp], [v[:, :, s:s + n] for s, n in grp],
                                self.bounds, self.opt, self.acc_o, self.acc_sum, self.acc_max, g0 > 0,
                                self.out if last else None, lse if last else None, stream)
             return self.out
         for i, (s, n) in enumerate(chunks):
             kc, vc = k[:, :, s:s + n], v[:, :, s:s + n]
+            self.bounds.out.next_key_offset = s  # the chunk's global key offset: any order works
             if fused_final and i == len(chunks) - 1:
                 fm_attn_chunk_final(q, kc, vc, self.bounds, self.opt, self.acc_o, self.acc_sum, self.acc_max, i > 0,
                                     self.out, lse, stream)

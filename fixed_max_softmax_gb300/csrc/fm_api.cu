@@ -162,13 +162,17 @@ int fm_bounds_workspace_size(int64_t B, int64_t H, int64_t N_total, int64_t D, s
   return FM_OK;
 }
 
-int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_full, const fm_opts *opts,
-              fm_bounds_out *out, void *workspace, size_t workspace_bytes, fm_stream_t stream) {
-  t_err.clear();
+}  // extern "C"
+
+namespace {
+// Validation and the host-side fields that fm_bounds and fm_bounds_local share.  N_total < 0
+// takes the key count of k (fm_bounds); the ring's rank gives the count over every shard.
+// On success `a` is ready for the launch and *empty says that there is nothing to launch.
+int setup_bounds(const fm_tensor *q, const fm_tensor *k, const fm_tensor *v, const fm_opts *opts, fm_bounds_out *out,
+                 int64_t N_total, void *workspace, size_t workspace_bytes, BoundsArgs *a, bool *empty) {
   View vq, vk, vv;
   int rc;
-  if ((rc = to_view(q, "q", &vq)) || (rc = to_view(k_full, "k_full", &vk)) || (rc = to_view(v_full, "v_full", &vv)))
-    return rc;
+  if ((rc = to_view(q, "q", &vq)) || (rc = to_view(k, "k", &vk)) || (rc = to_view(v, "v", &vv))) return rc;
   if ((rc = check_qkv(vq, vk, vv))) return rc;
   if (!out) return fail(FM_ERR_ARG, "out is NULL");
   if (opts && ((opts->centering != 0 && opts->centering != 1) || (opts->per_row != 0 && opts->per_row != 1)))
@@ -179,7 +183,8 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
   if (n_sink < 0 || n_sink > FM_MAX_SINKS) return fail(FM_ERR_ARG, "sink_keys = %d outside [0, %d]", n_sink, FM_MAX_SINKS);
   double alpha;
   if ((rc = make_alpha(opts, vq.D, &alpha))) return rc;
-  const int64_t B = vq.B, H = vq.H, Sq = vq.S, D = vq.D, N = vk.S;
+  const int64_t B = vq.B, H = vq.H, Sq = vq.S, D = vq.D;
+  const int64_t N = N_total < 0 ? vk.S : N_total;
   if (n_sink > 0 && B * H > 0 && (!out->sink_idx || !out->sink_k || !out->sink_v))
     return fail(FM_ERR_ARG, "fm_bounds_out: sink_idx, sink_k and sink_v must be set when sink_keys > 0");
   // the chunk kernels find a sink by its global key index in 32-bit arithmetic
@@ -191,7 +196,7 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
       (B * H * Sq > 0 && (!out->qkbar || !out->shift)) ||
       (B * H > 0 && (!out->kmax_sq || !out->kbar || !out->vmax_sq)))
     return fail(FM_ERR_ARG, "fm_bounds_out: every device array pointer must be set");
-  const size_t need = bounds_workspace_bytes(B, H, N, D);
+  const size_t need = bounds_workspace_bytes(B, H, vk.S, D);
   if (workspace_bytes < need) return fail(FM_ERR_ARG, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
   if (need > 0 && !workspace) return fail(FM_ERR_ARG, "workspace is NULL");
   if (reinterpret_cast<uintptr_t>(workspace) % 16) return fail(FM_ERR_ARG, "workspace must be 16-byte aligned");
@@ -219,38 +224,156 @@ int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_fu
   out->alpha = (float)alpha;
   out->dtype = vq.dtype;
   out->kv_seen = 0;
+  out->next_key_offset = -1;
   out->online_lock = -1;
   out->magic = 0;
-  if (B * H == 0) {
-    out->magic = FM_BOUNDS_MAGIC;
-    return FM_OK;
-  }
+  *empty = B * H == 0;
+  a->q = vq;
+  a->k = vk;
+  a->v = vv;
+  a->centering = centering;
+  a->per_row = per_row;
+  a->alpha = alpha;
+  a->C = C;
+  a->gate = gate;
+  a->nqb = nqb;
+  a->m = out->m;
+  a->flag = out->flag;
+  a->qmax_sq = out->qmax_sq;
+  a->kmax_sq = out->kmax_sq;
+  a->kbar = out->kbar;
+  a->qkbar = out->qkbar;
+  a->shift = out->shift;
+  a->vmax_sq = out->vmax_sq;
+  a->n_sink = n_sink;
+  a->sink_idx = out->sink_idx;
+  a->sink_k = out->sink_k;
+  a->sink_v = out->sink_v;
+  a->ws = workspace;
+  a->ws_bytes = workspace_bytes;
+  return FM_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tensor *v_full, const fm_opts *opts,
+              fm_bounds_out *out, void *workspace, size_t workspace_bytes, fm_stream_t stream) {
+  t_err.clear();
   BoundsArgs a;
-  a.q = vq;
-  a.k = vk;
-  a.v = vv;
-  a.centering = centering;
-  a.per_row = per_row;
-  a.alpha = alpha;
-  a.C = C;
-  a.gate = gate;
-  a.nqb = nqb;
-  a.m = out->m;
-  a.flag = out->flag;
-  a.qmax_sq = out->qmax_sq;
-  a.kmax_sq = out->kmax_sq;
-  a.kbar = out->kbar;
-  a.qkbar = out->qkbar;
-  a.shift = out->shift;
-  a.vmax_sq = out->vmax_sq;
-  a.n_sink = n_sink;
-  a.sink_idx = out->sink_idx;
-  a.sink_k = out->sink_k;
-  a.sink_v = out->sink_v;
-  a.ws = workspace;
-  a.ws_bytes = workspace_bytes;
-  cudaError_t e = launch_bounds(a, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "fm_bounds launch");
+  bool empty = false;
+  int rc = setup_bounds(q, k_full, v_full, opts, out, -1, workspace, workspace_bytes, &a, &empty);
+  if (rc) return rc;
+  if (!empty) {
+    cudaError_t e = launch_bounds(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fm_bounds launch");
+  }
+  out->magic = FM_BOUNDS_MAGIC;
+  return FM_OK;
+}
+
+int fm_ring_stats_bytes(int64_t B, int64_t H, int64_t D, int sink_keys, size_t *bytes) {
+  t_err.clear();
+  if (!bytes) return fail(FM_ERR_ARG, "bytes is NULL");
+  if (B < 0 || H < 0 || D < 0) return fail(FM_ERR_ARG, "negative size");
+  if (sink_keys < 0 || sink_keys > FM_MAX_SINKS) return fail(FM_ERR_ARG, "sink_keys outside [0, %d]", FM_MAX_SINKS);
+  *bytes = ring_stats_bytes(B, H, D, sink_keys);
+  return FM_OK;
+}
+
+int fm_ring_key_sums(const fm_tensor *k_shard, float *ksum, void *workspace, size_t workspace_bytes,
+                     fm_stream_t stream) {
+  t_err.clear();
+  View vk;
+  int rc;
+  if ((rc = to_view(k_shard, "k_shard", &vk))) return rc;
+  if (vk.B * vk.H * vk.D > 0 && !ksum) return fail(FM_ERR_ARG, "ksum is NULL");
+  const size_t need = bounds_workspace_bytes(vk.B, vk.H, vk.S, vk.D);
+  if (workspace_bytes < need) return fail(FM_ERR_ARG, "workspace of %zu bytes < %zu needed", workspace_bytes, need);
+  if (need > 0 && !workspace) return fail(FM_ERR_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) % 16) return fail(FM_ERR_ARG, "workspace must be 16-byte aligned");
+  cudaError_t e = launch_ring_key_sums(vk, ksum, workspace, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "fm_ring_key_sums launch");
+  return FM_OK;
+}
+
+int fm_bounds_local(const fm_tensor *q, const fm_tensor *k_shard, const fm_tensor *v_shard, int64_t key_offset,
+                    int64_t N_total, const float *ksum_total, const fm_opts *opts, fm_bounds_out *out, void *stats,
+                    void *workspace, size_t workspace_bytes, fm_stream_t stream) {
+  t_err.clear();
+  if (!k_shard) return fail(FM_ERR_ARG, "k_shard is NULL");
+  if (key_offset < 0 || N_total < 0 || k_shard->S < 0 || key_offset + k_shard->S > N_total)
+    return fail(FM_ERR_ARG, "the shard's keys [%lld, %lld) must lie in [0, N_total = %lld)", (long long)key_offset,
+                (long long)(key_offset + k_shard->S), (long long)N_total);
+  // checked before anything of `out` is written
+  const bool has_heads = q && q->B > 0 && q->H > 0;
+  if (has_heads && opts && opts->centering && !ksum_total)
+    return fail(FM_ERR_ARG, "centering needs ksum_total, the ring-wide key sums");
+  if (has_heads && !stats) return fail(FM_ERR_ARG, "stats is NULL");
+  if (reinterpret_cast<uintptr_t>(stats) % 16) return fail(FM_ERR_ARG, "stats must be 16-byte aligned");
+  if (opts && opts->sink_keys > 0 && key_offset + k_shard->S > (int64_t)INT32_MAX)
+    return fail(FM_ERR_UNSUPPORTED, "key sinks need global key indices below 2^31");
+  BoundsArgs a;
+  bool empty = false;
+  int rc = setup_bounds(q, k_shard, v_shard, opts, out, N_total, workspace, workspace_bytes, &a, &empty);
+  if (rc) return rc;
+  if (!empty) {
+    cudaError_t e = launch_bounds_local(a, ksum_total, N_total, key_offset, stats, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fm_bounds_local launch");
+  }
+  out->magic = FM_BOUNDS_LOCAL_MAGIC;
+  return FM_OK;
+}
+
+int fm_bounds_combine(const void *stats_all, int n_ranks, const fm_opts *opts, fm_bounds_out *out,
+                      fm_stream_t stream) {
+  t_err.clear();
+  if (!out) return fail(FM_ERR_ARG, "out is NULL");
+  if (out->magic != FM_BOUNDS_LOCAL_MAGIC)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "out was not prepared by fm_bounds_local (magic 0x%08x)", out->magic);
+  const int centering = opts ? opts->centering : 0;
+  const int per_row = opts ? opts->per_row : 0;
+  const int n_sink = opts ? opts->sink_keys : 0;
+  double alpha;
+  int rc;
+  if ((rc = make_alpha(opts, out->D, &alpha))) return rc;
+  if (centering != out->centered || per_row != out->per_row || n_sink != out->n_sink || (float)alpha != out->alpha)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "opts differ from the ones fm_bounds_local was given");
+  if (n_ranks < 1) return fail(FM_ERR_ARG, "n_ranks = %d", n_ranks);
+  const bool empty = out->B * out->H == 0;
+  if (!empty && !stats_all) return fail(FM_ERR_ARG, "stats_all is NULL");
+  if (reinterpret_cast<uintptr_t>(stats_all) % 16) return fail(FM_ERR_ARG, "stats_all must be 16-byte aligned");
+  if (!empty) {
+    BoundsArgs a;
+    a.q = View{nullptr, out->dtype, out->B, out->H, out->Sq, out->D, 0, 0, 0, 0};
+    a.k = a.v = a.q;
+    a.centering = centering;
+    a.per_row = per_row;
+    a.alpha = alpha;
+    a.C = out->C;
+    a.gate = out->gate;
+    a.nqb = out->n_qblocks;
+    a.m = out->m;
+    a.flag = out->flag;
+    a.qmax_sq = out->qmax_sq;
+    a.kmax_sq = out->kmax_sq;
+    a.kbar = out->kbar;
+    a.qkbar = out->qkbar;
+    a.shift = out->shift;
+    a.vmax_sq = out->vmax_sq;
+    a.n_sink = n_sink;
+    a.sink_idx = out->sink_idx;
+    a.sink_k = out->sink_k;
+    a.sink_v = out->sink_v;
+    a.ws = nullptr;
+    a.ws_bytes = 0;
+    cudaError_t e = launch_bounds_combine(a, stats_all, n_ranks, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "fm_bounds_combine launch");
+  }
+  out->kv_seen = 0;
+  out->next_key_offset = -1;
+  out->online_lock = -1;
+  out->sinks_folded = 0;
   out->magic = FM_BOUNDS_MAGIC;
   return FM_OK;
 }
@@ -328,6 +451,12 @@ int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_ten
     return fail(FM_ERR_BOUNDS_MISMATCH,
                 "the key sinks were already folded in: no chunk may be added after fm_fold_sinks");
   if (n_sink > 0 && vq.B * vq.H > 0 && !bounds->sink_idx) return fail(FM_ERR_ARG, "bounds sink_idx is NULL");
+  // the global index of this call's first key: given, or where the keys folded so far end
+  if (bounds->next_key_offset < -1) return fail(FM_ERR_ARG, "next_key_offset = %lld", (long long)bounds->next_key_offset);
+  const int64_t key_start = bounds->next_key_offset >= 0 ? bounds->next_key_offset : (accumulate ? bounds->kv_seen : 0);
+  if (key_start + keys > bounds->N_total)
+    return fail(FM_ERR_BOUNDS_MISMATCH, "keys [%lld, %lld) lie past the %lld keys the bounds cover",
+                (long long)key_start, (long long)(key_start + keys), (long long)bounds->N_total);
   const int64_t rows = vq.B * vq.H * vq.S;
   if (rows > 0 && (!acc_o || !acc_sum || !acc_max)) return fail(FM_ERR_ARG, "accumulator pointer is NULL");
   if (rows > 0 && (!bounds->flag || !bounds->shift)) return fail(FM_ERR_ARG, "bounds flag/shift pointer is NULL");
@@ -359,7 +488,7 @@ int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_ten
   // key sinks: the chunks skip them by global key index; the first chunk of this call
   // starts where the keys folded so far end
   a.sinks = n_sink > 0 ? bounds->sink_idx : nullptr;
-  a.key0 = accumulate ? bounds->kv_seen : 0;
+  a.key0 = key_start;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   bool finalize_separately = o_out != nullptr;
@@ -425,6 +554,7 @@ int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_ten
     if (e != cudaSuccess) return cuda_fail(e, "fm_attn_chunk_final finalize launch");
   }
   bounds->kv_seen = seen;
+  bounds->next_key_offset = -1;
   bounds->online_lock = force_online;
   bounds->sinks_folded = (o_out && n_sink > 0) ? 1 : 0;
   return FM_OK;

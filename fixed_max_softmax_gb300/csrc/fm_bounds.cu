@@ -431,6 +431,264 @@ __global__ void __launch_bounds__(kThreads)
   shift[i] = (float)mi + qkbar[i];
 }
 
+// ---- the bounds of a ring of ranks (each rank holds one shard of the keys and values) ----
+// One rank's statistics block, exchanged (all-gathered) before the ring:
+//   float    vmax_sq              (word 0 of a 16-byte header) max v^2 over the shard
+//   float    kmax_sq[BH]          max |k - kbar|^2 (or |k|^2) over the shard's keys
+//   SinkCand cand[BH][nc]         with key sinks (nc = n_sink + 1): the shard's nc loudest keys
+//                                 in sink order, global key index; v = -1 pads
+//   float    cand_k[BH][nc][D], cand_v[BH][nc][D]   their raw key and value rows
+struct RingLayout {
+  int nc;
+  size_t off_kmax, off_cand, off_ck, off_cv, total;
+};
+inline size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
+RingLayout ring_layout(int64_t BH, int64_t D, int n_sink) {
+  RingLayout L;
+  L.nc = n_sink > 0 ? n_sink + 1 : 0;
+  L.off_kmax = 16;
+  L.off_cand = align16(L.off_kmax + sizeof(float) * (size_t)BH);
+  L.off_ck = align16(L.off_cand + sizeof(SinkCand) * (size_t)(BH * L.nc));
+  L.off_cv = L.off_ck + sizeof(float) * (size_t)(BH * L.nc * D);
+  L.total = align16(L.off_cv + sizeof(float) * (size_t)(BH * L.nc * D));
+  return L;
+}
+
+// Block-wide max of non-negative values held one per thread (the result in every thread).
+__device__ __forceinline__ float block_max(float v, float *red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_max(v);
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float m = 0.f;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) m = fmaxf(m, red[w]);
+  return m;
+}
+
+// The nc loudest of M candidates (sink order: louder first, lower index first among equal
+// norms), one pick per round over the whole CTA; candidates with v < 0 are absent.  `get(e)`
+// returns candidate e.  Picks that run out are {-1, INT_MAX}.
+template <typename Get>
+__device__ void pick_loudest(int64_t M, int nc, Get get, float *pick_v, int32_t *pick_i, float *wv, int32_t *wi) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float pv = INFINITY;
+  int32_t pi = -1;
+  for (int t = 0; t < nc; ++t) {
+    float bv = -1.f;
+    int32_t bi = INT_MAX;
+    for (int64_t e = threadIdx.x; e < M; e += kThreads) {
+      const SinkCand x = get(e);
+      if (x.v >= 0.f && sink_after(x.v, x.idx, pv, pi) && sink_before(x.v, x.idx, bv, bi)) {
+        bv = x.v;
+        bi = x.idx;
+      }
+    }
+    warp_best_sink(bv, bi);
+    if (lane == 0) {
+      wv[warp] = bv;
+      wi[warp] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float fv = wv[0];
+      int32_t fi = wi[0];
+      for (int w = 1; w < kWarps; ++w)
+        if (sink_before(wv[w], wi[w], fv, fi)) {
+          fv = wv[w];
+          fi = wi[w];
+        }
+      pick_v[t] = fv;
+      pick_i[t] = fi;
+    }
+    __syncthreads();
+    pv = pick_v[t];
+    pi = pick_i[t];
+  }
+}
+
+// One rank's statistics block from the norms pass over its shard: per head the key max, the V
+// max over the whole shard, and (key sinks) the shard's nc loudest keys with their rows.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    ring_local_kernel(View k, View v, int64_t nkb, int64_t n_heads_total, int n_sink, int64_t key_offset,
+                      const float *kblk, const float *vblk, const SinkCand *cand, uint8_t *stats, RingLayout L) {
+  pdl_wait();  // inputs written by the kernels before this one
+  pdl_trigger();
+  const int64_t b = blockIdx.y, h = blockIdx.x;
+  const int64_t bh = b * k.H + h;
+  __shared__ float red[kWarps];
+  __shared__ float wv[kWarps];
+  __shared__ int32_t wi[kWarps];
+  __shared__ float pick_v[FM_MAX_SINKS + 1];
+  __shared__ int32_t pick_i[FM_MAX_SINKS + 1];
+  float km = 0.f;
+  for (int64_t i = threadIdx.x; i < nkb; i += kThreads) km = fmaxf(km, kblk[bh * nkb + i]);
+  km = block_max(km, red);
+  float *kmax = reinterpret_cast<float *>(stats + L.off_kmax);
+  if (threadIdx.x == 0) kmax[bh] = km;
+  if (bh == 0) {
+    float vm = 0.f;
+    for (int64_t i = threadIdx.x; i < n_heads_total * nkb; i += kThreads) vm = fmaxf(vm, vblk[i]);
+    vm = block_max(vm, red);
+    if (threadIdx.x == 0) reinterpret_cast<float *>(stats)[0] = vm;
+  }
+  if (L.nc == 0) return;
+  const SinkCand *c = cand + bh * nkb * kCandPerBlock;
+  const int per = n_sink + 1;  // candidates each K block kept
+  pick_loudest(nkb * per, L.nc, [&](int64_t e) { return c[(e / per) * kCandPerBlock + e % per]; }, pick_v, pick_i,
+               wv, wi);
+  SinkCand *out = reinterpret_cast<SinkCand *>(stats + L.off_cand) + bh * L.nc;
+  if (threadIdx.x < L.nc) {
+    const int t = threadIdx.x;
+    const bool have = pick_v[t] >= 0.f;
+    out[t] = have ? SinkCand{pick_v[t], (int32_t)(key_offset + pick_i[t])} : SinkCand{-1.f, INT_MAX};
+  }
+  const int D = (int)k.D;
+  const T *kp = reinterpret_cast<const T *>(k.ptr) + b * k.sB + h * k.sH;
+  const T *vp = reinterpret_cast<const T *>(v.ptr) + b * v.sB + h * v.sH;
+  float *ck = reinterpret_cast<float *>(stats + L.off_ck) + bh * L.nc * D;
+  float *cv = reinterpret_cast<float *>(stats + L.off_cv) + bh * L.nc * D;
+  for (int e = threadIdx.x; e < L.nc * D; e += kThreads) {
+    const int slot = e / D, d = e % D;
+    float kx = 0.f, vx = 0.f;
+    if (pick_v[slot] >= 0.f) {
+      const int64_t idx = pick_i[slot];
+      const T a = kp[idx * k.sS + (int64_t)d * k.sD];
+      const T w = vp[idx * v.sS + (int64_t)d * v.sD];
+      if constexpr (sizeof(T) == 2) {
+        kx = __bfloat162float(a);
+        vx = __bfloat162float(w);
+      } else {
+        kx = (float)a;
+        vx = (float)w;
+      }
+    }
+    ck[e] = kx;
+    cv[e] = vx;
+  }
+}
+
+// Every rank's statistics blocks (rank order) -> the bounds over all keys for this rank's
+// queries: the key max (or, with key sinks, the n_sink + 1 loudest keys of the union of the
+// shards' candidates: the sinks strictly above the (n_sink+1)-th, which is the key max), the
+// V max, then U, m and the flag per Q-block as fm_bounds does.
+__global__ void __launch_bounds__(kThreads)
+    ring_combine_kernel(const uint8_t *stats_all, size_t stats_bytes, int n_ranks, RingLayout L, int n_sink,
+                        int64_t H, int64_t nqb, int D, double alpha, int C, int gate, const float *qmax_sq,
+                        float *kmax_sq, float *vmax_sq, int32_t *m, uint8_t *flag, int32_t *sink_idx,
+                        float *sink_k, float *sink_v) {
+  pdl_wait();  // inputs written by the kernels before this one
+  pdl_trigger();
+  const int64_t bh = (int64_t)blockIdx.y * H + blockIdx.x;
+  __shared__ float wv[kWarps];
+  __shared__ int32_t wi[kWarps];
+  __shared__ float pick_v[FM_MAX_SINKS + 1];
+  __shared__ int32_t pick_i[FM_MAX_SINKS + 1];
+  __shared__ int32_t list[FM_MAX_SINKS];
+  __shared__ int src[FM_MAX_SINKS];
+  __shared__ float kmv[2];
+  if (threadIdx.x == 0) {
+    float km = 0.f, vm = 0.f;
+    for (int r = 0; r < n_ranks; ++r) {
+      const uint8_t *s = stats_all + (size_t)r * stats_bytes;
+      km = fmaxf(km, reinterpret_cast<const float *>(s + L.off_kmax)[bh]);
+      vm = fmaxf(vm, reinterpret_cast<const float *>(s)[0]);
+    }
+    kmv[0] = km;
+    kmv[1] = vm;
+  }
+  __syncthreads();
+  float km = kmv[0];
+  const float vm = kmv[1];
+  if (n_sink > 0) {
+    const int nc = L.nc;
+    auto get = [&](int64_t e) {
+      const uint8_t *s = stats_all + (size_t)(e / nc) * stats_bytes;
+      return reinterpret_cast<const SinkCand *>(s + L.off_cand)[bh * nc + e % nc];
+    };
+    pick_loudest((int64_t)n_ranks * nc, n_sink + 1, get, pick_v, pick_i, wv, wi);
+    if (threadIdx.x == 0) {
+      const float tau = pick_v[n_sink] >= 0.f ? pick_v[n_sink] : 0.f;
+      int n = 0;
+      for (int t = 0; t < n_sink; ++t)
+        if (pick_v[t] >= 0.f && pick_v[t] > tau) list[n++] = pick_i[t];
+      for (int i = 1; i < n; ++i)  // ascending key order
+        for (int j = i; j > 0 && list[j - 1] > list[j]; --j) {
+          const int32_t x = list[j];
+          list[j] = list[j - 1];
+          list[j - 1] = x;
+        }
+      for (int t = n; t < FM_MAX_SINKS; ++t) list[t] = INT_MAX;
+      // where each sink's rows sit among the candidates (global key indices are unique)
+      for (int t = 0; t < FM_MAX_SINKS; ++t) {
+        src[t] = -1;
+        for (int64_t e = 0; e < (int64_t)n_ranks * nc && list[t] != INT_MAX; ++e)
+          if (get(e).idx == list[t]) src[t] = (int)e;
+      }
+      for (int t = 0; t < FM_MAX_SINKS; ++t) sink_idx[bh * FM_MAX_SINKS + t] = list[t];
+      kmv[0] = tau;
+    }
+    __syncthreads();
+    km = kmv[0];
+    for (int e = threadIdx.x; e < FM_MAX_SINKS * D; e += kThreads) {
+      const int slot = e / D, d = e % D;
+      float kx = 0.f, vx = 0.f;
+      if (src[slot] >= 0) {
+        const uint8_t *s = stats_all + (size_t)(src[slot] / nc) * stats_bytes;
+        const int64_t row = bh * nc + src[slot] % nc;
+        kx = reinterpret_cast<const float *>(s + L.off_ck)[row * D + d];
+        vx = reinterpret_cast<const float *>(s + L.off_cv)[row * D + d];
+      }
+      sink_k[(bh * FM_MAX_SINKS + slot) * D + d] = kx;
+      sink_v[(bh * FM_MAX_SINKS + slot) * D + d] = vx;
+    }
+  }
+  if (threadIdx.x == 0) {
+    kmax_sq[bh] = km;
+    if (bh == 0) vmax_sq[0] = vm;
+  }
+  const bool v_ok = vm <= (float)FM_VMAX * (float)FM_VMAX;
+  const double ksq = sqrt((double)km);
+  for (int64_t i = threadIdx.x; i < nqb; i += kThreads) {
+    const double U = alpha * sqrt((double)qmax_sq[bh * nqb + i]) * ksq;
+    m[bh * nqb + i] = (int32_t)ceil(U) - C;
+    flag[bh * nqb + i] = (uint8_t)(v_ok && U <= (double)gate);
+  }
+}
+
+template <typename T, int EPL, bool CONTIG>
+cudaError_t launch_ring_local_typed(const BoundsArgs &a, const WsLayout &w, const float *ksum_total, int64_t N_total,
+                                    int64_t key_offset, void *stats, cudaStream_t st) {
+  const int64_t B = a.q.B, H = a.q.H;
+  char *ws = reinterpret_cast<char *>(a.ws);
+  float *kblk = reinterpret_cast<float *>(ws + w.off_kb);
+  float *vblk = reinterpret_cast<float *>(ws + w.off_vb);
+  SinkCand *cand = reinterpret_cast<SinkCand *>(ws + w.off_cand);
+  const int D = (int)a.q.D;
+  const dim3 heads((unsigned)H, (unsigned)B);
+  cudaError_t e;
+  // every rank divides the same ring-wide sums by the same count: one key mean for all
+  if (a.centering && N_total > 0)
+    e = launch_pdl(kmean_kernel, heads, dim3(128), 0, st, ksum_total, H, (int64_t)1, D, N_total, a.kbar);
+  else
+    e = cudaMemsetAsync(a.kbar, 0, sizeof(float) * (size_t)(B * H * D), st);
+  if (e != cudaSuccess) return e;
+  const int64_t nx = a.nqb + 2 * w.nkb;
+  if (nx > 0) {
+    e = launch_pdl(norms_kernel<T, EPL, CONTIG>, dim3((unsigned)nx, (unsigned)H, (unsigned)B), dim3(kThreads), 0, st,
+                   a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk,
+                   vblk, a.n_sink, cand);
+    if (e != cudaSuccess) return e;
+  }
+  const RingLayout L = ring_layout(B * H, D, a.n_sink);
+  e = launch_pdl(ring_local_kernel<T>, heads, dim3(kThreads), 0, st, a.k, a.v, w.nkb, B * H, a.n_sink, key_offset, kblk,
+                 vblk, cand, reinterpret_cast<uint8_t *>(stats), L);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <typename T, int EPL, bool CONTIG>
 cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st) {
   const int64_t B = a.q.B, H = a.q.H, N = a.k.S;
@@ -486,6 +744,69 @@ bool contiguous_rows(const View &t) {
 
 size_t bounds_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D) {
   return ws_layout(B, H, N, D).total;
+}
+
+size_t ring_stats_bytes(int64_t B, int64_t H, int64_t D, int n_sink) { return ring_layout(B * H, D, n_sink).total; }
+
+cudaError_t launch_ring_key_sums(const View &k, float *ksum, void *ws, cudaStream_t st) {
+  const int64_t B = k.B, H = k.H, N = k.S;
+  const int D = (int)k.D;
+  if (B * H == 0) return cudaSuccess;
+  if (N == 0) return cudaMemsetAsync(ksum, 0, sizeof(float) * (size_t)(B * H * D), st);
+  const WsLayout w = ws_layout(B, H, N, D);
+  float *part = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + w.off_part);
+  const bool contig = contiguous_rows(k);
+  const dim3 grid((unsigned)w.P, (unsigned)H, (unsigned)B), heads((unsigned)H, (unsigned)B);
+  cudaError_t e;
+  if (k.dtype == FM_BF16)
+    e = D == 128 ? (contig ? launch_pdl(ksum_kernel<__nv_bfloat16, 4, true>, grid, dim3(kThreads), 0, st, k, w.P, part)
+                           : launch_pdl(ksum_kernel<__nv_bfloat16, 4, false>, grid, dim3(kThreads), 0, st, k, w.P, part))
+                 : (contig ? launch_pdl(ksum_kernel<__nv_bfloat16, 2, true>, grid, dim3(kThreads), 0, st, k, w.P, part)
+                           : launch_pdl(ksum_kernel<__nv_bfloat16, 2, false>, grid, dim3(kThreads), 0, st, k, w.P, part));
+  else
+    e = D == 128 ? (contig ? launch_pdl(ksum_kernel<float, 4, true>, grid, dim3(kThreads), 0, st, k, w.P, part)
+                           : launch_pdl(ksum_kernel<float, 4, false>, grid, dim3(kThreads), 0, st, k, w.P, part))
+                 : (contig ? launch_pdl(ksum_kernel<float, 2, true>, grid, dim3(kThreads), 0, st, k, w.P, part)
+                           : launch_pdl(ksum_kernel<float, 2, false>, grid, dim3(kThreads), 0, st, k, w.P, part));
+  if (e != cudaSuccess) return e;
+  // the ordered sum of the partials, divided by 1
+  e = launch_pdl(kmean_kernel, heads, dim3(128), 0, st, part, H, w.P, D, (int64_t)1, ksum);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bounds_local(const BoundsArgs &a, const float *ksum_total, int64_t N_total, int64_t key_offset,
+                                void *stats, cudaStream_t st) {
+  const WsLayout w = ws_layout(a.q.B, a.q.H, a.k.S, a.q.D);
+  const bool contig = contiguous_rows(a.q) && contiguous_rows(a.k) && contiguous_rows(a.v);
+  const bool bf16 = a.q.dtype == FM_BF16;
+  const bool d128 = a.q.D == 128;
+#define FM_RING_LOCAL(T, E, C) launch_ring_local_typed<T, E, C>(a, w, ksum_total, N_total, key_offset, stats, st)
+  if (bf16) {
+    if (d128) return contig ? FM_RING_LOCAL(__nv_bfloat16, 4, true) : FM_RING_LOCAL(__nv_bfloat16, 4, false);
+    return contig ? FM_RING_LOCAL(__nv_bfloat16, 2, true) : FM_RING_LOCAL(__nv_bfloat16, 2, false);
+  }
+  if (d128) return contig ? FM_RING_LOCAL(float, 4, true) : FM_RING_LOCAL(float, 4, false);
+  return contig ? FM_RING_LOCAL(float, 2, true) : FM_RING_LOCAL(float, 2, false);
+#undef FM_RING_LOCAL
+}
+
+cudaError_t launch_bounds_combine(const BoundsArgs &a, const void *stats_all, int n_ranks, cudaStream_t st) {
+  const int64_t B = a.q.B, H = a.q.H;
+  const int D = (int)a.q.D;
+  const RingLayout L = ring_layout(B * H, D, a.n_sink);
+  const dim3 heads((unsigned)H, (unsigned)B);
+  cudaError_t e = launch_pdl(ring_combine_kernel, heads, dim3(kThreads), 0, st,
+                             reinterpret_cast<const uint8_t *>(stats_all), L.total, n_ranks, L, a.n_sink, H, a.nqb, D,
+                             a.alpha, a.C, a.gate, a.qmax_sq, a.kmax_sq, a.vmax_sq, a.m, a.flag, a.sink_idx,
+                             a.sink_k, a.sink_v);
+  if (e != cudaSuccess) return e;
+  if (a.q.S > 0) {
+    e = launch_pdl(shift_kernel, dim3((unsigned)ceil_div(a.q.S, kThreads), (unsigned)H, (unsigned)B), dim3(kThreads),
+                   0, st, H, a.q.S, a.nqb, a.per_row, a.alpha, a.C, a.kmax_sq, a.m, a.qkbar, a.shift);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_bounds(const BoundsArgs &a, cudaStream_t st) {

@@ -55,6 +55,13 @@ struct BoundsArgs {
 };
 size_t bounds_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D);
 cudaError_t launch_bounds(const BoundsArgs &a, cudaStream_t st);
+// The bounds of a ring of ranks (each holds one shard of the keys): the shard's key sums; one
+// rank's statistics block; the combine of every rank's blocks into the bounds.
+size_t ring_stats_bytes(int64_t B, int64_t H, int64_t D, int n_sink);
+cudaError_t launch_ring_key_sums(const View &k, float *ksum, void *ws, cudaStream_t st);
+cudaError_t launch_bounds_local(const BoundsArgs &a, const float *ksum_total, int64_t N_total, int64_t key_offset,
+                                void *stats, cudaStream_t st);
+cudaError_t launch_bounds_combine(const BoundsArgs &a, const void *stats_all, int n_ranks, cudaStream_t st);
 
 // ---- chunk kernels ----------------------------------------------------------
 struct ChunkArgs {

@@ -71,6 +71,7 @@ enum {
 };
 
 #define FM_BOUNDS_MAGIC 0x314D4246u /* tag written by fm_bounds ("FBM1") */
+#define FM_BOUNDS_LOCAL_MAGIC 0x314C4246u /* fm_bounds_local done, fm_bounds_combine pending ("FBL1") */
 #define FM_BLOCK_Q 128              /* rows per Q-block: the granularity of m and flag */
 #define FM_VMAX 256                 /* the V bound of [PR477]'s commit message */
 #define FM_SUM_CLAMP 1e-37f         /* [NKI] "Accumulate, then normalize once" */
@@ -162,6 +163,13 @@ typedef struct {
   int32_t dtype;
   /* updated by fm_attn_chunk (host-side bookkeeping of the chunk sequence) */
   int64_t kv_seen;
+  int64_t next_key_offset; /* -1 (as fm_bounds / fm_bounds_combine and every chunk call leave it):
+                              the next chunk's first key has global index kv_seen (0 with
+                              accumulate = 0), i.e. the chunks come in key order.  A caller that
+                              folds them in another order -- a ring hands rank r the shards in
+                              the rotated order r, r-1, ... -- sets it to the chunk's global offset
+                              before the call.  Only key sinks depend on it (they are found by
+                              global key index). */
   int32_t online_lock;
   int32_t sinks_folded; /* set by fm_fold_sinks; no chunk may follow it */
   uint32_t magic; /* FM_BOUNDS_MAGIC once fm_bounds has succeeded */
@@ -301,8 +309,66 @@ FM_API int fm_probe_wait_timeout(unsigned int timeout_ms, fm_stream_t stream);
  * thread's next fm_* call. */
 FM_API const char *fm_last_error(void);
 
-/* ABI version of this header: (major << 16) | minor.  1.2 added fm_opts.schedule. */
+/* ABI version of this header: (major << 16) | minor.  1.2 added fm_opts.schedule,
+ * fm_bounds_out.next_key_offset and the ring bounds calls. */
 FM_API int fm_version(void);
+
+/* ---- The bounds of a ring of ranks ---------------------------------------------------------
+ * In a multi-GPU ring each rank keeps its own query rows and holds one shard of the keys and
+ * values; the shards rotate through the ranks, so no rank ever sees all keys at once.  The bounds
+ * still need ring-wide key statistics, and the pages exchange them once before the ring: the key
+ * mean over real tokens reduced across the ring so every rank centers against the same mean
+ * ([PR478] Summary, "Global Virtual K-Centering"), then one max-reduction of the per-head key
+ * norms and the V maximum ([NKI] "Global key max"; [PR478] folds the centered key max and the V
+ * max into one pmax).  The library computes each rank's part and combines the exchanged parts;
+ * the caller moves the bytes with its own collectives:
+ *   1. (centering only) fm_ring_key_sums(k_shard) -> ksum f32 [B, H, D], the shard's key sums;
+ *      the caller all-reduces (sum) ksum over the ring;
+ *   2. fm_bounds_local(q, k_shard, v_shard, key_offset, N_total, ksum) -> the query-side arrays
+ *      of `out` and this rank's statistics block (fm_ring_stats_bytes bytes); the caller
+ *      all-gathers the blocks, in rank order, into one buffer;
+ *   3. fm_bounds_combine(stats_all, n_ranks) -> the rest of `out`: kmax_sq, vmax_sq, the key
+ *      sinks, m, flag and shift, as fm_bounds would give over (q, every key, every value), up to
+ *      the fp32 summation order of the key mean (m and flag can then differ only where U is
+ *      within fp32 rounding of an integer or of the gate).
+ * Every rank then folds the shards with fm_attn_chunk in ring order, setting
+ * out->next_key_offset to each shard's global offset.  The statistics block holds, per head, the
+ * shard's key max and, with key sinks, its sink_keys + 1 loudest keys (norm, global index, key
+ * and value rows): the ring-wide loudest keys are among the union of those. */
+
+/* Bytes of one rank's statistics block for q of [B, H, *, D] and opts.sink_keys.  Returns FM_OK. */
+FM_API int fm_ring_stats_bytes(int64_t B, int64_t H, int64_t D, int sink_keys, size_t *bytes);
+
+/* fm_ring_key_sums -- ksum[b,h,:] = sum of this rank's keys of (b, h) in fp32 (fixed order).
+ *   k_shard [B, H, Nr, D];  ksum f32 [B, H, D] device, written;
+ *   workspace of fm_bounds_workspace_size(B, H, Nr, D) bytes.
+ * Errors: FM_ERR_ARG, FM_ERR_DTYPE, FM_ERR_UNSUPPORTED, FM_ERR_CUDA. */
+FM_API int fm_ring_key_sums(const fm_tensor *k_shard, float *ksum, void *workspace, size_t workspace_bytes,
+                            fm_stream_t stream);
+
+/* fm_bounds_local -- this rank's part of the bounds.
+ *   q        [B, H, Sq, D] this rank's queries
+ *   k_shard, v_shard [B, H, Nr, D] its shard of the keys and values; key_offset = the global
+ *            index of the shard's first key (0 <= key_offset, key_offset + Nr <= N_total)
+ *   N_total  keys over every shard of the ring (C(N) is computed from it)
+ *   ksum_total f32 [B, H, D]: the ring-wide key sums (step 1) when opts->centering, else NULL
+ *   out      as for fm_bounds; the query-side arrays (qmax_sq, qkbar, kbar) are written here, the
+ *            rest by fm_bounds_combine; out->magic becomes FM_BOUNDS_LOCAL_MAGIC
+ *   stats    device buffer of fm_ring_stats_bytes bytes, written (16-byte aligned)
+ *   workspace of fm_bounds_workspace_size(B, H, Nr, D) bytes
+ * Errors: those of fm_bounds, FM_ERR_ARG for a bad key_offset / N_total or a missing ksum_total. */
+FM_API int fm_bounds_local(const fm_tensor *q, const fm_tensor *k_shard, const fm_tensor *v_shard, int64_t key_offset,
+                           int64_t N_total, const float *ksum_total, const fm_opts *opts, fm_bounds_out *out,
+                           void *stats, void *workspace, size_t workspace_bytes, fm_stream_t stream);
+
+/* fm_bounds_combine -- finish `out` from every rank's statistics block.
+ *   stats_all  device buffer of n_ranks blocks of fm_ring_stats_bytes bytes, in rank order
+ *   opts       the same opts as fm_bounds_local
+ *   out        as left by fm_bounds_local on this rank; becomes ready for fm_attn_chunk
+ * Errors: FM_ERR_BOUNDS_MISMATCH when out was not prepared by fm_bounds_local or opts differ,
+ * FM_ERR_ARG, FM_ERR_CUDA. */
+FM_API int fm_bounds_combine(const void *stats_all, int n_ranks, const fm_opts *opts, fm_bounds_out *out,
+                             fm_stream_t stream);
 
 /* Upper bound of the scratch fm_bounds_noalloc can use: 4 MiB.  That covers, at D = 128,
  * up to 74 heads of 75,600 keys (fm_bounds_workspace_size gives the exact need). */
