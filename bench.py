@@ -229,8 +229,14 @@ def run_ours(args, rank, world, local_rank):
         if dist is not None:
             dist.barrier()
 
-    def step(ev=None):
+    def step(ev=None, bev=None):
+        if bev is not None:
+            bev.append(torch.cuda.Event(enable_timing=True))
+            bev[-1].record(stream)
         fm.fm_bounds(q, k, v, fa.opt, fa.bounds, fa.workspace, stream)
+        if bev is not None:
+            bev.append(torch.cuda.Event(enable_timing=True))
+            bev[-1].record(stream)
         for i, (s, n) in enumerate(chunks):
             if ev is not None:
                 ev.append(torch.cuda.Event(enable_timing=True))
@@ -263,6 +269,7 @@ def run_ours(args, rank, world, local_rank):
     if tensor_bytes <= L2_BYTES:
         flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
     chunk_events = []
+    bounds_events = []
     step_events = []
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
@@ -274,7 +281,7 @@ def run_ours(args, rank, world, local_rank):
                 flush.fill_(1)
                 step_events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
                 step_events[-1][0].record(stream)
-            step(chunk_events)
+            step(chunk_events, bounds_events)
             if flush is not None:
                 step_events[-1][1].record(stream)
         end.record(stream)
@@ -283,6 +290,8 @@ def run_ours(args, rank, world, local_rank):
     fm.fm_sync_status(stream)
     t_ms = start.elapsed_time(end) if flush is None else sum(a.elapsed_time(b) for a, b in step_events)
     chunk_ms = [chunk_events[i].elapsed_time(chunk_events[i + 1]) for i in range(0, len(chunk_events), 2)]
+    bounds_ms = statistics.mean(bounds_events[i].elapsed_time(bounds_events[i + 1])
+                                for i in range(0, len(bounds_events), 2))
     t_ms = max_over_ranks(t_ms, dev)
     ms_per_step = t_ms / args.steps
     value = whole_job_tflops(world, step_flops, args.steps, t_ms)
@@ -374,6 +383,13 @@ def run_ours(args, rank, world, local_rank):
                 "algorithmic_bytes_per_launch": algo_bytes,
                 "peak_kind": f"bf16 sustained ({peak_src})",
                 "frac_of_burst_peak": achieved / peaks["bf16_tflops"], "launch_ms": chunk_avg_ms}
+    # the bounds pass: Q, K and V read once, K once more for the key mean when centering
+    bounds_bytes = q.element_size() * w.B * H * w.D * (w.Sq + (3 if centering else 2) * w.N)
+    bounds_line = {"ms": bounds_ms, "algorithmic_bytes": bounds_bytes, "achieved": bounds_bytes / (bounds_ms * 1e-3) / 1e9,
+                   "unit": "GB/s", "peak": peaks["hbm_gbs"],
+                   "frac": bounds_bytes / (bounds_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                   "kernels": "ksum + kmean (centering), norms, finish, shift",
+                   "how": "CUDA events around fm_bounds in each timed step"}
     cpu = None
     if world == 1 and not args.no_cpu_baseline and w.name == WORKLOAD:
         cv, info = cpu_oracle_sample(args.cpu_seconds)
@@ -399,6 +415,7 @@ def run_ours(args, rank, world, local_rank):
                    "fixed_m_tile_fraction": eligible},
         "pct_of_peak": 100.0 * value / peak,
         "roofline": roofline,
+        "bounds_pass": bounds_line,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,

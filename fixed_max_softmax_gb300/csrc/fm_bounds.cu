@@ -165,6 +165,95 @@ __global__ void __launch_bounds__(kThreads) ksum_kernel(View k, int64_t P, float
   }
 }
 
+// ---- rows that start on 16-byte boundaries: 16-byte loads, several rows in flight per lane --
+// A row of D elements is spread over LPR lanes with VEC consecutive elements each, so one warp
+// load covers RPW = 32 / LPR rows; each lane keeps kUnroll such loads in flight before it
+// reduces, which is what keeps HBM busy (one 256-byte row per warp at a time is not enough).
+constexpr int kUnroll = 4;
+template <typename T, int D>
+struct Vec16 {
+  static constexpr int VEC = 16 / (int)sizeof(T);
+  static constexpr int LPR = D / VEC;
+  static constexpr int RPW = 32 / LPR;
+};
+template <typename T, int VEC>
+__device__ __forceinline__ void load16(const T *p, float (&x)[VEC]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  } else {
+    x[0] = __uint_as_float(u.x);
+    x[1] = __uint_as_float(u.y);
+    x[2] = __uint_as_float(u.z);
+    x[3] = __uint_as_float(u.w);
+  }
+}
+// Sum over the LPR lanes of one row (lanes lane ^ o for o < LPR).
+template <int LPR>
+__device__ __forceinline__ float row_sum(float v) {
+#pragma unroll
+  for (int o = LPR / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// 1'. Partial key sums with 16-byte loads (the same partition of rows as ksum_kernel, a fixed
+// order of additions within it).
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads) ksum_vec_kernel(View k, int64_t P, float *part) {
+  pdl_wait();  // inputs written by the kernels before this one
+  pdl_trigger();
+  using V = Vec16<T, D>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane / V::LPR, li = lane % V::LPR;
+  const int64_t b = blockIdx.z, h = blockIdx.y, p = blockIdx.x;
+  const int64_t len = ceil_div(k.S, P);
+  const int64_t r0 = p * len, r1 = min(k.S, r0 + len);
+  const T *base = reinterpret_cast<const T *>(k.ptr) + b * k.sB + h * k.sH + li * V::VEC;
+  const int64_t step = (int64_t)kWarps * V::RPW;
+  float acc[V::VEC];
+#pragma unroll
+  for (int e = 0; e < V::VEC; ++e) acc[e] = 0.f;
+  int64_t r = r0 + warp * V::RPW + sub;
+  for (; r + (kUnroll - 1) * step < r1; r += kUnroll * step) {
+    float x[kUnroll][V::VEC];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) load16<T, V::VEC>(base + (r + u * step) * k.sS, x[u]);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+      for (int e = 0; e < V::VEC; ++e) acc[e] += x[u][e];
+  }
+  for (; r < r1; r += step) {
+    float x[V::VEC];
+    load16<T, V::VEC>(base + r * k.sS, x);
+#pragma unroll
+    for (int e = 0; e < V::VEC; ++e) acc[e] += x[e];
+  }
+  // the warp's sub-rows, then its warps, in a fixed order
+#pragma unroll
+  for (int o = V::LPR; o < 32; o <<= 1)
+#pragma unroll
+    for (int e = 0; e < V::VEC; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+  __shared__ float red[kWarps][128];
+  if (sub == 0) {
+#pragma unroll
+    for (int e = 0; e < V::VEC; ++e) red[warp][li * V::VEC + e] = acc[e];
+  }
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += red[w][threadIdx.x];
+    part[((b * k.H + h) * P + p) * D + threadIdx.x] = s;
+  }
+}
+
 // 2. Key mean: ordered sum of the P partials of head (b, h), divided by N.
 __global__ void kmean_kernel(const float *part, int64_t H, int64_t P, int D, int64_t N, float *kbar) {
   pdl_wait();  // inputs written by the kernels before this one
@@ -272,6 +361,141 @@ __global__ void __launch_bounds__(kThreads)
         const int32_t i = (int32_t)(r0 + e);
         if (sink_after(v, i, pv, pi) && sink_before(v, i, bv, bi)) {
           bv = v;
+          bi = i;
+        }
+      }
+      warp_best_sink(bv, bi);
+      if (lane == 0) out[t] = SinkCand{bv, bi};
+      pv = bv;
+      pi = bi;
+    }
+  }
+}
+
+// 3'. The norms pass with 16-byte loads: the same blocks and outputs as norms_kernel.
+template <typename T, int D>
+__global__ void __launch_bounds__(kThreads)
+    norms_vec_kernel(View q, View k, View v, int64_t nqb, int64_t nkb, int centering, float alpha,
+                     const float *kbar, float *qmax_sq, float *qkbar, float *qsq, float *kblk, float *vblk,
+                     int n_sink, SinkCand *cand) {
+  pdl_wait();  // inputs written by the kernels before this one
+  pdl_trigger();
+  using V = Vec16<T, D>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane / V::LPR, li = lane % V::LPR;
+  const int64_t b = blockIdx.z, h = blockIdx.y, bx = blockIdx.x;
+  const int64_t bh = b * q.H + h;
+  const int64_t step = (int64_t)kWarps * V::RPW;
+  __shared__ float wmax[kWarps];
+  __shared__ float knorm[kKVRows];  // key blocks with sinks: each row's squared norm
+  float kb[V::VEC];
+#pragma unroll
+  for (int e = 0; e < V::VEC; ++e) kb[e] = centering ? kbar[bh * D + li * V::VEC + e] : 0.f;
+
+  float best = 0.f;  // maxima of non-negative quantities start at 0
+  if (bx < nqb) {
+    // Q-block: per-row |q|^2 and alpha * q.kbar
+    const T *base = reinterpret_cast<const T *>(q.ptr) + b * q.sB + h * q.sH + li * V::VEC;
+    const int64_t r0 = bx * kQRows, r1 = min(q.S, r0 + kQRows);
+    for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += kUnroll * step) {  // warp-uniform trip count
+      const int64_t r = rb + sub;
+      float x[kUnroll][V::VEC];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (r + u * step < r1) load16<T, V::VEC>(base + (r + u * step) * q.sS, x[u]);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        float ss = 0.f, dk = 0.f;
+        if (r + u * step < r1) {
+#pragma unroll
+          for (int e = 0; e < V::VEC; ++e) {
+            ss = fmaf(x[u][e], x[u][e], ss);
+            dk = fmaf(x[u][e], kb[e], dk);
+          }
+        }
+        ss = row_sum<V::LPR>(ss);
+        dk = row_sum<V::LPR>(dk);
+        if (r + u * step < r1) {
+          best = fmaxf(best, ss);
+          if (li == 0) {
+            qkbar[bh * q.S + r + u * step] = alpha * dk;
+            qsq[bh * q.S + r + u * step] = ss;  // per-row |q|^2, turned into the row's shift by shift_kernel
+          }
+        }
+      }
+    }
+  } else if (bx < nqb + nkb) {
+    // K rows: |k - kbar|^2 (kbar = 0 when not centering)
+    const T *base = reinterpret_cast<const T *>(k.ptr) + b * k.sB + h * k.sH + li * V::VEC;
+    const int64_t r0 = (bx - nqb) * kKVRows, r1 = min(k.S, r0 + kKVRows);
+    for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += kUnroll * step) {  // warp-uniform trip count
+      const int64_t r = rb + sub;
+      float x[kUnroll][V::VEC];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (r + u * step < r1) load16<T, V::VEC>(base + (r + u * step) * k.sS, x[u]);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        float ss = 0.f;
+        if (r + u * step < r1) {
+#pragma unroll
+          for (int e = 0; e < V::VEC; ++e) {
+            const float c = x[u][e] - kb[e];
+            ss = fmaf(c, c, ss);
+          }
+        }
+        ss = row_sum<V::LPR>(ss);
+        if (r + u * step < r1) {
+          best = fmaxf(best, ss);
+          if (n_sink > 0 && li == 0) knorm[r + u * step - r0] = ss;
+        }
+      }
+    }
+  } else {
+    // V rows: max element square
+    const T *base = reinterpret_cast<const T *>(v.ptr) + b * v.sB + h * v.sH + li * V::VEC;
+    const int64_t r0 = (bx - nqb - nkb) * kKVRows, r1 = min(v.S, r0 + kKVRows);
+    for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += kUnroll * step) {  // warp-uniform trip count
+      const int64_t r = rb + sub;
+      float x[kUnroll][V::VEC];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (r + u * step < r1) load16<T, V::VEC>(base + (r + u * step) * v.sS, x[u]);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (r + u * step < r1) {
+#pragma unroll
+          for (int e = 0; e < V::VEC; ++e) best = fmaxf(best, x[u][e] * x[u][e]);
+        }
+    }
+  }
+  best = warp_max(best);
+  if (lane == 0) wmax[warp] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, wmax[w]);
+    if (bx < nqb) qmax_sq[bh * nqb + bx] = mx;
+    else if (bx < nqb + nkb) kblk[bh * nkb + (bx - nqb)] = mx;
+    else vblk[bh * nkb + (bx - nqb - nkb)] = mx;
+  }
+  if (n_sink > 0 && bx >= nqb && bx < nqb + nkb && warp == 0) {
+    // this block's n_sink + 1 loudest keys, in sink order (its rows' norms are in knorm,
+    // written before the barrier above)
+    const int64_t r0 = (bx - nqb) * kKVRows;
+    const int cnt = (int)min((int64_t)kKVRows, k.S - r0);
+    SinkCand *out = cand + (bh * nkb + (bx - nqb)) * kCandPerBlock;
+    float pv = INFINITY;
+    int32_t pi = -1;
+    for (int t = 0; t <= n_sink; ++t) {
+      float bv = -1.f;
+      int32_t bi = INT_MAX;
+      for (int e = lane; e < cnt; e += 32) {
+        const float vv = knorm[e];
+        const int32_t i = (int32_t)(r0 + e);
+        if (sink_after(vv, i, pv, pi) && sink_before(vv, i, bv, bi)) {
+          bv = vv;
           bi = i;
         }
       }
@@ -658,6 +882,35 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Every row of t starts on a 16-byte boundary (unit D stride).
+bool rows16(const View &t) {
+  const int64_t es = t.dtype == FM_F32 ? 4 : 2;
+  if (t.sD != 1 || reinterpret_cast<uintptr_t>(t.ptr) % 16) return false;
+  return ((t.sB * es) % 16 == 0 || t.B <= 1) && ((t.sH * es) % 16 == 0 || t.H <= 1) &&
+         ((t.sS * es) % 16 == 0 || t.S <= 1);
+}
+
+template <typename T, int EPL, bool CONTIG>
+cudaError_t launch_ksum(const View &k, int64_t P, float *part, cudaStream_t st) {
+  const dim3 grid((unsigned)P, (unsigned)k.H, (unsigned)k.B);
+  if (CONTIG && rows16(k))
+    return launch_pdl(ksum_vec_kernel<T, 32 * EPL>, grid, dim3(kThreads), 0, st, k, P, part);
+  return launch_pdl(ksum_kernel<T, EPL, CONTIG>, grid, dim3(kThreads), 0, st, k, P, part);
+}
+
+template <typename T, int EPL, bool CONTIG>
+cudaError_t launch_norms(const BoundsArgs &a, const WsLayout &w, float *kblk, float *vblk, SinkCand *cand,
+                         cudaStream_t st) {
+  const int64_t nx = a.nqb + 2 * w.nkb;
+  if (nx == 0) return cudaSuccess;
+  const dim3 grid((unsigned)nx, (unsigned)a.q.H, (unsigned)a.q.B);
+  if (CONTIG && rows16(a.q) && rows16(a.k) && rows16(a.v))
+    return launch_pdl(norms_vec_kernel<T, 32 * EPL>, grid, dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb,
+                      a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand);
+  return launch_pdl(norms_kernel<T, EPL, CONTIG>, grid, dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb,
+                    a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand);
+}
+
 template <typename T, int EPL, bool CONTIG>
 cudaError_t launch_ring_local_typed(const BoundsArgs &a, const WsLayout &w, const float *ksum_total, int64_t N_total,
                                     int64_t key_offset, void *stats, cudaStream_t st) {
@@ -675,13 +928,8 @@ cudaError_t launch_ring_local_typed(const BoundsArgs &a, const WsLayout &w, cons
   else
     e = cudaMemsetAsync(a.kbar, 0, sizeof(float) * (size_t)(B * H * D), st);
   if (e != cudaSuccess) return e;
-  const int64_t nx = a.nqb + 2 * w.nkb;
-  if (nx > 0) {
-    e = launch_pdl(norms_kernel<T, EPL, CONTIG>, dim3((unsigned)nx, (unsigned)H, (unsigned)B), dim3(kThreads), 0, st,
-                   a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk,
-                   vblk, a.n_sink, cand);
-    if (e != cudaSuccess) return e;
-  }
+  e = launch_norms<T, EPL, CONTIG>(a, w, kblk, vblk, cand, st);
+  if (e != cudaSuccess) return e;
   const RingLayout L = ring_layout(B * H, D, a.n_sink);
   e = launch_pdl(ring_local_kernel<T>, heads, dim3(kThreads), 0, st, a.k, a.v, w.nkb, B * H, a.n_sink, key_offset, kblk,
                  vblk, cand, reinterpret_cast<uint8_t *>(stats), L);
@@ -701,20 +949,14 @@ cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st
   const dim3 heads((unsigned)H, (unsigned)B);
   cudaError_t e = cudaSuccess;
   if (a.centering && N > 0) {
-    e = launch_pdl(ksum_kernel<T, EPL, CONTIG>, dim3((unsigned)w.P, (unsigned)H, (unsigned)B), dim3(kThreads), 0, st,
-                   a.k, w.P, part);
+    e = launch_ksum<T, EPL, CONTIG>(a.k, w.P, part, st);
     if (e == cudaSuccess) e = launch_pdl(kmean_kernel, heads, dim3(128), 0, st, part, H, w.P, D, N, a.kbar);
   } else {
     e = cudaMemsetAsync(a.kbar, 0, sizeof(float) * (size_t)(B * H * D), st);
   }
   if (e != cudaSuccess) return e;
-  const int64_t nx = a.nqb + 2 * w.nkb;
-  if (nx > 0) {
-    e = launch_pdl(norms_kernel<T, EPL, CONTIG>, dim3((unsigned)nx, (unsigned)H, (unsigned)B), dim3(kThreads), 0, st,
-                   a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk,
-                   vblk, a.n_sink, cand);
-    if (e != cudaSuccess) return e;
-  }
+  e = launch_norms<T, EPL, CONTIG>(a, w, kblk, vblk, cand, st);
+  if (e != cudaSuccess) return e;
   if (a.n_sink > 0) {
     e = launch_pdl(sink_select_kernel<T>, heads, dim3(kThreads), 0, st, a.k, a.v, w.nkb, a.n_sink, cand, a.sink_idx,
                    a.sink_k, a.sink_v, a.kmax_sq);
@@ -756,18 +998,16 @@ cudaError_t launch_ring_key_sums(const View &k, float *ksum, void *ws, cudaStrea
   const WsLayout w = ws_layout(B, H, N, D);
   float *part = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + w.off_part);
   const bool contig = contiguous_rows(k);
-  const dim3 grid((unsigned)w.P, (unsigned)H, (unsigned)B), heads((unsigned)H, (unsigned)B);
+  const dim3 heads((unsigned)H, (unsigned)B);
   cudaError_t e;
   if (k.dtype == FM_BF16)
-    e = D == 128 ? (contig ? launch_pdl(ksum_kernel<__nv_bfloat16, 4, true>, grid, dim3(kThreads), 0, st, k, w.P, part)
-                           : launch_pdl(ksum_kernel<__nv_bfloat16, 4, false>, grid, dim3(kThreads), 0, st, k, w.P, part))
-                 : (contig ? launch_pdl(ksum_kernel<__nv_bfloat16, 2, true>, grid, dim3(kThreads), 0, st, k, w.P, part)
-                           : launch_pdl(ksum_kernel<__nv_bfloat16, 2, false>, grid, dim3(kThreads), 0, st, k, w.P, part));
+    e = D == 128 ? (contig ? launch_ksum<__nv_bfloat16, 4, true>(k, w.P, part, st)
+                           : launch_ksum<__nv_bfloat16, 4, false>(k, w.P, part, st))
+                 : (contig ? launch_ksum<__nv_bfloat16, 2, true>(k, w.P, part, st)
+                           : launch_ksum<__nv_bfloat16, 2, false>(k, w.P, part, st));
   else
-    e = D == 128 ? (contig ? launch_pdl(ksum_kernel<float, 4, true>, grid, dim3(kThreads), 0, st, k, w.P, part)
-                           : launch_pdl(ksum_kernel<float, 4, false>, grid, dim3(kThreads), 0, st, k, w.P, part))
-                 : (contig ? launch_pdl(ksum_kernel<float, 2, true>, grid, dim3(kThreads), 0, st, k, w.P, part)
-                           : launch_pdl(ksum_kernel<float, 2, false>, grid, dim3(kThreads), 0, st, k, w.P, part));
+    e = D == 128 ? (contig ? launch_ksum<float, 4, true>(k, w.P, part, st) : launch_ksum<float, 4, false>(k, w.P, part, st))
+                 : (contig ? launch_ksum<float, 2, true>(k, w.P, part, st) : launch_ksum<float, 2, false>(k, w.P, part, st));
   if (e != cudaSuccess) return e;
   // the ordered sum of the partials, divided by 1
   e = launch_pdl(kmean_kernel, heads, dim3(128), 0, st, part, H, w.P, D, (int64_t)1, ksum);
