@@ -328,10 +328,9 @@ def run_ours(args, rank, world, local_rank):
                   "ms_per_step": t_one / args.steps,
                   "how": "fm_bounds + fm_attn_chunks (all chunks and the normalise in one launch)"}
 
-    # ---- end to end through the public API with host buffers (pinned), copies timed:
-    # every step uploads its Q/K/V from pinned host memory and reads its output back; the
-    # package's HostPipeline overlaps step i+1's upload and step i-1's read-back with step
-    # i's kernels
+    # ---- end to end through the C ABI with host buffers (pinned), copies timed: every step
+    # uploads its Q/K/V from pinned host memory and reads its output back; fm_attention_host
+    # overlaps step i+1's upload and step i-1's read-back with step i's kernels
     e2e = None
     if args.e2e_steps > 0:
         qh = q.cpu().pin_memory()
@@ -353,7 +352,8 @@ def run_ours(args, rank, world, local_rank):
                "d2h_bytes_per_step": int(fa.out.numel() * fa.out.element_size()),
                "ms_per_step": te / args.e2e_steps, "steps": args.e2e_steps,
                "timing": "host wall clock between device synchronisations",
-               "overlap": "upload of step i+1 and read-back of step i-1 run during step i (HostPipeline)"}
+               "overlap": "upload of step i+1 and read-back of step i-1 run during step i",
+               "how": "fm_attention_host (C ABI, host buffers in page-locked memory, three streams)"}
 
     if rank != 0:
         return

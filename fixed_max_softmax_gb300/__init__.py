@@ -40,7 +40,7 @@ ERROR_NAMES = {0: "FM_OK", 1: "FM_ERR_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_DTYPE"
 ABI_SYMBOLS = ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
                "fm_last_error", "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout",
                "fm_attn_chunk_final", "fm_attn_chunks", "fm_fold_sinks", "fm_ring_stats_bytes", "fm_ring_key_sums",
-               "fm_bounds_local", "fm_bounds_combine")
+               "fm_bounds_local", "fm_bounds_combine", "fm_attention_host")
 FM_MAX_CHUNKS = 8
 FM_MAX_SINKS = 8
 FM_NOALLOC_SCRATCH_BYTES = 4 << 20
@@ -79,6 +79,13 @@ class fm_bounds_out(ctypes.Structure):
                 ("magic", ctypes.c_uint32)]
 
 
+class fm_host_buffers(ctypes.Structure):
+    _fields_ = [("q", fm_tensor * 2), ("k", fm_tensor * 2), ("v", fm_tensor * 2), ("o", fm_tensor * 2),
+                ("acc_o", ctypes.c_void_p), ("acc_sum", ctypes.c_void_p), ("acc_max", ctypes.c_void_p),
+                ("bounds", ctypes.POINTER(fm_bounds_out)), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t)]
+
+
 _lib = None
 
 
@@ -107,6 +114,7 @@ def load(path: str | None = None):
     lib.fm_ring_key_sums.argtypes = [P, P, P, ctypes.c_size_t, P]
     lib.fm_bounds_local.argtypes = [P, P, P, i64, i64, P, P, P, P, P, ctypes.c_size_t, P]
     lib.fm_bounds_combine.argtypes = [P, ctypes.c_int, P, P, P]
+    lib.fm_attention_host.argtypes = [P, P, P, P, ctypes.c_int, P, ctypes.c_int, P, P, P]
     lib.fm_sync_status.argtypes = [P]
     lib.fm_last_error.restype = ctypes.c_char_p
     lib.fm_last_error.argtypes = []
@@ -114,7 +122,7 @@ def load(path: str | None = None):
     for name in ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
                  "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout",
                  "fm_attn_chunk_final", "fm_attn_chunks", "fm_fold_sinks", "fm_ring_stats_bytes", "fm_ring_key_sums",
-                 "fm_bounds_local", "fm_bounds_combine"):
+                 "fm_bounds_local", "fm_bounds_combine", "fm_attention_host"):
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -384,13 +392,12 @@ def attention(q, k, v, chunks=None, centering=False, softmax_scale=0.0, force_on
 
 
 class HostPipeline:
-    """Fixed-m attention over a stream of batches that live in (pinned) host memory.
-
-    Batch i+1's inputs are copied to the device on one stream while batch i computes on
-    another, and batch i-1's output is read back on a third: every batch still makes the
-    full host -> device -> host round trip, but the copies hide behind the kernels.  Two
-    device copies of the inputs and of the output alternate between batches; the bounds
-    and accumulators of `fa` are reused in order on the compute stream.
+    """Fixed-m attention over a stream of batches that live in (pinned) host memory, through
+    fm_attention_host: batch i+1's inputs are copied to the device on one stream while batch i
+    computes on another, and batch i-1's output is read back on a third.  Every batch still makes
+    the full host -> device -> host round trip, but the copies hide behind the kernels.  Two
+    device copies of the inputs and of the output alternate between batches; the bounds,
+    accumulators and workspace of `fa` are reused in order.
     """
 
     def __init__(self, fa: FixedMAttention, in_dtype, device="cuda"):
@@ -401,45 +408,32 @@ class HostPipeline:
         self.k = [torch.empty(B, H, N, D, dtype=in_dtype, device=device) for _ in range(2)]
         self.v = [torch.empty(B, H, N, D, dtype=in_dtype, device=device) for _ in range(2)]
         self.o = [torch.empty_like(fa.out) for _ in range(2)]
-        self.s_h2d = torch.cuda.Stream(device=device)
-        self.s_d2h = torch.cuda.Stream(device=device)
-        self.s_comp = torch.cuda.Stream(device=device)
+        self.streams = [torch.cuda.Stream(device=device) for _ in range(3)]
+        self.dev = fm_host_buffers()
+        for i in range(2):
+            self.dev.q[i], self.dev.k[i], self.dev.v[i], self.dev.o[i] = (tensor(self.q[i]), tensor(self.k[i]),
+                                                                          tensor(self.v[i]), tensor(self.o[i]))
+        self.dev.acc_o, self.dev.acc_sum, self.dev.acc_max = (fa.acc_o.data_ptr(), fa.acc_sum.data_ptr(),
+                                                              fa.acc_max.data_ptr())
+        self.dev.bounds = ctypes.pointer(fa.bounds.out)
+        self.dev.workspace = fa.workspace.data_ptr()
+        self.dev.workspace_bytes = fa.workspace.numel() * fa.workspace.element_size()
 
     def run(self, batches, chunks=None):
-        """batches: iterable of (q_host, k_host, v_host, o_host); o_host is filled.  Returns
-        when every output is back in host memory."""
-        ev = lambda: torch.cuda.Event()  # noqa: E731
-        computed = [None, None]  # compute of the batch that last used each slot has finished
-        read_back = [None, None]  # its output has left the slot
-        for i, (qh, kh, vh, oh) in enumerate(batches):
-            s = i % 2
-            with torch.cuda.stream(self.s_h2d):
-                if computed[s] is not None:
-                    self.s_h2d.wait_event(computed[s])
-                self.q[s].copy_(qh, non_blocking=True)
-                self.k[s].copy_(kh, non_blocking=True)
-                self.v[s].copy_(vh, non_blocking=True)
-                uploaded = ev()
-                uploaded.record(self.s_h2d)
-            fa = self.fa
-            with torch.cuda.stream(self.s_comp):
-                self.s_comp.wait_event(uploaded)
-                if read_back[s] is not None:
-                    self.s_comp.wait_event(read_back[s])
-                N = self.k[s].shape[2]
-                cs = [(0, N)] if chunks is None else chunks
-                fm_bounds(self.q[s], self.k[s], self.v[s], fa.opt, fa.bounds, fa.workspace, self.s_comp)
-                for j, (st, n) in enumerate(cs):
-                    call = fm_attn_chunk_final if j == len(cs) - 1 else fm_attn_chunk
-                    extra = (self.o[s],) if j == len(cs) - 1 else ()
-                    call(self.q[s], self.k[s][:, :, st:st + n], self.v[s][:, :, st:st + n], fa.bounds, fa.opt,
-                         fa.acc_o, fa.acc_sum, fa.acc_max, j > 0, *extra, stream=self.s_comp)
-                computed[s] = ev()
-                computed[s].record(self.s_comp)
-            with torch.cuda.stream(self.s_d2h):
-                self.s_d2h.wait_event(computed[s])
-                oh.copy_(self.o[s], non_blocking=True)
-                read_back[s] = ev()
-                read_back[s].record(self.s_d2h)
-        for st in (self.s_h2d, self.s_comp, self.s_d2h):
-            st.synchronize()
+        """batches: a list of (q_host, k_host, v_host, o_host); o_host is filled.  chunks: the
+        (start, length) key ranges, consecutive from 0.  Returns when every output is back in
+        host memory."""
+        batches = list(batches)
+        N = self.k[0].shape[2]
+        chunks = [(0, N)] if chunks is None else chunks
+        if [s for s, _ in chunks] != [sum(n for _, n in chunks[:i]) for i in range(len(chunks))]:
+            raise ValueError("chunks must be consecutive key ranges from 0")
+        n = len(batches)
+        qs = (fm_tensor * max(n, 1))(*[tensor(b[0]) for b in batches])
+        ks = (fm_tensor * max(n, 1))(*[tensor(b[1]) for b in batches])
+        vs = (fm_tensor * max(n, 1))(*[tensor(b[2]) for b in batches])
+        os_ = (fm_tensor * max(n, 1))(*[tensor(b[3]) for b in batches])
+        lens = (ctypes.c_int64 * len(chunks))(*[c for _, c in chunks])
+        st = (ctypes.c_void_p * 3)(*[s.cuda_stream for s in self.streams])
+        return _check(load().fm_attention_host(qs, ks, vs, os_, n, lens, len(chunks), ctypes.byref(self.fa.opt),
+                                               ctypes.byref(self.dev), st))

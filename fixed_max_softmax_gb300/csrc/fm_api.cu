@@ -727,3 +727,128 @@ extern "C" int fm_bounds_noalloc(const fm_tensor *q, const fm_tensor *k_full, co
   if (rc != FM_OK) return rc;
   return fm_bounds(q, k_full, v_full, opts, out, scratch, FM_NOALLOC_SCRATCH_BYTES, stream);
 }
+
+// ---------------------------------------------------------------------------------
+// fm_attention_host: whole forwards on host buffers, copies overlapped with the kernels.
+namespace {
+
+bool contiguous4(const fm_tensor *t) {
+  return t->stride[3] == 1 && t->stride[2] == t->D && t->stride[1] == t->S * t->D && t->stride[0] == t->H * t->S * t->D;
+}
+size_t tensor_bytes(const fm_tensor *t) {
+  return (size_t)(t->B * t->H * t->S * t->D) * (t->dtype == FM_F32 ? 4 : 2);
+}
+bool same_shape(const fm_tensor *a, const fm_tensor *b) {
+  return a->dtype == b->dtype && a->B == b->B && a->H == b->H && a->S == b->S && a->D == b->D;
+}
+
+// Events of one call, destroyed on every return path.
+struct EventSet {
+  cudaEvent_t ev[6] = {};
+  int n = 0;
+  cudaError_t create() {
+    for (; n < 6; ++n) {
+      cudaError_t e = cudaEventCreateWithFlags(&ev[n], cudaEventDisableTiming);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  ~EventSet() {
+    for (int i = 0; i < n; ++i) cudaEventDestroy(ev[i]);
+  }
+};
+
+}  // namespace
+
+extern "C" int fm_attention_host(const fm_tensor *q_host, const fm_tensor *k_host, const fm_tensor *v_host,
+                                 const fm_tensor *o_host, int n_batches, const int64_t *chunk_lens, int n_chunks,
+                                 const fm_opts *opts, const fm_host_buffers *dev, const fm_stream_t *streams) {
+  t_err.clear();
+  if (!q_host || !k_host || !v_host || !o_host || !dev || !streams || !chunk_lens)
+    return fail(FM_ERR_ARG, "fm_attention_host: NULL argument");
+  if (n_batches < 0 || n_chunks < 1) return fail(FM_ERR_ARG, "n_batches = %d, n_chunks = %d", n_batches, n_chunks);
+  if (!streams[0] || !streams[1] || !streams[2])
+    return fail(FM_ERR_ARG, "fm_attention_host needs three streams (upload, compute, read-back)");
+  // every buffer contiguous, the host ones shaped like the device ones
+  for (int s = 0; s < 2; ++s) {
+    const fm_tensor *d[4] = {&dev->q[s], &dev->k[s], &dev->v[s], &dev->o[s]};
+    for (const fm_tensor *t : d)
+      if (!contiguous4(t)) return fail(FM_ERR_UNSUPPORTED, "fm_attention_host: device buffers must be contiguous");
+    if (!same_shape(&dev->q[s], &dev->q[0]) || !same_shape(&dev->k[s], &dev->k[0]) ||
+        !same_shape(&dev->v[s], &dev->v[0]) || !same_shape(&dev->o[s], &dev->o[0]))
+      return fail(FM_ERR_SHAPE, "fm_attention_host: the two buffer sets differ");
+  }
+  int64_t N = 0;
+  for (int c = 0; c < n_chunks; ++c) {
+    if (chunk_lens[c] < 0) return fail(FM_ERR_ARG, "negative chunk length");
+    N += chunk_lens[c];
+  }
+  if (N != dev->k[0].S) return fail(FM_ERR_SHAPE, "chunk lengths sum to %lld, k has %lld keys", (long long)N,
+                                    (long long)dev->k[0].S);
+  for (int i = 0; i < n_batches; ++i) {
+    const fm_tensor *h[4] = {&q_host[i], &k_host[i], &v_host[i], &o_host[i]};
+    const fm_tensor *d[4] = {&dev->q[0], &dev->k[0], &dev->v[0], &dev->o[0]};
+    for (int j = 0; j < 4; ++j) {
+      if (!contiguous4(h[j])) return fail(FM_ERR_UNSUPPORTED, "fm_attention_host: host buffers must be contiguous");
+      if (!same_shape(h[j], d[j])) return fail(FM_ERR_SHAPE, "fm_attention_host: batch %d's host buffer %d differs", i, j);
+      if (tensor_bytes(h[j]) > 0 && !h[j]->ptr) return fail(FM_ERR_ARG, "fm_attention_host: NULL host pointer");
+    }
+  }
+  cudaStream_t up = reinterpret_cast<cudaStream_t>(streams[0]), comp = reinterpret_cast<cudaStream_t>(streams[1]),
+               down = reinterpret_cast<cudaStream_t>(streams[2]);
+  EventSet es;
+  cudaError_t e = es.create();
+  if (e != cudaSuccess) return cuda_fail(e, "fm_attention_host: cudaEventCreate");
+  cudaEvent_t *uploaded = es.ev, *computed = es.ev + 2, *read_back = es.ev + 4;
+  bool used[2] = {false, false};
+  fm_bounds_out *bounds = dev->bounds;
+  for (int i = 0; i < n_batches; ++i) {
+    const int s = i & 1;
+    // upload into slot s once the batch that last used it has finished reading its inputs
+    if (used[s] && (e = cudaStreamWaitEvent(up, computed[s], 0)) != cudaSuccess) return cuda_fail(e, "wait");
+    const fm_tensor *src[3] = {&q_host[i], &k_host[i], &v_host[i]};
+    const fm_tensor *dst[3] = {&dev->q[s], &dev->k[s], &dev->v[s]};
+    for (int j = 0; j < 3; ++j)
+      if (tensor_bytes(src[j]) > 0 &&
+          (e = cudaMemcpyAsync(dst[j]->ptr, src[j]->ptr, tensor_bytes(src[j]),
+                               cudaMemcpyHostToDevice, up)) != cudaSuccess)
+        return cuda_fail(e, "fm_attention_host: upload");
+    if ((e = cudaEventRecord(uploaded[s], up)) != cudaSuccess) return cuda_fail(e, "record");
+    // compute once the inputs are in and the output slot has been read back
+    if ((e = cudaStreamWaitEvent(comp, uploaded[s], 0)) != cudaSuccess) return cuda_fail(e, "wait");
+    if (used[s] && (e = cudaStreamWaitEvent(comp, read_back[s], 0)) != cudaSuccess) return cuda_fail(e, "wait");
+    int rc = fm_bounds(&dev->q[s], &dev->k[s], &dev->v[s], opts, bounds, dev->workspace, dev->workspace_bytes,
+                       streams[1]);
+    if (rc) return rc;
+    int64_t start = 0;
+    for (int c = 0; c < n_chunks; ++c) {
+      fm_tensor kc = dev->k[s], vc = dev->v[s];
+      const size_t es2 = kc.dtype == FM_F32 ? 4 : 2;
+      kc.ptr = static_cast<char *>(kc.ptr) + (size_t)(start * kc.stride[2]) * es2;
+      vc.ptr = static_cast<char *>(vc.ptr) + (size_t)(start * vc.stride[2]) * es2;
+      kc.S = vc.S = chunk_lens[c];
+      // the chunk's slice [start, start + len) of a contiguous K/V keeps the full tensor's strides
+      bounds->next_key_offset = start;
+      if (c == n_chunks - 1)
+        rc = fm_attn_chunk_final(&dev->q[s], &kc, &vc, bounds, opts, dev->acc_o, dev->acc_sum, dev->acc_max, c > 0,
+                                 &dev->o[s], nullptr, streams[1]);
+      else
+        rc = fm_attn_chunk(&dev->q[s], &kc, &vc, bounds, opts, dev->acc_o, dev->acc_sum, dev->acc_max, c > 0,
+                           streams[1]);
+      if (rc) return rc;
+      start += chunk_lens[c];
+    }
+    if ((e = cudaEventRecord(computed[s], comp)) != cudaSuccess) return cuda_fail(e, "record");
+    // read the output back once it is computed
+    if ((e = cudaStreamWaitEvent(down, computed[s], 0)) != cudaSuccess) return cuda_fail(e, "wait");
+    if (tensor_bytes(&o_host[i]) > 0 &&
+        (e = cudaMemcpyAsync(o_host[i].ptr, dev->o[s].ptr, tensor_bytes(&o_host[i]),
+                             cudaMemcpyDeviceToHost, down)) != cudaSuccess)
+      return cuda_fail(e, "fm_attention_host: read-back");
+    if ((e = cudaEventRecord(read_back[s], down)) != cudaSuccess) return cuda_fail(e, "record");
+    used[s] = true;
+  }
+  for (cudaStream_t st : {up, comp, down})
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "fm_attention_host: synchronize");
+  return FM_OK;
+}

@@ -193,9 +193,12 @@ __device__ __forceinline__ void red_add_v4(float *dst, uint32_t a, uint32_t b, u
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
 }
-__device__ __forceinline__ void bulk_commit_and_wait() {
+// Commit the bulk operations issued so far and wait until they have read their shared-memory
+// source, so that it may be reused or released; their global writes complete with the grid,
+// before the next kernel in the stream (or its griddepcontrol.wait) proceeds.
+__device__ __forceinline__ void bulk_commit_and_wait_smem_read() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 // Shared-memory writes of this thread become visible to the bulk-copy (async) proxy.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -855,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             tma_acc_3d(&maps.acc, sbase + c * (kBQ * 128), c * 32, (int)(qb * kBQ), (int)bh, p.accumulate != 0);
-          bulk_commit_and_wait();
+          bulk_commit_and_wait_smem_read();
         }
         if (row_ok) {
           p.acc_sum[rflat] = sum_new;

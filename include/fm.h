@@ -370,6 +370,36 @@ FM_API int fm_bounds_local(const fm_tensor *q, const fm_tensor *k_shard, const f
 FM_API int fm_bounds_combine(const void *stats_all, int n_ranks, const fm_opts *opts, fm_bounds_out *out,
                              fm_stream_t stream);
 
+/* ---- Whole forwards on host buffers --------------------------------------------------------
+ * Device buffers of fm_attention_host, all owned by the caller: two sets of inputs and outputs,
+ * which consecutive batches alternate between, and one set of accumulators, bounds and workspace,
+ * which the batches reuse in order. */
+typedef struct {
+  fm_tensor q[2], k[2], v[2]; /* device, contiguous [B, H, Sq, D] / [B, H, N, D], the inputs' dtype */
+  fm_tensor o[2];             /* device, contiguous [B, H, Sq, D], the outputs' dtype */
+  float *acc_o, *acc_sum, *acc_max;
+  fm_bounds_out *bounds;      /* host struct whose device arrays are set, as for fm_bounds */
+  void *workspace;
+  size_t workspace_bytes;
+} fm_host_buffers;
+
+/* fm_attention_host -- n_batches whole forwards whose inputs and outputs live in host memory.
+ * For batch i: q_host[i], k_host[i], v_host[i] are copied to the device, the path runs
+ * (fm_bounds, one fm_attn_chunk per chunk of chunk_lens, the last chunk fused with the
+ * normalise), and o is copied back into o_host[i].  Batch i+1's upload and batch i-1's read-back
+ * run on their own streams while batch i computes, so the copies hide behind the kernels (host
+ * memory must be page-locked for that; pageable memory works but does not overlap).
+ *   q_host, k_host, v_host, o_host  arrays of n_batches contiguous host tensors, shaped and typed
+ *                  like the device buffers
+ *   chunk_lens     n_chunks >= 1 key counts summing to N (the ring steps run one after another)
+ *   streams        three caller-created streams: upload, compute, read-back
+ * Returns when every output is in host memory.  Creates and destroys a few CUDA events; allocates
+ * no device memory.  Errors: those of the calls it makes, FM_ERR_ARG / FM_ERR_SHAPE for buffers
+ * that do not match, FM_ERR_UNSUPPORTED for non-contiguous ones. */
+FM_API int fm_attention_host(const fm_tensor *q_host, const fm_tensor *k_host, const fm_tensor *v_host,
+                             const fm_tensor *o_host, int n_batches, const int64_t *chunk_lens, int n_chunks,
+                             const fm_opts *opts, const fm_host_buffers *dev, const fm_stream_t *streams);
+
 /* Upper bound of the scratch fm_bounds_noalloc can use: 4 MiB.  That covers, at D = 128,
  * up to 74 heads of 75,600 keys (fm_bounds_workspace_size gives the exact need). */
 #define FM_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)

@@ -40,10 +40,11 @@ def test_exports_nothing_else():
 
 
 def test_struct_layouts_match_header(tmp_path):
-    """The ctypes mirrors of fm_tensor, fm_opts and fm_bounds_out have the size and field
-    offsets the C compiler gives the header's structs."""
+    """The ctypes mirrors of fm_tensor, fm_opts, fm_bounds_out and fm_host_buffers have the size
+    and field offsets the C compiler gives the header's structs."""
     import subprocess
-    structs = {"fm_tensor": fm.fm_tensor, "fm_opts": fm.fm_opts, "fm_bounds_out": fm.fm_bounds_out}
+    structs = {"fm_tensor": fm.fm_tensor, "fm_opts": fm.fm_opts, "fm_bounds_out": fm.fm_bounds_out,
+               "fm_host_buffers": fm.fm_host_buffers}
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "fm.h"', "int main(void) {"]
     for name, cls in structs.items():
         lines.append(f'  printf("{name} size %zu\\n", sizeof({name}));')
