@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kThreads) ksum_kernel(View k, int64_t P, float
 // load covers RPW = 32 / LPR rows; each lane keeps kUnroll such loads in flight before it
 // reduces, which is what keeps HBM busy (one 256-byte row per warp at a time is not enough).
 constexpr int kUnroll = 4;
+constexpr int kNormsCtasPerSm = 4;  // resident CTAs of norms_vec_kernel (64 registers x 256 threads)
 template <typename T, int D>
 struct Vec16 {
   static constexpr int VEC = 16 / (int)sizeof(T);
@@ -372,7 +373,10 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// 3'. The norms pass with 16-byte loads: the same blocks and outputs as norms_kernel.
+// 3'. The norms pass with 16-byte loads: the same blocks and outputs as norms_kernel, but each
+// CTA walks blocks blockIdx.x, blockIdx.x + gridDim.x, ... of its head, so that a CTA streams
+// for long (a block alone is only 32-64 KiB, too little to cover a CTA's start and its closing
+// reduction).
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
     norms_vec_kernel(View q, View k, View v, int64_t nqb, int64_t nkb, int centering, float alpha,
@@ -383,7 +387,7 @@ __global__ void __launch_bounds__(kThreads)
   using V = Vec16<T, D>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane / V::LPR, li = lane % V::LPR;
-  const int64_t b = blockIdx.z, h = blockIdx.y, bx = blockIdx.x;
+  const int64_t b = blockIdx.z, h = blockIdx.y;
   const int64_t bh = b * q.H + h;
   const int64_t step = (int64_t)kWarps * V::RPW;
   __shared__ float wmax[kWarps];
@@ -392,6 +396,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
   for (int e = 0; e < V::VEC; ++e) kb[e] = centering ? kbar[bh * D + li * V::VEC + e] : 0.f;
 
+  for (int64_t bx = blockIdx.x; bx < nqb + 2 * nkb; bx += gridDim.x) {
   float best = 0.f;  // maxima of non-negative quantities start at 0
   if (bx < nqb) {
     // Q-block: per-row |q|^2 and alpha * q.kbar
@@ -504,6 +509,8 @@ __global__ void __launch_bounds__(kThreads)
       pv = bv;
       pi = bi;
     }
+  }
+  __syncthreads();  // wmax and knorm are reused by the next block
   }
 }
 
@@ -904,9 +911,14 @@ cudaError_t launch_norms(const BoundsArgs &a, const WsLayout &w, float *kblk, fl
   const int64_t nx = a.nqb + 2 * w.nkb;
   if (nx == 0) return cudaSuccess;
   const dim3 grid((unsigned)nx, (unsigned)a.q.H, (unsigned)a.q.B);
-  if (CONTIG && rows16(a.q) && rows16(a.k) && rows16(a.v))
-    return launch_pdl(norms_vec_kernel<T, 32 * EPL>, grid, dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb,
+  if (CONTIG && rows16(a.q) && rows16(a.k) && rows16(a.v)) {
+    // about two waves of resident CTAs over all heads, each walking several blocks
+    const int64_t heads = a.q.H * a.q.B;
+    const int64_t want = ceil_div((int64_t)current_device_sm_count() * kNormsCtasPerSm * 2, heads);
+    const dim3 g2((unsigned)(want < 1 ? 1 : (want < nx ? want : nx)), (unsigned)a.q.H, (unsigned)a.q.B);
+    return launch_pdl(norms_vec_kernel<T, 32 * EPL>, g2, dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb,
                       a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand);
+  }
   return launch_pdl(norms_kernel<T, EPL, CONTIG>, grid, dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb,
                     a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand);
 }

@@ -64,7 +64,6 @@ constexpr int kPanelBytes = 128 * 64 * 2;     // 128 rows x 64 bf16 (one 128-byt
 constexpr int kThreads = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLazyRescale = 8.0f;          // online path: rescale when the max grows by > 2^8
-constexpr int kPersistentMaxTiles = 16;       // launches of at most this many key tiles run persistent
 
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr int kOffQ = 0;
@@ -602,17 +601,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      int last_round[kStages];
-      for (int s = 0; s < kStages; ++s) last_round[s] = -1;
+      int last_phase[kStages];  // phase of the last load issued into each stage, -1: none
+      for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
       bool ok = true;
-      int64_t q_loads = 0;  // Q tile pairs issued
-      int64_t g = 0;        // key tiles of earlier items (the ring position carries over)
-      for (int64_t item = item0; item < p.n_items && ok; item += item_step, g += n_kv) {
+      uint32_t q_loads = 0;      // Q tile pairs issued
+      int st = 0;                // ring position of the next K/V load (carries over items)
+      uint32_t ph = 0;
+      for (int64_t item = item0; item < p.n_items && ok; item += item_step) {
         const int64_t bh = item_bh(item), qb0 = item_qb0(item);
         const int h = (int)(bh % p.H), b = (int)(bh / p.H);
         // Q of the previous item must have been read by all of its S MMAs
         if (q_loads > 0)
-          ok = wait_phase(bar(kBarQEmpty), (uint32_t)((q_loads - 1) & 1), abort_flag, p.timeout_ns, p.err,
+          ok = wait_phase(bar(kBarQEmpty), (q_loads - 1) & 1u, abort_flag, p.timeout_ns, p.err,
                           kDevErrTimeoutProducer, wtag(kBarQEmpty, 0));
         if (!ok) break;
         mbar_expect_tx(bar(kBarQFull), 4 * kPanelBytes);
@@ -626,28 +626,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           while (j >= p.tile0[c + 1]) ++c;
           const int jl = j - p.tile0[c];  // tile within its chunk
           for (int w = 0; w < 2 && ok; ++w) {
-            const int64_t idx = 2 * (g + j) + w;
-            const int s = (int)(idx % kStages), round = (int)(idx / kStages);
-            ok = wait_phase(bar(kBarKVEmpty + s), (uint32_t)((round & 1) ^ 1), abort_flag, p.timeout_ns, p.err,
-                            kDevErrTimeoutProducer, wtag(kBarKVEmpty + s, j));
+            ok = wait_phase(bar(kBarKVEmpty + st), ph ^ 1u, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutProducer,
+                            wtag(kBarKVEmpty + st, j));
             if (!ok) break;
-            mbar_expect_tx(bar(kBarKVFull + s), kTileBytes);
+            mbar_expect_tx(bar(kBarKVFull + st), kTileBytes);
             const CUtensorMap *tm = w ? &maps.v[c] : &maps.k[c];
             for (int pn = 0; pn < 2; ++pn)
-              tma_load_4d(base + kOffKV + s * kTileBytes + pn * kPanelBytes, tm, bar(kBarKVFull + s), pn * 64,
+              tma_load_4d(base + kOffKV + st * kTileBytes + pn * kPanelBytes, tm, bar(kBarKVFull + st), pn * 64,
                           jl * kBK, h, b);
-            last_round[s] = round;
+            last_phase[st] = (int)ph;
+            if (++st == kStages) {
+              st = 0;
+              ph ^= 1u;
+            }
           }
         }
       }
       if (!ok) {
         // let every copy already issued land before the CTA can exit
         if (q_loads > 0)
-          wait_phase(bar(kBarQFull), (uint32_t)((q_loads - 1) & 1), nullptr, p.timeout_ns, p.err,
-                     kDevErrTimeoutDrain, wtag(kBarQFull, 0));
+          wait_phase(bar(kBarQFull), (q_loads - 1) & 1u, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain,
+                     wtag(kBarQFull, 0));
         for (int s = 0; s < kStages; ++s)
-          if (last_round[s] >= 0)
-            wait_phase(bar(kBarKVFull + s), (uint32_t)(last_round[s] & 1), nullptr, p.timeout_ns, p.err,
+          if (last_phase[s] >= 0)
+            wait_phase(bar(kBarKVFull + s), (uint32_t)last_phase[s], nullptr, p.timeout_ns, p.err,
                        kDevErrTimeoutDrain, wtag(kBarKVFull + s, 0));
       }
     }
@@ -665,28 +667,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         return smem_desc(base + kOffKV + s * kTileBytes + kk * 2048, kPanelBytes, 1024);
       };
       bool ok = true;
-      int64_t g = 0;
-      int64_t k = 0;  // items done by this CTA
-      for (int64_t item = item0; item < p.n_items && ok; item += item_step, g += n_kv, ++k) {
+      uint32_t k = 0;    // items done by this CTA
+      uint32_t tix = 0;  // key tiles consumed so far: the phase of the S-full / P-ready barriers
+      int st = 0;        // ring position of the next K/V tile to consume
+      uint32_t ph = 0;
+      for (int64_t item = item0; item < p.n_items && ok; item += item_step, ++k) {
         // MMAs of one CTA run in issue order, so S(j) of this item may overwrite the S/P
         // columns that the previous item's last PV MMAs read; O is overwritten only by PV(0),
         // issued after the softmax group's P-ready arrival, which follows its epilogue reads.
-        ok = wait_phase(bar(kBarQFull), (uint32_t)(k & 1), abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma,
+        ok = wait_phase(bar(kBarQFull), k & 1u, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma,
                         wtag(kBarQFull, 0));
         int vs_prev = 0;
-        for (int j = 0; j < n_kv && ok; ++j) {
-          const int64_t gj = g + j;
-          const int64_t ki = 2 * gj;
-          const int ks = (int)(ki % kStages);
-          ok = wait_phase(bar(kBarKVFull + ks), (uint32_t)((ki / kStages) & 1), abort_flag, p.timeout_ns, p.err,
-                          kDevErrTimeoutMma, wtag(kBarKVFull + ks, j));
+        for (int j = 0; j < n_kv && ok; ++j, ++tix) {
+          const int ks = st;
+          const uint32_t kph = ph;
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1u;
+          }
+          ok = wait_phase(bar(kBarKVFull + ks), kph, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma,
+                          wtag(kBarKVFull + ks, j));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) mma_ss(tS0, q_desc(0, kk), k_desc(ks, kk), kIdescQK, kk > 0);
           mma_commit(bar(kBarSFull + 0));
           if (j > 0) {
-            ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((gj - 1) & 1), abort_flag, p.timeout_ns, p.err,
+            ok = wait_phase(bar(kBarPReady + 1), (tix - 1) & 1u, abort_flag, p.timeout_ns, p.err,
                             kDevErrTimeoutMma, wtag(kBarPReady + 1, j));
             if (!ok) break;
             tc_fence_after();
@@ -700,12 +707,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(bar(kBarSFull + 1));
           mma_commit(bar(kBarKVEmpty + ks));
           if (j == n_kv - 1) mma_commit(bar(kBarQEmpty));  // the producer may load the next Q
-          const int64_t vi = 2 * gj + 1;
-          const int vs = (int)(vi % kStages);
-          ok = wait_phase(bar(kBarKVFull + vs), (uint32_t)((vi / kStages) & 1), abort_flag, p.timeout_ns, p.err,
-                          kDevErrTimeoutMma, wtag(kBarKVFull + vs, j)) &&
-               wait_phase(bar(kBarPReady + 0), (uint32_t)(gj & 1), abort_flag, p.timeout_ns, p.err,
-                          kDevErrTimeoutMma, wtag(kBarPReady + 0, j));
+          const int vs = st;
+          const uint32_t vph = ph;
+          if (++st == kStages) {
+            st = 0;
+            ph ^= 1u;
+          }
+          ok = wait_phase(bar(kBarKVFull + vs), vph, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma,
+                          wtag(kBarKVFull + vs, j)) &&
+               wait_phase(bar(kBarPReady + 0), tix & 1u, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma,
+                          wtag(kBarPReady + 0, j));
           if (!ok) break;
           tc_fence_after();
 #pragma unroll
@@ -714,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           vs_prev = vs;
         }
         if (ok) {
-          ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((g + n_kv - 1) & 1), abort_flag, p.timeout_ns, p.err,
+          ok = wait_phase(bar(kBarPReady + 1), (tix - 1) & 1u, abort_flag, p.timeout_ns, p.err,
                           kDevErrTimeoutMma, wtag(kBarPReady + 1, n_kv));
           if (ok) {
             tc_fence_after();
@@ -742,12 +753,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(t * 128);
     int32_t *ssk = reinterpret_cast<int32_t *>(gbase + kOffSinks) + t * FM_MAX_SINKS;
     bool ok = true;
-    int64_t g = 0;
-    int64_t k = 0;
+    uint32_t g = 0;  // key tiles of earlier items: the phase of the S-full barrier carries over
+    uint32_t k = 0;
     // Every thread of the group takes the same named barriers in the same order: a wait that
     // gave up ends this thread's tile loop, and the group agrees on the outcome at one barrier
     // that each of its threads reaches, before any other barrier of the item.
-    for (int64_t item = item0; item < p.n_items; item += item_step, g += n_kv, ++k) {
+    for (int64_t item = item0; item < p.n_items; item += item_step, g += (uint32_t)n_kv, ++k) {
       const int64_t bh = item_bh(item);
       const int64_t qb = item_qb0(item) + t;
       const bool tile_ok = qb < p.nqb;
@@ -763,6 +774,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // merge is a plain add
       else if (p.accumulate && row_ok) shv = p.acc_max[bh * p.Sq + row];
       const float shift_prev = shv;
+      // the earlier chunks' row sum, loaded now so that its memory latency hides behind the tiles
+      const float sum_prev = (p.accumulate && row_ok) ? p.acc_sum[bh * p.Sq + row] : 0.f;
       float l[4] = {0.f, 0.f, 0.f, 0.f};
       // key sinks of this item's head (ascending global key indices, INT_MAX pads): columns to
       // drop.  Every thread of the group finished the previous item's tiles (their P-ready
@@ -777,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int c = 0;  // chunk of key tile j
       for (int j = 0; j < n_kv; ++j) {
         while (j >= p.tile0[c + 1]) ++c;
-        ok = wait_phase(bar(kBarSFull + t), (uint32_t)((g + j) & 1), abort_flag, p.timeout_ns, p.err,
+        ok = wait_phase(bar(kBarSFull + t), (g + (uint32_t)j) & 1u, abort_flag, p.timeout_ns, p.err,
                         kDevErrTimeoutSoftmax, wtag(kBarSFull + t, j));
         ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
         if (!ok) break;
@@ -796,8 +809,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(kBarPReady + t));
       }
       if (ok) {
-        ok = wait_phase(bar(kBarODone + t), (uint32_t)(k & 1), abort_flag, p.timeout_ns, p.err,
-                        kDevErrTimeoutSoftmax, wtag(kBarODone + t, n_kv));
+        ok = wait_phase(bar(kBarODone + t), k & 1u, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutSoftmax,
+                        wtag(kBarODone + t, n_kv));
         ok = __all_sync(0xffffffffu, ok);
       }
       ok = named_barrier_and(1 + t, 128, ok);
@@ -814,7 +827,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // the row's sum and shift after this chunk
       float sum_new = lsum;
-      if (row_ok && p.accumulate) sum_new = fixed ? p.acc_sum[rflat] + lsum : fmaf(p.acc_sum[rflat], cprev, lsum * cnew);
+      if (row_ok && p.accumulate) sum_new = fixed ? sum_prev + lsum : fmaf(sum_prev, cprev, lsum * cnew);
       const float shift_new = nr;  // b_i on fixed-m rows
       const bool final_out = p.out != nullptr;
       // with the normalise fused in, o = acc / max(sum, 1e-37) goes straight to `out`
@@ -1009,15 +1022,11 @@ bool encode_acc_map(CUtensorMap *map, float *acc_o, const View &q) {
   return r == CUDA_SUCCESS;
 }
 
-// Schedule of a launch (fm_opts.schedule).  AUTO takes the persistent schedule for launches of
-// more than one wave whose items are short (few key tiles), where each CTA's prologue,
-// pipeline fill and epilogue are a large share of its time and can overlap the next item's
-// loads and first MMAs.
-bool use_persistent(int schedule, int64_t n_items, int n_kv, int sms) {
-  if (schedule == FM_SCHEDULE_GRID) return false;
-  if (schedule == FM_SCHEDULE_PERSISTENT) return true;
-  return n_items > sms && n_kv <= kPersistentMaxTiles;
-}
+// Schedule of a launch (fm_opts.schedule).  AUTO takes one CTA per item: the persistent schedule
+// overlaps the next item's Q load and first S MMAs with the current item's epilogue, but its
+// epilogue adds O from registers with vector reductions scattered over 128 rows, which takes
+// 5-9 us per item against 3-4 us for the staged bulk-tensor reduce, so it only runs on request.
+bool use_persistent(int schedule) { return schedule == FM_SCHEDULE_PERSISTENT; }
 
 bool tma_view_ok(const View &t) {
   if (t.dtype != FM_BF16 || t.D != kHD || t.sD != 1) return false;
@@ -1115,7 +1124,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   p.n_pairs = (a.nqb + 1) / 2;
   p.n_items = p.n_pairs * a.q.H * a.q.B;
   const int sms = current_device_sm_count();
-  p.persistent = use_persistent(a.schedule, p.n_items, p.n_kv, sms) ? 1 : 0;
+  p.persistent = use_persistent(a.schedule) ? 1 : 0;
   // non-final chunks of the one-item-per-CTA schedule add O into acc_o with bulk tensor
   // operations where the map encodes (the persistent schedule needs that shared memory for the
   // next item and adds from registers instead)

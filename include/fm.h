@@ -112,9 +112,8 @@ typedef struct {
  * tile of the call.  GRID launches one CTA per item.  PERSISTENT launches one CTA per SM that
  * walks the items in turn, loading the next item's Q and K/V tiles and running its first S
  * MMAs while the softmax warps finish the current item's epilogue (the accumulator add then
- * comes from registers as vector reductions rather than through shared memory).  AUTO picks
- * PERSISTENT for launches of more than one wave with at most 16 key tiles per item, where the
- * per-item prologue and epilogue are a large share of the time, and GRID otherwise. */
+ * comes from registers as vector reductions rather than through shared memory).  AUTO is GRID:
+ * measured on GB300, the register reductions cost more per item than the overlap saves. */
 enum { FM_SCHEDULE_AUTO = 0, FM_SCHEDULE_GRID = 1, FM_SCHEDULE_PERSISTENT = 2 };
 
 /* Bounds of one attention call ([PR477] Summary, "Dynamic eligibility bounding").
