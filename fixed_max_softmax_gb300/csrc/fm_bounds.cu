@@ -170,7 +170,6 @@ __global__ void __launch_bounds__(kThreads) ksum_kernel(View k, int64_t P, float
 // load covers RPW = 32 / LPR rows; each lane keeps kUnroll such loads in flight before it
 // reduces, which is what keeps HBM busy (one 256-byte row per warp at a time is not enough).
 constexpr int kUnroll = 4;
-constexpr int kNormsCtasPerSm = 3;  // resident CTAs of norms_vec_kernel per SM (78 registers x 256 threads)
 template <typename T, int D>
 struct Vec16 {
   static constexpr int VEC = 16 / (int)sizeof(T);
@@ -373,21 +372,25 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// 3'. The norms pass with 16-byte loads: the same blocks and outputs as norms_kernel.  The CTAs
-// of a head split into three equal groups, for Q-, K- and V-blocks; CTA i of a group walks
-// blocks i, i + G, i + 2G, ... of its kind, so that each CTA streams for long (one block alone is
-// only 32-64 KiB, too little to cover a CTA's start and its closing reduction).
-// The max over a block's rows of `best`, written to out[idx] by thread 0.
-__device__ __forceinline__ void close_block(float best, float *wmax, float *out) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  best = warp_max(best);
-  if (lane == 0) wmax[warp] = best;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float mx = 0.f;
+// 3'. The norms pass with 16-byte loads: the same blocks and outputs as norms_kernel, one block per
+// CTA.  Each lane keeps kRawLoads 16-byte loads in flight as raw words and converts them only
+// when it uses them, so that many loads stay in flight for few registers.
+constexpr int kRawLoads = 8;
+template <typename T, int VEC>
+__device__ __forceinline__ void unpack16(const uint4 &u, float (&x)[VEC]) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, wmax[w]);
-    *out = mx;
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[i]));
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  } else {
+    x[0] = __uint_as_float(u.x);
+    x[1] = __uint_as_float(u.y);
+    x[2] = __uint_as_float(u.z);
+    x[3] = __uint_as_float(u.w);
   }
 }
 
@@ -399,135 +402,138 @@ __global__ void __launch_bounds__(kThreads)
   pdl_wait();  // inputs written by the kernels before this one
   pdl_trigger();
   using V = Vec16<T, D>;
+  constexpr int U = kRawLoads;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane / V::LPR, li = lane % V::LPR;
-  const int64_t b = blockIdx.z, h = blockIdx.y;
+  const int64_t b = blockIdx.z, h = blockIdx.y, bx = blockIdx.x;
   const int64_t bh = b * q.H + h;
-  const int64_t G = gridDim.x / 3;  // CTAs per kind
-  const int kind = (int)(blockIdx.x / G), i0 = (int)(blockIdx.x % G);
   const int64_t step = (int64_t)kWarps * V::RPW;
   __shared__ float wmax[kWarps];
   __shared__ float knorm[kKVRows];  // key blocks with sinks: each row's squared norm
 
-  if (kind == 0) {
-    // Q-blocks: per-row |q|^2 and alpha * q.kbar
+  float best = 0.f;  // maxima of non-negative quantities start at 0
+  if (bx < nqb) {
+    // Q-block: per-row |q|^2 and alpha * q.kbar
     float kb[V::VEC];
 #pragma unroll
     for (int e = 0; e < V::VEC; ++e) kb[e] = centering ? kbar[bh * D + li * V::VEC + e] : 0.f;
     const T *base = reinterpret_cast<const T *>(q.ptr) + b * q.sB + h * q.sH + li * V::VEC;
-    for (int64_t bx = i0; bx < nqb; bx += G) {
-      float best = 0.f;  // maxima of non-negative quantities start at 0
-      const int64_t r0 = bx * kQRows, r1 = min(q.S, r0 + kQRows);
-      for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += kUnroll * step) {  // warp-uniform trip count
-        const int64_t r = rb + sub;
-        float x[kUnroll][V::VEC];
+    const int64_t r0 = bx * kQRows, r1 = min(q.S, r0 + kQRows);
+    for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += U * step) {  // warp-uniform trip count
+      const int64_t r = rb + sub;
+      uint4 raw[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-          if (r + u * step < r1) load16<T, V::VEC>(base + (r + u * step) * q.sS, x[u]);
+      for (int u = 0; u < U; ++u)
+        if (r + u * step < r1) raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + (r + u * step) * q.sS));
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          float ss = 0.f, dk = 0.f;
-          if (r + u * step < r1) {
+      for (int u = 0; u < U; ++u) {
+        float ss = 0.f, dk = 0.f;
+        if (r + u * step < r1) {
+          float x[V::VEC];
+          unpack16<T, V::VEC>(raw[u], x);
 #pragma unroll
-            for (int e = 0; e < V::VEC; ++e) {
-              ss = fmaf(x[u][e], x[u][e], ss);
-              dk = fmaf(x[u][e], kb[e], dk);
-            }
+          for (int e = 0; e < V::VEC; ++e) {
+            ss = fmaf(x[e], x[e], ss);
+            dk = fmaf(x[e], kb[e], dk);
           }
-          ss = row_sum<V::LPR>(ss);
-          dk = row_sum<V::LPR>(dk);
-          if (r + u * step < r1) {
-            best = fmaxf(best, ss);
-            if (li == 0) {
-              qkbar[bh * q.S + r + u * step] = alpha * dk;
-              qsq[bh * q.S + r + u * step] = ss;  // per-row |q|^2, turned into the row's shift by shift_kernel
-            }
+        }
+        ss = row_sum<V::LPR>(ss);
+        dk = row_sum<V::LPR>(dk);
+        if (r + u * step < r1) {
+          best = fmaxf(best, ss);
+          if (li == 0) {
+            qkbar[bh * q.S + r + u * step] = alpha * dk;
+            qsq[bh * q.S + r + u * step] = ss;  // per-row |q|^2, turned into the row's shift by shift_kernel
           }
         }
       }
-      close_block(best, wmax, qmax_sq + bh * nqb + bx);
-      __syncthreads();  // wmax is reused by the next block
     }
-  } else if (kind == 1) {
-    // K-blocks: |k - kbar|^2 (kbar = 0 when not centering)
+  } else if (bx < nqb + nkb) {
+    // K rows: |k - kbar|^2 (kbar = 0 when not centering)
     float kb[V::VEC];
 #pragma unroll
     for (int e = 0; e < V::VEC; ++e) kb[e] = centering ? kbar[bh * D + li * V::VEC + e] : 0.f;
     const T *base = reinterpret_cast<const T *>(k.ptr) + b * k.sB + h * k.sH + li * V::VEC;
-    for (int64_t bx = i0; bx < nkb; bx += G) {
-      float best = 0.f;
-      const int64_t r0 = bx * kKVRows, r1 = min(k.S, r0 + kKVRows);
-      for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += kUnroll * step) {  // warp-uniform trip count
-        const int64_t r = rb + sub;
-        float x[kUnroll][V::VEC];
+    const int64_t r0 = (bx - nqb) * kKVRows, r1 = min(k.S, r0 + kKVRows);
+    for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += U * step) {  // warp-uniform trip count
+      const int64_t r = rb + sub;
+      uint4 raw[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-          if (r + u * step < r1) load16<T, V::VEC>(base + (r + u * step) * k.sS, x[u]);
+      for (int u = 0; u < U; ++u)
+        if (r + u * step < r1) raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + (r + u * step) * k.sS));
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u) {
-          float ss = 0.f;
-          if (r + u * step < r1) {
+      for (int u = 0; u < U; ++u) {
+        float ss = 0.f;
+        if (r + u * step < r1) {
+          float x[V::VEC];
+          unpack16<T, V::VEC>(raw[u], x);
 #pragma unroll
-            for (int e = 0; e < V::VEC; ++e) {
-              const float c = x[u][e] - kb[e];
-              ss = fmaf(c, c, ss);
-            }
-          }
-          ss = row_sum<V::LPR>(ss);
-          if (r + u * step < r1) {
-            best = fmaxf(best, ss);
-            if (n_sink > 0 && li == 0) knorm[r + u * step - r0] = ss;
+          for (int e = 0; e < V::VEC; ++e) {
+            const float c = x[e] - kb[e];
+            ss = fmaf(c, c, ss);
           }
         }
-      }
-      close_block(best, wmax, kblk + bh * nkb + bx);
-      if (n_sink > 0 && warp == 0) {
-        // this block's n_sink + 1 loudest keys, in sink order (its rows' norms are in knorm,
-        // written before the barrier in close_block)
-        const int cnt = (int)min((int64_t)kKVRows, k.S - r0);
-        SinkCand *out = cand + (bh * nkb + bx) * kCandPerBlock;
-        float pv = INFINITY;
-        int32_t pi = -1;
-        for (int t = 0; t <= n_sink; ++t) {
-          float bv = -1.f;
-          int32_t bi = INT_MAX;
-          for (int e = lane; e < cnt; e += 32) {
-            const float vv = knorm[e];
-            const int32_t i = (int32_t)(r0 + e);
-            if (sink_after(vv, i, pv, pi) && sink_before(vv, i, bv, bi)) {
-              bv = vv;
-              bi = i;
-            }
-          }
-          warp_best_sink(bv, bi);
-          if (lane == 0) out[t] = SinkCand{bv, bi};
-          pv = bv;
-          pi = bi;
+        ss = row_sum<V::LPR>(ss);
+        if (r + u * step < r1) {
+          best = fmaxf(best, ss);
+          if (n_sink > 0 && li == 0) knorm[r + u * step - r0] = ss;
         }
       }
-      __syncthreads();  // wmax and knorm are reused by the next block
     }
   } else {
-    // V-blocks: max element square
+    // V rows: max element square
     const T *base = reinterpret_cast<const T *>(v.ptr) + b * v.sB + h * v.sH + li * V::VEC;
-    for (int64_t bx = i0; bx < nkb; bx += G) {
-      float best = 0.f;
-      const int64_t r0 = bx * kKVRows, r1 = min(v.S, r0 + kKVRows);
-      for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += kUnroll * step) {
-        const int64_t r = rb + sub;
-        float x[kUnroll][V::VEC];
+    const int64_t r0 = (bx - nqb - nkb) * kKVRows, r1 = min(v.S, r0 + kKVRows);
+    for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += U * step) {
+      const int64_t r = rb + sub;
+      uint4 raw[U];
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-          if (r + u * step < r1) load16<T, V::VEC>(base + (r + u * step) * v.sS, x[u]);
+      for (int u = 0; u < U; ++u)
+        if (r + u * step < r1) raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + (r + u * step) * v.sS));
 #pragma unroll
-        for (int u = 0; u < kUnroll; ++u)
-          if (r + u * step < r1) {
+      for (int u = 0; u < U; ++u)
+        if (r + u * step < r1) {
+          float x[V::VEC];
+          unpack16<T, V::VEC>(raw[u], x);
 #pragma unroll
-            for (int e = 0; e < V::VEC; ++e) best = fmaxf(best, x[u][e] * x[u][e]);
-          }
+          for (int e = 0; e < V::VEC; ++e) best = fmaxf(best, x[e] * x[e]);
+        }
+    }
+  }
+  best = warp_max(best);
+  if (lane == 0) wmax[warp] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mx = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, wmax[w]);
+    if (bx < nqb) qmax_sq[bh * nqb + bx] = mx;
+    else if (bx < nqb + nkb) kblk[bh * nkb + (bx - nqb)] = mx;
+    else vblk[bh * nkb + (bx - nqb - nkb)] = mx;
+  }
+  if (n_sink > 0 && bx >= nqb && bx < nqb + nkb && warp == 0) {
+    // this block's n_sink + 1 loudest keys, in sink order (its rows' norms are in knorm,
+    // written before the barrier above)
+    const int64_t r0 = (bx - nqb) * kKVRows;
+    const int cnt = (int)min((int64_t)kKVRows, k.S - r0);
+    SinkCand *out = cand + (bh * nkb + (bx - nqb)) * kCandPerBlock;
+    float pv = INFINITY;
+    int32_t pi = -1;
+    for (int t = 0; t <= n_sink; ++t) {
+      float bv = -1.f;
+      int32_t bi = INT_MAX;
+      for (int e = lane; e < cnt; e += 32) {
+        const float vv = knorm[e];
+        const int32_t i = (int32_t)(r0 + e);
+        if (sink_after(vv, i, pv, pi) && sink_before(vv, i, bv, bi)) {
+          bv = vv;
+          bi = i;
+        }
       }
-      close_block(best, wmax, vblk + bh * nkb + bx);
-      __syncthreads();  // wmax is reused by the next block
+      warp_best_sink(bv, bi);
+      if (lane == 0) out[t] = SinkCand{bv, bi};
+      pv = bv;
+      pi = bi;
     }
   }
 }
@@ -929,17 +935,9 @@ cudaError_t launch_norms(const BoundsArgs &a, const WsLayout &w, float *kblk, fl
   const int64_t nx = a.nqb + 2 * w.nkb;
   if (nx == 0) return cudaSuccess;
   const dim3 grid((unsigned)nx, (unsigned)a.q.H, (unsigned)a.q.B);
-  if (CONTIG && rows16(a.q) && rows16(a.k) && rows16(a.v)) {
-    // about two waves of resident CTAs over all heads, a third of them per kind of block, each
-    // walking several blocks (and at most one CTA per block)
-    const int64_t heads = a.q.H * a.q.B;
-    int64_t per_kind = ceil_div(ceil_div((int64_t)current_device_sm_count() * kNormsCtasPerSm * 2, heads), 3);
-    const int64_t most = a.nqb > w.nkb ? a.nqb : w.nkb;
-    per_kind = per_kind < 1 ? 1 : (per_kind > most ? most : per_kind);
-    const dim3 g2((unsigned)(3 * per_kind), (unsigned)a.q.H, (unsigned)a.q.B);
-    return launch_pdl(norms_vec_kernel<T, 32 * EPL>, g2, dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb,
+  if (CONTIG && rows16(a.q) && rows16(a.k) && rows16(a.v))
+    return launch_pdl(norms_vec_kernel<T, 32 * EPL>, grid, dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb,
                       a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand);
-  }
   return launch_pdl(norms_kernel<T, EPL, CONTIG>, grid, dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb,
                     a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand);
 }

@@ -555,6 +555,9 @@ __device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, fl
   }
 }
 
+// kPersist: each CTA walks several work items (the persistent schedule); otherwise a CTA does one
+// item and the item loops below run once.
+template <bool kPersist>
 __global__ void __launch_bounds__(kThreads, 1)
     fm_chunk_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
   pdl_wait();  // bounds and accumulators written by the kernels before this one
@@ -569,9 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return base + (uint32_t)(kOffBar + 8 * i); };
   // this CTA's work items: one, or (persistent) every gridDim.x-th from blockIdx.x on.  Item
   // -> (b, h, Q-tile pair); consecutive items share a head and so its K/V tiles in L2.
-  const int64_t item0 = p.persistent ? (int64_t)blockIdx.x
-                                     : (int64_t)blockIdx.x + p.n_pairs * ((int64_t)blockIdx.y + (int64_t)p.H * blockIdx.z);
-  const int64_t item_step = p.persistent ? (int64_t)gridDim.x : p.n_items;
+  const int64_t item0 = kPersist ? (int64_t)blockIdx.x
+                                 : (int64_t)blockIdx.x + p.n_pairs * ((int64_t)blockIdx.y + (int64_t)p.H * blockIdx.z);
+  const int64_t item_step = kPersist ? (int64_t)gridDim.x : p.n_items;
   auto item_bh = [&](int64_t item) -> int64_t { return item / p.n_pairs; };
   auto item_qb0 = [&](int64_t item) -> int64_t { return 2 * (item % p.n_pairs); };
 
@@ -641,6 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (!kPersist) break;
       }
       if (!ok) {
         // let every copy already issued land before the CTA can exit
@@ -736,6 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(kBarODone + 1));
           }
         }
+        if (!kPersist) break;
       }
       if (!ok) {
         // every MMA issued so far must finish reading shared memory and TMEM before exit
@@ -850,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       //  - persistent: those regions already hold the next item's Q and K/V, so each row adds
       //    its O from registers with vector reductions (stores on the first chunk).
       bool plain_add = fixed || !p.accumulate;
-      if (!plain_add && (p.acc_tma || p.persistent) && !final_out)
+      if (!plain_add && (p.acc_tma || kPersist) && !final_out)
         plain_add = named_barrier_and(1 + t, 128, !row_ok || (shift_prev != -INFINITY && shv == shift_prev));
       if (p.acc_tma && plain_add && !final_out) {
         uint8_t *stage = gbase + (t == 0 ? kOffQ : kOffKV);
@@ -877,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.acc_sum[rflat] = sum_new;
           p.acc_max[rflat] = shift_new;
         }
-      } else if (p.persistent && plain_add && !final_out) {
+      } else if (kPersist && plain_add && !final_out) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -948,6 +953,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (final_out && p.lse) p.lse[rflat] = 0.69314718055994531f * (shift_new + log2f(sum_new));
       }
       }
+      if (!kPersist) break;
     }
   }
 
@@ -1079,7 +1085,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(fm_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(fm_chunk_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fm_chunk_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
@@ -1131,7 +1139,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   p.acc_tma = (!p.persistent && !a.out && a.q.B * a.q.H <= INT_MAX && encode_acc_map(&maps.acc, a.acc_o, a.q)) ? 1 : 0;
   const dim3 grid = p.persistent ? dim3((unsigned)(p.n_items < sms ? p.n_items : sms))
                                  : dim3((unsigned)p.n_pairs, (unsigned)a.q.H, (unsigned)a.q.B);
-  return launch_pdl(fm_chunk_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, maps, p);
+  return p.persistent ? launch_pdl(fm_chunk_tc_kernel<true>, grid, dim3(kThreads), kSmemBytes, st, maps, p)
+                      : launch_pdl(fm_chunk_tc_kernel<false>, grid, dim3(kThreads), kSmemBytes, st, maps, p);
 }
 
 cudaError_t launch_wait_probe(unsigned int *err, unsigned long long timeout_ns, cudaStream_t st) {
