@@ -347,7 +347,17 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
         te = max_over_ranks((time.perf_counter() - t0) * 1e3, dev)
         fm.fm_sync_status(stream)
+        # the machine's host link, for reading the figure: one 774 MB pinned copy each way, timed alone
+        link = {}
+        for name, (dst, src) in {"h2d_gbs": (q, qh), "d2h_gbs": (outs[0], fa.out)}.items():
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            dst.copy_(src, non_blocking=True)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            link[name] = src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
         e2e = {"value": whole_job_tflops(world, step_flops, args.e2e_steps, te), "unit": "TFLOP/s",
+               "host_link": {k2: round(v2, 1) for k2, v2 in link.items()},
                "h2d_bytes_per_step": int(3 * q.numel() * q.element_size()),
                "d2h_bytes_per_step": int(fa.out.numel() * fa.out.element_size()),
                "ms_per_step": te / args.e2e_steps, "steps": args.e2e_steps,

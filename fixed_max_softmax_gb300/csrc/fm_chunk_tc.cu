@@ -29,7 +29,8 @@
 // CTA = two 128-row Q tiles of one (batch, head) (256 rows) against every KV tile of the
 // launch: one chunk, or several consecutive chunks (up to 8), whose key tiles are walked in
 // order with each chunk's own tensor maps and ragged end, so that O and the row sums stay
-// on chip across the chunk boundaries.  12 warps:
+// on chip across the chunk boundaries.  (fm_chunk_tc_persistent_kernel is the same pipeline
+// with each CTA walking several such work items.)  12 warps:
 //   warp 0      TMA producer: Q tiles once, then K_j, V_j into a 5-stage ring
 //   warp 1      TMEM allocator; lane 0 issues every MMA and commit
 //   warps 4-7   softmax + epilogue of Q tile 0 (TMEM lanes 0-127)
@@ -69,8 +70,8 @@ constexpr float kLazyRescale = 8.0f;          // online path: rescale when the m
 constexpr int kOffQ = 0;
 constexpr int kOffKV = 2 * kTileBytes;
 constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-constexpr int kBarQFull = 0;
-constexpr int kBarKVFull = 1;
+constexpr int kBarQFull = 0;  // + t: Q tile t has landed
+constexpr int kBarKVFull = 2;
 constexpr int kBarKVEmpty = kBarKVFull + kStages;
 constexpr int kBarSFull = kBarKVEmpty + kStages;
 constexpr int kBarPReady = kBarSFull + 2;
@@ -555,9 +556,8 @@ __device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, fl
   }
 }
 
-// kPersist: each CTA walks several work items (the persistent schedule); otherwise a CTA does one
-// item and the item loops below run once.
-template <bool kPersist>
+// One CTA per work item (grid (pairs, H, B)): the schedule every launch takes unless the
+// persistent one is asked for.
 __global__ void __launch_bounds__(kThreads, 1)
     fm_chunk_tc_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
   pdl_wait();  // bounds and accumulators written by the kernels before this one
@@ -569,18 +569,358 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffAbort);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffTmemSlot);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z, h = blockIdx.y;
+  const int64_t qb0 = 2 * (int64_t)blockIdx.x;
   auto bar = [&](int i) -> uint32_t { return base + (uint32_t)(kOffBar + 8 * i); };
-  // this CTA's work items: one, or (persistent) every gridDim.x-th from blockIdx.x on.  Item
-  // -> (b, h, Q-tile pair); consecutive items share a head and so its K/V tiles in L2.
-  const int64_t item0 = kPersist ? (int64_t)blockIdx.x
-                                 : (int64_t)blockIdx.x + p.n_pairs * ((int64_t)blockIdx.y + (int64_t)p.H * blockIdx.z);
-  const int64_t item_step = kPersist ? (int64_t)gridDim.x : p.n_items;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(bar(kBarQFull + 0), 1);
+    mbar_init(bar(kBarQFull + 1), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarKVFull + s), 1);
+      mbar_init(bar(kBarKVEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(kBarSFull + t), 1);
+      mbar_init(bar(kBarPReady + t), 128);
+      mbar_init(bar(kBarODone + t), 1);
+    }
+    mbar_init(bar(kBarDrain), 1);
+    fence_mbar_init();
+    int32_t *ssk = reinterpret_cast<int32_t *>(gbase + kOffSinks);
+    for (int t = 0; t < FM_MAX_SINKS; ++t)
+      ssk[t] = p.sinks ? p.sinks[((int64_t)b * p.H + h) * FM_MAX_SINKS + t] : INT_MAX;
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_kv = p.n_kv;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int last_round[kStages];
+      for (int s = 0; s < kStages; ++s) last_round[s] = -1;
+      // one barrier per Q tile, so that S0 can start before tile 1 has landed
+      for (int t = 0; t < 2; ++t) {
+        mbar_expect_tx(bar(kBarQFull + t), 2 * kPanelBytes);
+        for (int pn = 0; pn < 2; ++pn)
+          tma_load_4d(base + kOffQ + t * kTileBytes + pn * kPanelBytes, &maps.q, bar(kBarQFull + t), pn * 64,
+                      (int)((qb0 + t) * kBQ), h, b);
+      }
+      bool ok = true;
+      int c = 0;  // chunk of key tile j
+      for (int j = 0; j < n_kv && ok; ++j) {
+        while (j >= p.tile0[c + 1]) ++c;
+        const int jl = j - p.tile0[c];  // tile within its chunk
+        for (int w = 0; w < 2 && ok; ++w) {
+          const int idx = 2 * j + w, s = idx % kStages, round = idx / kStages;
+          ok = wait_phase(bar(kBarKVEmpty + s), (uint32_t)((round & 1) ^ 1), abort_flag, p.timeout_ns, p.err,
+                          kDevErrTimeoutProducer, wtag(kBarKVEmpty + s, j));
+          if (!ok) break;
+          mbar_expect_tx(bar(kBarKVFull + s), kTileBytes);
+          const CUtensorMap *tm = w ? &maps.v[c] : &maps.k[c];
+          for (int pn = 0; pn < 2; ++pn)
+            tma_load_4d(base + kOffKV + s * kTileBytes + pn * kPanelBytes, tm, bar(kBarKVFull + s), pn * 64,
+                        jl * kBK, h, b);
+          last_round[s] = round;
+        }
+      }
+      if (!ok) {
+        // let every copy already issued land before the CTA can exit
+        for (int t = 0; t < 2; ++t)
+          wait_phase(bar(kBarQFull + t), 0, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain, wtag(kBarQFull + t, 0));
+        for (int s = 0; s < kStages; ++s)
+          if (last_round[s] >= 0)
+            wait_phase(bar(kBarKVFull + s), (uint32_t)(last_round[s] & 1), nullptr, p.timeout_ns, p.err,
+                       kDevErrTimeoutDrain, wtag(kBarKVFull + s, 0));
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t tS0 = tmem + 0, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+      auto q_desc = [&](int t, int kk) {
+        return smem_desc(base + kOffQ + t * kTileBytes + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
+      };
+      auto k_desc = [&](int s, int kk) {
+        return smem_desc(base + kOffKV + s * kTileBytes + (kk >> 2) * kPanelBytes + (kk & 3) * 32, 16, 1024);
+      };
+      auto v_desc = [&](int s, int kk) {
+        return smem_desc(base + kOffKV + s * kTileBytes + kk * 2048, kPanelBytes, 1024);
+      };
+      bool ok = wait_phase(bar(kBarQFull + 0), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma,
+                           wtag(kBarQFull + 0, 0));
+      int vs_prev = 0;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int ki = 2 * j, ks = ki % kStages;
+        ok = wait_phase(bar(kBarKVFull + ks), (uint32_t)((ki / kStages) & 1), abort_flag, p.timeout_ns, p.err,
+                        kDevErrTimeoutMma, wtag(kBarKVFull + ks, j));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tS0, q_desc(0, kk), k_desc(ks, kk), kIdescQK, kk > 0);
+        mma_commit(bar(kBarSFull + 0));
+        if (j > 0) {
+          ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((j - 1) & 1), abort_flag, p.timeout_ns, p.err,
+                          kDevErrTimeoutMma, wtag(kBarPReady + 1, j));
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tO1, tS1 + kk * 8, v_desc(vs_prev, kk), kIdescPV, (j - 1 > 0 || kk > 0));
+          mma_commit(bar(kBarKVEmpty + vs_prev));
+        }
+        if (j == 0) {  // Q tile 1 may land after tile 0
+          ok = wait_phase(bar(kBarQFull + 1), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma,
+                          wtag(kBarQFull + 1, 0));
+          if (!ok) break;
+          tc_fence_after();
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tS1, q_desc(1, kk), k_desc(ks, kk), kIdescQK, kk > 0);
+        mma_commit(bar(kBarSFull + 1));
+        mma_commit(bar(kBarKVEmpty + ks));
+        const int vi = 2 * j + 1, vs = vi % kStages;
+        ok = wait_phase(bar(kBarKVFull + vs), (uint32_t)((vi / kStages) & 1), abort_flag, p.timeout_ns, p.err,
+                        kDevErrTimeoutMma, wtag(kBarKVFull + vs, j)) &&
+             wait_phase(bar(kBarPReady + 0), (uint32_t)(j & 1), abort_flag, p.timeout_ns, p.err,
+                        kDevErrTimeoutMma, wtag(kBarPReady + 0, j));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ts(tO0, tS0 + kk * 8, v_desc(vs, kk), kIdescPV, (j > 0 || kk > 0));
+        if (j == n_kv - 1) mma_commit(bar(kBarODone + 0));
+        vs_prev = vs;
+      }
+      if (ok) {
+        ok = wait_phase(bar(kBarPReady + 1), (uint32_t)((n_kv - 1) & 1), abort_flag, p.timeout_ns, p.err,
+                        kDevErrTimeoutMma, wtag(kBarPReady + 1, n_kv));
+        if (ok) {
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tO1, tS1 + kk * 8, v_desc(vs_prev, kk), kIdescPV, (n_kv - 1 > 0 || kk > 0));
+          mma_commit(bar(kBarKVEmpty + vs_prev));
+          mma_commit(bar(kBarODone + 1));
+        }
+      }
+      if (!ok) {
+        // every MMA issued so far must finish reading shared memory and TMEM before exit
+        mma_commit(bar(kBarDrain));
+        wait_phase(bar(kBarDrain), 0, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain, wtag(kBarDrain, 0));
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax groups
+    const int t = (warp - 4) >> 2;   // Q tile of this group
+    const int wq = warp & 3;         // TMEM lane quarter of this warp
+    const int r = wq * 32 + lane;    // row within the tile
+    const int64_t qb = qb0 + t;
+    const bool tile_ok = qb < p.nqb;
+    const int64_t row = qb * kBQ + r;
+    const bool row_ok = tile_ok && row < p.Sq;
+    const int64_t bh = (int64_t)b * p.H + h;
+    const bool fixed = !tile_ok || (!p.force_online && p.flag[bh * p.nqb + qb] != 0);
+    // the row's shift: fixed-m rows subtract b_i from fm_bounds; online rows their running
+    // max (one register serves both, the kernel is at its register limit)
+    float shv = -INFINITY;
+    if (fixed) shv = row_ok ? p.shift[bh * p.Sq + row] : 0.f;
+    // an online row that adds into earlier chunks starts from their shift: as long as this
+    // chunk's scores stay within 2^8 of it, O comes out at the accumulator's own shift and the
+    // merge is a plain add
+    else if (p.accumulate && row_ok) shv = p.acc_max[bh * p.Sq + row];
+    const float shift_prev = shv;
+    // the earlier chunks' row sum, loaded now so that its memory latency hides behind the tiles
+    const float sum_prev = (p.accumulate && row_ok) ? p.acc_sum[bh * p.Sq + row] : 0.f;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (uint32_t)(t * 128);
+    const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(t * 128);
+    float l[4] = {0.f, 0.f, 0.f, 0.f};
+    // key sinks of this head (ascending global key indices, INT_MAX pads): columns to drop
+    int next_sink = sink_after_key(reinterpret_cast<const int32_t *>(gbase + kOffSinks), INT_MIN);
+    bool ok = true;
+    int c = 0;  // chunk of key tile j
+    for (int j = 0; j < n_kv; ++j) {
+      while (j >= p.tile0[c + 1]) ++c;
+      ok = wait_phase(bar(kBarSFull + t), (uint32_t)(j & 1), abort_flag, p.timeout_ns, p.err,
+                      kDevErrTimeoutSoftmax, wtag(kBarSFull + t, j));
+      ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
+      if (!ok) break;
+      tc_fence_after();
+      const int jl = (j - p.tile0[c]) * kBK;  // first key of the tile within its chunk
+      const int nvalid = min(kBK, p.len[c] - jl);  // ragged end of each chunk
+      const int g0 = p.key0[c] + jl;               // global index of the tile's first key
+      if (next_sink < g0)  // sinks before this tile
+        next_sink = sink_after_key(reinterpret_cast<const int32_t *>(gbase + kOffSinks), g0 - 1);
+      // -inf over the key sinks in this tile and over the columns past the chunk's end
+      if (next_sink < g0 + nvalid || nvalid < kBK)
+        mask_tile(tS, nvalid, g0, reinterpret_cast<const int32_t *>(gbase + kOffSinks), next_sink);
+      if (fixed) softmax_fixed_tile(tS, p.alpha, -shv, l);
+      else softmax_online_tile(tS, tO, p.alpha, j > 0, shv, l);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(kBarPReady + t));
+    }
+    if (ok) {
+      ok = wait_phase(bar(kBarODone + t), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutSoftmax,
+                      wtag(kBarODone + t, n_kv));
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float lsum = (l[0] + l[1]) + (l[2] + l[3]);
+      const int64_t rflat = bh * p.Sq + row;
+      float cprev = 0.f, cnew = 1.f, nr = shv;
+      if (!fixed && row_ok && p.accumulate) {
+        const float R = shift_prev;  // the previous chunks' shift (acc_max)
+        nr = fmaxf(R, shv);
+        cprev = (R == -INFINITY) ? 0.f : exp2f(R - nr);
+        cnew = (shv == -INFINITY) ? 0.f : exp2f(shv - nr);
+      }
+      // the row's sum and shift after this chunk
+      float sum_new = lsum;
+      if (row_ok && p.accumulate) sum_new = fixed ? sum_prev + lsum : fmaf(sum_prev, cprev, lsum * cnew);
+      const float shift_new = nr;  // b_i on fixed-m rows
+      const bool final_out = p.out != nullptr;
+      // with the normalise fused in, o = acc / max(sum, 1e-37) goes straight to `out`
+      // ("Kernel reference: ring_attention_const_max_fwd": the last ring step folds and
+      // normalises); acc_o itself is then not written back
+      const float inv = final_out ? 1.0f / fmaxf(sum_new, FM_SUM_CLAMP) : 1.0f;
+      const int64_t hh = bh % p.H, bb = bh / p.H;
+      const int64_t ooff = bb * p.osB + hh * p.osH + row * p.osS;
+      const float4 *src = reinterpret_cast<const float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
+      float4 *dst = reinterpret_cast<float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
+      // A chunk that is not the last, on a tile whose O needs no rescale of the accumulator
+      // (fixed-m; any tile of a first chunk, whose O is simply stored; an online tile whose
+      // every row kept the accumulator's shift, so that cprev = cnew = 1): O goes through
+      // shared memory, and one bulk tensor operation per 32 columns adds it into acc_o (or
+      // stores it there) in the memory system, so the SM never reads the accumulator.  The
+      // staging tile (64 KiB of 128-byte-swizzled 32-column boxes) is the Q region for tile 0,
+      // free once the last S MMA is done, which the O-done commit covers, and the first two
+      // K/V stages for tile 1, free once every MMA is done.
+      bool plain_add = fixed || !p.accumulate;
+      if (!plain_add && p.acc_tma && !final_out)
+        plain_add = named_barrier_and(1 + t, 128, !row_ok || (shift_prev != -INFINITY && shv == shift_prev));
+      if (p.acc_tma && plain_add && !final_out) {
+        uint8_t *stage = gbase + (t == 0 ? kOffQ : kOffKV);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          uint8_t *line = stage + c * (kBQ * 128) + r * 128;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            *reinterpret_cast<uint4 *>(line + ((q4 ^ (r & 7)) << 4)) =
+                make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+        }
+        fence_proxy_async_smem();
+        named_barrier(1 + t, 128);
+        if (wq == 0 && lane == 0 && tile_ok) {
+          const uint32_t sbase = base + (t == 0 ? kOffQ : kOffKV);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            tma_acc_3d(&maps.acc, sbase + c * (kBQ * 128), c * 32, (int)(qb * kBQ), (int)bh, p.accumulate != 0);
+          bulk_commit_and_wait_smem_read();
+        }
+        if (row_ok) {
+          p.acc_sum[rflat] = sum_new;
+          p.acc_max[rflat] = shift_new;
+        }
+      } else {
+      // the accumulator row comes in 32-column pieces, each loaded while the previous piece is
+      // combined, so that the row pays one memory latency instead of four
+      const bool rd = row_ok && p.accumulate;
+      float4 ya[8], yb[8];
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4) ya[q4] = rd ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float4(&ycur)[8] = (c & 1) ? yb : ya;
+        float4(&ynext)[8] = (c & 1) ? ya : yb;
+        if (c < 3) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) ynext[q4] = rd ? src[(c + 1) * 8 + q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        if (row_ok) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float4 x = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
+                                   __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
+            if (p.accumulate) {
+              const float4 y = ycur[q4];
+              if (fixed) {
+                x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
+              } else {
+                x.x = fmaf(y.x, cprev, x.x * cnew); x.y = fmaf(y.y, cprev, x.y * cnew);
+                x.z = fmaf(y.z, cprev, x.z * cnew); x.w = fmaf(y.w, cprev, x.w * cnew);
+              }
+            }
+            if (!final_out) {
+              dst[c * 8 + q4] = x;
+            } else if (p.out_bf16) {
+              uint2 u;
+              u.x = pack_bf16(x.x * inv, x.y * inv);
+              u.y = pack_bf16(x.z * inv, x.w * inv);
+              *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + ooff + c * 32 + q4 * 4) = u;
+            } else {
+              *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + ooff + c * 32 + q4 * 4) =
+                  make_float4(x.x * inv, x.y * inv, x.z * inv, x.w * inv);
+            }
+          }
+        }
+      }
+      if (row_ok) {
+        p.acc_sum[rflat] = sum_new;
+        p.acc_max[rflat] = shift_new;
+        if (final_out && p.lse) p.lse[rflat] = 0.69314718055994531f * (shift_new + log2f(sum_new));
+      }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// The persistent schedule (fm_opts.schedule = FM_SCHEDULE_PERSISTENT): one CTA per SM walks work
+// items blockIdx.x, blockIdx.x + gridDim.x, ...; barrier phases and the K/V ring position carry
+// over from item to item, and a Q-empty commit after an item's last S MMA lets the producer load
+// the next item's Q while the softmax warps run the epilogue.  The accumulator add comes from
+// registers (vector reductions), since the next item's Q and K/V already occupy the shared
+// memory the staged epilogue would use.
+__global__ void __launch_bounds__(kThreads, 1)
+    fm_chunk_tc_persistent_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
+  pdl_wait();  // bounds and accumulators written by the kernels before this one
+  pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t *gbase = smem_raw + (base - raw);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(gbase + kOffAbort);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(gbase + kOffTmemSlot);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) -> uint32_t { return base + (uint32_t)(kOffBar + 8 * i); };
+  // this CTA's work items: every gridDim.x-th from blockIdx.x on.  Item -> (b, h, Q-tile pair);
+  // consecutive items share a head and so its K/V tiles in L2.
+  const int64_t item0 = blockIdx.x;
+  const int64_t item_step = gridDim.x;
   auto item_bh = [&](int64_t item) -> int64_t { return item / p.n_pairs; };
   auto item_qb0 = [&](int64_t item) -> int64_t { return 2 * (item % p.n_pairs); };
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    mbar_init(bar(kBarQFull), 1);
+    mbar_init(bar(kBarQFull + 0), 1);
+    mbar_init(bar(kBarQFull + 1), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarKVFull + s), 1);
       mbar_init(bar(kBarKVEmpty + s), 1);
@@ -618,11 +958,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = wait_phase(bar(kBarQEmpty), (q_loads - 1) & 1u, abort_flag, p.timeout_ns, p.err,
                           kDevErrTimeoutProducer, wtag(kBarQEmpty, 0));
         if (!ok) break;
-        mbar_expect_tx(bar(kBarQFull), 4 * kPanelBytes);
-        for (int t = 0; t < 2; ++t)
+        // one barrier per Q tile, so that S0 can start before tile 1 has landed
+        for (int t = 0; t < 2; ++t) {
+          mbar_expect_tx(bar(kBarQFull + t), 2 * kPanelBytes);
           for (int pn = 0; pn < 2; ++pn)
-            tma_load_4d(base + kOffQ + t * kTileBytes + pn * kPanelBytes, &maps.q, bar(kBarQFull), pn * 64,
+            tma_load_4d(base + kOffQ + t * kTileBytes + pn * kPanelBytes, &maps.q, bar(kBarQFull + t), pn * 64,
                         (int)((qb0 + t) * kBQ), h, b);
+        }
         ++q_loads;
         int c = 0;  // chunk of key tile j
         for (int j = 0; j < n_kv && ok; ++j) {
@@ -644,13 +986,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (!kPersist) break;
       }
       if (!ok) {
         // let every copy already issued land before the CTA can exit
-        if (q_loads > 0)
-          wait_phase(bar(kBarQFull), (q_loads - 1) & 1u, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain,
-                     wtag(kBarQFull, 0));
+        for (int t = 0; t < 2 && q_loads > 0; ++t)
+          wait_phase(bar(kBarQFull + t), (q_loads - 1) & 1u, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain,
+                     wtag(kBarQFull + t, 0));
         for (int s = 0; s < kStages; ++s)
           if (last_phase[s] >= 0)
             wait_phase(bar(kBarKVFull + s), (uint32_t)last_phase[s], nullptr, p.timeout_ns, p.err,
@@ -679,8 +1020,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // MMAs of one CTA run in issue order, so S(j) of this item may overwrite the S/P
         // columns that the previous item's last PV MMAs read; O is overwritten only by PV(0),
         // issued after the softmax group's P-ready arrival, which follows its epilogue reads.
-        ok = wait_phase(bar(kBarQFull), k & 1u, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma,
-                        wtag(kBarQFull, 0));
+        ok = wait_phase(bar(kBarQFull + 0), k & 1u, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma,
+                        wtag(kBarQFull + 0, 0));
         int vs_prev = 0;
         for (int j = 0; j < n_kv && ok; ++j, ++tix) {
           const int ks = st;
@@ -705,6 +1046,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < 8; ++kk)
               mma_ts(tO1, tS1 + kk * 8, v_desc(vs_prev, kk), kIdescPV, (j - 1 > 0 || kk > 0));
             mma_commit(bar(kBarKVEmpty + vs_prev));
+          }
+          if (j == 0) {  // Q tile 1 may land after tile 0
+            ok = wait_phase(bar(kBarQFull + 1), k & 1u, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutMma,
+                            wtag(kBarQFull + 1, 0));
+            if (!ok) break;
+            tc_fence_after();
           }
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) mma_ss(tS1, q_desc(1, kk), k_desc(ks, kk), kIdescQK, kk > 0);
@@ -740,7 +1087,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(kBarODone + 1));
           }
         }
-        if (!kPersist) break;
       }
       if (!ok) {
         // every MMA issued so far must finish reading shared memory and TMEM before exit
@@ -846,43 +1192,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A chunk that is not the last, on a tile whose O needs no rescale of the accumulator
       // (fixed-m; any tile of a first chunk, whose O is simply stored; an online tile whose
       // every row kept the accumulator's shift, so that cprev = cnew = 1), adds O into acc_o
-      // (or stores it there) without reading the accumulator through the SM:
-      //  - one CTA per item: O goes through shared memory, and one bulk tensor operation per
-      //    32 columns does it in the memory system.  The staging tile (64 KiB of
-      //    128-byte-swizzled 32-column boxes) is the Q region for tile 0, free once the last S
-      //    MMA is done, which the O-done commit covers, and the first two K/V stages for tile
-      //    1, free once every MMA is done.
-      //  - persistent: those regions already hold the next item's Q and K/V, so each row adds
-      //    its O from registers with vector reductions (stores on the first chunk).
+      // (or stores it there) from registers with vector reductions, without reading the
+      // accumulator through the SM.
       bool plain_add = fixed || !p.accumulate;
-      if (!plain_add && (p.acc_tma || kPersist) && !final_out)
+      if (!plain_add && !final_out)
         plain_add = named_barrier_and(1 + t, 128, !row_ok || (shift_prev != -INFINITY && shv == shift_prev));
-      if (p.acc_tma && plain_add && !final_out) {
-        uint8_t *stage = gbase + (t == 0 ? kOffQ : kOffKV);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          uint8_t *line = stage + c * (kBQ * 128) + r * 128;
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            *reinterpret_cast<uint4 *>(line + ((q4 ^ (r & 7)) << 4)) =
-                make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
-        }
-        fence_proxy_async_smem();
-        named_barrier(1 + t, 128);
-        if (wq == 0 && lane == 0 && tile_ok) {
-          const uint32_t sbase = base + (t == 0 ? kOffQ : kOffKV);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tma_acc_3d(&maps.acc, sbase + c * (kBQ * 128), c * 32, (int)(qb * kBQ), (int)bh, p.accumulate != 0);
-          bulk_commit_and_wait_smem_read();
-        }
-        if (row_ok) {
-          p.acc_sum[rflat] = sum_new;
-          p.acc_max[rflat] = shift_new;
-        }
-      } else if (kPersist && plain_add && !final_out) {
+      if (plain_add && !final_out) {
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -953,7 +1268,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (final_out && p.lse) p.lse[rflat] = 0.69314718055994531f * (shift_new + log2f(sum_new));
       }
       }
-      if (!kPersist) break;
     }
   }
 
@@ -1085,9 +1399,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-    e = cudaFuncSetAttribute(fm_chunk_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(fm_chunk_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fm_chunk_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      e = cudaFuncSetAttribute(fm_chunk_tc_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
@@ -1139,8 +1453,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   p.acc_tma = (!p.persistent && !a.out && a.q.B * a.q.H <= INT_MAX && encode_acc_map(&maps.acc, a.acc_o, a.q)) ? 1 : 0;
   const dim3 grid = p.persistent ? dim3((unsigned)(p.n_items < sms ? p.n_items : sms))
                                  : dim3((unsigned)p.n_pairs, (unsigned)a.q.H, (unsigned)a.q.B);
-  return p.persistent ? launch_pdl(fm_chunk_tc_kernel<true>, grid, dim3(kThreads), kSmemBytes, st, maps, p)
-                      : launch_pdl(fm_chunk_tc_kernel<false>, grid, dim3(kThreads), kSmemBytes, st, maps, p);
+  return p.persistent ? launch_pdl(fm_chunk_tc_persistent_kernel, grid, dim3(kThreads), kSmemBytes, st, maps, p)
+                      : launch_pdl(fm_chunk_tc_kernel, grid, dim3(kThreads), kSmemBytes, st, maps, p);
 }
 
 cudaError_t launch_wait_probe(unsigned int *err, unsigned long long timeout_ns, cudaStream_t st) {
