@@ -372,10 +372,14 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// 3'. The norms pass with 16-byte loads: the same blocks and outputs as norms_kernel, one block per
-// CTA.  Each lane keeps kRawLoads 16-byte loads in flight as raw words and converts them only
-// when it uses them, so that many loads stay in flight for few registers.
-constexpr int kRawLoads = 8;
+// 3'. The norms pass with 16-byte loads: the same outputs as norms_kernel, for rows that start on
+// 16-byte boundaries.  A CTA streams kBlocksPerCta consecutive blocks of one kind (Q-blocks of
+// 128 rows, K- or V-blocks of 256): one pass of the CTA covers at most 128 rows (8 warps x RPW
+// rows x up to kRawLoads loads per lane), and the next pass's loads are issued before the current
+// pass is reduced, so the loads never drain at a block boundary.  Each thread keeps one maximum
+// per block; the CTA reduces them once at the end.
+constexpr int kRawLoads = 8;  // most 16-byte loads per lane and pass
+constexpr int kBlocksPerCta = 4;
 template <typename T, int VEC>
 __device__ __forceinline__ void unpack16(const uint4 &u, float (&x)[VEC]) {
   if constexpr (sizeof(T) == 2) {
@@ -394,6 +398,15 @@ __device__ __forceinline__ void unpack16(const uint4 &u, float (&x)[VEC]) {
   }
 }
 
+// One pass of a CTA: rows rb + sub + u*step (u < kRawLoads) that lie below r1.
+template <typename T, int U>
+__device__ __forceinline__ void load_pass(const T *base, int64_t sS, int64_t r, int64_t step, int64_t r1,
+                                          uint4 (&raw)[U]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u)
+    if (r + u * step < r1) raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + (r + u * step) * sS));
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
     norms_vec_kernel(View q, View k, View v, int64_t nqb, int64_t nkb, int centering, float alpha,
@@ -402,136 +415,130 @@ __global__ void __launch_bounds__(kThreads)
   pdl_wait();  // inputs written by the kernels before this one
   pdl_trigger();
   using V = Vec16<T, D>;
-  constexpr int U = kRawLoads;
+  constexpr int U = kRawLoads * kWarps * V::RPW <= 128 ? kRawLoads : 128 / (kWarps * V::RPW);
+  constexpr int kPass = kWarps * V::RPW * U;  // rows one pass covers (64 or 128)
+  static_assert(kQRows % kPass == 0 && kKVRows % kPass == 0, "a pass stays inside one block");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int sub = lane / V::LPR, li = lane % V::LPR;
-  const int64_t b = blockIdx.z, h = blockIdx.y, bx = blockIdx.x;
+  const int64_t b = blockIdx.z, h = blockIdx.y;
   const int64_t bh = b * q.H + h;
   const int64_t step = (int64_t)kWarps * V::RPW;
-  __shared__ float wmax[kWarps];
-  __shared__ float knorm[kKVRows];  // key blocks with sinks: each row's squared norm
+  const int64_t nq4 = ceil_div(nqb, kBlocksPerCta), nk4 = ceil_div(nkb, kBlocksPerCta);
+  const int64_t cx = blockIdx.x;
+  const int kind = cx < nq4 ? 0 : (cx < nq4 + nk4 ? 1 : 2);  // Q, K or V blocks
+  const int64_t blk0 = (kind == 0 ? cx : (kind == 1 ? cx - nq4 : cx - nq4 - nk4)) * kBlocksPerCta;
+  const int64_t rows_per_blk = kind == 0 ? kQRows : kKVRows;
+  const View &t = kind == 0 ? q : (kind == 1 ? k : v);
+  const int64_t n_blk = kind == 0 ? nqb : nkb;
+  const int nb = (int)min((int64_t)kBlocksPerCta, n_blk - blk0);  // blocks of this CTA
+  const int64_t r0 = blk0 * rows_per_blk, r1 = min(t.S, r0 + nb * rows_per_blk);
+  __shared__ float wmax[kBlocksPerCta][kWarps];
+  __shared__ float knorm[kBlocksPerCta * kKVRows];  // key blocks with sinks: each row's squared norm
 
-  float best = 0.f;  // maxima of non-negative quantities start at 0
-  if (bx < nqb) {
-    // Q-block: per-row |q|^2 and alpha * q.kbar
-    float kb[V::VEC];
+  float kb[V::VEC];
 #pragma unroll
-    for (int e = 0; e < V::VEC; ++e) kb[e] = centering ? kbar[bh * D + li * V::VEC + e] : 0.f;
-    const T *base = reinterpret_cast<const T *>(q.ptr) + b * q.sB + h * q.sH + li * V::VEC;
-    const int64_t r0 = bx * kQRows, r1 = min(q.S, r0 + kQRows);
-    for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += U * step) {  // warp-uniform trip count
-      const int64_t r = rb + sub;
-      uint4 raw[U];
+  for (int e = 0; e < V::VEC; ++e) kb[e] = (centering && kind < 2) ? kbar[bh * D + li * V::VEC + e] : 0.f;
+  float best[kBlocksPerCta];
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (r + u * step < r1) raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + (r + u * step) * q.sS));
+  for (int i = 0; i < kBlocksPerCta; ++i) best[i] = 0.f;  // maxima of non-negative quantities start at 0
+  const T *base = reinterpret_cast<const T *>(t.ptr) + b * t.sB + h * t.sH + li * V::VEC;
+  const int n_pass = (int)ceil_div(r1 - r0, (int64_t)kPass);
+  const int pass_per_blk = (int)(rows_per_blk / kPass);
+
+  // one pass: the rows' norms (Q: |q|^2 and alpha*q.kbar per row; K: |k - kbar|^2; V: max v^2)
+  auto reduce_pass = [&](const uint4 (&raw)[U], int pass) {
+    const int64_t r = r0 + (int64_t)pass * kPass + warp * V::RPW + sub;
+    const int bi = pass / pass_per_blk;
+    float bm = 0.f;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float ss = 0.f, dk = 0.f;
-        if (r + u * step < r1) {
-          float x[V::VEC];
-          unpack16<T, V::VEC>(raw[u], x);
+    for (int u = 0; u < U; ++u) {
+      const bool ok = r + u * step < r1;
+      float x[V::VEC];
+      unpack16<T, V::VEC>(raw[u], x);
+      if (kind == 2) {
+        if (ok) {
 #pragma unroll
-          for (int e = 0; e < V::VEC; ++e) {
-            ss = fmaf(x[e], x[e], ss);
-            dk = fmaf(x[e], kb[e], dk);
-          }
+          for (int e = 0; e < V::VEC; ++e) bm = fmaxf(bm, x[e] * x[e]);
         }
-        ss = row_sum<V::LPR>(ss);
-        dk = row_sum<V::LPR>(dk);
-        if (r + u * step < r1) {
-          best = fmaxf(best, ss);
-          if (li == 0) {
-            qkbar[bh * q.S + r + u * step] = alpha * dk;
-            qsq[bh * q.S + r + u * step] = ss;  // per-row |q|^2, turned into the row's shift by shift_kernel
-          }
+        continue;
+      }
+      float ss = 0.f, dk = 0.f;
+      if (ok) {
+#pragma unroll
+        for (int e = 0; e < V::VEC; ++e) {
+          const float c = x[e] - (kind == 1 ? kb[e] : 0.f);
+          ss = fmaf(c, c, ss);
+          dk = fmaf(x[e], kb[e], dk);
         }
       }
-    }
-  } else if (bx < nqb + nkb) {
-    // K rows: |k - kbar|^2 (kbar = 0 when not centering)
-    float kb[V::VEC];
-#pragma unroll
-    for (int e = 0; e < V::VEC; ++e) kb[e] = centering ? kbar[bh * D + li * V::VEC + e] : 0.f;
-    const T *base = reinterpret_cast<const T *>(k.ptr) + b * k.sB + h * k.sH + li * V::VEC;
-    const int64_t r0 = (bx - nqb) * kKVRows, r1 = min(k.S, r0 + kKVRows);
-    for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += U * step) {  // warp-uniform trip count
-      const int64_t r = rb + sub;
-      uint4 raw[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (r + u * step < r1) raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + (r + u * step) * k.sS));
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float ss = 0.f;
-        if (r + u * step < r1) {
-          float x[V::VEC];
-          unpack16<T, V::VEC>(raw[u], x);
-#pragma unroll
-          for (int e = 0; e < V::VEC; ++e) {
-            const float c = x[e] - kb[e];
-            ss = fmaf(c, c, ss);
-          }
+      ss = row_sum<V::LPR>(ss);
+      if (kind == 0) dk = row_sum<V::LPR>(dk);
+      if (ok) {
+        bm = fmaxf(bm, ss);
+        const int64_t row = r + u * step;
+        if (kind == 0 && li == 0) {
+          qkbar[bh * q.S + row] = alpha * dk;
+          qsq[bh * q.S + row] = ss;  // per-row |q|^2, turned into the row's shift by shift_kernel
         }
-        ss = row_sum<V::LPR>(ss);
-        if (r + u * step < r1) {
-          best = fmaxf(best, ss);
-          if (n_sink > 0 && li == 0) knorm[r + u * step - r0] = ss;
-        }
+        if (kind == 1 && n_sink > 0 && li == 0) knorm[row - r0] = ss;
       }
     }
-  } else {
-    // V rows: max element square
-    const T *base = reinterpret_cast<const T *>(v.ptr) + b * v.sB + h * v.sH + li * V::VEC;
-    const int64_t r0 = (bx - nqb - nkb) * kKVRows, r1 = min(v.S, r0 + kKVRows);
-    for (int64_t rb = r0 + warp * V::RPW; rb < r1; rb += U * step) {
-      const int64_t r = rb + sub;
-      uint4 raw[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (r + u * step < r1) raw[u] = __ldg(reinterpret_cast<const uint4 *>(base + (r + u * step) * v.sS));
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (r + u * step < r1) {
-          float x[V::VEC];
-          unpack16<T, V::VEC>(raw[u], x);
-#pragma unroll
-          for (int e = 0; e < V::VEC; ++e) best = fmaxf(best, x[e] * x[e]);
-        }
+    for (int i = 0; i < kBlocksPerCta; ++i)
+      if (i == bi) best[i] = fmaxf(best[i], bm);
+  };
+
+  // passes two at a time, the next pass's loads in flight while the current one is reduced
+  uint4 ra[U], rb2[U];
+  const int64_t rw = r0 + warp * V::RPW + sub;
+  if (n_pass > 0) load_pass<T, U>(base, t.sS, rw, step, r1, ra);
+  for (int pass = 0; pass < n_pass; pass += 2) {
+    if (pass + 1 < n_pass) load_pass<T, U>(base, t.sS, rw + (int64_t)(pass + 1) * kPass, step, r1, rb2);
+    reduce_pass(ra, pass);
+    if (pass + 1 < n_pass) {
+      if (pass + 2 < n_pass) load_pass<T, U>(base, t.sS, rw + (int64_t)(pass + 2) * kPass, step, r1, ra);
+      reduce_pass(rb2, pass + 1);
     }
   }
-  best = warp_max(best);
-  if (lane == 0) wmax[warp] = best;
+  // the block maxima over the CTA, once
+#pragma unroll
+  for (int i = 0; i < kBlocksPerCta; ++i) {
+    const float m = warp_max(best[i]);
+    if (lane == 0) wmax[i][warp] = m;
+  }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < nb) {
+    const int i = threadIdx.x;
     float mx = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, wmax[w]);
-    if (bx < nqb) qmax_sq[bh * nqb + bx] = mx;
-    else if (bx < nqb + nkb) kblk[bh * nkb + (bx - nqb)] = mx;
-    else vblk[bh * nkb + (bx - nqb - nkb)] = mx;
+    for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, wmax[i][w]);
+    const int64_t blk = blk0 + i;
+    if (kind == 0) qmax_sq[bh * nqb + blk] = mx;
+    else if (kind == 1) kblk[bh * nkb + blk] = mx;
+    else vblk[bh * nkb + blk] = mx;
   }
-  if (n_sink > 0 && bx >= nqb && bx < nqb + nkb && warp == 0) {
-    // this block's n_sink + 1 loudest keys, in sink order (its rows' norms are in knorm,
-    // written before the barrier above)
-    const int64_t r0 = (bx - nqb) * kKVRows;
-    const int cnt = (int)min((int64_t)kKVRows, k.S - r0);
-    SinkCand *out = cand + (bh * nkb + (bx - nqb)) * kCandPerBlock;
+  if (n_sink > 0 && kind == 1 && warp < nb) {
+    // key block blk0 + warp: its n_sink + 1 loudest keys, in sink order (its rows' norms are in
+    // knorm, written before the barrier above)
+    const int64_t blk = blk0 + warp;
+    const int64_t kr0 = blk * kKVRows;
+    const int cnt = (int)min((int64_t)kKVRows, k.S - kr0);
+    SinkCand *out = cand + (bh * nkb + blk) * kCandPerBlock;
     float pv = INFINITY;
     int32_t pi = -1;
-    for (int t = 0; t <= n_sink; ++t) {
+    for (int tt = 0; tt <= n_sink; ++tt) {
       float bv = -1.f;
       int32_t bi = INT_MAX;
       for (int e = lane; e < cnt; e += 32) {
-        const float vv = knorm[e];
-        const int32_t i = (int32_t)(r0 + e);
+        const float vv = knorm[warp * kKVRows + e];
+        const int32_t i = (int32_t)(kr0 + e);
         if (sink_after(vv, i, pv, pi) && sink_before(vv, i, bv, bi)) {
           bv = vv;
           bi = i;
         }
       }
       warp_best_sink(bv, bi);
-      if (lane == 0) out[t] = SinkCand{bv, bi};
+      if (lane == 0) out[tt] = SinkCand{bv, bi};
       pv = bv;
       pi = bi;
     }
@@ -935,9 +942,12 @@ cudaError_t launch_norms(const BoundsArgs &a, const WsLayout &w, float *kblk, fl
   const int64_t nx = a.nqb + 2 * w.nkb;
   if (nx == 0) return cudaSuccess;
   const dim3 grid((unsigned)nx, (unsigned)a.q.H, (unsigned)a.q.B);
-  if (CONTIG && rows16(a.q) && rows16(a.k) && rows16(a.v))
-    return launch_pdl(norms_vec_kernel<T, 32 * EPL>, grid, dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb,
-                      a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand);
+  if (CONTIG && rows16(a.q) && rows16(a.k) && rows16(a.v)) {
+    const int64_t nx4 = ceil_div(a.nqb, kBlocksPerCta) + 2 * ceil_div(w.nkb, kBlocksPerCta);
+    return launch_pdl(norms_vec_kernel<T, 32 * EPL>, dim3((unsigned)nx4, (unsigned)a.q.H, (unsigned)a.q.B),
+                      dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar,
+                      a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand);
+  }
   return launch_pdl(norms_kernel<T, EPL, CONTIG>, grid, dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb,
                     a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand);
 }

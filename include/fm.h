@@ -211,12 +211,14 @@ FM_API int fm_bounds(const fm_tensor *q, const fm_tensor *k_full, const fm_tenso
  *            row's sum of 2^z.
  *   accumulate  0: overwrite the accumulators (first chunk); 1: add into them
  * Key sinks (bounds->n_sink > 0): a key whose global index is in bounds->sink_idx adds
- * nothing here.  The global index of a chunk's first key is the number of keys folded
- * before it (bounds->kv_seen), so the chunks must come in the key order fm_bounds saw.
+ * nothing here.  The global index of a chunk's first key is bounds->next_key_offset when the
+ * caller set it (chunks in any order, e.g. a ring's rotated order), else the number of keys
+ * folded before it (bounds->kv_seen: chunks in the key order fm_bounds saw).
  * Errors: FM_ERR_BOUNDS_MISMATCH when bounds->magic is wrong, the bounds' shape is
  * not [B, H, ceil(Sq/128)], bounds->centered != opts->centering (raw-key bounds must
  * never pair with centered logits: [PR477] "matched pair"), the softmax scale
- * differs, more keys arrive than bounds->N_total, force_online changes within a call,
+ * differs, more keys arrive than bounds->N_total (or, at the chunk's offset, lie past it),
+ * force_online changes within a call,
  * opts->sink_keys differs from bounds->n_sink, or the sinks were already folded in
  * (accumulate = 1 after fm_fold_sinks); plus the errors of fm_bounds. */
 FM_API int fm_attn_chunk(const fm_tensor *q, const fm_tensor *k_chunk, const fm_tensor *v_chunk,
