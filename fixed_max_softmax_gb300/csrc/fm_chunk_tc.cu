@@ -491,18 +491,25 @@ __device__ __forceinline__ void softmax_fixed_tile(uint32_t tS, float alpha, flo
   l[3] += y1;
 }
 
+// max(a, b, c) in one instruction (the three-input form of max.f32; a NaN operand is ignored,
+// as fmaxf does).
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 // The max of 64 scores in four independent chains (one chain would put every max
-// operation on the tile's critical path).
+// operation on the tile's critical path), two new scores per instruction.
 __device__ __forceinline__ float max64(const uint32_t (&a)[32], const uint32_t (&b)[32], float mx) {
   float m0 = mx, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    m0 = fmaxf(m0, __uint_as_float(a[e]));
-    m1 = fmaxf(m1, __uint_as_float(a[e + 1]));
-    m2 = fmaxf(m2, __uint_as_float(b[e]));
-    m3 = fmaxf(m3, __uint_as_float(b[e + 1]));
+  for (int e = 0; e < 32; e += 4) {
+    m0 = max3f(m0, __uint_as_float(a[e]), __uint_as_float(a[e + 2]));
+    m1 = max3f(m1, __uint_as_float(a[e + 1]), __uint_as_float(a[e + 3]));
+    m2 = max3f(m2, __uint_as_float(b[e]), __uint_as_float(b[e + 2]));
+    m3 = max3f(m3, __uint_as_float(b[e + 1]), __uint_as_float(b[e + 3]));
   }
-  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+  return max3f(m0, m1, fmaxf(m2, m3));
 }
 
 // Online softmax of one S tile for this thread's row, in two passes over TMEM: the first
