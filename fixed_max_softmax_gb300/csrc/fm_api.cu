@@ -231,6 +231,8 @@ int setup_bounds(const fm_tensor *q, const fm_tensor *k, const fm_tensor *v, con
   a->q = vq;
   a->k = vk;
   a->v = vv;
+  a->err = dev_error_ptr();
+  a->timeout_ns = wait_timeout_ns();
   a->centering = centering;
   a->per_row = per_row;
   a->alpha = alpha;

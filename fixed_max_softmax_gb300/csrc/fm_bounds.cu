@@ -398,6 +398,45 @@ __device__ __forceinline__ void unpack16(const uint4 &u, float (&x)[VEC]) {
   }
 }
 
+// fp32x2 arithmetic: two floats in one 64-bit register, one instruction for both (sm_100 on).
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_sum(uint64_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+// One lane's part of a row's sums over its VEC consecutive elements: ss = sum (x - kb)^2
+// (CENTER) or sum x^2, and dk = sum x*kb (DOT).  Two fp32x2 chains (the even and the odd
+// elements) are added at the end; the kernels whose outputs must agree bit for bit all sum
+// this way.
+template <int VEC, bool CENTER, bool DOT>
+__device__ __forceinline__ void lane_sums(const float (&x)[VEC], const float (&kb)[VEC], float &ss, float &dk) {
+  uint64_t s2 = 0, d2 = 0;  // (+0, +0)
+#pragma unroll
+  for (int e = 0; e < VEC; e += 2) {
+    const uint64_t x2 = f2(x[e], x[e + 1]);
+    const uint64_t c2 = CENTER ? f2_add(x2, f2(-kb[e], -kb[e + 1])) : x2;  // x + (-kb) is x - kb
+    s2 = f2_fma(c2, c2, s2);
+    if (DOT) d2 = f2_fma(x2, f2(kb[e], kb[e + 1]), d2);
+  }
+  ss = f2_sum(s2);
+  if (DOT) dk = f2_sum(d2);
+}
+
 // One pass of a CTA: rows rb + sub + u*step (u < kRawLoads) that lie below r1.
 template <typename T, int U>
 __device__ __forceinline__ void load_pass(const T *base, int64_t sS, int64_t r, int64_t step, int64_t r1,
@@ -464,12 +503,8 @@ __global__ void __launch_bounds__(kThreads)
       }
       float ss = 0.f, dk = 0.f;
       if (ok) {
-#pragma unroll
-        for (int e = 0; e < V::VEC; ++e) {
-          const float c = x[e] - (kind == 1 ? kb[e] : 0.f);
-          ss = fmaf(c, c, ss);
-          dk = fmaf(x[e], kb[e], dk);
-        }
+        if (kind == 0) lane_sums<V::VEC, false, true>(x, kb, ss, dk);
+        else lane_sums<V::VEC, true, false>(x, kb, ss, dk);
       }
       ss = row_sum<V::LPR>(ss);
       if (kind == 0) dk = row_sum<V::LPR>(dk);
@@ -541,6 +576,398 @@ __global__ void __launch_bounds__(kThreads)
       if (lane == 0) out[tt] = SinkCand{bv, bi};
       pv = bv;
       pi = bi;
+    }
+  }
+}
+
+// 3''. The norms pass staged through shared memory by bulk copies, for bf16 rows of D = 128 that
+// lie back to back (unit D stride, row stride D, 16-byte aligned).
+//
+// One CTA per SM takes a contiguous run of the blocks of every head -- Q-blocks of 128 rows,
+// then K-blocks and V-blocks of 256, runs cut by bytes so that every CTA streams about as much.
+// One producer lane copies the run's rows into a ring of 32 KiB shared-memory stages
+// (cp.async.bulk, one copy per 128 rows, completion counted in bytes on the stage's mbarrier);
+// the copies run ahead of the arithmetic by the whole ring.  Each of the kNbWarps consumer warps
+// takes 8 rows of every stage (16 lanes a row, 8 elements a lane), moves them to registers and
+// releases the stage at once.  Per pair of rows the four rows' sums (|q|^2 and q.kbar, or
+// |k - kbar|^2) are reduced over their 16 lanes together: at each of the four shuffle levels a
+// lane keeps half of its remaining sums and sends the other half, so four rows take 5 shuffles
+// instead of 16.  The pairs added at each level are the ones of norms_vec_kernel's row_sum, so
+// the sums are the same bits.  V needs only max v^2: the max of |v| is taken on the bf16 values
+// widened by a shift or a mask (no conversion), and squared once at the end -- the same value,
+// since squaring is monotonic, and a NaN is skipped as fmaxf skips it.  The block's
+// maximum over the warps goes through a shared-memory slot; the last warp to finish a block
+// (an atomic count) writes its results, and with key sinks picks its candidates, while the
+// others go on.  Eight slots: a warp can run at most kNbStages blocks ahead of the slowest.
+// Every wait is bounded in time; on expiry the kernel records the failure in the device error
+// word and every role stops at its next wait (the producer after its own copies have landed).
+constexpr int kNbWarps = 16;                     // consumer warps
+constexpr int kNbThreads = 32 * (kNbWarps + 1);  // + the producer warp
+constexpr int kNbStages = 6;
+constexpr int kNbSlots = 8;  // > kNbStages
+constexpr int kNbTileRows = 128;
+constexpr int kNbRowBytes = 128 * 2;  // D = 128 bf16
+constexpr int kNbTileBytes = kNbTileRows * kNbRowBytes;
+constexpr int kNbRowsPerWarp = kNbTileRows / kNbWarps;       // rows of a stage per consumer warp
+constexpr int kNbGroups = kNbRowsPerWarp / 8;                 // groups of four row pairs
+constexpr int kNbOffBar = kNbStages * kNbTileBytes;          // full[s], then empty[s]
+constexpr int kNbOffMax = kNbOffBar + 2 * kNbStages * 8;     // [kNbSlots] block maxima (fp32 bits)
+constexpr int kNbOffCnt = kNbOffMax + kNbSlots * 4;          // [kNbSlots] warps done with the block
+constexpr int kNbOffKnorm = kNbOffCnt + kNbSlots * 4;        // [kNbSlots][kKVRows] key norms (sinks)
+constexpr int kNbOffAbort = kNbOffKnorm + kNbSlots * kKVRows * 4;
+constexpr int kNbSmem = kNbOffAbort + 16 + 128;  // + slack to align the base to 128 bytes
+static_assert(kNbRowsPerWarp % 8 == 0, "each consumer warp reduces whole groups of 4 row pairs per stage");
+static_assert(kNbSlots > kNbStages && (kNbSlots & (kNbSlots - 1)) == 0, "slots outnumber the stages");
+
+__device__ __forceinline__ uint32_t nb_smem(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ bool nb_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Poll until the phase of `bar` with parity `parity` completes (true), the time limit passes,
+// or -- when `abort_flag` is given -- another role of the CTA has given up (false).  The first
+// wait of the launch to run out records itself: role code, tag, block, thread.
+__device__ __noinline__ bool nb_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned long long timeout_ns, unsigned int *err, unsigned int tag) {
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (uint32_t it = 1;; ++it) {
+    if (nb_try(bar, parity)) return true;
+    if ((it & 31) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      uint64_t t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      if (t - t0 > timeout_ns) {
+        if (abort_flag) *abort_flag = 1;
+        if (err && atomicCAS(err, 0u, kDevErrTimeoutBounds) == 0u) {
+          err[1] = tag;
+          err[2] = blockIdx.x;
+          err[3] = blockIdx.y;
+          err[4] = blockIdx.z;
+          err[5] = threadIdx.x;
+        }
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool nb_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                        unsigned long long timeout_ns, unsigned int *err, unsigned int tag) {
+  if (nb_try(bar, parity)) return true;
+  return nb_wait_slow(bar, parity, abort_flag, timeout_ns, err, tag);
+}
+// Sums over the 16 lanes of a row for four rows at once: v[u] is this lane's part of row u's sum;
+// the result is the whole sum of row li >> 2 (li = lane % 16).  Level by level the pairs added
+// are those of row_sum<16> (lane ^ 8, ^ 4, ^ 2, ^ 1), so each row's sum has the same bits.
+__device__ __forceinline__ float row_sums4(const float (&v)[4], int li) {
+  const bool b3 = (li & 8) != 0, b2 = (li & 4) != 0;
+  const float r0 = __shfl_xor_sync(0xffffffffu, b3 ? v[0] : v[2], 8);
+  const float r1 = __shfl_xor_sync(0xffffffffu, b3 ? v[1] : v[3], 8);
+  const float a0 = (b3 ? v[2] : v[0]) + r0;  // row 2*b3
+  const float a1 = (b3 ? v[3] : v[1]) + r1;  // row 2*b3 + 1
+  const float r = __shfl_xor_sync(0xffffffffu, b2 ? a0 : a1, 4);
+  float c = (b2 ? a1 : a0) + r;  // row 2*b3 + b2
+  c += __shfl_xor_sync(0xffffffffu, c, 2);
+  c += __shfl_xor_sync(0xffffffffu, c, 1);
+  return c;
+}
+// max(m, |lo|, |hi|) of the two bf16 values of a word (lo in the low half), NaNs skipped.
+__device__ __forceinline__ float max_abs_bf16x2(float m, uint32_t w) {
+  m = fmaxf(m, fabsf(__uint_as_float(w << 16)));
+  return fmaxf(m, fabsf(__uint_as_float(w & 0xffff0000u)));
+}
+
+__global__ void __launch_bounds__(kNbThreads, 1)
+    norms_bulk_kernel(View q, View k, View v, int64_t nqb, int64_t nkb, int centering, float alpha,
+                      const float *kbar, float *qmax_sq, float *qkbar, float *qsq, float *kblk, float *vblk,
+                      int n_sink, SinkCand *cand, unsigned int *err, unsigned long long timeout_ns) {
+  pdl_wait();  // inputs written by the kernels before this one
+  pdl_trigger();
+  extern __shared__ uint8_t nb_raw[];
+  const uint32_t raw = nb_smem(nb_raw);
+  const uint32_t base = (raw + 127u) & ~127u;
+  uint8_t *g = nb_raw + (base - raw);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(g + kNbOffAbort);
+  int *smax = reinterpret_cast<int *>(g + kNbOffMax);
+  unsigned int *scnt = reinterpret_cast<unsigned int *>(g + kNbOffCnt);
+  float *knorm = reinterpret_cast<float *>(g + kNbOffKnorm);
+  auto full = [&](int s) -> uint32_t { return base + (uint32_t)(kNbOffBar + 8 * s); };
+  auto empty = [&](int s) -> uint32_t { return base + (uint32_t)(kNbOffBar + 8 * (kNbStages + s)); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t BH = q.B * q.H;
+  const int64_t nQ = BH * nqb, nK = BH * nkb, n_items = nQ + 2 * nK;
+  // This CTA's blocks: an even share of each kind (a contiguous run of the Q-blocks, of the
+  // K-blocks and of the V-blocks), since the kinds cost different arithmetic per byte.  Items are
+  // numbered Q-blocks, then K-blocks, then V-blocks; seg_range gives run `seg` as [a, e).
+  const int64_t G = gridDim.x, c = blockIdx.x;
+  auto seg_range = [&](int seg, int64_t &a, int64_t &e) {
+    const int64_t n = seg == 0 ? nQ : nK, off = seg == 0 ? 0 : (seg == 1 ? nQ : nQ + nK);
+    a = off + c * n / G;
+    e = off + (c + 1) * n / G;
+  };
+  // The run's items in order: kind (0 Q, 1 K, 2 V), batch, head, block.  One division finds the
+  // first; every next one is a step of the cursor (a division per item would cost about as many
+  // instructions as a Q-block's arithmetic).
+  struct Cursor {
+    int kind;
+    int64_t b, h, blk;
+  };
+  auto first_cursor = [&](int64_t i) -> Cursor {
+    Cursor c{3, 0, 0, 0};
+    if (i >= n_items) return c;  // an empty run (and no division by an empty kind's count)
+    int64_t j = i, nb = nqb;
+    c.kind = 0;
+    if (i >= nQ) {
+      c.kind = i < nQ + nK ? 1 : 2;
+      j = i < nQ + nK ? i - nQ : i - nQ - nK;
+      nb = nkb;
+    }
+    const int64_t bh = j / nb;
+    c.blk = j - bh * nb;
+    c.b = bh / q.H;
+    c.h = bh - c.b * q.H;
+    return c;
+  };
+  auto step = [&](Cursor &c) {
+    if (++c.blk < (c.kind == 0 ? nqb : nkb)) return;
+    c.blk = 0;
+    if (++c.h < q.H) return;
+    c.h = 0;
+    if (++c.b < q.B) return;
+    c.b = 0;
+    ++c.kind;
+  };
+  // rows [r0, r1) of the cursor's block
+  auto rows_of = [&](const Cursor &c, int64_t &r0, int64_t &r1) {
+    if (c.kind == 0) {
+      r0 = c.blk * kQRows;
+      r1 = min(q.S, r0 + kQRows);
+    } else {
+      r0 = c.blk * kKVRows;
+      r1 = min(k.S, r0 + kKVRows);
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < kNbStages; ++s) {
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full(s)), "r"(1) : "memory");
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empty(s)), "r"(kNbWarps) : "memory");
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (threadIdx.x < kNbSlots) {
+    smax[threadIdx.x] = 0;  // +0.0f: maxima of non-negative quantities start at 0
+    scnt[threadIdx.x] = 0;
+  }
+  __syncthreads();
+
+  if (warp == kNbWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int last[kNbStages];  // phase of the last copy issued into each stage, -1: none
+      for (int s = 0; s < kNbStages; ++s) last[s] = -1;
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int seg = 0; seg < 3 && ok; ++seg) {
+        int64_t i_begin, i_end;
+        seg_range(seg, i_begin, i_end);
+        Cursor cur = first_cursor(i_begin);
+        for (int64_t i = i_begin; i < i_end && ok; ++i, step(cur)) {
+          const int kind = cur.kind;
+          int64_t r0, r1;
+          rows_of(cur, r0, r1);
+          // the fields of q, k or v picked one by one (a reference to one of the three would put
+          // the kernel parameters on the stack)
+          const void *ptr = kind == 0 ? q.ptr : (kind == 1 ? k.ptr : v.ptr);
+          const int64_t sB = kind == 0 ? q.sB : (kind == 1 ? k.sB : v.sB);
+          const int64_t sH = kind == 0 ? q.sH : (kind == 1 ? k.sH : v.sH);
+          const int64_t sS = kind == 0 ? q.sS : (kind == 1 ? k.sS : v.sS);
+          const char *src = reinterpret_cast<const char *>(ptr) +
+                            (cur.b * sB + cur.h * sH + r0 * sS) * (int64_t)sizeof(__nv_bfloat16);
+          for (int64_t r = r0; r < r1; r += kNbTileRows) {
+            ok = nb_wait(empty(s), ph ^ 1u, abort_flag, timeout_ns, err, (uint32_t)(kNbStages + s) << 16);
+            if (!ok) break;
+            const uint32_t bytes = (uint32_t)min((int64_t)kNbTileRows, r1 - r) * kNbRowBytes;
+            asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full(s)), "r"(bytes)
+                         : "memory");
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                    base + (uint32_t)(s * kNbTileBytes)),
+                "l"(src + (r - r0) * kNbRowBytes), "r"(bytes), "r"(full(s))
+                : "memory");
+            last[s] = (int)ph;
+            if (++s == kNbStages) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        // let every copy already issued land before the CTA can exit
+        for (int st = 0; st < kNbStages; ++st)
+          if (last[st] >= 0) nb_wait(full(st), (uint32_t)last[st], nullptr, timeout_ns, err, (uint32_t)st << 16);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int sub = lane >> 4, li = lane & 15;  // row of the pair, 8 elements of it
+  const int my_u = li >> 2;                   // the pair whose reduced sums this lane ends with
+  const bool writer = (li & 3) == 0;          // one lane per row writes the row's outputs
+  int s = 0;
+  uint32_t ph = 0;
+  int64_t kb_head = -1;
+  float kb[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) kb[e] = 0.f;
+  int n_done = 0;  // items of this CTA so far: the slot of an item is n_done % kNbSlots
+  for (int seg = 0; seg < 3; ++seg) {
+    int64_t i_begin, i_end;
+    seg_range(seg, i_begin, i_end);
+    Cursor cur = first_cursor(i_begin);
+    for (int64_t i = i_begin; i < i_end; ++i, step(cur), ++n_done) {
+      const int kind = cur.kind;
+      const int64_t bh = cur.b * q.H + cur.h, blk = cur.blk;
+      int64_t r0, r1;
+      rows_of(cur, r0, r1);
+      const int slot = n_done & (kNbSlots - 1);
+      if (centering && kind < 2 && bh != kb_head) {
+        kb_head = bh;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) kb[e] = kbar[bh * 128 + li * 8 + e];
+      }
+      float bm = 0.f;    // Q, K: the largest row sum of this warp's rows
+      float vm = 0.f;    // V: the largest |v|
+      for (int64_t r = r0; r < r1; r += kNbTileRows) {
+        bool ok = nb_wait(full(s), ph, abort_flag, timeout_ns, err, (uint32_t)s << 16);
+        if (!__all_sync(0xffffffffu, ok)) return;  // every role stops: the error word says why
+        const uint8_t *rows = g + s * kNbTileBytes + (warp * kNbRowsPerWarp + sub) * kNbRowBytes + li * 16;
+        uint4 w[kNbGroups][4];
+#pragma unroll
+        for (int gi = 0; gi < kNbGroups; ++gi)
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            w[gi][u] = *reinterpret_cast<const uint4 *>(rows + (gi * 8 + u * 2) * kNbRowBytes);
+        // the rows are in registers: the stage may be refilled
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty(s)) : "memory");
+        if (++s == kNbStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+#pragma unroll
+        for (int gi = 0; gi < kNbGroups; ++gi) {
+          // this lane's row of pair u in group gi is row0 + 2u
+          const int64_t row0 = r + warp * kNbRowsPerWarp + gi * 8 + sub;
+          if (kind == 2) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (row0 + 2 * u < r1) {  // rows past a ragged end hold stale bytes
+                vm = max_abs_bf16x2(vm, w[gi][u].x);
+                vm = max_abs_bf16x2(vm, w[gi][u].y);
+                vm = max_abs_bf16x2(vm, w[gi][u].z);
+                vm = max_abs_bf16x2(vm, w[gi][u].w);
+              }
+            }
+            continue;
+          }
+          const int64_t row = row0 + 2 * my_u;  // the row whose sums this lane ends with
+          const bool valid = row < r1;
+          float ss[4];
+          if (kind == 0) {
+            float dk[4];  // |q|^2 and q.kbar
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              float x[8];
+              unpack16<__nv_bfloat16, 8>(w[gi][u], x);
+              lane_sums<8, false, true>(x, kb, ss[u], dk[u]);
+            }
+            const float rs = row_sums4(ss, li), rd = row_sums4(dk, li);
+            if (valid) {
+              bm = fmaxf(bm, rs);
+              if (writer) {
+                qkbar[bh * q.S + row] = alpha * rd;
+                qsq[bh * q.S + row] = rs;  // per-row |q|^2, turned into the row's shift by shift_kernel
+              }
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {  // |k - kbar|^2
+              float x[8], unused;
+              unpack16<__nv_bfloat16, 8>(w[gi][u], x);
+              lane_sums<8, true, false>(x, kb, ss[u], unused);
+            }
+            const float rs = row_sums4(ss, li);
+            if (valid) {
+              bm = fmaxf(bm, rs);
+              if (n_sink > 0 && writer) knorm[slot * kKVRows + (row - r0)] = rs;
+            }
+          }
+        }
+      }
+      if (kind == 2) {
+        bm = warp_max(vm * vm);
+      } else {  // the four lanes of a quad end with the same row's sums: three levels suffice
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+      }
+      // the block's maximum over the warps; the last warp to finish the block writes the results
+      unsigned int last = 0;
+      if (lane == 0) {
+        atomicMax(&smax[slot], __float_as_int(bm));  // non-negative floats order as their bits
+        __threadfence_block();
+        last = atomicAdd(&scnt[slot], 1u) == (unsigned)(kNbWarps - 1);
+      }
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (!last) continue;
+      __threadfence_block();
+      const float mx = __int_as_float(*reinterpret_cast<volatile int *>(&smax[slot]));
+      if (lane == 0) {
+        if (kind == 0) qmax_sq[bh * nqb + blk] = mx;
+        else if (kind == 1) kblk[bh * nkb + blk] = mx;
+        else vblk[bh * nkb + blk] = mx;
+      }
+      if (n_sink > 0 && kind == 1) {
+        // the block's n_sink + 1 loudest keys, in sink order
+        const volatile float *kn = knorm + slot * kKVRows;
+        const int cnt = (int)(r1 - r0);
+        SinkCand *out = cand + (bh * nkb + blk) * kCandPerBlock;
+        float pv = INFINITY;
+        int32_t pi = -1;
+        for (int tt = 0; tt <= n_sink; ++tt) {
+          float bv = -1.f;
+          int32_t bi = INT_MAX;
+          for (int e = lane; e < cnt; e += 32) {
+            const float vv = kn[e];
+            const int32_t ix = (int32_t)(r0 + e);
+            if (sink_after(vv, ix, pv, pi) && sink_before(vv, ix, bv, bi)) {
+              bv = vv;
+              bi = ix;
+            }
+          }
+          warp_best_sink(bv, bi);
+          if (lane == 0) out[tt] = SinkCand{bv, bi};
+          pv = bv;
+          pi = bi;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        smax[slot] = 0;
+        scnt[slot] = 0;
+      }
     }
   }
 }
@@ -936,11 +1363,34 @@ cudaError_t launch_ksum(const View &k, int64_t P, float *part, cudaStream_t st) 
   return launch_pdl(ksum_kernel<T, EPL, CONTIG>, grid, dim3(kThreads), 0, st, k, P, part);
 }
 
+// bf16 rows of D = 128 stored back to back within each head (the staged norms pass).
+bool bulk_rows(const View &t) { return t.dtype == FM_BF16 && t.D == 128 && t.sS == t.D && rows16(t); }
+
+cudaError_t launch_norms_bulk(const BoundsArgs &a, const WsLayout &w, float *kblk, float *vblk, SinkCand *cand,
+                              cudaStream_t st) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    e = cudaFuncSetAttribute(norms_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kNbSmem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const int64_t n_items = a.q.B * a.q.H * (a.nqb + 2 * w.nkb);
+  const int64_t grid = min(n_items, (int64_t)current_device_sm_count());
+  return launch_pdl(norms_bulk_kernel, dim3((unsigned)grid), dim3(kNbThreads), (size_t)kNbSmem, st, a.q, a.k, a.v,
+                    a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk,
+                    a.n_sink, cand, a.err, a.timeout_ns);
+}
+
 template <typename T, int EPL, bool CONTIG>
 cudaError_t launch_norms(const BoundsArgs &a, const WsLayout &w, float *kblk, float *vblk, SinkCand *cand,
                          cudaStream_t st) {
   const int64_t nx = a.nqb + 2 * w.nkb;
   if (nx == 0) return cudaSuccess;
+  if (CONTIG && sizeof(T) == 2 && EPL == 4 && bulk_rows(a.q) && bulk_rows(a.k) && bulk_rows(a.v))
+    return launch_norms_bulk(a, w, kblk, vblk, cand, st);
   const dim3 grid((unsigned)nx, (unsigned)a.q.H, (unsigned)a.q.B);
   if (CONTIG && rows16(a.q) && rows16(a.k) && rows16(a.v)) {
     const int64_t nx4 = ceil_div(a.nqb, kBlocksPerCta) + 2 * ceil_div(w.nkb, kBlocksPerCta);

@@ -741,8 +741,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // merge is a plain add
     else if (p.accumulate && row_ok) shv = p.acc_max[bh * p.Sq + row];
     const float shift_prev = shv;
-    // the earlier chunks' row sum, loaded now so that its memory latency hides behind the tiles
-    const float sum_prev = (p.accumulate && row_ok) ? p.acc_sum[bh * p.Sq + row] : 0.f;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)(t * 128);
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(t * 128);
@@ -750,27 +748,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     // key sinks of this head (ascending global key indices, INT_MAX pads): columns to drop
     int next_sink = sink_after_key(reinterpret_cast<const int32_t *>(gbase + kOffSinks), INT_MIN);
     bool ok = true;
-    int c = 0;  // chunk of key tile j
-    for (int j = 0; j < n_kv; ++j) {
-      while (j >= p.tile0[c + 1]) ++c;
-      ok = wait_phase(bar(kBarSFull + t), (uint32_t)(j & 1), abort_flag, p.timeout_ns, p.err,
-                      kDevErrTimeoutSoftmax, wtag(kBarSFull + t, j));
-      ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
-      if (!ok) break;
-      tc_fence_after();
-      const int jl = (j - p.tile0[c]) * kBK;  // first key of the tile within its chunk
-      const int nvalid = min(kBK, p.len[c] - jl);  // ragged end of each chunk
-      const int g0 = p.key0[c] + jl;               // global index of the tile's first key
-      if (next_sink < g0)  // sinks before this tile
-        next_sink = sink_after_key(reinterpret_cast<const int32_t *>(gbase + kOffSinks), g0 - 1);
-      // -inf over the key sinks in this tile and over the columns past the chunk's end
-      if (next_sink < g0 + nvalid || nvalid < kBK)
-        mask_tile(tS, nvalid, g0, reinterpret_cast<const int32_t *>(gbase + kOffSinks), next_sink);
-      if (fixed) softmax_fixed_tile(tS, p.alpha, -shv, l);
-      else softmax_online_tile(tS, tO, p.alpha, j > 0, shv, l);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(kBarPReady + t));
+    // the tile loop, instantiated once per kind of group (fixed-m or online), so that each copy
+    // keeps only its own values live across the tiles
+    auto tile_loop = [&](auto softmax_tile) {
+      int c = 0;  // chunk of key tile j
+      for (int j = 0; j < n_kv; ++j) {
+        while (j >= p.tile0[c + 1]) ++c;
+        ok = wait_phase(bar(kBarSFull + t), (uint32_t)(j & 1), abort_flag, p.timeout_ns, p.err,
+                        kDevErrTimeoutSoftmax, wtag(kBarSFull + t, j));
+        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld/st below are warp-collective
+        if (!ok) break;
+        tc_fence_after();
+        const int jl = (j - p.tile0[c]) * kBK;  // first key of the tile within its chunk
+        const int nvalid = min(kBK, p.len[c] - jl);  // ragged end of each chunk
+        const int g0 = p.key0[c] + jl;               // global index of the tile's first key
+        if (next_sink < g0)  // sinks before this tile
+          next_sink = sink_after_key(reinterpret_cast<const int32_t *>(gbase + kOffSinks), g0 - 1);
+        // -inf over the key sinks in this tile and over the columns past the chunk's end
+        if (next_sink < g0 + nvalid || nvalid < kBK)
+          mask_tile(tS, nvalid, g0, reinterpret_cast<const int32_t *>(gbase + kOffSinks), next_sink);
+        softmax_tile(j);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar(kBarPReady + t));
+      }
+    };
+    // the earlier chunks' row sum: a fixed-m group loads it before its tiles, so that the load's
+    // latency hides behind them; an online group after them (a register held across its tiles,
+    // which need more of them, slows the online tiles)
+    float sum_prev = 0.f;
+    if (fixed) {
+      if (p.accumulate && row_ok) sum_prev = p.acc_sum[bh * p.Sq + row];
+      tile_loop([&](int) { softmax_fixed_tile(tS, p.alpha, -shv, l); });
+    } else {
+      tile_loop([&](int j) { softmax_online_tile(tS, tO, p.alpha, j > 0, shv, l); });
+      if (ok && p.accumulate && row_ok) sum_prev = p.acc_sum[bh * p.Sq + row];
     }
     if (ok) {
       ok = wait_phase(bar(kBarODone + t), 0, abort_flag, p.timeout_ns, p.err, kDevErrTimeoutSoftmax,

@@ -19,6 +19,7 @@ enum : unsigned int {
   kDevErrTimeoutSoftmax = 3,
   kDevErrTimeoutDrain = 4,
   kDevErrTimeoutProbe = 5,
+  kDevErrTimeoutBounds = 6,
 };
 
 // Default limit of a pipeline wait inside a kernel.  One CTA of the chunk kernel runs
@@ -52,6 +53,8 @@ struct BoundsArgs {
   float *sink_v = nullptr;      // [B,H,FM_MAX_SINKS,D] their value rows
   void *ws;
   size_t ws_bytes;
+  unsigned int *err = nullptr;  // device error word (bounded waits of the staged norms pass)
+  unsigned long long timeout_ns = kWaitTimeoutNs;
 };
 size_t bounds_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t D);
 cudaError_t launch_bounds(const BoundsArgs &a, cudaStream_t st);
