@@ -396,9 +396,10 @@ struct TcParams {
 };
 
 // p = 2^(alpha*s - bias) for 32 scores of one full chunk, two at a time with fp32x2 FMA and
-// adds; the row sum goes to two pair accumulators, P to 16 bf16x2 words.
+// adds; the row sum goes to two pair accumulators, P to 16 bf16x2 words pk[OFF..OFF+16).
+template <int OFF, int NPK>
 __device__ __forceinline__ void exp_chunk_full(const uint32_t (&s)[32], uint64_t a2, uint64_t nb2, uint64_t &acc0,
-                                               uint64_t &acc1, uint32_t (&pk)[16]) {
+                                               uint64_t &acc1, uint32_t (&pk)[NPK]) {
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     float z0, z1;
@@ -406,7 +407,7 @@ __device__ __forceinline__ void exp_chunk_full(const uint32_t (&s)[32], uint64_t
     const float p0 = ex2(z0), p1 = ex2(z1);
     const uint64_t pp = f2_pack(__float_as_uint(p0), __float_as_uint(p1));
     if (e & 1) acc1 = f2_add(acc1, pp); else acc0 = f2_add(acc0, pp);
-    pk[e] = pack_bf16(p0, p1);
+    pk[OFF + e] = pack_bf16(p0, p1);
   }
 }
 
@@ -459,29 +460,44 @@ __device__ __noinline__ void mask_tile(uint32_t tS, int nvalid, int g0, const in
 
 // Fixed-m softmax of one 128x128 S tile for this thread's row; P overwrites S.  The four
 // 32-column TMEM loads are double-buffered: chunk c+1 is in flight while chunk c is
-// exponentiated.  Key columns to leave out hold -inf (mask_tile) and give p = 0.
+// exponentiated.  Key columns to leave out hold -inf (mask_tile) and give p = 0.  P leaves in
+// 16-column stores, one per chunk, or with WIDE (the fixed-m tile loop, which has the
+// registers) in one 32-column store per 64 keys: fewer TMEM stores, measured faster there.
+template <bool WIDE>
 __device__ __forceinline__ void softmax_fixed_tile(uint32_t tS, float alpha, float nbias, float (&l)[4]) {
+  constexpr int NPK = WIDE ? 32 : 16;
   uint32_t sa[32], sb[32];
-  uint32_t pk[16];
+  uint32_t pk[NPK];
   tmem_ld32_async(tS, sa);
   tmem_ld_wait(sa);
   const uint64_t a2 = f2_pack(__float_as_uint(alpha), __float_as_uint(alpha));
   const uint64_t nb2 = f2_pack(__float_as_uint(nbias), __float_as_uint(nbias));
   uint64_t acc0 = 0, acc1 = 0;  // +0.0f pairs
+  // P columns [16c, 16c+16) of chunk c lie in S columns already read
   tmem_ld32_async(tS + 32, sb);
-  exp_chunk_full(sa, a2, nb2, acc0, acc1, pk);
-  tmem_st16(tS + 0, pk);  // P columns [16c, 16c+16) lie in S columns already read
+  exp_chunk_full<0>(sa, a2, nb2, acc0, acc1, pk);
+  if constexpr (!WIDE) tmem_st16(tS + 0, pk);
   tmem_ld_wait(sb);
   tmem_ld32_async(tS + 64, sa);
-  exp_chunk_full(sb, a2, nb2, acc0, acc1, pk);
-  tmem_st16(tS + 16, pk);
+  if constexpr (WIDE) {
+    exp_chunk_full<16>(sb, a2, nb2, acc0, acc1, pk);
+    tmem_st32(tS + 0, pk);
+  } else {
+    exp_chunk_full<0>(sb, a2, nb2, acc0, acc1, pk);
+    tmem_st16(tS + 16, pk);
+  }
   tmem_ld_wait(sa);
   tmem_ld32_async(tS + 96, sb);
-  exp_chunk_full(sa, a2, nb2, acc0, acc1, pk);
-  tmem_st16(tS + 32, pk);
+  exp_chunk_full<0>(sa, a2, nb2, acc0, acc1, pk);
+  if constexpr (!WIDE) tmem_st16(tS + 32, pk);
   tmem_ld_wait(sb);
-  exp_chunk_full(sb, a2, nb2, acc0, acc1, pk);
-  tmem_st16(tS + 48, pk);
+  if constexpr (WIDE) {
+    exp_chunk_full<16>(sb, a2, nb2, acc0, acc1, pk);
+    tmem_st32(tS + 32, pk);
+  } else {
+    exp_chunk_full<0>(sb, a2, nb2, acc0, acc1, pk);
+    tmem_st16(tS + 48, pk);
+  }
   float x0, x1, y0, y1;
   f2_unpack(acc0, x0, x1);
   f2_unpack(acc1, y0, y1);
@@ -550,7 +566,7 @@ __device__ __forceinline__ void softmax_online_tile(uint32_t tS, uint32_t tO, fl
 #pragma unroll
     for (int i = 0; i < 4; ++i) l[i] *= sc;
   }
-  softmax_fixed_tile(tS, alpha, run == -INFINITY ? 0.f : -run, l);
+  softmax_fixed_tile<false>(tS, alpha, run == -INFINITY ? 0.f : -run, l);
   if (any && have_o) {
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -779,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float sum_prev = 0.f;
     if (fixed) {
       if (p.accumulate && row_ok) sum_prev = p.acc_sum[bh * p.Sq + row];
-      tile_loop([&](int) { softmax_fixed_tile(tS, p.alpha, -shv, l); });
+      tile_loop([&](int) { softmax_fixed_tile<true>(tS, p.alpha, -shv, l); });
     } else {
       tile_loop([&](int j) { softmax_online_tile(tS, tO, p.alpha, j > 0, shv, l); });
       if (ok && p.accumulate && row_ok) sum_prev = p.acc_sum[bh * p.Sq + row];
@@ -1172,7 +1188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           next_sink = sink_after_key(ssk, g0 - 1);
         // -inf over the key sinks in this tile and over the columns past the chunk's end
         if (next_sink < g0 + nvalid || nvalid < kBK) mask_tile(tS, nvalid, g0, ssk, next_sink);
-        if (fixed) softmax_fixed_tile(tS, p.alpha, -shv, l);
+        if (fixed) softmax_fixed_tile<false>(tS, p.alpha, -shv, l);
         else softmax_online_tile(tS, tO, p.alpha, j > 0, shv, l);
         tmem_st_wait();
         tc_fence_before();
