@@ -165,7 +165,14 @@ def cpu_oracle_sample(target_s: float = 12.0, max_rows: int = 24576):
             break
         rows = min(max_rows, max(rows * 2, int(rows * target_s / max(dt, 1e-3))))
     flops = w.flops(heads=1, rows=rows)
-    return flops / dt / 1e12, {"rows": rows, "seconds": dt, "threads": threads}
+    # the same on one core, on as many rows as that core's share of the sample
+    rows1 = max(16, rows // max(threads, 1))
+    t0 = time.perf_counter()
+    oracle.attention(q[0, :, :rows1], k[0], v[0], threads=1)
+    dt1 = time.perf_counter() - t0
+    one_core = w.flops(heads=1, rows=rows1) / dt1 / 1e12
+    return flops / dt / 1e12, {"rows": rows, "seconds": dt, "threads": threads, "one_core": one_core,
+                               "rows_one_core": rows1, "seconds_one_core": dt1}
 
 
 def run_reference(args, rank, world):
@@ -417,7 +424,10 @@ def run_ours(args, rank, world, local_rank):
         cv, info = cpu_oracle_sample(args.cpu_seconds)
         cpu = {"value": cv, "unit": "TFLOP/s", "cores": info["threads"], "kind": "oracle",
                "sample": f"1 head x {info['rows']} query rows x all {w.N} keys, fp64, "
-                         f"{info['seconds']:.1f} s"}
+                         f"{info['seconds']:.1f} s",
+               "value_one_core": info["one_core"],
+               "sample_one_core": f"1 head x {info['rows_one_core']} query rows x all {w.N} keys, "
+                                  f"{info['seconds_one_core']:.1f} s"}
     clocks = clk.summary()
     line = {
         "metric": METRIC if w.name == WORKLOAD else f"fixed-m attn fwd TFLOP/s ({w.name})",

@@ -101,12 +101,13 @@ int fmo_num_threads(void) {
 void fmo_attention(const double *q, const double *k, const double *v, int64_t G, int64_t R,
                    int64_t N, int64_t D, double scale, double *o, double *lse, int nthreads) {
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
+  /* a per-call team size: omp_set_num_threads would stay in force for later calls */
+  const int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
 #else
   (void)nthreads;
 #endif
   int64_t total = G * R;
-#pragma omp parallel
+#pragma omp parallel num_threads(nt)
   {
     double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
 #pragma omp for schedule(dynamic, 1)
@@ -171,13 +172,13 @@ void fmo_attention_bf16p(const double *q, const double *k, const double *v, int6
                          int64_t N, int64_t D, double scale, const double *shift, double *o,
                          int nthreads) {
 #ifdef _OPENMP
-  if (nthreads > 0) omp_set_num_threads(nthreads);
+  const int nt = nthreads > 0 ? nthreads : omp_get_max_threads();
 #else
   (void)nthreads;
 #endif
   const double alpha = scale * FMO_LOG2E;
   int64_t total = G * R;
-#pragma omp parallel
+#pragma omp parallel num_threads(nt)
   {
     double *z = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
 #pragma omp for schedule(dynamic, 1)
