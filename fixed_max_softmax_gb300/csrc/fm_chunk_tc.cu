@@ -78,13 +78,17 @@ constexpr int kBarPReady = kBarSFull + 2;
 constexpr int kBarODone = kBarPReady + 2;
 constexpr int kBarDrain = kBarODone + 2;
 constexpr int kBarQEmpty = kBarDrain + 1;  // every S MMA of an item has read Q
-constexpr int kBarQFree = kBarQEmpty + 1;  // + t: the persistent epilogue is done with Q tile t's space
-constexpr int kNumBars = kBarQFree + 2;
+constexpr int kNumBars = kBarQEmpty + 1;
 constexpr int kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 8;
 constexpr int kOffSinks = kOffAbort + 8;  // per softmax group: its item's key sinks (FM_MAX_SINKS int32)
 constexpr int kSmemUsed = kOffSinks + 2 * 4 * FM_MAX_SINKS;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for aligning the base
+// The persistent kernel's K/V ring has one stage fewer; the fifth stage's space holds each softmax
+// group's 16 KiB box of O on its way to the bulk reduce.
+constexpr int kPStages = kStages - 1;
+constexpr int kOffPStage = kOffKV + kPStages * kTileBytes;
+constexpr int kBoxBytes = kBQ * 128;  // 32 fp32 columns x 128 rows
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits 4-5 = 1),
 // A and B bf16 (bits 7-9 = 1, bits 10-12 = 1), A K-major, B K-major (bit 16 = 0) or
@@ -968,8 +972,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(kBarDrain), 1);
     mbar_init(bar(kBarQEmpty), 1);
-    mbar_init(bar(kBarQFree + 0), 1);
-    mbar_init(bar(kBarQFree + 1), 1);
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -986,7 +988,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
       bool ok = true;
       uint32_t q_loads = 0;      // Q tile pairs issued
-      int q_last[2] = {-1, -1};  // phase of the last load issued into each Q tile, -1: none
       int st = 0;                // ring position of the next K/V load (carries over items)
       uint32_t ph = 0;
       for (int64_t item = item0; item < p.n_items && ok; item += item_step) {
@@ -998,19 +999,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                           kDevErrTimeoutProducer, wtag(kBarQEmpty, 0));
         if (!ok) break;
         // one barrier per Q tile, so that S0 can start before tile 1 has landed
-        for (int t = 0; t < 2 && ok; ++t) {
-          // the previous item's epilogue may have staged O in this tile's space
-          if (q_loads > 0)
-            ok = wait_phase(bar(kBarQFree + t), (q_loads - 1) & 1u, abort_flag, p.timeout_ns, p.err,
-                            kDevErrTimeoutProducer, wtag(kBarQFree + t, 0));
-          if (!ok) break;
+        for (int t = 0; t < 2; ++t) {
           mbar_expect_tx(bar(kBarQFull + t), 2 * kPanelBytes);
           for (int pn = 0; pn < 2; ++pn)
             tma_load_4d(base + kOffQ + t * kTileBytes + pn * kPanelBytes, &maps.q, bar(kBarQFull + t), pn * 64,
                         (int)((qb0 + t) * kBQ), h, b);
-          q_last[t] = (int)(q_loads & 1u);
         }
-        if (!ok) break;
         ++q_loads;
         int c = 0;  // chunk of key tile j
         for (int j = 0; j < n_kv && ok; ++j) {
@@ -1026,7 +1020,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_4d(base + kOffKV + st * kTileBytes + pn * kPanelBytes, tm, bar(kBarKVFull + st), pn * 64,
                           jl * kBK, h, b);
             last_phase[st] = (int)ph;
-            if (++st == kStages) {
+            if (++st == kPStages) {
               st = 0;
               ph ^= 1u;
             }
@@ -1035,11 +1029,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         // let every copy already issued land before the CTA can exit
-        for (int t = 0; t < 2; ++t)
-          if (q_last[t] >= 0)
-            wait_phase(bar(kBarQFull + t), (uint32_t)q_last[t], nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain,
-                       wtag(kBarQFull + t, 0));
-        for (int s = 0; s < kStages; ++s)
+        for (int t = 0; t < 2 && q_loads > 0; ++t)
+          wait_phase(bar(kBarQFull + t), (q_loads - 1) & 1u, nullptr, p.timeout_ns, p.err, kDevErrTimeoutDrain,
+                     wtag(kBarQFull + t, 0));
+        for (int s = 0; s < kPStages; ++s)
           if (last_phase[s] >= 0)
             wait_phase(bar(kBarKVFull + s), (uint32_t)last_phase[s], nullptr, p.timeout_ns, p.err,
                        kDevErrTimeoutDrain, wtag(kBarKVFull + s, 0));
@@ -1073,7 +1066,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < n_kv && ok; ++j, ++tix) {
           const int ks = st;
           const uint32_t kph = ph;
-          if (++st == kStages) {
+          if (++st == kPStages) {
             st = 0;
             ph ^= 1u;
           }
@@ -1107,7 +1100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j == n_kv - 1) mma_commit(bar(kBarQEmpty));  // the producer may load the next Q
           const int vs = st;
           const uint32_t vph = ph;
-          if (++st == kStages) {
+          if (++st == kPStages) {
             st = 0;
             ph ^= 1u;
           }
@@ -1239,45 +1232,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       // A chunk that is not the last, on a tile whose O needs no rescale of the accumulator
       // (fixed-m; any tile of a first chunk, whose O is simply stored; an online tile whose
       // every row kept the accumulator's shift, so that cprev = cnew = 1), adds O into acc_o
-      // (or stores it there) without reading the accumulator through the SM: through this Q
-      // tile's own shared memory (free: every S MMA of the item is done), two 32-column boxes
-      // at a time, with bulk tensor reductions, or, without an accumulator map, from registers
-      // with vector reductions.  The producer loads the next item's Q tile into that space once
-      // the group arrives on the Q-free barrier (at once on the other paths).
+      // (or stores it there) without reading the accumulator through the SM: one 32-column box
+      // at a time through the group's 16 KiB in the ring's fifth stage, with bulk tensor
+      // reductions (the next item's Q and K/V load meanwhile), or, without an accumulator map,
+      // from registers with vector reductions.
       bool plain_add = fixed || !p.accumulate;
       if (!plain_add && !final_out)
         plain_add = named_barrier_and(1 + t, 128, !row_ok || (shift_prev != -INFINITY && shv == shift_prev));
-      const bool stage_o = p.acc_tma && plain_add && !final_out;
-      if (!stage_o && wq == 0 && lane == 0) mbar_arrive(bar(kBarQFree + t));
-      if (stage_o) {
-        uint8_t *stage = gbase + kOffQ + t * kTileBytes;
-        const uint32_t sbase = base + kOffQ + t * kTileBytes;
+      if (p.acc_tma && plain_add && !final_out) {
+        uint8_t *box = gbase + kOffPStage + t * kBoxBytes;
+        const uint32_t sbox = base + (uint32_t)(kOffPStage + t * kBoxBytes);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          if (half == 1) named_barrier(1 + t, 128);  // the first two boxes have been read
+        for (int c = 0; c < 4; ++c) {
+          if (c > 0) named_barrier(1 + t, 128);  // the previous box has been read
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32, o);
+          uint8_t *line = box + r * 128;
 #pragma unroll
-          for (int c2 = 0; c2 < 2; ++c2) {
-            uint32_t o[32];
-            tmem_ld32(tO + (2 * half + c2) * 32, o);
-            uint8_t *line = stage + c2 * (kBQ * 128) + r * 128;
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4)
-              *reinterpret_cast<uint4 *>(line + ((q4 ^ (r & 7)) << 4)) =
-                  make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
-          }
+          for (int q4 = 0; q4 < 8; ++q4)
+            *reinterpret_cast<uint4 *>(line + ((q4 ^ (r & 7)) << 4)) =
+                make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
           fence_proxy_async_smem();
           named_barrier(1 + t, 128);
           if (wq == 0 && lane == 0) {
-            if (tile_ok) {
-#pragma unroll
-              for (int c2 = 0; c2 < 2; ++c2)
-                tma_acc_3d(&maps.acc, sbase + c2 * (kBQ * 128), (2 * half + c2) * 32, (int)(qb * kBQ), (int)bh,
-                           p.accumulate != 0);
-            }
+            if (tile_ok) tma_acc_3d(&maps.acc, sbox, c * 32, (int)(qb * kBQ), (int)bh, p.accumulate != 0);
             bulk_commit_and_wait_smem_read();
           }
         }
-        if (wq == 0 && lane == 0) mbar_arrive(bar(kBarQFree + t));
         if (row_ok) {
           p.acc_sum[rflat] = sum_new;
           p.acc_max[rflat] = shift_new;
