@@ -37,7 +37,7 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 # grows with the head count).
 # Valid only for the kernel code it was measured on (comments aside): the bench reports null
 # otherwise.
-CHUNK_TRAFFIC = {"code_sha256_16": "0980f16b661c5dd8", "bytes_per_launch": 5 * (622.217e6 + 829.119e6) / 2}
+CHUNK_TRAFFIC = {"code_sha256_16": "24bedfc0ea483f4d", "bytes_per_launch": 5 * (627.781e6 + 827.253e6) / 2}
 
 
 def kernel_code_hash(path: str) -> str:
@@ -403,9 +403,16 @@ def run_ours(args, rank, world, local_rank):
     chunk_avg_ms = statistics.mean(chunk_ms)
     achieved = per_launch_flops / (chunk_avg_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops_sustained"]
+    # the schedule the library resolves AUTO to, per chunk launch (the rule of fm_api.cu: the
+    # persistent kernel for a call of at most 8 key tiles with at least twice the SMs in items)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    items = w.B * H * math.ceil(math.ceil(w.Sq / 128) / 2)
+    persistent = args.schedule == "persistent" or (
+        args.schedule == "auto" and all(math.ceil(n / 128) <= 8 for _, n in chunks) and items >= 2 * sms)
+    kernel_name = "fm_chunk_tc_persistent_kernel" if persistent else "fm_chunk_tc_kernel"
     traffic = args.traffic if args.traffic is not None else (
-        chunk_traffic() if (H == w.H and w.name == WORKLOAD and not args.force_online) else None)
-    roofline = {"bound": "tensor", "kernel": "fm_chunk_tc_kernel", "achieved": achieved, "peak": peak,
+        chunk_traffic() if (H == w.H and w.name == WORKLOAD and not args.force_online and not persistent) else None)
+    roofline = {"bound": "tensor", "kernel": kernel_name, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                 "traffic_unit": "bytes per launch (dram read + write)",
                 "algorithmic_bytes_per_launch": algo_bytes,
@@ -443,7 +450,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": (f"inputs larger than L2 ({tensor_bytes / 1e6:.0f} MB per tensor), no flush" if flush is None
                           else f"{tensor_bytes / 1e6:.0f} MB per tensor fits in L2: a {2 * L2_BYTES / 1e6:.0f} MB "
                                "buffer is written before each step, outside its timing"),
-                   "schedule": args.schedule,
+                   "schedule": args.schedule + (f" ({'persistent' if persistent else 'grid'})" if args.schedule == "auto" else ""),
                    "fixed_m_tile_fraction": eligible},
         "pct_of_peak": 100.0 * value / peak,
         "roofline": roofline,

@@ -478,7 +478,19 @@ int attn_chunks_impl(const fm_tensor *q, const fm_tensor *k_chunks, const fm_ten
   a.q = vq;
   a.alpha = (float)alpha;
   a.force_online = force_online;
+  // AUTO: the persistent schedule where a launch's work items are short (at most 8 key tiles,
+  // e.g. one 1024-key chunk of a ring) and outnumber the SMs at least twice, so that its overlap
+  // of the next item's Q load and first MMAs with the current epilogue pays (measured on GB300,
+  // H40 S4096 in 1024-key chunks: chunk launches 778 against 761 TFLOP/s); one CTA per item
+  // otherwise (2-chunk S4096: 1138 against 1153; Wan: 1483 against 1523).
   a.schedule = schedule;
+  if (schedule == FM_SCHEDULE_AUTO) {
+    int64_t tiles = 0;
+    for (int c = 0; c < n_chunks; ++c) tiles += ceil_div(vk[c].S, 128);
+    const int64_t items = vq.B * vq.H * ceil_div(nqb, 2);
+    a.schedule = (tiles <= 8 && items >= 2 * (int64_t)current_device_sm_count()) ? FM_SCHEDULE_PERSISTENT
+                                                                                  : FM_SCHEDULE_GRID;
+  }
   a.nqb = nqb;
   a.flag = bounds->flag;
   a.shift = bounds->shift;

@@ -1408,10 +1408,8 @@ bool encode_acc_map(CUtensorMap *map, float *acc_o, const View &q) {
   return r == CUDA_SUCCESS;
 }
 
-// Schedule of a launch (fm_opts.schedule).  AUTO takes one CTA per item: the persistent schedule
-// overlaps the next item's Q load and first S MMAs with the current item's epilogue, but its
-// epilogue adds O from registers with vector reductions scattered over 128 rows, which takes
-// 5-9 us per item against 3-4 us for the staged bulk-tensor reduce, so it only runs on request.
+// Schedule of a launch: fm_opts.schedule, with AUTO already resolved by the caller into one of
+// the two (the persistent schedule for launches of short work items, fm_api.cu).
 bool use_persistent(int schedule) { return schedule == FM_SCHEDULE_PERSISTENT; }
 
 bool tma_view_ok(const View &t) {

@@ -111,9 +111,11 @@ typedef struct {
 /* fm_opts.schedule.  A work item is two 128-row Q tiles of one (batch, head) against every key
  * tile of the call.  GRID launches one CTA per item.  PERSISTENT launches one CTA per SM that
  * walks the items in turn, loading the next item's Q and K/V tiles and running its first S
- * MMAs while the softmax warps finish the current item's epilogue (the accumulator add then
- * comes from registers as vector reductions rather than through shared memory).  AUTO is GRID:
- * measured on GB300, the register reductions cost more per item than the overlap saves. */
+ * MMAs while the softmax warps finish the current item's epilogue (its K/V ring has one stage
+ * fewer; that space stages O for the bulk accumulator add).  AUTO takes PERSISTENT when the
+ * call has at most 8 key tiles (1024 keys) and at least twice as many items as the GPU has SMs,
+ * GRID otherwise: measured on GB300, the overlap pays on such short items and the simpler grid
+ * wins on longer ones. */
 enum { FM_SCHEDULE_AUTO = 0, FM_SCHEDULE_GRID = 1, FM_SCHEDULE_PERSISTENT = 2 };
 
 /* Bounds of one attention call ([PR477] Summary, "Dynamic eligibility bounding").
