@@ -13,9 +13,12 @@
 // Launches (all deterministic: fixed-order sums, maxima without atomics):
 //   1. ksum    (centering only) partial key sums, P row ranges per head  -> workspace
 //   2. kmean   (centering only) ordered sum of the P partials / N          -> kbar
-//   3. main    one grid over Q-blocks, K row-blocks and V row-blocks: row norms via warp
+//   3. main    the norms over Q-blocks, K row-blocks and V row-blocks: row norms via warp
 //              shuffles; per-block maxima -> qmax_sq (Q) and the workspace (K, V);
-//              qkbar per row; with key sinks, each K block's n_sink + 1 loudest keys
+//              qkbar per row; with key sinks, each K block's n_sink + 1 loudest keys.  One of
+//              three kernels by layout: norms_bulk_kernel (packed bf16 rows of D = 128, staged
+//              through shared memory by bulk copies), norms_vec_kernel (rows on 16-byte
+//              boundaries), norms_kernel (any strides)
 //   3b. sinks  (key sinks only) per head: the n_sink + 1 loudest keys over the blocks'
 //              candidates; the sinks and the max over the other keys ("Kernel reference:
 //              ring_attention_const_max_fwd", section "Adapting this kernel")
@@ -1100,7 +1103,7 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // 5. Row shifts: b_i = m_i + alpha*q_i.kbar, with m_i = ceil(alpha*|q_i|*sqrt(kmax)) - C
-// (per row) or the row's Q-block m.  `shift` holds |q_i|^2 on entry (from norms_kernel).
+// (per row) or the row's Q-block m.  `shift` holds |q_i|^2 on entry (from the norms pass).
 __global__ void __launch_bounds__(kThreads)
     shift_kernel(int64_t H, int64_t Sq, int64_t nqb, int per_row, double alpha, int C, const float *kmax_sq,
                  const int32_t *m, const float *qkbar, float *shift) {
