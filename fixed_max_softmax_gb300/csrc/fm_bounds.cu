@@ -22,8 +22,9 @@
 //   3b. sinks  (key sinks only) per head: the n_sink + 1 loudest keys over the blocks'
 //              candidates; the sinks and the max over the other keys ("Kernel reference:
 //              ring_attention_const_max_fwd", section "Adapting this kernel")
-//   4. finish  per head: key max, global V max, U, m, flag
-//   5. shift   per row: b_i = m_i + alpha*q_i.kbar (m_i per row or per Q-block)
+//   4. finish  per 2048 query rows of a head: the head's key max, the global V max (folded in by
+//              the norms pass with atomics on a zeroed word), U, m and flag of its two Q-blocks,
+//              and every row's shift b_i = m_i + alpha*q_i.kbar (m_i per row or per Q-block)
 // Bytes: Q + K + V once each, plus K once more for the mean when centering.
 #include <cuda_bf16.h>
 #include <limits.h>
@@ -274,7 +275,7 @@ template <typename T, int EPL, bool CONTIG>
 __global__ void __launch_bounds__(kThreads)
     norms_kernel(View q, View k, View v, int64_t nqb, int64_t nkb, int centering, float alpha,
                  const float *kbar, float *qmax_sq, float *qkbar, float *qsq, float *kblk, float *vblk,
-                 int n_sink, SinkCand *cand) {
+                 int n_sink, SinkCand *cand, float *vmax_all) {
   pdl_wait();  // inputs written by the kernels before this one
   pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -346,7 +347,10 @@ __global__ void __launch_bounds__(kThreads)
     for (int w = 0; w < kWarps; ++w) mx = fmaxf(mx, wmax[w]);
     if (bx < nqb) qmax_sq[bh * nqb + bx] = mx;
     else if (bx < nqb + nkb) kblk[bh * nkb + (bx - nqb)] = mx;
-    else vblk[bh * nkb + (bx - nqb - nkb)] = mx;
+    else {
+      vblk[bh * nkb + (bx - nqb - nkb)] = mx;
+      if (vmax_all) atomicMax(reinterpret_cast<int *>(vmax_all), __float_as_int(mx));  // v^2 >= 0: bits order as values
+    }
   }
   if (n_sink > 0 && bx >= nqb && bx < nqb + nkb && warp == 0) {
     // this block's n_sink + 1 loudest keys, in sink order (its rows' norms are in knorm,
@@ -453,7 +457,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kThreads)
     norms_vec_kernel(View q, View k, View v, int64_t nqb, int64_t nkb, int centering, float alpha,
                      const float *kbar, float *qmax_sq, float *qkbar, float *qsq, float *kblk, float *vblk,
-                     int n_sink, SinkCand *cand) {
+                     int n_sink, SinkCand *cand, float *vmax_all) {
   pdl_wait();  // inputs written by the kernels before this one
   pdl_trigger();
   using V = Vec16<T, D>;
@@ -553,7 +557,10 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t blk = blk0 + i;
     if (kind == 0) qmax_sq[bh * nqb + blk] = mx;
     else if (kind == 1) kblk[bh * nkb + blk] = mx;
-    else vblk[bh * nkb + blk] = mx;
+    else {
+      vblk[bh * nkb + blk] = mx;
+      if (vmax_all) atomicMax(reinterpret_cast<int *>(vmax_all), __float_as_int(mx));  // v^2 >= 0: bits order as values
+    }
   }
   if (n_sink > 0 && kind == 1 && warp < nb) {
     // key block blk0 + warp: its n_sink + 1 loudest keys, in sink order (its rows' norms are in
@@ -601,7 +608,9 @@ __global__ void __launch_bounds__(kThreads)
 // since squaring is monotonic, and a NaN is skipped as fmaxf skips it.  The block's
 // maximum over the warps goes through a shared-memory slot; the last warp to finish a block
 // (an atomic count) writes its results, and with key sinks picks its candidates, while the
-// others go on.  Eight slots: a warp can run at most kNbStages blocks ahead of the slowest.
+// others go on.  Eight slots: a warp can run at most kNbStages blocks ahead of the slowest.  The
+// V blocks' maxima also go into one shared-memory word, which the last consumer warp to finish
+// folds into the global V max (vmax_all, when given) with one atomic per CTA.
 // Every wait is bounded in time; on expiry the kernel records the failure in the device error
 // word and every role stops at its next wait (the producer after its own copies have landed).
 constexpr int kNbWarps = 16;                     // consumer warps
@@ -690,7 +699,7 @@ __device__ __forceinline__ float max_abs_bf16x2(float m, uint32_t w) {
 __global__ void __launch_bounds__(kNbThreads, 1)
     norms_bulk_kernel(View q, View k, View v, int64_t nqb, int64_t nkb, int centering, float alpha,
                       const float *kbar, float *qmax_sq, float *qkbar, float *qsq, float *kblk, float *vblk,
-                      int n_sink, SinkCand *cand, unsigned int *err, unsigned long long timeout_ns) {
+                      int n_sink, SinkCand *cand, float *vmax_all, unsigned int *err, unsigned long long timeout_ns) {
   pdl_wait();  // inputs written by the kernels before this one
   pdl_trigger();
   extern __shared__ uint8_t nb_raw[];
@@ -698,6 +707,8 @@ __global__ void __launch_bounds__(kNbThreads, 1)
   const uint32_t base = (raw + 127u) & ~127u;
   uint8_t *g = nb_raw + (base - raw);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(g + kNbOffAbort);
+  int *cta_vmax = reinterpret_cast<int *>(g + kNbOffAbort + 4);              // this CTA's V max (fp32 bits)
+  unsigned int *warps_done = reinterpret_cast<unsigned int *>(g + kNbOffAbort + 8);
   int *smax = reinterpret_cast<int *>(g + kNbOffMax);
   unsigned int *scnt = reinterpret_cast<unsigned int *>(g + kNbOffCnt);
   float *knorm = reinterpret_cast<float *>(g + kNbOffKnorm);
@@ -760,6 +771,8 @@ __global__ void __launch_bounds__(kNbThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    *cta_vmax = 0;
+    *warps_done = 0;
     for (int s = 0; s < kNbStages; ++s) {
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(full(s)), "r"(1) : "memory");
       asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empty(s)), "r"(kNbWarps) : "memory");
@@ -940,7 +953,10 @@ __global__ void __launch_bounds__(kNbThreads, 1)
       if (lane == 0) {
         if (kind == 0) qmax_sq[bh * nqb + blk] = mx;
         else if (kind == 1) kblk[bh * nkb + blk] = mx;
-        else vblk[bh * nkb + blk] = mx;
+        else {
+          vblk[bh * nkb + blk] = mx;
+          atomicMax(cta_vmax, __float_as_int(mx));  // v^2 >= 0: bits order as values
+        }
       }
       if (n_sink > 0 && kind == 1) {
         // the block's n_sink + 1 loudest keys, in sink order
@@ -971,6 +987,14 @@ __global__ void __launch_bounds__(kNbThreads, 1)
         smax[slot] = 0;
         scnt[slot] = 0;
       }
+    }
+  }
+  // the global V max, folded in once per CTA by the last consumer warp to finish its items
+  if (vmax_all && lane == 0) {
+    __threadfence_block();
+    if (atomicAdd(warps_done, 1u) == (unsigned)(kNbWarps - 1)) {
+      __threadfence_block();
+      atomicMax(reinterpret_cast<int *>(vmax_all), *reinterpret_cast<volatile int *>(cta_vmax));
     }
   }
 }
@@ -1067,42 +1091,82 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// 4. Per head: key max, global V max, then U, m, flag for every Q-block.
+// 4+5. Per block of kFinishRows query rows of one head: the head's key max (over its K blocks, or
+// the key-sink pass's value), the global V max (folded in by the norms pass), then U, m and flag
+// of the block's Q-blocks and every row's shift b_i = m_i + alpha*q_i.kbar (m_i per row or per
+// Q-block), in one launch: the per-head finish and the per-row shift of earlier versions, with
+// the same arithmetic.  Every CTA of a head reduces the head's K-block maxima itself (nkb
+// floats), so a CTA takes enough rows (8 a thread, their loads in flight together) for that and
+// for its two rounds of memory latency to be paid rarely; the first CTA of a head writes kmax_sq.
+// `shift` holds |q_i|^2 on entry (from the norms pass).
+constexpr int kFinishRowsPerThread = 8;
+constexpr int kFinishRows = kThreads * kFinishRowsPerThread;  // 2048 rows, 16 Q-blocks
+constexpr int kFinishBlocks = kFinishRows / kQRows;
+static_assert(kFinishRows % kQRows == 0 && kFinishBlocks <= kThreads, "whole Q-blocks per CTA");
 __global__ void __launch_bounds__(kThreads)
-    finish_kernel(int64_t H, int64_t nqb, int64_t nkb, int64_t n_heads_total, const float *kblk,
-                  const float *vblk, double alpha, int C, int gate, const float *qmax_sq,
-                  float *kmax_sq, float *vmax_sq, int32_t *m, uint8_t *flag, int kmax_given) {
+    finish_shift_kernel(int64_t H, int64_t Sq, int64_t nqb, int64_t nkb, const float *kblk, const float *vmax_all,
+                        double alpha, int C, int gate, int per_row, const float *qmax_sq, float *kmax_sq,
+                        int32_t *m, uint8_t *flag, const float *qkbar, float *shift, int kmax_given) {
   pdl_wait();  // inputs written by the kernels before this one
   pdl_trigger();
-  const int64_t bh = blockIdx.y * H + blockIdx.x;
-  __shared__ float red[2][kWarps];
-  float km = 0.f, vm = 0.f;
-  for (int64_t i = threadIdx.x; i < nkb; i += kThreads) km = fmaxf(km, kblk[bh * nkb + i]);
-  for (int64_t i = threadIdx.x; i < n_heads_total * nkb; i += kThreads) vm = fmaxf(vm, vblk[i]);
-  km = warp_max(km);
-  vm = warp_max(vm);
+  const int64_t bh = blockIdx.z * H + blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) { red[0][warp] = km; red[1][warp] = vm; }
-  __syncthreads();
-  km = 0.f; vm = 0.f;
+  __shared__ float red[kWarps];
+  __shared__ int32_t mblk[kFinishBlocks];
+  float km;
+  if (kmax_given) {
+    km = kmax_sq[bh];  // the key sinks' pass left the max over the other keys
+  } else {
+    float x = 0.f;
+    for (int64_t i = threadIdx.x; i < nkb; i += kThreads) x = fmaxf(x, kblk[bh * nkb + i]);
+    x = warp_max(x);
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    km = 0.f;
 #pragma unroll
-  for (int w = 0; w < kWarps; ++w) { km = fmaxf(km, red[0][w]); vm = fmaxf(vm, red[1][w]); }
-  if (kmax_given) km = kmax_sq[bh];  // the key sinks' pass left the max over the other keys
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    kmax_sq[bh] = km;
-    if (bh == 0) vmax_sq[0] = vm;
+    for (int w = 0; w < kWarps; ++w) km = fmaxf(km, red[w]);
+    if (blockIdx.x == 0 && threadIdx.x == 0) kmax_sq[bh] = km;
   }
+  const float vm = *vmax_all;
   const bool v_ok = vm <= (float)FM_VMAX * (float)FM_VMAX;
   const double ksq = sqrt((double)km);
-  for (int64_t i = threadIdx.x; i < nqb; i += kThreads) {
-    const double U = alpha * sqrt((double)qmax_sq[bh * nqb + i]) * ksq;
-    m[bh * nqb + i] = (int32_t)ceil(U) - C;
-    flag[bh * nqb + i] = (uint8_t)(v_ok && U <= (double)gate);
+  const int64_t r0 = (int64_t)blockIdx.x * kFinishRows;
+  if (threadIdx.x < kFinishBlocks) {
+    const int64_t qb = r0 / kQRows + threadIdx.x;
+    if (qb < nqb) {
+      const double U = alpha * sqrt((double)qmax_sq[bh * nqb + qb]) * ksq;
+      const int32_t mv = (int32_t)ceil(U) - C;
+      m[bh * nqb + qb] = mv;
+      flag[bh * nqb + qb] = (uint8_t)(v_ok && U <= (double)gate);
+      mblk[threadIdx.x] = mv;
+    }
+  }
+  __syncthreads();
+  // rows r0 + threadIdx.x + u * kThreads: coalesced, all loads of the thread in flight together
+  float qk[kFinishRowsPerThread], qs[kFinishRowsPerThread];
+#pragma unroll
+  for (int u = 0; u < kFinishRowsPerThread; ++u) {
+    const int64_t r = r0 + threadIdx.x + (int64_t)u * kThreads;
+    qk[u] = r < Sq ? qkbar[bh * Sq + r] : 0.f;
+    qs[u] = (per_row && r < Sq) ? shift[bh * Sq + r] : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kFinishRowsPerThread; ++u) {
+    const int64_t r = r0 + threadIdx.x + (int64_t)u * kThreads;
+    if (r >= Sq) break;
+    int32_t mi;
+    if (per_row) {
+      const double U = alpha * sqrt((double)qs[u]) * ksq;
+      mi = (int32_t)ceil(U) - C;
+    } else {
+      mi = mblk[(threadIdx.x + u * kThreads) / kQRows];
+    }
+    shift[bh * Sq + r] = (float)mi + qk[u];
   }
 }
 
-// 5. Row shifts: b_i = m_i + alpha*q_i.kbar, with m_i = ceil(alpha*|q_i|*sqrt(kmax)) - C
+// Row shifts alone, for the bounds of a ring (after ring_combine_kernel has written m and flag):
+// b_i = m_i + alpha*q_i.kbar, with m_i = ceil(alpha*|q_i|*sqrt(kmax)) - C
 // (per row) or the row's Q-block m.  `shift` holds |q_i|^2 on entry (from the norms pass).
 __global__ void __launch_bounds__(kThreads)
     shift_kernel(int64_t H, int64_t Sq, int64_t nqb, int per_row, double alpha, int C, const float *kmax_sq,
@@ -1370,7 +1434,7 @@ cudaError_t launch_ksum(const View &k, int64_t P, float *part, cudaStream_t st) 
 bool bulk_rows(const View &t) { return t.dtype == FM_BF16 && t.D == 128 && t.sS == t.D && rows16(t); }
 
 cudaError_t launch_norms_bulk(const BoundsArgs &a, const WsLayout &w, float *kblk, float *vblk, SinkCand *cand,
-                              cudaStream_t st) {
+                              float *vmax_all, cudaStream_t st) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1384,25 +1448,26 @@ cudaError_t launch_norms_bulk(const BoundsArgs &a, const WsLayout &w, float *kbl
   const int64_t grid = min(n_items, (int64_t)current_device_sm_count());
   return launch_pdl(norms_bulk_kernel, dim3((unsigned)grid), dim3(kNbThreads), (size_t)kNbSmem, st, a.q, a.k, a.v,
                     a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk,
-                    a.n_sink, cand, a.err, a.timeout_ns);
+                    a.n_sink, cand, vmax_all, a.err, a.timeout_ns);
 }
 
 template <typename T, int EPL, bool CONTIG>
 cudaError_t launch_norms(const BoundsArgs &a, const WsLayout &w, float *kblk, float *vblk, SinkCand *cand,
-                         cudaStream_t st) {
+                         float *vmax_all, cudaStream_t st) {
   const int64_t nx = a.nqb + 2 * w.nkb;
   if (nx == 0) return cudaSuccess;
   if (CONTIG && sizeof(T) == 2 && EPL == 4 && bulk_rows(a.q) && bulk_rows(a.k) && bulk_rows(a.v))
-    return launch_norms_bulk(a, w, kblk, vblk, cand, st);
+    return launch_norms_bulk(a, w, kblk, vblk, cand, vmax_all, st);
   const dim3 grid((unsigned)nx, (unsigned)a.q.H, (unsigned)a.q.B);
   if (CONTIG && rows16(a.q) && rows16(a.k) && rows16(a.v)) {
     const int64_t nx4 = ceil_div(a.nqb, kBlocksPerCta) + 2 * ceil_div(w.nkb, kBlocksPerCta);
     return launch_pdl(norms_vec_kernel<T, 32 * EPL>, dim3((unsigned)nx4, (unsigned)a.q.H, (unsigned)a.q.B),
                       dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb, a.centering, (float)a.alpha, a.kbar,
-                      a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand);
+                      a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand, vmax_all);
   }
   return launch_pdl(norms_kernel<T, EPL, CONTIG>, grid, dim3(kThreads), 0, st, a.q, a.k, a.v, a.nqb, w.nkb,
-                    a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand);
+                    a.centering, (float)a.alpha, a.kbar, a.qmax_sq, a.qkbar, a.shift, kblk, vblk, a.n_sink, cand,
+                    vmax_all);
 }
 
 template <typename T, int EPL, bool CONTIG>
@@ -1422,7 +1487,7 @@ cudaError_t launch_ring_local_typed(const BoundsArgs &a, const WsLayout &w, cons
   else
     e = cudaMemsetAsync(a.kbar, 0, sizeof(float) * (size_t)(B * H * D), st);
   if (e != cudaSuccess) return e;
-  e = launch_norms<T, EPL, CONTIG>(a, w, kblk, vblk, cand, st);
+  e = launch_norms<T, EPL, CONTIG>(a, w, kblk, vblk, cand, nullptr, st);
   if (e != cudaSuccess) return e;
   const RingLayout L = ring_layout(B * H, D, a.n_sink);
   e = launch_pdl(ring_local_kernel<T>, heads, dim3(kThreads), 0, st, a.k, a.v, w.nkb, B * H, a.n_sink, key_offset, kblk,
@@ -1441,7 +1506,9 @@ cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st
   SinkCand *cand = reinterpret_cast<SinkCand *>(ws + w.off_cand);
   const int D = (int)a.q.D;
   const dim3 heads((unsigned)H, (unsigned)B);
-  cudaError_t e = cudaSuccess;
+  // the global V max: every V block of the norms pass folds its max in with an integer atomicMax
+  cudaError_t e = cudaMemsetAsync(a.vmax_sq, 0, sizeof(float), st);
+  if (e != cudaSuccess) return e;
   if (a.centering && N > 0) {
     e = launch_ksum<T, EPL, CONTIG>(a.k, w.P, part, st);
     if (e == cudaSuccess) e = launch_pdl(kmean_kernel, heads, dim3(128), 0, st, part, H, w.P, D, N, a.kbar);
@@ -1449,21 +1516,19 @@ cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st
     e = cudaMemsetAsync(a.kbar, 0, sizeof(float) * (size_t)(B * H * D), st);
   }
   if (e != cudaSuccess) return e;
-  e = launch_norms<T, EPL, CONTIG>(a, w, kblk, vblk, cand, st);
+  e = launch_norms<T, EPL, CONTIG>(a, w, kblk, vblk, cand, a.vmax_sq, st);
   if (e != cudaSuccess) return e;
   if (a.n_sink > 0) {
     e = launch_pdl(sink_select_kernel<T>, heads, dim3(kThreads), 0, st, a.k, a.v, w.nkb, a.n_sink, cand, a.sink_idx,
                    a.sink_k, a.sink_v, a.kmax_sq);
     if (e != cudaSuccess) return e;
   }
-  e = launch_pdl(finish_kernel, heads, dim3(kThreads), 0, st, H, a.nqb, w.nkb, B * H, kblk, vblk, a.alpha, a.C, a.gate,
-                 a.qmax_sq, a.kmax_sq, a.vmax_sq, a.m, a.flag, (int)(a.n_sink > 0));
+  // one CTA per kFinishRows query rows of each head (at least one per head, which writes kmax_sq)
+  const int64_t nx = ceil_div(a.q.S, kFinishRows) > 0 ? ceil_div(a.q.S, kFinishRows) : 1;
+  e = launch_pdl(finish_shift_kernel, dim3((unsigned)nx, (unsigned)H, (unsigned)B), dim3(kThreads), 0, st, H, a.q.S,
+                 a.nqb, w.nkb, kblk, a.vmax_sq, a.alpha, a.C, a.gate, a.per_row, a.qmax_sq, a.kmax_sq, a.m, a.flag,
+                 a.qkbar, a.shift, (int)(a.n_sink > 0));
   if (e != cudaSuccess) return e;
-  if (a.q.S > 0) {
-    e = launch_pdl(shift_kernel, dim3((unsigned)ceil_div(a.q.S, kThreads), (unsigned)H, (unsigned)B), dim3(kThreads),
-                   0, st, H, a.q.S, a.nqb, a.per_row, a.alpha, a.C, a.kmax_sq, a.m, a.qkbar, a.shift);
-    if (e != cudaSuccess) return e;
-  }
   return cudaGetLastError();
 }
 
