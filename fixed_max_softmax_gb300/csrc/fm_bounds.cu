@@ -11,8 +11,9 @@
 // mean over real tokens of PR #478, Summary.
 //
 // Launches (all deterministic: fixed-order sums, maxima without atomics):
-//   1. ksum    (centering only) partial key sums, P row ranges per head  -> workspace
-//   2. kmean   (centering only) ordered sum of the P partials / N          -> kbar
+//   1. ksum    (centering only) partial key sums, P row ranges per head  -> workspace; the last
+//              CTA of a head to finish adds the P partials in their fixed order and
+//              divides by N                                                -> kbar
 //   3. main    the norms over Q-blocks, K row-blocks and V row-blocks: row norms via warp
 //              shuffles; per-block maxima -> qmax_sq (Q) and the workspace (K, V);
 //              qkbar per row; with key sinks, each K block's n_sink + 1 loudest keys.  One of
@@ -23,8 +24,10 @@
 //              candidates; the sinks and the max over the other keys ("Kernel reference:
 //              ring_attention_const_max_fwd", section "Adapting this kernel")
 //   4. finish  per 2048 query rows of a head: the head's key max, the global V max (folded in by
-//              the norms pass with atomics on a zeroed word), U, m and flag of its two Q-blocks,
-//              and every row's shift b_i = m_i + alpha*q_i.kbar (m_i per row or per Q-block)
+//              the norms pass with atomics on a zeroed workspace word), U, m and flag of its 16
+//              Q-blocks, and every row's shift b_i = m_i + alpha*q_i.kbar (m_i per row or per
+//              Q-block)
+// One memset before them zeroes the V-max word and the per-head arrival counters of step 1.
 // Bytes: Q + K + V once each, plus K once more for the mean when centering.
 #include <cuda_bf16.h>
 #include <limits.h>
@@ -60,6 +63,8 @@ constexpr int kCandPerBlock = FM_MAX_SINKS + 1;  // each K block keeps its top n
 struct WsLayout {
   int64_t P, nkb, nvb;
   size_t off_part, off_kb, off_vb, off_cand, total;
+  // zeroed at the start of each bounds pass: the V-max word, then one arrival counter per head
+  size_t off_zero, zero_bytes;
 };
 
 WsLayout ws_layout(int64_t B, int64_t H, int64_t N, int64_t D) {
@@ -72,8 +77,10 @@ WsLayout ws_layout(int64_t B, int64_t H, int64_t N, int64_t D) {
   w.off_vb = w.off_kb + sizeof(float) * (size_t)(B * H * w.nkb);
   w.off_cand = w.off_vb + sizeof(float) * (size_t)(B * H * w.nvb);
   w.off_cand = (w.off_cand + 15) & ~(size_t)15;
-  w.total = w.off_cand + sizeof(SinkCand) * (size_t)(B * H * w.nkb * kCandPerBlock);
-  w.total = (w.total + 255) & ~(size_t)255;
+  w.off_zero = w.off_cand + sizeof(SinkCand) * (size_t)(B * H * w.nkb * kCandPerBlock);
+  w.off_zero = (w.off_zero + 15) & ~(size_t)15;
+  w.zero_bytes = 16 + sizeof(unsigned int) * (size_t)(B * H);
+  w.total = (w.off_zero + w.zero_bytes + 255) & ~(size_t)255;
   return w;
 }
 
@@ -136,9 +143,31 @@ __device__ __forceinline__ void warp_best_sink(float &bv, int32_t &bi) {
   }
 }
 
+// The key mean from the P partial sums of head bh, by the last of the head's P CTAs to write
+// its partial (a counter per head, zeroed before the launch): the partials added in the order
+// p = 0 .. P-1 whichever CTA arrives last, then divided by N.  count == nullptr: no mean (the
+// ring's key sums, which another launch adds up).
+__device__ __forceinline__ void key_mean_if_last(const float *part, int64_t bh, int64_t P, int D,
+                                                 unsigned int *count, int64_t N, float *kbar) {
+  if (count == nullptr) return;
+  __shared__ unsigned int arrived;
+  __threadfence();  // this CTA's partial, visible before its arrival is counted
+  __syncthreads();
+  if (threadIdx.x == 0) arrived = atomicAdd(&count[bh], 1u);
+  __syncthreads();
+  if (arrived != (unsigned int)(P - 1)) return;
+  __threadfence();
+  if (threadIdx.x < D) {
+    float s = 0.f;
+    for (int64_t p = 0; p < P; ++p) s += __ldcg(&part[(bh * P + p) * D + threadIdx.x]);
+    kbar[bh * D + threadIdx.x] = N > 0 ? s / (float)N : 0.f;
+  }
+}
+
 // 1. Partial key sums: CTA (p, h, b) sums rows [p*len, (p+1)*len) of head (b, h).
 template <typename T, int EPL, bool CONTIG>
-__global__ void __launch_bounds__(kThreads) ksum_kernel(View k, int64_t P, float *part) {
+__global__ void __launch_bounds__(kThreads)
+    ksum_kernel(View k, int64_t P, float *part, unsigned int *count, int64_t N, float *kbar) {
   pdl_wait();  // inputs written by the kernels before this one
   pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -167,6 +196,7 @@ __global__ void __launch_bounds__(kThreads) ksum_kernel(View k, int64_t P, float
     for (int w = 0; w < kWarps; ++w) s += red[w][threadIdx.x];
     part[((b * k.H + h) * P + p) * D + threadIdx.x] = s;
   }
+  key_mean_if_last(part, b * k.H + h, P, D, count, N, kbar);
 }
 
 // ---- rows that start on 16-byte boundaries: 16-byte loads, several rows in flight per lane --
@@ -209,7 +239,8 @@ __device__ __forceinline__ float row_sum(float v) {
 // 1'. Partial key sums with 16-byte loads (the same partition of rows as ksum_kernel, a fixed
 // order of additions within it).
 template <typename T, int D>
-__global__ void __launch_bounds__(kThreads) ksum_vec_kernel(View k, int64_t P, float *part) {
+__global__ void __launch_bounds__(kThreads)
+    ksum_vec_kernel(View k, int64_t P, float *part, unsigned int *count, int64_t N, float *kbar) {
   pdl_wait();  // inputs written by the kernels before this one
   pdl_trigger();
   using V = Vec16<T, D>;
@@ -256,9 +287,11 @@ __global__ void __launch_bounds__(kThreads) ksum_vec_kernel(View k, int64_t P, f
     for (int w = 0; w < kWarps; ++w) s += red[w][threadIdx.x];
     part[((b * k.H + h) * P + p) * D + threadIdx.x] = s;
   }
+  key_mean_if_last(part, b * k.H + h, P, D, count, N, kbar);
 }
 
-// 2. Key mean: ordered sum of the P partials of head (b, h), divided by N.
+// 2. Key mean: ordered sum of the P partials of head (b, h), divided by N (the ring's key sums
+// and key mean; the single-GPU pass folds this into step 1).
 __global__ void kmean_kernel(const float *part, int64_t H, int64_t P, int D, int64_t N, float *kbar) {
   pdl_wait();  // inputs written by the kernels before this one
   pdl_trigger();
@@ -1094,10 +1127,10 @@ __global__ void __launch_bounds__(kThreads)
 // 4+5. Per block of kFinishRows query rows of one head: the head's key max (over its K blocks, or
 // the key-sink pass's value), the global V max (folded in by the norms pass), then U, m and flag
 // of the block's Q-blocks and every row's shift b_i = m_i + alpha*q_i.kbar (m_i per row or per
-// Q-block), in one launch: the per-head finish and the per-row shift of earlier versions, with
-// the same arithmetic.  Every CTA of a head reduces the head's K-block maxima itself (nkb
-// floats), so a CTA takes enough rows (8 a thread, their loads in flight together) for that and
-// for its two rounds of memory latency to be paid rarely; the first CTA of a head writes kmax_sq.
+// Q-block), in one launch.  Every CTA of a head reduces the head's K-block maxima itself (nkb
+// floats), so a CTA takes enough rows (8 a thread, their loads issued before that reduction) for
+// the reduction's latency to be paid rarely; the first CTA of a head writes kmax_sq, the first
+// CTA of all copies the V max out of the workspace into vmax_sq.
 // `shift` holds |q_i|^2 on entry (from the norms pass).
 constexpr int kFinishRowsPerThread = 8;
 constexpr int kFinishRows = kThreads * kFinishRowsPerThread;  // 2048 rows, 16 Q-blocks
@@ -1106,13 +1139,24 @@ static_assert(kFinishRows % kQRows == 0 && kFinishBlocks <= kThreads, "whole Q-b
 __global__ void __launch_bounds__(kThreads)
     finish_shift_kernel(int64_t H, int64_t Sq, int64_t nqb, int64_t nkb, const float *kblk, const float *vmax_all,
                         double alpha, int C, int gate, int per_row, const float *qmax_sq, float *kmax_sq,
-                        int32_t *m, uint8_t *flag, const float *qkbar, float *shift, int kmax_given) {
+                        float *vmax_sq, int32_t *m, uint8_t *flag, const float *qkbar, float *shift,
+                        int kmax_given) {
   pdl_wait();  // inputs written by the kernels before this one
   pdl_trigger();
   const int64_t bh = blockIdx.z * H + blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ float red[kWarps];
   __shared__ int32_t mblk[kFinishBlocks];
+  // rows r0 + threadIdx.x + u * kThreads: coalesced, all loads of the thread in flight together,
+  // and in flight while the key max is reduced
+  const int64_t r0 = (int64_t)blockIdx.x * kFinishRows;
+  float qk[kFinishRowsPerThread], qs[kFinishRowsPerThread];
+#pragma unroll
+  for (int u = 0; u < kFinishRowsPerThread; ++u) {
+    const int64_t r = r0 + threadIdx.x + (int64_t)u * kThreads;
+    qk[u] = r < Sq ? qkbar[bh * Sq + r] : 0.f;
+    qs[u] = (per_row && r < Sq) ? shift[bh * Sq + r] : 0.f;
+  }
   float km;
   if (kmax_given) {
     km = kmax_sq[bh];  // the key sinks' pass left the max over the other keys
@@ -1128,9 +1172,9 @@ __global__ void __launch_bounds__(kThreads)
     if (blockIdx.x == 0 && threadIdx.x == 0) kmax_sq[bh] = km;
   }
   const float vm = *vmax_all;
+  if (bh == 0 && blockIdx.x == 0 && threadIdx.x == 0) vmax_sq[0] = vm;
   const bool v_ok = vm <= (float)FM_VMAX * (float)FM_VMAX;
   const double ksq = sqrt((double)km);
-  const int64_t r0 = (int64_t)blockIdx.x * kFinishRows;
   if (threadIdx.x < kFinishBlocks) {
     const int64_t qb = r0 / kQRows + threadIdx.x;
     if (qb < nqb) {
@@ -1142,14 +1186,6 @@ __global__ void __launch_bounds__(kThreads)
     }
   }
   __syncthreads();
-  // rows r0 + threadIdx.x + u * kThreads: coalesced, all loads of the thread in flight together
-  float qk[kFinishRowsPerThread], qs[kFinishRowsPerThread];
-#pragma unroll
-  for (int u = 0; u < kFinishRowsPerThread; ++u) {
-    const int64_t r = r0 + threadIdx.x + (int64_t)u * kThreads;
-    qk[u] = r < Sq ? qkbar[bh * Sq + r] : 0.f;
-    qs[u] = (per_row && r < Sq) ? shift[bh * Sq + r] : 0.f;
-  }
 #pragma unroll
   for (int u = 0; u < kFinishRowsPerThread; ++u) {
     const int64_t r = r0 + threadIdx.x + (int64_t)u * kThreads;
@@ -1422,12 +1458,14 @@ bool rows16(const View &t) {
          ((t.sS * es) % 16 == 0 || t.S <= 1);
 }
 
+// count == nullptr: partial sums only; else also the key mean (count zeroed beforehand).
 template <typename T, int EPL, bool CONTIG>
-cudaError_t launch_ksum(const View &k, int64_t P, float *part, cudaStream_t st) {
+cudaError_t launch_ksum(const View &k, int64_t P, float *part, unsigned int *count, int64_t N, float *kbar,
+                        cudaStream_t st) {
   const dim3 grid((unsigned)P, (unsigned)k.H, (unsigned)k.B);
   if (CONTIG && rows16(k))
-    return launch_pdl(ksum_vec_kernel<T, 32 * EPL>, grid, dim3(kThreads), 0, st, k, P, part);
-  return launch_pdl(ksum_kernel<T, EPL, CONTIG>, grid, dim3(kThreads), 0, st, k, P, part);
+    return launch_pdl(ksum_vec_kernel<T, 32 * EPL>, grid, dim3(kThreads), 0, st, k, P, part, count, N, kbar);
+  return launch_pdl(ksum_kernel<T, EPL, CONTIG>, grid, dim3(kThreads), 0, st, k, P, part, count, N, kbar);
 }
 
 // bf16 rows of D = 128 stored back to back within each head (the staged norms pass).
@@ -1504,19 +1542,20 @@ cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st
   float *kblk = reinterpret_cast<float *>(ws + w.off_kb);
   float *vblk = reinterpret_cast<float *>(ws + w.off_vb);
   SinkCand *cand = reinterpret_cast<SinkCand *>(ws + w.off_cand);
-  const int D = (int)a.q.D;
   const dim3 heads((unsigned)H, (unsigned)B);
-  // the global V max: every V block of the norms pass folds its max in with an integer atomicMax
-  cudaError_t e = cudaMemsetAsync(a.vmax_sq, 0, sizeof(float), st);
+  // the global V max (every CTA of the norms pass folds its V max in with an integer atomicMax)
+  // and the key sums' arrival counters start at zero
+  float *vmax_ws = reinterpret_cast<float *>(ws + w.off_zero);
+  unsigned int *count = reinterpret_cast<unsigned int *>(ws + w.off_zero + 16);
+  cudaError_t e = cudaMemsetAsync(ws + w.off_zero, 0, w.zero_bytes, st);
   if (e != cudaSuccess) return e;
   if (a.centering && N > 0) {
-    e = launch_ksum<T, EPL, CONTIG>(a.k, w.P, part, st);
-    if (e == cudaSuccess) e = launch_pdl(kmean_kernel, heads, dim3(128), 0, st, part, H, w.P, D, N, a.kbar);
+    e = launch_ksum<T, EPL, CONTIG>(a.k, w.P, part, count, N, a.kbar, st);
   } else {
-    e = cudaMemsetAsync(a.kbar, 0, sizeof(float) * (size_t)(B * H * D), st);
+    e = cudaMemsetAsync(a.kbar, 0, sizeof(float) * (size_t)(B * H * a.q.D), st);
   }
   if (e != cudaSuccess) return e;
-  e = launch_norms<T, EPL, CONTIG>(a, w, kblk, vblk, cand, a.vmax_sq, st);
+  e = launch_norms<T, EPL, CONTIG>(a, w, kblk, vblk, cand, vmax_ws, st);
   if (e != cudaSuccess) return e;
   if (a.n_sink > 0) {
     e = launch_pdl(sink_select_kernel<T>, heads, dim3(kThreads), 0, st, a.k, a.v, w.nkb, a.n_sink, cand, a.sink_idx,
@@ -1526,8 +1565,8 @@ cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st
   // one CTA per kFinishRows query rows of each head (at least one per head, which writes kmax_sq)
   const int64_t nx = ceil_div(a.q.S, kFinishRows) > 0 ? ceil_div(a.q.S, kFinishRows) : 1;
   e = launch_pdl(finish_shift_kernel, dim3((unsigned)nx, (unsigned)H, (unsigned)B), dim3(kThreads), 0, st, H, a.q.S,
-                 a.nqb, w.nkb, kblk, a.vmax_sq, a.alpha, a.C, a.gate, a.per_row, a.qmax_sq, a.kmax_sq, a.m, a.flag,
-                 a.qkbar, a.shift, (int)(a.n_sink > 0));
+                 a.nqb, w.nkb, kblk, vmax_ws, a.alpha, a.C, a.gate, a.per_row, a.qmax_sq, a.kmax_sq, a.vmax_sq, a.m,
+                 a.flag, a.qkbar, a.shift, (int)(a.n_sink > 0));
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1560,13 +1599,13 @@ cudaError_t launch_ring_key_sums(const View &k, float *ksum, void *ws, cudaStrea
   const dim3 heads((unsigned)H, (unsigned)B);
   cudaError_t e;
   if (k.dtype == FM_BF16)
-    e = D == 128 ? (contig ? launch_ksum<__nv_bfloat16, 4, true>(k, w.P, part, st)
-                           : launch_ksum<__nv_bfloat16, 4, false>(k, w.P, part, st))
-                 : (contig ? launch_ksum<__nv_bfloat16, 2, true>(k, w.P, part, st)
-                           : launch_ksum<__nv_bfloat16, 2, false>(k, w.P, part, st));
+#define FM_KSUM(T, E, C) launch_ksum<T, E, C>(k, w.P, part, nullptr, 0, nullptr, st)
+    e = D == 128 ? (contig ? FM_KSUM(__nv_bfloat16, 4, true) : FM_KSUM(__nv_bfloat16, 4, false))
+                 : (contig ? FM_KSUM(__nv_bfloat16, 2, true) : FM_KSUM(__nv_bfloat16, 2, false));
   else
-    e = D == 128 ? (contig ? launch_ksum<float, 4, true>(k, w.P, part, st) : launch_ksum<float, 4, false>(k, w.P, part, st))
-                 : (contig ? launch_ksum<float, 2, true>(k, w.P, part, st) : launch_ksum<float, 2, false>(k, w.P, part, st));
+    e = D == 128 ? (contig ? FM_KSUM(float, 4, true) : FM_KSUM(float, 4, false))
+                 : (contig ? FM_KSUM(float, 2, true) : FM_KSUM(float, 2, false));
+#undef FM_KSUM
   if (e != cudaSuccess) return e;
   // the ordered sum of the partials, divided by 1
   e = launch_pdl(kmean_kernel, heads, dim3(128), 0, st, part, H, w.P, D, (int64_t)1, ksum);
