@@ -132,6 +132,18 @@ int check_qkv(const View &q, const View &k, const View &v) {
 
 }  // namespace
 
+int current_device_l2_bytes() {
+  static int sizes[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (!sizes[dev]) {
+    int c = 0;
+    cudaDeviceGetAttribute(&c, cudaDevAttrL2CacheSize, dev);
+    sizes[dev] = c > 0 ? c : -1;
+  }
+  return sizes[dev] > 0 ? sizes[dev] : 0;
+}
+
 int current_device_sm_count() {
   static int counts[kMaxDevices] = {};
   int dev = 0;

@@ -180,16 +180,47 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *tm,
       : "memory");
 }
 
+// L2 eviction priorities for bulk copies (createpolicy): evict_last for data read again soon
+// (an accumulator that the next chunk adds into, when it fits in L2), evict_first for data
+// read once (a Q tile of the persistent schedule).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void tma_load_4d_hint(uint32_t dst, const CUtensorMap *tm, uint32_t bar, int c0, int c1,
+                                                 int c2, int c3, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "l"(pol)
+      : "memory");
+}
+
 // O of one Q tile from shared memory into the fp32 accumulator (3-D map over [B*H, Sq, D]):
-// added to it (reduce) or written over it (store).  Rows past Sq are clipped by the map.
-__device__ __forceinline__ void tma_acc_3d(const CUtensorMap *tm, uint32_t src, int c0, int c1, int c2, bool add) {
+// added to it (reduce) or written over it (store), with the L2 priority `pol`.  Rows past Sq
+// are clipped by the map.
+__device__ __forceinline__ void tma_acc_3d(const CUtensorMap *tm, uint32_t src, int c0, int c1, int c2, bool add,
+                                           uint64_t pol) {
   if (add)
-    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
-                     "l"(reinterpret_cast<uint64_t>(tm)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group.L2::cache_hint"
+                 " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(tm)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
                  : "memory");
   else
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
-                     "l"(reinterpret_cast<uint64_t>(tm)), "r"(src), "r"(c0), "r"(c1), "r"(c2)
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+                 " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(tm)),
+                 "r"(src), "r"(c0), "r"(c1), "r"(c2), "l"(pol)
                  : "memory");
 }
 // acc += v (4 consecutive fp32) as one reduction in the memory system: the same fp32 add
@@ -358,6 +389,40 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// O of one warp's 32 rows (its TMEM lane quarter) into the fp32 accumulator, added (red) or
+// stored, without reading it through the SM: each 32-column piece goes from TMEM through the
+// warp's own 4 KiB of shared memory (32 rows x 128 bytes, 16-byte chunks XOR-swizzled by row,
+// so that neither the row-wise writes nor the chunk-wise reads conflict on banks), so that each
+// global access covers four whole 128-byte row pieces.  The reductions are posted, not waited
+// for: the warp moves on while the memory system applies them.  row0 is the warp's first row and
+// acc_row0 its accumulator row; rows at or past Sq are left out.
+__device__ __forceinline__ void o_to_acc_warp(uint8_t *slab, uint32_t tO, int lane, bool tile_ok, int64_t row0,
+                                              int64_t Sq, float *acc_row0, bool add) {
+  const int ch = lane & 7;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t o[32];
+    tmem_ld32(tO + c * 32, o);
+    uint8_t *line = slab + lane * 128;
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4)
+      *reinterpret_cast<uint4 *>(line + ((q4 ^ (lane & 7)) << 4)) =
+          make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = i * 4 + (lane >> 3);
+      const uint4 v = *reinterpret_cast<const uint4 *>(slab + rr * 128 + ((ch ^ (rr & 7)) << 4));
+      if (tile_ok && row0 + rr < Sq) {
+        float *dst = acc_row0 + rr * kHD + c * 32 + ch * 4;
+        if (add) red_add_v4(dst, v.x, v.y, v.z, v.w);
+        else *reinterpret_cast<uint4 *>(dst) = v;
+      }
+    }
+    __syncwarp();  // the slab is read before the next piece overwrites it
+  }
+}
+
 constexpr int kMaxChunks = FM_MAX_CHUNKS;  // consecutive KV chunks one launch can fold
 
 // Tensor maps of Q and of each chunk's K and V (kernel parameter space).
@@ -390,9 +455,10 @@ struct TcParams {
   // nullptr; key0[c] is the global index of chunk c's first key
   const int32_t *sinks;
   int key0[kMaxChunks];
-  // the fixed-m epilogue of a chunk that is not the last stages O in shared memory and adds
-  // it into (or stores it over) acc_o with one bulk tensor operation per 32 columns
-  int acc_tma;
+  // the persistent schedule's epilogue of a chunk that is not the last stages O in shared
+  // memory and adds it into (or stores it over) acc_o with one bulk tensor operation per 32
+  // columns, with L2 priority evict_last when acc_keep (the accumulator fits in L2)
+  int acc_tma, acc_keep;
   // persistent schedule: each CTA walks work items (batch, head, Q-tile pair) item =
   // blockIdx.x, blockIdx.x + gridDim.x, ...; otherwise one item per CTA of a
   // (pairs, H, B) grid.  n_items = B * H * pairs.
@@ -826,6 +892,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row_ok && p.accumulate) sum_new = fixed ? sum_prev + lsum : fmaf(sum_prev, cprev, lsum * cnew);
       const float shift_new = nr;  // b_i on fixed-m rows
       const bool final_out = p.out != nullptr;
+      // A chunk that is not the last, on a tile whose O needs no rescale of the accumulator
+      // (fixed-m; any tile of a first chunk, whose O is simply stored; an online tile whose
+      // every row kept the accumulator's shift, so that cprev = cnew = 1): each warp posts its
+      // rows' O as whole-row reductions (or stores) through 4 KiB of shared memory, so the SM
+      // never reads the accumulator and the CTA need not wait for them before it exits (which
+      // measured 1 % faster per step than staging the tile for bulk tensor reductions).  The
+      // slabs are the Q region for tile 0, free once the last S MMA is done, which the O-done
+      // commit covers, and the first K/V stage for tile 1, free once every MMA is done.
+      bool plain_add = fixed || !p.accumulate;
+      if (!plain_add && !final_out)
+        plain_add = named_barrier_and(1 + t, 128, !row_ok || (shift_prev != -INFINITY && shv == shift_prev));
+      if (plain_add && !final_out) {
+        // the warp's first row is row - lane
+        o_to_acc_warp(gbase + (t == 0 ? kOffQ : kOffKV) + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
+                      p.acc_o + (rflat - lane) * kHD, p.accumulate != 0);
+        if (row_ok) {
+          p.acc_sum[rflat] = sum_new;
+          p.acc_max[rflat] = shift_new;
+        }
+      } else {
+      // the accumulator row comes in 32-column pieces, each loaded while the previous piece is
+      // combined, so that the row pays one memory latency instead of four
       // with the normalise fused in, o = acc / max(sum, 1e-37) goes straight to `out`
       // ("Kernel reference: ring_attention_const_max_fwd": the last ring step folds and
       // normalises); acc_o itself is then not written back
@@ -834,45 +922,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t ooff = bb * p.osB + hh * p.osH + row * p.osS;
       const float4 *src = reinterpret_cast<const float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
       float4 *dst = reinterpret_cast<float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
-      // A chunk that is not the last, on a tile whose O needs no rescale of the accumulator
-      // (fixed-m; any tile of a first chunk, whose O is simply stored; an online tile whose
-      // every row kept the accumulator's shift, so that cprev = cnew = 1): O goes through
-      // shared memory, and one bulk tensor operation per 32 columns adds it into acc_o (or
-      // stores it there) in the memory system, so the SM never reads the accumulator.  The
-      // staging tile (64 KiB of 128-byte-swizzled 32-column boxes) is the Q region for tile 0,
-      // free once the last S MMA is done, which the O-done commit covers, and the first two
-      // K/V stages for tile 1, free once every MMA is done.
-      bool plain_add = fixed || !p.accumulate;
-      if (!plain_add && p.acc_tma && !final_out)
-        plain_add = named_barrier_and(1 + t, 128, !row_ok || (shift_prev != -INFINITY && shv == shift_prev));
-      if (p.acc_tma && plain_add && !final_out) {
-        uint8_t *stage = gbase + (t == 0 ? kOffQ : kOffKV);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          uint8_t *line = stage + c * (kBQ * 128) + r * 128;
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            *reinterpret_cast<uint4 *>(line + ((q4 ^ (r & 7)) << 4)) =
-                make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
-        }
-        fence_proxy_async_smem();
-        named_barrier(1 + t, 128);
-        if (wq == 0 && lane == 0 && tile_ok) {
-          const uint32_t sbase = base + (t == 0 ? kOffQ : kOffKV);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            tma_acc_3d(&maps.acc, sbase + c * (kBQ * 128), c * 32, (int)(qb * kBQ), (int)bh, p.accumulate != 0);
-          bulk_commit_and_wait_smem_read();
-        }
-        if (row_ok) {
-          p.acc_sum[rflat] = sum_new;
-          p.acc_max[rflat] = shift_new;
-        }
-      } else {
-      // the accumulator row comes in 32-column pieces, each loaded while the previous piece is
-      // combined, so that the row pays one memory latency instead of four
       const bool rd = row_ok && p.accumulate;
       float4 ya[8], yb[8];
 #pragma unroll
@@ -990,6 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t q_loads = 0;      // Q tile pairs issued
       int st = 0;                // ring position of the next K/V load (carries over items)
       uint32_t ph = 0;
+      const uint64_t q_pol = policy_evict_first();  // each Q tile is read once per launch
       for (int64_t item = item0; item < p.n_items && ok; item += item_step) {
         const int64_t bh = item_bh(item), qb0 = item_qb0(item);
         const int h = (int)(bh % p.H), b = (int)(bh / p.H);
@@ -1002,8 +1052,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < 2; ++t) {
           mbar_expect_tx(bar(kBarQFull + t), 2 * kPanelBytes);
           for (int pn = 0; pn < 2; ++pn)
-            tma_load_4d(base + kOffQ + t * kTileBytes + pn * kPanelBytes, &maps.q, bar(kBarQFull + t), pn * 64,
-                        (int)((qb0 + t) * kBQ), h, b);
+            tma_load_4d_hint(base + kOffQ + t * kTileBytes + pn * kPanelBytes, &maps.q, bar(kBarQFull + t),
+                             pn * 64, (int)((qb0 + t) * kBQ), h, b, q_pol);
         }
         ++q_loads;
         int c = 0;  // chunk of key tile j
@@ -1242,6 +1292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.acc_tma && plain_add && !final_out) {
         uint8_t *box = gbase + kOffPStage + t * kBoxBytes;
         const uint32_t sbox = base + (uint32_t)(kOffPStage + t * kBoxBytes);
+        // an accumulator that fits in L2 stays there for the next chunk to add into
+        const uint64_t acc_pol = p.acc_keep ? policy_evict_last() : policy_evict_normal();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           if (c > 0) named_barrier(1 + t, 128);  // the previous box has been read
@@ -1255,7 +1307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_smem();
           named_barrier(1 + t, 128);
           if (wq == 0 && lane == 0) {
-            if (tile_ok) tma_acc_3d(&maps.acc, sbox, c * 32, (int)(qb * kBQ), (int)bh, p.accumulate != 0);
+            if (tile_ok) tma_acc_3d(&maps.acc, sbox, c * 32, (int)(qb * kBQ), (int)bh, p.accumulate != 0, acc_pol);
             bulk_commit_and_wait_smem_read();
           }
         }
@@ -1511,10 +1563,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   p.n_items = p.n_pairs * a.q.H * a.q.B;
   const int sms = current_device_sm_count();
   p.persistent = use_persistent(a.schedule) ? 1 : 0;
-  // non-final chunks of the one-item-per-CTA schedule add O into acc_o with bulk tensor
-  // operations where the map encodes (the persistent schedule needs that shared memory for the
-  // next item and adds from registers instead)
-  p.acc_tma = (!a.out && a.q.B * a.q.H <= INT_MAX && encode_acc_map(&maps.acc, a.acc_o, a.q)) ? 1 : 0;
+  // non-final chunks of the persistent schedule add O into acc_o with bulk tensor operations
+  // where the map encodes (the one-item-per-CTA schedule posts whole-row reductions instead);
+  // an accumulator within three quarters of L2 is kept there for the next chunk
+  p.acc_tma = (p.persistent && !a.out && a.q.B * a.q.H <= INT_MAX && encode_acc_map(&maps.acc, a.acc_o, a.q)) ? 1 : 0;
+  const double acc_bytes = 4.0 * (double)kHD * (double)a.q.S * (double)(a.q.B * a.q.H);
+  p.acc_keep = acc_bytes <= 0.75 * (double)current_device_l2_bytes() ? 1 : 0;
   const dim3 grid = p.persistent ? dim3((unsigned)(p.n_items < sms ? p.n_items : sms))
                                  : dim3((unsigned)p.n_pairs, (unsigned)a.q.H, (unsigned)a.q.B);
   return p.persistent ? launch_pdl(fm_chunk_tc_persistent_kernel, grid, dim3(kThreads), kSmemBytes, st, maps, p)

@@ -123,6 +123,8 @@ cudaError_t launch_fold_sinks_final(const View &q, float alpha, const int32_t *s
 
 // ---- helpers shared by host code -------------------------------------------
 int current_device_sm_count();
+// L2 cache size of the current device in bytes (0 if unknown).
+int current_device_l2_bytes();
 
 // Programmatic dependent launch: the kernel may be scheduled while the kernel before it in
 // the stream is still finishing, so its launch latency and block scheduling overlap that
