@@ -313,6 +313,16 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr)
       : "memory");
 }
+// 16 columns of this warp's 32 TMEM lanes (one fp32 column per register), waited for.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+      "%13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : FM_R8(0), FM_R8(8)
+      : "r"(taddr)
+      : "memory");
+}
 // The same load without waiting: the registers are valid only after tmem_ld_wait(r).
 __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
@@ -465,6 +475,106 @@ struct TcParams {
   int persistent;
   int64_t n_items, n_pairs;
 };
+
+// The epilogue that reads the accumulator, for one warp's 32 rows: x = acc + O on fixed-m rows,
+// x = acc*cprev + O*cnew on online rows (x = O when !rd), then either acc = x (out == nullptr)
+// or o = x * inv into `out` (bf16 or fp32; with the normalise fused in).  cprev, cnew and inv
+// are this lane's row's.  As in o_to_acc_warp, every global access covers whole row pieces:
+// each 32-column piece of the rows' accumulator is loaded four rows of 128 bytes per access
+// (the next piece's loads in flight while this one is combined), turned to one row per lane
+// through the warp's 4 KiB of shared memory, combined with O from TMEM, and turned back the
+// same way for the stores.  acc_row0 / out_row0 are the warp's first row (row0); rows at or
+// past Sq are neither read nor written.
+__device__ __forceinline__ void acc_merge_warp(uint8_t *slab, uint32_t tO, int lane, bool tile_ok, int64_t row0,
+                                               int64_t Sq, float *acc_row0, bool rd, bool fixed, float cprev,
+                                               float cnew, float inv, void *out_row0, int64_t osS, bool out_bf16) {
+  const int ch = lane & 7;
+  const int nrows = tile_ok ? (int)max((int64_t)0, min((int64_t)32, Sq - row0)) : 0;  // valid rows of the warp
+  const bool final_out = out_row0 != nullptr;
+  // this lane's row and chunk in the whole-row layout: rows lane / 8 + 4 i, 16-byte chunk lane % 8
+  const float *acc_lane = acc_row0 + (lane >> 3) * kHD + ch * 4;
+  uint4 nxt[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    nxt[i] = (rd && i * 4 + (lane >> 3) < nrows) ? __ldcg(reinterpret_cast<const uint4 *>(acc_lane + i * 4 * kHD))
+                                                 : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rr = i * 4 + (lane >> 3);
+      *reinterpret_cast<uint4 *>(slab + rr * 128 + ((ch ^ (rr & 7)) << 4)) = nxt[i];
+    }
+    __syncwarp();
+    uint4 y[8];  // this lane's row of the piece
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) y[q4] = *reinterpret_cast<const uint4 *>(slab + lane * 128 + ((q4 ^ (lane & 7)) << 4));
+    __syncwarp();  // every lane has its row before the slab is overwritten
+    if (c < 3) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        nxt[i] = (rd && i * 4 + (lane >> 3) < nrows)
+                     ? __ldcg(reinterpret_cast<const uint4 *>(acc_lane + i * 4 * kHD + (c + 1) * 32))
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+    uint32_t o[16];  // O in two 16-column halves, to keep the registers live at once down
+    float x[8];      // two 16-byte chunks at a time
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if ((q & 1) == 0) tmem_ld16(tO + c * 32 + q * 8, o);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 yy = y[2 * q + h];
+        const float yv[4] = {__uint_as_float(yy.x), __uint_as_float(yy.y), __uint_as_float(yy.z), __uint_as_float(yy.w)};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float ov = __uint_as_float(o[8 * (q & 1) + 4 * h + e]);
+          x[4 * h + e] = !rd ? ov : (fixed ? ov + yv[e] : fmaf(yv[e], cprev, ov * cnew));
+        }
+      }
+      if (final_out && out_bf16) {
+        // 64 bytes per row piece: four 16-byte chunks, XOR-swizzled by row pair
+        *reinterpret_cast<uint4 *>(slab + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+            make_uint4(pack_bf16(x[0] * inv, x[1] * inv), pack_bf16(x[2] * inv, x[3] * inv),
+                       pack_bf16(x[4] * inv, x[5] * inv), pack_bf16(x[6] * inv, x[7] * inv));
+      } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int q4 = 2 * q + h;
+          const float *xv = x + 4 * h;
+          *reinterpret_cast<uint4 *>(slab + lane * 128 + ((q4 ^ (lane & 7)) << 4)) =
+              final_out ? make_uint4(__float_as_uint(xv[0] * inv), __float_as_uint(xv[1] * inv),
+                                     __float_as_uint(xv[2] * inv), __float_as_uint(xv[3] * inv))
+                        : make_uint4(__float_as_uint(xv[0]), __float_as_uint(xv[1]), __float_as_uint(xv[2]),
+                                     __float_as_uint(xv[3]));
+        }
+      }
+    }
+    __syncwarp();
+    if (final_out && out_bf16) {
+      const int c4 = lane & 3;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int rr = i * 8 + (lane >> 2);
+        const uint4 v = *reinterpret_cast<const uint4 *>(slab + rr * 64 + ((c4 ^ ((rr >> 1) & 3)) << 4));
+        if (rr < nrows)
+          *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(out_row0) + rr * osS + c * 32 + c4 * 8) = v;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = i * 4 + (lane >> 3);
+        const uint4 v = *reinterpret_cast<const uint4 *>(slab + rr * 128 + ((ch ^ (rr & 7)) << 4));
+        if (rr < nrows) {
+          float *dst = final_out ? reinterpret_cast<float *>(out_row0) + rr * osS + c * 32 + ch * 4
+                                 : acc_row0 + rr * kHD + c * 32 + ch * 4;
+          *reinterpret_cast<uint4 *>(dst) = v;
+        }
+      }
+    }
+    __syncwarp();  // the slab is read before the next piece overwrites it
+  }
+}
 
 // p = 2^(alpha*s - bias) for 32 scores of one full chunk, two at a time with fp32x2 FMA and
 // adds; the row sum goes to two pair accumulators, P to 16 bf16x2 words pk[OFF..OFF+16).
@@ -912,58 +1022,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.acc_max[rflat] = shift_new;
         }
       } else {
-      // the accumulator row comes in 32-column pieces, each loaded while the previous piece is
-      // combined, so that the row pays one memory latency instead of four
-      // with the normalise fused in, o = acc / max(sum, 1e-37) goes straight to `out`
-      // ("Kernel reference: ring_attention_const_max_fwd": the last ring step folds and
-      // normalises); acc_o itself is then not written back
+      // the accumulator is read: the last chunk (o = (acc + O) / sum goes to `out`; "Kernel
+      // reference: ring_attention_const_max_fwd": the last ring step folds and normalises, and
+      // acc_o itself is not written back) or an online tile whose shift moved (acc = acc*cprev +
+      // O*cnew); whole-row accesses per warp through its 4 KiB slab
       const float inv = final_out ? 1.0f / fmaxf(sum_new, FM_SUM_CLAMP) : 1.0f;
-      const int64_t hh = bh % p.H, bb = bh / p.H;
-      const int64_t ooff = bb * p.osB + hh * p.osH + row * p.osS;
-      const float4 *src = reinterpret_cast<const float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
-      float4 *dst = reinterpret_cast<float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
-      const bool rd = row_ok && p.accumulate;
-      float4 ya[8], yb[8];
-#pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) ya[q4] = rd ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float4(&ycur)[8] = (c & 1) ? yb : ya;
-        float4(&ynext)[8] = (c & 1) ? ya : yb;
-        if (c < 3) {
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) ynext[q4] = rd ? src[(c + 1) * 8 + q4] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
-        if (row_ok) {
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            float4 x = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
-                                   __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
-            if (p.accumulate) {
-              const float4 y = ycur[q4];
-              if (fixed) {
-                x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-              } else {
-                x.x = fmaf(y.x, cprev, x.x * cnew); x.y = fmaf(y.y, cprev, x.y * cnew);
-                x.z = fmaf(y.z, cprev, x.z * cnew); x.w = fmaf(y.w, cprev, x.w * cnew);
-              }
-            }
-            if (!final_out) {
-              dst[c * 8 + q4] = x;
-            } else if (p.out_bf16) {
-              uint2 u;
-              u.x = pack_bf16(x.x * inv, x.y * inv);
-              u.y = pack_bf16(x.z * inv, x.w * inv);
-              *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + ooff + c * 32 + q4 * 4) = u;
-            } else {
-              *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + ooff + c * 32 + q4 * 4) =
-                  make_float4(x.x * inv, x.y * inv, x.z * inv, x.w * inv);
-            }
-          }
-        }
+      void *out_row0 = nullptr;
+      if (final_out) {
+        const int64_t ooff0 = (bh / p.H) * p.osB + (bh % p.H) * p.osH + (row - lane) * p.osS;
+        out_row0 = p.out_bf16 ? static_cast<void *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + ooff0)
+                              : static_cast<void *>(reinterpret_cast<float *>(p.out) + ooff0);
       }
+      acc_merge_warp(gbase + (t == 0 ? kOffQ : kOffKV) + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
+                     p.acc_o + (rflat - lane) * kHD, p.accumulate != 0, fixed, cprev, cnew, inv, out_row0, p.osS,
+                     p.out_bf16 != 0);
       if (row_ok) {
         p.acc_sum[rflat] = sum_new;
         p.acc_max[rflat] = shift_new;
@@ -1271,14 +1343,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row_ok && p.accumulate) sum_new = fixed ? sum_prev + lsum : fmaf(sum_prev, cprev, lsum * cnew);
       const float shift_new = nr;  // b_i on fixed-m rows
       const bool final_out = p.out != nullptr;
-      // with the normalise fused in, o = acc / max(sum, 1e-37) goes straight to `out`
-      // ("Kernel reference: ring_attention_const_max_fwd": the last ring step folds and
-      // normalises); acc_o itself is then not written back
-      const float inv = final_out ? 1.0f / fmaxf(sum_new, FM_SUM_CLAMP) : 1.0f;
-      const int64_t hh = bh % p.H, bb = bh / p.H;
-      const int64_t ooff = bb * p.osB + hh * p.osH + row * p.osS;
-      const float4 *src = reinterpret_cast<const float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
-      float4 *dst = reinterpret_cast<float4 *>(p.acc_o + (row_ok ? rflat : 0) * kHD);
       // A chunk that is not the last, on a tile whose O needs no rescale of the accumulator
       // (fixed-m; any tile of a first chunk, whose O is simply stored; an online tile whose
       // every row kept the accumulator's shift, so that cprev = cnew = 1), adds O into acc_o
@@ -1316,70 +1380,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.acc_max[rflat] = shift_new;
         }
       } else if (plain_add && !final_out) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          if (row_ok) {
-            float *rowp = p.acc_o + rflat * kHD + c * 32;
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              if (p.accumulate)
-                red_add_v4(rowp + 4 * q4, o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
-              else
-                *reinterpret_cast<uint4 *>(rowp + 4 * q4) = make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
-            }
-          }
-        }
+        o_to_acc_warp(gbase + kOffPStage + t * kBoxBytes + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
+                      p.acc_o + (rflat - lane) * kHD, p.accumulate != 0);
         if (row_ok) {
           p.acc_sum[rflat] = sum_new;
           p.acc_max[rflat] = shift_new;
         }
       } else {
-      // the accumulator row comes in 32-column pieces, each loaded while the previous piece is
-      // combined, so that the row pays one memory latency instead of four
-      const bool rd = row_ok && p.accumulate;
-      float4 ya[8], yb[8];
-#pragma unroll
-      for (int q4 = 0; q4 < 8; ++q4) ya[q4] = rd ? src[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float4(&ycur)[8] = (c & 1) ? yb : ya;
-        float4(&ynext)[8] = (c & 1) ? ya : yb;
-        if (c < 3) {
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) ynext[q4] = rd ? src[(c + 1) * 8 + q4] : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
-        if (row_ok) {
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            float4 x = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
-                                   __uint_as_float(o[4 * q4 + 2]), __uint_as_float(o[4 * q4 + 3]));
-            if (p.accumulate) {
-              const float4 y = ycur[q4];
-              if (fixed) {
-                x.x += y.x; x.y += y.y; x.z += y.z; x.w += y.w;
-              } else {
-                x.x = fmaf(y.x, cprev, x.x * cnew); x.y = fmaf(y.y, cprev, x.y * cnew);
-                x.z = fmaf(y.z, cprev, x.z * cnew); x.w = fmaf(y.w, cprev, x.w * cnew);
-              }
-            }
-            if (!final_out) {
-              dst[c * 8 + q4] = x;
-            } else if (p.out_bf16) {
-              uint2 u;
-              u.x = pack_bf16(x.x * inv, x.y * inv);
-              u.y = pack_bf16(x.z * inv, x.w * inv);
-              *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + ooff + c * 32 + q4 * 4) = u;
-            } else {
-              *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.out) + ooff + c * 32 + q4 * 4) =
-                  make_float4(x.x * inv, x.y * inv, x.z * inv, x.w * inv);
-            }
-          }
-        }
+      // the accumulator is read: the last chunk (o = (acc + O) / sum goes to `out`; "Kernel
+      // reference: ring_attention_const_max_fwd": the last ring step folds and normalises, and
+      // acc_o itself is not written back) or an online tile whose shift moved (acc = acc*cprev +
+      // O*cnew); whole-row accesses per warp through its 4 KiB slab
+      const float inv = final_out ? 1.0f / fmaxf(sum_new, FM_SUM_CLAMP) : 1.0f;
+      void *out_row0 = nullptr;
+      if (final_out) {
+        const int64_t ooff0 = (bh / p.H) * p.osB + (bh % p.H) * p.osH + (row - lane) * p.osS;
+        out_row0 = p.out_bf16 ? static_cast<void *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + ooff0)
+                              : static_cast<void *>(reinterpret_cast<float *>(p.out) + ooff0);
       }
+      acc_merge_warp(gbase + kOffPStage + t * kBoxBytes + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
+                     p.acc_o + (rflat - lane) * kHD, p.accumulate != 0, fixed, cprev, cnew, inv, out_row0, p.osS,
+                     p.out_bf16 != 0);
       if (row_ok) {
         p.acc_sum[rflat] = sum_new;
         p.acc_max[rflat] = shift_new;
@@ -1490,7 +1511,7 @@ bool chunk_tc_supported(const ChunkArgs &a) {
 
 bool chunk_tc_final_supported(const ChunkArgs &a, const View &o) {
   const int64_t es = o.dtype == FM_F32 ? 4 : 2;
-  const int64_t vec = 4 * es;  // bytes of one vector store (4 elements)
+  const int64_t vec = 16;  // bytes of one vector store (4 fp32 or 8 bf16 elements)
   return o.D == kHD && o.sD == 1 && reinterpret_cast<uintptr_t>(o.ptr) % 16 == 0 &&
          (o.sS * es) % vec == 0 && (o.sH * es) % vec == 0 && (o.sB * es) % vec == 0 && o.B == a.q.B &&
          o.H == a.q.H && o.S == a.q.S;
