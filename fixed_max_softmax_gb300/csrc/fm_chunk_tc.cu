@@ -1056,9 +1056,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The persistent schedule (fm_opts.schedule = FM_SCHEDULE_PERSISTENT): one CTA per SM walks work
 // items blockIdx.x, blockIdx.x + gridDim.x, ...; barrier phases and the K/V ring position carry
 // over from item to item, and a Q-empty commit after an item's last S MMA lets the producer load
-// the next item's Q while the softmax warps run the epilogue.  The accumulator add comes from
-// registers (vector reductions), since the next item's Q and K/V already occupy the shared
-// memory the staged epilogue would use.
+// the next item's Q while the softmax warps run the epilogue.  Its K/V ring has one stage fewer
+// than the grid schedule's: that stage's space stages O for the bulk tensor reductions into the
+// accumulator, one 16 KiB box per softmax group, while the next item's Q and K/V load.
 __global__ void __launch_bounds__(kThreads, 1)
     fm_chunk_tc_persistent_kernel(const __grid_constant__ TcMaps maps, const __grid_constant__ TcParams p) {
   pdl_wait();  // bounds and accumulators written by the kernels before this one
@@ -1349,7 +1349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // (or stores it there) without reading the accumulator through the SM: one 32-column box
       // at a time through the group's 16 KiB in the ring's fifth stage, with bulk tensor
       // reductions (the next item's Q and K/V load meanwhile), or, without an accumulator map,
-      // from registers with vector reductions.
+      // with whole-row vector reductions per warp through the same box.
       bool plain_add = fixed || !p.accumulate;
       if (!plain_add && !final_out)
         plain_add = named_barrier_and(1 + t, 128, !row_ok || (shift_prev != -INFINITY && shv == shift_prev));
