@@ -399,6 +399,15 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// The lane index, read where it is used: arithmetic on it cannot be hoisted out of an enclosing
+// loop (IN_LOOP: the epilogue helpers run once per item inside the persistent kernel's item
+// loop, and their lane-dependent addresses would otherwise stay live across every key tile).
+__device__ __forceinline__ int opaque_laneid() {
+  int l;
+  asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
+  return l;
+}
+
 // O of one warp's 32 rows (its TMEM lane quarter) into the fp32 accumulator, added (red) or
 // stored, without reading it through the SM: each 32-column piece goes from TMEM through the
 // warp's own 4 KiB of shared memory (32 rows x 128 bytes, 16-byte chunks XOR-swizzled by row,
@@ -406,8 +415,10 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // global access covers four whole 128-byte row pieces.  The reductions are posted, not waited
 // for: the warp moves on while the memory system applies them.  row0 is the warp's first row and
 // acc_row0 its accumulator row; rows at or past Sq are left out.
+template <bool IN_LOOP = false>
 __device__ __forceinline__ void o_to_acc_warp(uint8_t *slab, uint32_t tO, int lane, bool tile_ok, int64_t row0,
                                               int64_t Sq, float *acc_row0, bool add) {
+  if constexpr (IN_LOOP) lane = opaque_laneid();
   const int ch = lane & 7;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -479,20 +490,29 @@ struct TcParams {
 // The epilogue that reads the accumulator, for one warp's 32 rows: x = acc + O on fixed-m rows,
 // x = acc*cprev + O*cnew on online rows (x = O when !rd), then either acc = x (out == nullptr)
 // or o = x * inv into `out` (bf16 or fp32; with the normalise fused in).  cprev, cnew and inv
-// are this lane's row's.  As in o_to_acc_warp, every global access covers whole row pieces:
-// each 32-column piece of the rows' accumulator is loaded four rows of 128 bytes per access
-// (the next piece's loads in flight while this one is combined), turned to one row per lane
-// through the warp's 4 KiB of shared memory, combined with O from TMEM, and turned back the
-// same way for the stores.  acc_row0 / out_row0 are the warp's first row (row0); rows at or
-// past Sq are neither read nor written.
+// are this lane's row's.  As in o_to_acc_warp, every global access covers whole row pieces.
+// Per 32-column piece, through the warp's 4 KiB of shared memory (32 rows x 128 bytes, 16-byte
+// chunks XOR-swizzled by row):
+//   1. the rows' accumulator piece comes in four rows of 128 bytes per load (the next piece's
+//      loads are in flight while this one is combined) and is parked in the rows;
+//   2. each lane combines its own row with O from TMEM and writes the result back into its own
+//      row (fp32 in place; bf16 into the even chunks), so no lane touches another's row here;
+//   3. the rows go out four (fp32) or eight (bf16) to a store.
+// acc_row0 / out_row0 are the warp's first row (row0); rows at or past Sq are neither read nor
+// written.
+template <bool IN_LOOP = false>
 __device__ __forceinline__ void acc_merge_warp(uint8_t *slab, uint32_t tO, int lane, bool tile_ok, int64_t row0,
                                                int64_t Sq, float *acc_row0, bool rd, bool fixed, float cprev,
                                                float cnew, float inv, void *out_row0, int64_t osS, bool out_bf16) {
+  if constexpr (IN_LOOP) lane = opaque_laneid();
   const int ch = lane & 7;
   const int nrows = tile_ok ? (int)max((int64_t)0, min((int64_t)32, Sq - row0)) : 0;  // valid rows of the warp
   const bool final_out = out_row0 != nullptr;
+  const bool bf16_out = final_out && out_bf16;
   // this lane's row and chunk in the whole-row layout: rows lane / 8 + 4 i, 16-byte chunk lane % 8
   const float *acc_lane = acc_row0 + (lane >> 3) * kHD + ch * 4;
+  uint8_t *own = slab + lane * 128;  // this lane's row
+  const int sw = lane & 7;
   uint4 nxt[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
@@ -506,10 +526,6 @@ __device__ __forceinline__ void acc_merge_warp(uint8_t *slab, uint32_t tO, int l
       *reinterpret_cast<uint4 *>(slab + rr * 128 + ((ch ^ (rr & 7)) << 4)) = nxt[i];
     }
     __syncwarp();
-    uint4 y[8];  // this lane's row of the piece
-#pragma unroll
-    for (int q4 = 0; q4 < 8; ++q4) y[q4] = *reinterpret_cast<const uint4 *>(slab + lane * 128 + ((q4 ^ (lane & 7)) << 4));
-    __syncwarp();  // every lane has its row before the slab is overwritten
     if (c < 3) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
@@ -517,32 +533,30 @@ __device__ __forceinline__ void acc_merge_warp(uint8_t *slab, uint32_t tO, int l
                      ? __ldcg(reinterpret_cast<const uint4 *>(acc_lane + i * 4 * kHD + (c + 1) * 32))
                      : make_uint4(0u, 0u, 0u, 0u);
     }
-    uint32_t o[16];  // O in two 16-column halves, to keep the registers live at once down
-    float x[8];      // two 16-byte chunks at a time
+    uint32_t o[16];  // O in two 16-column halves
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       if ((q & 1) == 0) tmem_ld16(tO + c * 32 + q * 8, o);
+      float x[8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 yy = y[2 * q + h];
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint4 yy = *reinterpret_cast<const uint4 *>(own + (((2 * q + hh) ^ sw) << 4));
         const float yv[4] = {__uint_as_float(yy.x), __uint_as_float(yy.y), __uint_as_float(yy.z), __uint_as_float(yy.w)};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float ov = __uint_as_float(o[8 * (q & 1) + 4 * h + e]);
-          x[4 * h + e] = !rd ? ov : (fixed ? ov + yv[e] : fmaf(yv[e], cprev, ov * cnew));
+          const float ov = __uint_as_float(o[8 * (q & 1) + 4 * hh + e]);
+          x[4 * hh + e] = !rd ? ov : (fixed ? ov + yv[e] : fmaf(yv[e], cprev, ov * cnew));
         }
       }
-      if (final_out && out_bf16) {
-        // 64 bytes per row piece: four 16-byte chunks, XOR-swizzled by row pair
-        *reinterpret_cast<uint4 *>(slab + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+      if (bf16_out) {
+        *reinterpret_cast<uint4 *>(own + (((2 * q) ^ sw) << 4)) =
             make_uint4(pack_bf16(x[0] * inv, x[1] * inv), pack_bf16(x[2] * inv, x[3] * inv),
                        pack_bf16(x[4] * inv, x[5] * inv), pack_bf16(x[6] * inv, x[7] * inv));
       } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int q4 = 2 * q + h;
-          const float *xv = x + 4 * h;
-          *reinterpret_cast<uint4 *>(slab + lane * 128 + ((q4 ^ (lane & 7)) << 4)) =
+        for (int hh = 0; hh < 2; ++hh) {
+          const float *xv = x + 4 * hh;
+          *reinterpret_cast<uint4 *>(own + (((2 * q + hh) ^ sw) << 4)) =
               final_out ? make_uint4(__float_as_uint(xv[0] * inv), __float_as_uint(xv[1] * inv),
                                      __float_as_uint(xv[2] * inv), __float_as_uint(xv[3] * inv))
                         : make_uint4(__float_as_uint(xv[0]), __float_as_uint(xv[1]), __float_as_uint(xv[2]),
@@ -551,12 +565,13 @@ __device__ __forceinline__ void acc_merge_warp(uint8_t *slab, uint32_t tO, int l
       }
     }
     __syncwarp();
-    if (final_out && out_bf16) {
+    if (bf16_out) {
+      // 64 bytes per row piece in its even chunks: eight rows per store
       const int c4 = lane & 3;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int rr = i * 8 + (lane >> 2);
-        const uint4 v = *reinterpret_cast<const uint4 *>(slab + rr * 64 + ((c4 ^ ((rr >> 1) & 3)) << 4));
+        const uint4 v = *reinterpret_cast<const uint4 *>(slab + rr * 128 + (((2 * c4) ^ (rr & 7)) << 4));
         if (rr < nrows)
           *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(out_row0) + rr * osS + c * 32 + c4 * 8) = v;
       }
@@ -1363,10 +1378,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c > 0) named_barrier(1 + t, 128);  // the previous box has been read
           uint32_t o[32];
           tmem_ld32(tO + c * 32, o);
-          uint8_t *line = box + r * 128;
+          const int rl = wq * 32 + opaque_laneid();  // r, computed here (see opaque_laneid)
+          uint8_t *line = box + rl * 128;
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4)
-            *reinterpret_cast<uint4 *>(line + ((q4 ^ (r & 7)) << 4)) =
+            *reinterpret_cast<uint4 *>(line + ((q4 ^ (rl & 7)) << 4)) =
                 make_uint4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
           fence_proxy_async_smem();
           named_barrier(1 + t, 128);
@@ -1380,7 +1396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.acc_max[rflat] = shift_new;
         }
       } else if (plain_add && !final_out) {
-        o_to_acc_warp(gbase + kOffPStage + t * kBoxBytes + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
+        o_to_acc_warp<true>(gbase + kOffPStage + t * kBoxBytes + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
                       p.acc_o + (rflat - lane) * kHD, p.accumulate != 0);
         if (row_ok) {
           p.acc_sum[rflat] = sum_new;
@@ -1398,7 +1414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         out_row0 = p.out_bf16 ? static_cast<void *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + ooff0)
                               : static_cast<void *>(reinterpret_cast<float *>(p.out) + ooff0);
       }
-      acc_merge_warp(gbase + kOffPStage + t * kBoxBytes + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
+      acc_merge_warp<true>(gbase + kOffPStage + t * kBoxBytes + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
                      p.acc_o + (rflat - lane) * kHD, p.accumulate != 0, fixed, cprev, cnew, inv, out_row0, p.osS,
                      p.out_bf16 != 0);
       if (row_ok) {
