@@ -125,7 +125,7 @@ class ClockSampler:
                 self.out = ""
 
     def summary(self):
-        sms, maxs, reasons = [], [], set()
+        sms, maxs, watts, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in (self.out or "").splitlines():
             parts = [x.strip() for x in line.split(",")]
@@ -136,13 +136,17 @@ class ClockSampler:
                 maxs.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                watts.append(float(parts[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, parts[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sms:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
         return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
-                "samples": len(sms)}
+                "samples": len(sms), "power_w": statistics.median(watts) if watts else None}
 
 
 def cpu_oracle_sample(target_s: float = 12.0, max_rows: int = 24576):
@@ -359,10 +363,12 @@ def run_ours(args, rank, world, local_rank):
         fm.fm_sync_status(stream)
         barrier()
         torch.cuda.synchronize(dev)
-        t0 = time.perf_counter()
-        hp.run([(qh, kh, vh, outs[i % 2]) for i in range(args.e2e_steps)], chunks)
-        torch.cuda.synchronize(dev)
-        te = max_over_ranks((time.perf_counter() - t0) * 1e3, dev)
+        with ClockSampler(local_rank) as clk_e2e:
+            t0 = time.perf_counter()
+            hp.run([(qh, kh, vh, outs[i % 2]) for i in range(args.e2e_steps)], chunks)
+            torch.cuda.synchronize(dev)
+            te = max_over_ranks((time.perf_counter() - t0) * 1e3, dev)
+        ce = clk_e2e.summary()
         fm.fm_sync_status(stream)
         # the machine's host link, for reading the figure: one 774 MB pinned copy each way, timed alone
         link = {}
@@ -376,6 +382,7 @@ def run_ours(args, rank, world, local_rank):
             link[name] = src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
         e2e = {"value": whole_job_tflops(world, step_flops, args.e2e_steps, te), "unit": "TFLOP/s",
                "host_link": {k2: round(v2, 1) for k2, v2 in link.items()},
+               "clocks": {k2: ce[k2] for k2 in ("sm_mhz", "power_w", "reasons", "samples")},
                "h2d_bytes_per_step": int(3 * q.numel() * q.element_size()),
                "d2h_bytes_per_step": int(fa.out.numel() * fa.out.element_size()),
                "ms_per_step": te / args.e2e_steps, "steps": args.e2e_steps,
@@ -459,7 +466,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "one_launch": one_launch,
-        "clocks": {k2: clocks[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons")},
+        "clocks": {k2: clocks[k2] for k2 in ("sm_mhz", "sm_max_mhz", "reasons", "power_w")},
     }
     print(json.dumps(line), flush=True)
 
