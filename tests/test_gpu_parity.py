@@ -775,10 +775,9 @@ def test_randomised_shapes_and_options(dev):
 @pytest.mark.parametrize("force_online", [False, True])
 @pytest.mark.parametrize("mode", ["chunks", "fused", "one_launch", "sinks"])
 def test_persistent_schedule_gives_the_grid_bits(dev, mode, force_online):
-    """The persistent schedule (one CTA per SM walking work items, accumulator adds from
-    registers) and the one-CTA-per-item grid (adds through shared memory and bulk tensor
-    reductions) do the same fp32 arithmetic in the same order: identical bits, on more work
-    items (20 heads x 8 Q-tile pairs, the last pair half past Sq) than a GB300 has SMs."""
+    """The persistent schedule (one CTA per SM walking work items) and the grid schedule (one
+    CTA per work item) do the same fp32 arithmetic in the same order: identical bits, on more
+    work items (20 heads x 8 Q-tile pairs, the last pair half past Sq) than a GB300 has SMs."""
     H, Sq, N = 20, 1900, 1500
     name = "sinks" if mode == "sinks" else "mix"
     q, k, v = workloads.make_inputs(name, device="cpu", heads=range(H), Sq=Sq, N=N)
