@@ -144,7 +144,7 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sms:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "power_w": None}
         return {"sm_mhz": statistics.median(sms), "sm_max_mhz": max(maxs), "reasons": sorted(reasons),
                 "samples": len(sms), "power_w": statistics.median(watts) if watts else None}
 
@@ -313,6 +313,23 @@ def run_ours(args, rank, world, local_rank):
     chunk_ms = [chunk_events[i].elapsed_time(chunk_events[i + 1]) for i in range(0, len(chunk_events), 2)]
     bounds_ms = statistics.mean(bounds_events[i].elapsed_time(bounds_events[i + 1])
                                 for i in range(0, len(bounds_events), 2))
+    # the bounds pass again without centering (no key sums; the same norms and finish): with it,
+    # the two kernels' shares of the pass, each against its own bytes
+    bounds_off_ms = None
+    if centering and not args.sink_keys:
+        off = fm.opts(fa.opt.softmax_scale, False, bool(fa.opt.force_online), bool(fa.opt.per_row), 0,
+                      int(fa.opt.schedule))
+        off_events = []
+        for _ in range(args.steps):
+            if flush is not None:
+                flush.fill_(1)
+            off_events.append((torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)))
+            off_events[-1][0].record(stream)
+            fm.fm_bounds(q, k, v, off, fa.bounds, fa.workspace, stream)
+            off_events[-1][1].record(stream)
+        torch.cuda.synchronize(dev)
+        fm.fm_sync_status(stream)
+        bounds_off_ms = statistics.mean(a.elapsed_time(b) for a, b in off_events)
     t_ms = max_over_ranks(t_ms, dev)
     ms_per_step = t_ms / args.steps
     value = whole_job_tflops(world, step_flops, args.steps, t_ms)
@@ -433,6 +450,16 @@ def run_ours(args, rank, world, local_rank):
                    "frac": bounds_bytes / (bounds_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
                    "kernels": "key sums with the key mean (centering), norms, finish with the row shifts",
                    "how": "CUDA events around fm_bounds, in as many steps again right after the timed region"}
+    if bounds_off_ms is not None:
+        kb = k.element_size() * w.B * H * w.N * w.D  # the key sums read K once
+        nb = bounds_bytes - kb                          # the norms read Q, K and V once
+        ks_ms = bounds_ms - bounds_off_ms
+        bounds_line["per_kernel"] = {
+            "key_sums": {"ms": ks_ms, "bytes": kb, "achieved": kb / (ks_ms * 1e-3) / 1e9 if ks_ms > 0 else None},
+            "norms_and_finish": {"ms": bounds_off_ms, "bytes": nb, "achieved": nb / (bounds_off_ms * 1e-3) / 1e9},
+            "unit": "GB/s",
+            "how": "the pass timed again without centering (norms and finish only, the same bytes): the key sums "
+                   "are the difference"}
     cpu = None
     if world == 1 and not args.no_cpu_baseline and w.name == WORKLOAD:
         cv, info = cpu_oracle_sample(args.cpu_seconds)

@@ -49,3 +49,19 @@ def test_two_gloo_ranks_take_the_slowest_time():
 def test_single_process_is_unchanged():
     assert bench.max_over_ranks(12.5) == 12.5
     assert bench.whole_job_tflops(1, 2e12, 5, 1000.0) == pytest.approx(10.0)
+
+
+def test_clock_summary_keys_with_and_without_samples():
+    """The clock record always carries the keys the bench line reads, also when the timed
+    region was too short for any nvidia-smi sample."""
+    keys = {"sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w"}
+    c = bench.ClockSampler(0)
+    c.out = ""
+    empty = c.summary()
+    assert keys <= set(empty) and empty["samples"] == 0 and empty["sm_mhz"] is None
+    c.out = ("0, 1980, 2070, 1215.37, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n"
+             "0, 1990, 2070, 1200.00, 0x0000000000000004, Not Active, Not Active, Not Active, Active\n")
+    full = c.summary()
+    assert keys <= set(full) and full["samples"] == 2
+    assert full["sm_mhz"] == 1985.0 and full["sm_max_mhz"] == 2070.0 and full["reasons"] == ["sw_power_cap"]
+    assert abs(full["power_w"] - 1207.685) < 1e-9
