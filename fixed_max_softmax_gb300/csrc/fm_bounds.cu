@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kThreads)
 // A row of D elements is spread over LPR lanes with VEC consecutive elements each, so one warp
 // load covers RPW = 32 / LPR rows; each lane keeps kUnroll such loads in flight before it
 // reduces, which is what keeps HBM busy (one 256-byte row per warp at a time is not enough).
-constexpr int kUnroll = 4;
+constexpr int kUnroll = 8;
 template <typename T, int D>
 struct Vec16 {
   static constexpr int VEC = 16 / (int)sizeof(T);
