@@ -10,10 +10,12 @@
 // ring_attention_const_max_fwd", section "Transpose prologue with fused norms"; the key
 // mean over real tokens of PR #478, Summary.
 //
-// Launches (all deterministic: fixed-order sums, maxima without atomics):
+// Launches (all deterministic: sums in a fixed order; maxima in shared memory or by integer
+// atomicMax on the bits of non-negative floats, whose result does not depend on the order):
 //   1. ksum    (centering only) partial key sums, P row ranges per head  -> workspace; the last
 //              CTA of a head to finish adds the P partials in their fixed order and
 //              divides by N                                                -> kbar
+//   (2. kmean  the same ordered sum as a launch of its own, for the ring's key sums)
 //   3. main    the norms over Q-blocks, K row-blocks and V row-blocks: row norms via warp
 //              shuffles; per-block maxima -> qmax_sq (Q) and the workspace (K, V);
 //              qkbar per row; with key sinks, each K block's n_sink + 1 loudest keys.  One of
@@ -1130,7 +1132,7 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// 4+5. Per block of kFinishRows query rows of one head: the head's key max (over its K blocks, or
+// 4. Per block of kFinishRows query rows of one head: the head's key max (over its K blocks, or
 // the key-sink pass's value), the global V max (folded in by the norms pass), then U, m and flag
 // of the block's Q-blocks and every row's shift b_i = m_i + alpha*q_i.kbar (m_i per row or per
 // Q-block), in one launch.  Every CTA of a head reduces the head's K-block maxima itself (nkb
