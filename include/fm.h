@@ -112,7 +112,9 @@ typedef struct {
  * tile of the call.  GRID launches one CTA per item.  PERSISTENT launches one CTA per SM that
  * walks the items in turn, loading the next item's Q and K/V tiles and running its first S
  * MMAs while the softmax warps finish the current item's epilogue (its K/V ring has one stage
- * fewer; that space stages O for the bulk accumulator add).  AUTO takes PERSISTENT when the
+ * fewer; that space stages O for the bulk accumulator add; the CTAs with one item fewer start
+ * spread over an item's time, so that the CTAs' epilogues do not all meet the memory system at
+ * once).  AUTO takes PERSISTENT when the
  * call has at most 8 key tiles (1024 keys) and at least twice as many items as the GPU has SMs,
  * GRID otherwise: measured on GB300, the overlap pays on such short items and the simpler grid
  * wins on longer ones. */
