@@ -756,10 +756,26 @@ __global__ void __launch_bounds__(kNbThreads, 1)
   // K-blocks and of the V-blocks), since the kinds cost different arithmetic per byte.  Items are
   // numbered Q-blocks, then K-blocks, then V-blocks; seg_range gives run `seg` as [a, e).
   const int64_t G = gridDim.x, c = blockIdx.x;
+  // Where a CTA's share is a few blocks of each kind (fewer than 16 K-blocks), the block left
+  // over per kind would land on the same CTAs three times (up to 15 % more bytes for them at
+  // 4,096 keys): there the first n mod G CTAs of a rotated order take one block more, and the
+  // rotations put those CTAs of the three kinds next to one another (Q's at CTAs [0, rQ), K's at
+  // [rQ, rQ + rK), V's after, wrapping round G): the H40 S4096 pass 45.7 -> 42.7 us.  Larger
+  // shares keep the plain even cut (the rotated one measured 1 % slower at Wan).
+  const int64_t rQ = nQ % G, rK = nK % G;
+  const bool rotate = nK < 16 * G;
   auto seg_range = [&](int seg, int64_t &a, int64_t &e) {
     const int64_t n = seg == 0 ? nQ : nK, off = seg == 0 ? 0 : (seg == 1 ? nQ : nQ + nK);
-    a = off + c * n / G;
-    e = off + (c + 1) * n / G;
+    if (!rotate) {
+      a = off + c * n / G;
+      e = off + (c + 1) * n / G;
+      return;
+    }
+    const int64_t first = seg == 0 ? 0 : (seg == 1 ? rQ : rQ + rK);  // CTA of the rotated slot 0
+    const int64_t cc = ((c - first) % G + G) % G;                     // this CTA's rotated slot
+    const int64_t qn = n / G, r = n % G;
+    a = off + cc * qn + (cc < r ? cc : r);
+    e = a + qn + (cc < r ? 1 : 0);
   };
   // The runs in the order Q, K, V; with centering K, Q, V: the key sums have just read K, so at
   // sizes where K fits in L2 the K-blocks come from there (the 4,096-key pass 57.0 -> 54.9 us;
