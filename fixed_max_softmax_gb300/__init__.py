@@ -28,15 +28,16 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libfm.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "_build_debug", "libfm.so")  # build(debug=True): kernel index checks
 
 FM_F32, FM_BF16, FM_F16, FM_F8E4M3, FM_F8E5M2 = 0, 1, 2, 3, 4
 FM_OK, FM_ERR_ARG, FM_ERR_SHAPE, FM_ERR_DTYPE, FM_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
-FM_ERR_BOUNDS_MISMATCH, FM_ERR_CUDA, FM_ERR_TIMEOUT = 5, 6, 7
+FM_ERR_BOUNDS_MISMATCH, FM_ERR_CUDA, FM_ERR_TIMEOUT, FM_ERR_INDEX = 5, 6, 7, 8
 FM_BOUNDS_MAGIC = 0x314D4246
 FM_BOUNDS_LOCAL_MAGIC = 0x314C4246
 FM_BLOCK_Q = 128
 ERROR_NAMES = {0: "FM_OK", 1: "FM_ERR_ARG", 2: "FM_ERR_SHAPE", 3: "FM_ERR_DTYPE", 4: "FM_ERR_UNSUPPORTED",
-               5: "FM_ERR_BOUNDS_MISMATCH", 6: "FM_ERR_CUDA", 7: "FM_ERR_TIMEOUT"}
+               5: "FM_ERR_BOUNDS_MISMATCH", 6: "FM_ERR_CUDA", 7: "FM_ERR_TIMEOUT", 8: "FM_ERR_INDEX"}
 ABI_SYMBOLS = ("fm_bounds_workspace_size", "fm_bounds", "fm_attn_chunk", "fm_finalize", "fm_sync_status",
                "fm_last_error", "fm_version", "fm_bounds_noalloc", "fm_finalize_lse", "fm_probe_wait_timeout",
                "fm_attn_chunk_final", "fm_attn_chunks", "fm_fold_sinks", "fm_ring_stats_bytes", "fm_ring_key_sums",

@@ -2,7 +2,8 @@
 
 Each translation unit under csrc/ is compiled in parallel to an object file, then the
 objects are linked into fixed_max_softmax_gb300/_build/libfm.so (static CUDA runtime).
-Only the fm_* entry points of include/fm.h are exported.
+Only the fm_* entry points of include/fm.h are exported.  build(debug=True) makes the same
+library with -DFM_DEBUG in _build_debug/: the kernels' index checks on (FM_ERR_INDEX).
 """
 from __future__ import annotations
 
@@ -16,6 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libfm.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
 SOURCES = ["fm_api.cu", "fm_bounds.cu", "fm_chunk_simt.cu", "fm_chunk_tc.cu", "fm_finalize.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc" if os.path.exists("/usr/local/cuda/bin/nvcc") else "nvcc")
@@ -33,17 +35,19 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, debug: bool = False) -> str:
+    build_dir = BUILD_DEBUG if debug else BUILD
+    lib = os.path.join(build_dir, "libfm.so")
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, "fm_internal.h"), os.path.join(ROOT, "include", "fm.h")]
     objs = []
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or ptxas_info or _stale(o, [s] + headers):
-            extra = ["-Xptxas", "-v"] if ptxas_info else []
+            extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DFM_DEBUG"] if debug else [])
             jobs.append([NVCC, *_flags(extra), "-c", s, "-o", o])
 
     def run(cmd):
@@ -56,12 +60,12 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with ThreadPoolExecutor(max_workers=min(8, max(1, len(jobs)))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([NVCC, *ARCH, "-shared", "-o", tmp, *objs])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv, debug="--debug" in sys.argv))

@@ -696,6 +696,11 @@ int fm_sync_status(fm_stream_t stream) {
   if (w[0] != 0) {
     const unsigned int zero[kErrWords] = {};
     cudaMemcpyToSymbol(g_dev_error, zero, sizeof zero);
+    if (w[0] == kDevErrDebugIndex)
+      return fail(FM_ERR_INDEX,
+                  "a debug build's index check failed and skipped the access (site %u, index %llu, block %u, "
+                  "thread %u); outputs are invalid",
+                  w[1], (unsigned long long)w[2] | ((unsigned long long)w[3] << 32), w[4], w[5]);
     return fail(FM_ERR_TIMEOUT,
                 "a kernel pipeline wait ran past its limit (role %u, barrier %u, tile %u, block (%u,%u,%u), "
                 "thread %u); outputs are invalid",

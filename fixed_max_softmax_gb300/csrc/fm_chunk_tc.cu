@@ -408,6 +408,14 @@ __device__ __forceinline__ int opaque_laneid() {
   return l;
 }
 
+// What the debug build (FM_DEBUG) checks a warp's epilogue accesses against; unused otherwise:
+// the flat row index of the warp's first row over [B, H, Sq], the rows of the accumulators, the
+// offset of the warp's first row of o and the span of o, in elements.
+struct EpiCheck {
+  unsigned int *err;
+  int64_t flat0, rows, out_off0, out_span;
+};
+
 // O of one warp's 32 rows (its TMEM lane quarter) into the fp32 accumulator, added (red) or
 // stored, without reading it through the SM: each 32-column piece goes from TMEM through the
 // warp's own 4 KiB of shared memory (32 rows x 128 bytes, 16-byte chunks XOR-swizzled by row,
@@ -417,7 +425,7 @@ __device__ __forceinline__ int opaque_laneid() {
 // acc_row0 its accumulator row; rows at or past Sq are left out.
 template <bool IN_LOOP = false>
 __device__ __forceinline__ void o_to_acc_warp(uint8_t *slab, uint32_t tO, int lane, bool tile_ok, int64_t row0,
-                                              int64_t Sq, float *acc_row0, bool add) {
+                                              int64_t Sq, float *acc_row0, bool add, EpiCheck ck) {
   if constexpr (IN_LOOP) lane = opaque_laneid();
   const int ch = lane & 7;
 #pragma unroll
@@ -434,7 +442,7 @@ __device__ __forceinline__ void o_to_acc_warp(uint8_t *slab, uint32_t tO, int la
     for (int i = 0; i < 8; ++i) {
       const int rr = i * 4 + (lane >> 3);
       const uint4 v = *reinterpret_cast<const uint4 *>(slab + rr * 128 + ((ch ^ (rr & 7)) << 4));
-      if (tile_ok && row0 + rr < Sq) {
+      if (tile_ok && row0 + rr < Sq && FM_DCHECK(ck.flat0 + rr < ck.rows, ck.err, 1u, ck.flat0 + rr)) {
         float *dst = acc_row0 + rr * kHD + c * 32 + ch * 4;
         if (add) red_add_v4(dst, v.x, v.y, v.z, v.w);
         else *reinterpret_cast<uint4 *>(dst) = v;
@@ -488,6 +496,9 @@ struct TcParams {
   // persistent schedule: CTAs x >= n_items mod gridDim.x, which have one item fewer than the
   // others, start (x - that) * stagger_ns later (0: no stagger)
   unsigned long long stagger_ns;
+  // debug builds: the accumulator rows (B*H*Sq) and the span of `out` in elements that the
+  // epilogue's index checks compare against
+  int64_t dbg_rows, dbg_out_span;
 };
 
 // The epilogue that reads the accumulator, for one warp's 32 rows: x = acc + O on fixed-m rows,
@@ -506,7 +517,8 @@ struct TcParams {
 template <bool IN_LOOP = false>
 __device__ __forceinline__ void acc_merge_warp(uint8_t *slab, uint32_t tO, int lane, bool tile_ok, int64_t row0,
                                                int64_t Sq, float *acc_row0, bool rd, bool fixed, float cprev,
-                                               float cnew, float inv, void *out_row0, int64_t osS, bool out_bf16) {
+                                               float cnew, float inv, void *out_row0, int64_t osS, bool out_bf16,
+                                               EpiCheck ck) {
   if constexpr (IN_LOOP) lane = opaque_laneid();
   const int ch = lane & 7;
   const int nrows = tile_ok ? (int)max((int64_t)0, min((int64_t)32, Sq - row0)) : 0;  // valid rows of the warp
@@ -519,8 +531,10 @@ __device__ __forceinline__ void acc_merge_warp(uint8_t *slab, uint32_t tO, int l
   uint4 nxt[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i)
-    nxt[i] = (rd && i * 4 + (lane >> 3) < nrows) ? __ldcg(reinterpret_cast<const uint4 *>(acc_lane + i * 4 * kHD))
-                                                 : make_uint4(0u, 0u, 0u, 0u);
+    nxt[i] = (rd && i * 4 + (lane >> 3) < nrows &&
+              FM_DCHECK(ck.flat0 + i * 4 + (lane >> 3) < ck.rows, ck.err, 2u, ck.flat0 + i * 4 + (lane >> 3)))
+                 ? __ldcg(reinterpret_cast<const uint4 *>(acc_lane + i * 4 * kHD))
+                 : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -532,7 +546,8 @@ __device__ __forceinline__ void acc_merge_warp(uint8_t *slab, uint32_t tO, int l
     if (c < 3) {
 #pragma unroll
       for (int i = 0; i < 8; ++i)
-        nxt[i] = (rd && i * 4 + (lane >> 3) < nrows)
+        nxt[i] = (rd && i * 4 + (lane >> 3) < nrows &&
+                  FM_DCHECK(ck.flat0 + i * 4 + (lane >> 3) < ck.rows, ck.err, 2u, ck.flat0 + i * 4 + (lane >> 3)))
                      ? __ldcg(reinterpret_cast<const uint4 *>(acc_lane + i * 4 * kHD + (c + 1) * 32))
                      : make_uint4(0u, 0u, 0u, 0u);
     }
@@ -575,7 +590,8 @@ __device__ __forceinline__ void acc_merge_warp(uint8_t *slab, uint32_t tO, int l
       for (int i = 0; i < 4; ++i) {
         const int rr = i * 8 + (lane >> 2);
         const uint4 v = *reinterpret_cast<const uint4 *>(slab + rr * 128 + (((2 * c4) ^ (rr & 7)) << 4));
-        if (rr < nrows)
+        if (rr < nrows && FM_DCHECK(ck.out_off0 + rr * osS + c * 32 + c4 * 8 + 7 < ck.out_span, ck.err, 4u,
+                                    ck.out_off0 + rr * osS + c * 32 + c4 * 8))
           *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(out_row0) + rr * osS + c * 32 + c4 * 8) = v;
       }
     } else {
@@ -583,7 +599,10 @@ __device__ __forceinline__ void acc_merge_warp(uint8_t *slab, uint32_t tO, int l
       for (int i = 0; i < 8; ++i) {
         const int rr = i * 4 + (lane >> 3);
         const uint4 v = *reinterpret_cast<const uint4 *>(slab + rr * 128 + ((ch ^ (rr & 7)) << 4));
-        if (rr < nrows) {
+        if (rr < nrows &&
+            (final_out ? FM_DCHECK(ck.out_off0 + rr * osS + c * 32 + ch * 4 + 3 < ck.out_span, ck.err, 4u,
+                                   ck.out_off0 + rr * osS + c * 32 + ch * 4)
+                       : FM_DCHECK(ck.flat0 + rr < ck.rows, ck.err, 3u, ck.flat0 + rr))) {
           float *dst = final_out ? reinterpret_cast<float *>(out_row0) + rr * osS + c * 32 + ch * 4
                                  : acc_row0 + rr * kHD + c * 32 + ch * 4;
           *reinterpret_cast<uint4 *>(dst) = v;
@@ -1034,8 +1053,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (plain_add && !final_out) {
         // the warp's first row is row - lane
         o_to_acc_warp(gbase + (t == 0 ? kOffQ : kOffKV) + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
-                      p.acc_o + (rflat - lane) * kHD, p.accumulate != 0);
-        if (row_ok) {
+                      p.acc_o + (rflat - lane) * kHD, p.accumulate != 0,
+                      EpiCheck{p.err, rflat - lane, p.dbg_rows, 0, 0});
+        if (row_ok && FM_DCHECK(rflat < p.dbg_rows, p.err, 5u, rflat)) {
           p.acc_sum[rflat] = sum_new;
           p.acc_max[rflat] = shift_new;
         }
@@ -1046,15 +1066,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O*cnew); whole-row accesses per warp through its 4 KiB slab
       const float inv = final_out ? 1.0f / fmaxf(sum_new, FM_SUM_CLAMP) : 1.0f;
       void *out_row0 = nullptr;
+      int64_t out_off0 = 0;
       if (final_out) {
         const int64_t ooff0 = (bh / p.H) * p.osB + (bh % p.H) * p.osH + (row - lane) * p.osS;
+        out_off0 = ooff0;
         out_row0 = p.out_bf16 ? static_cast<void *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + ooff0)
                               : static_cast<void *>(reinterpret_cast<float *>(p.out) + ooff0);
       }
       acc_merge_warp(gbase + (t == 0 ? kOffQ : kOffKV) + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
                      p.acc_o + (rflat - lane) * kHD, p.accumulate != 0, fixed, cprev, cnew, inv, out_row0, p.osS,
-                     p.out_bf16 != 0);
-      if (row_ok) {
+                     p.out_bf16 != 0,
+                     EpiCheck{p.err, rflat - lane, p.dbg_rows, out_off0, p.dbg_out_span});
+      if (row_ok && FM_DCHECK(rflat < p.dbg_rows, p.err, 5u, rflat)) {
         p.acc_sum[rflat] = sum_new;
         p.acc_max[rflat] = shift_new;
         if (final_out && p.lse) p.lse[rflat] = 0.69314718055994531f * (shift_new + log2f(sum_new));
@@ -1405,14 +1428,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit_and_wait_smem_read();
           }
         }
-        if (row_ok) {
+        if (row_ok && FM_DCHECK(rflat < p.dbg_rows, p.err, 5u, rflat)) {
           p.acc_sum[rflat] = sum_new;
           p.acc_max[rflat] = shift_new;
         }
       } else if (plain_add && !final_out) {
         o_to_acc_warp<true>(gbase + kOffPStage + t * kBoxBytes + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
-                      p.acc_o + (rflat - lane) * kHD, p.accumulate != 0);
-        if (row_ok) {
+                            p.acc_o + (rflat - lane) * kHD, p.accumulate != 0,
+                            EpiCheck{p.err, rflat - lane, p.dbg_rows, 0, 0});
+        if (row_ok && FM_DCHECK(rflat < p.dbg_rows, p.err, 5u, rflat)) {
           p.acc_sum[rflat] = sum_new;
           p.acc_max[rflat] = shift_new;
         }
@@ -1423,15 +1447,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O*cnew); whole-row accesses per warp through its 4 KiB slab
       const float inv = final_out ? 1.0f / fmaxf(sum_new, FM_SUM_CLAMP) : 1.0f;
       void *out_row0 = nullptr;
+      int64_t out_off0 = 0;
       if (final_out) {
         const int64_t ooff0 = (bh / p.H) * p.osB + (bh % p.H) * p.osH + (row - lane) * p.osS;
+        out_off0 = ooff0;
         out_row0 = p.out_bf16 ? static_cast<void *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + ooff0)
                               : static_cast<void *>(reinterpret_cast<float *>(p.out) + ooff0);
       }
       acc_merge_warp<true>(gbase + kOffPStage + t * kBoxBytes + wq * 4096, tO, lane, tile_ok, row - lane, p.Sq,
                      p.acc_o + (rflat - lane) * kHD, p.accumulate != 0, fixed, cprev, cnew, inv, out_row0, p.osS,
-                     p.out_bf16 != 0);
-      if (row_ok) {
+                     p.out_bf16 != 0,
+                     EpiCheck{p.err, rflat - lane, p.dbg_rows, out_off0, p.dbg_out_span});
+      if (row_ok && FM_DCHECK(rflat < p.dbg_rows, p.err, 5u, rflat)) {
         p.acc_sum[rflat] = sum_new;
         p.acc_max[rflat] = shift_new;
         if (final_out && p.lse) p.lse[rflat] = 0.69314718055994531f * (shift_new + log2f(sum_new));
@@ -1612,6 +1639,17 @@ cudaError_t launch_chunk_tc(const ChunkArgs &a, cudaStream_t st) {
   }
   p.n_pairs = (a.nqb + 1) / 2;
   p.n_items = p.n_pairs * a.q.H * a.q.B;
+  // what the debug build's epilogue index checks compare against: the accumulator rows, and
+  // the elements from o's first one to one past its last (positive strides on the fused path)
+  p.dbg_rows = a.q.B * a.q.H * a.q.S;
+  p.dbg_out_span = a.out ? (a.out->B - 1) * a.out->sB + (a.out->H - 1) * a.out->sH + (a.out->S - 1) * a.out->sS +
+                               (a.out->D - 1) * a.out->sD + 1
+                         : 0;
+#ifdef FM_DEBUG
+  // test hook of debug builds: FM_DEBUG_SHRINK_ROWS=n declares the accumulators n rows short,
+  // so that the checks must catch (and skip) the last rows' accesses
+  if (const char *shrink = getenv("FM_DEBUG_SHRINK_ROWS")) p.dbg_rows -= atoll(shrink);
+#endif
   const int sms = current_device_sm_count();
   p.persistent = use_persistent(a.schedule) ? 1 : 0;
   // non-final chunks of the persistent schedule add O into acc_o with bulk tensor operations

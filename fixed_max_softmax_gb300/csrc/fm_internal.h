@@ -20,7 +20,31 @@ enum : unsigned int {
   kDevErrTimeoutDrain = 4,
   kDevErrTimeoutProbe = 5,
   kDevErrTimeoutBounds = 6,
+  kDevErrDebugIndex = 7,  // debug builds: an index check failed (the access was skipped)
 };
+
+// Debug builds (nvcc -DFM_DEBUG): FM_DCHECK(ok, err, site, index) is false when `ok` is, and then
+// records the first failure of the launch in the error word (code, site, the index, block and
+// thread) for fm_sync_status to report as FM_ERR_INDEX; the caller skips the access.  Release
+// builds: always true, nothing is checked.
+#ifdef FM_DEBUG
+#ifdef __CUDACC__
+__device__ __forceinline__ bool fm_dcheck(bool ok, unsigned int *err, unsigned int site, long long index) {
+  if (ok) return true;
+  if (err && atomicCAS(err, 0u, (unsigned int)kDevErrDebugIndex) == 0u) {
+    err[1] = site;
+    err[2] = (unsigned int)((unsigned long long)index & 0xffffffffull);
+    err[3] = (unsigned int)((unsigned long long)index >> 32);
+    err[4] = blockIdx.x;
+    err[5] = threadIdx.x;
+  }
+  return false;
+}
+#endif
+#define FM_DCHECK(ok, err, site, index) fm_dcheck((ok), (err), (site), (long long)(index))
+#else
+#define FM_DCHECK(ok, err, site, index) true
+#endif
 
 // Default limit of a pipeline wait inside a kernel.  One CTA of the chunk kernel runs
 // for well under 10 ms at the largest sizes, so a wait that lasts seconds means a

@@ -67,7 +67,8 @@ enum {
   FM_ERR_UNSUPPORTED = 4,     /* D not in {64, 128}; GQA (k.H != q.H); misaligned data */
   FM_ERR_BOUNDS_MISMATCH = 5, /* bounds do not belong to this call (see fm_attn_chunk) */
   FM_ERR_CUDA = 6,            /* a CUDA runtime call or kernel launch failed */
-  FM_ERR_TIMEOUT = 7          /* a kernel's pipeline wait ran past its limit */
+  FM_ERR_TIMEOUT = 7,         /* a kernel's pipeline wait ran past its limit */
+  FM_ERR_INDEX = 8            /* debug builds only (FM_DEBUG): a kernel's index check failed */
 };
 
 #define FM_BOUNDS_MAGIC 0x314D4246u /* tag written by fm_bounds ("FBM1") */
@@ -299,7 +300,9 @@ FM_API int fm_fold_sinks(const fm_tensor *q, fm_bounds_out *bounds, const fm_opt
 
 /* fm_sync_status -- synchronise `stream`, then report and clear this GPU's device
  * error word: FM_ERR_TIMEOUT if a kernel gave up on a pipeline wait (its outputs are
- * then invalid), FM_ERR_CUDA on an asynchronous CUDA error, else FM_OK. */
+ * then invalid), FM_ERR_INDEX if a debug build's index check failed (the library built with
+ * -DFM_DEBUG: the chunk kernels check their epilogue accesses to the accumulators and o, skip
+ * a failing one and record the first), FM_ERR_CUDA on an asynchronous CUDA error, else FM_OK. */
 FM_API int fm_sync_status(fm_stream_t stream);
 
 /* fm_probe_wait_timeout -- exercise the failure path of the kernels' bounded waits: one

@@ -306,3 +306,15 @@ int main(void) {
     major, rc, ws, *msg = r.stdout.split()
     assert int(major) == 1 and int(rc) == fm.FM_ERR_DTYPE and int(ws) == fm.fm_bounds_workspace_size(1, 40, 75600, 128)
     assert "fp16" in " ".join(msg)
+
+
+def test_debug_build_exports_the_same_abi():
+    """The debug build (-DFM_DEBUG, the kernels' index checks on) is the same C ABI: the same
+    exported symbols and nothing else."""
+    from fixed_max_softmax_gb300 import build as fmbuild
+
+    dbg = fmbuild.build(debug=True)
+    assert dbg == fm.DEBUG_LIB_PATH and os.path.exists(dbg)
+    names = lambda p: {ln.split()[-1] for ln in os.popen(f"nm -D --defined-only {p}").read().split("\n")
+                       if ln.strip() and ln.split()[-1].startswith("fm_")}
+    assert names(dbg) == names(fm.LIB_PATH) == set(fm.ABI_SYMBOLS)
