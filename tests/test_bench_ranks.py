@@ -65,3 +65,31 @@ def test_clock_summary_keys_with_and_without_samples():
     assert keys <= set(full) and full["samples"] == 2
     assert full["sm_mhz"] == 1985.0 and full["sm_max_mhz"] == 2070.0 and full["reasons"] == ["sw_power_cap"]
     assert abs(full["power_w"] - 1207.685) < 1e-9
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` runs on host cores alone (the CPU oracle on a bounded sample)
+    and prints one JSON line with the keys of the bench contract, for the same metric and
+    workload as the GPU arm."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "2",
+                        "--warmup", "0", "--ref-rows", "4"], cwd=root, env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["steps"] == 2 and d["warmup"] == 3 and d["n_gpus"] == 1 and d["higher_is_better"] is True
+    assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["cores"] >= 1 and "4 query rows" in d["cpu_baseline"]["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("wan")
