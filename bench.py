@@ -397,8 +397,28 @@ def run_ours(args, rank, world, local_rank):
             b.record(stream)
             torch.cuda.synchronize(dev)
             link[name] = src.numel() * src.element_size() / (a.elapsed_time(b) * 1e-3) / 1e9
+        # the same upload (Q, K and V of one step) on a second stream beside one step's kernels:
+        # does the link keep its rate under load, and does the step keep its time?
+        side = torch.cuda.Stream(dev)
+        up_dst = [torch.empty_like(t) for t in (q, k, v)]
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c.record(side)
+        a.record(stream)
+        with torch.cuda.stream(side):
+            for dst, src in zip(up_dst, (qh, kh, vh)):
+                dst.copy_(src, non_blocking=True)
+        step()
+        b.record(stream)
+        d.record(side)
+        torch.cuda.synchronize(dev)
+        fm.fm_sync_status(stream)
+        link["h2d_gbs_beside_step"] = 3 * tensor_bytes / (c.elapsed_time(d) * 1e-3) / 1e9
+        link["step_ms_beside_upload"] = a.elapsed_time(b)
+        del up_dst
         e2e = {"value": whole_job_tflops(world, step_flops, args.e2e_steps, te), "unit": "TFLOP/s",
-               "host_link": {k2: round(v2, 1) for k2, v2 in link.items()},
+               "host_link": {k2: round(v2, 2 if k2.startswith("step") else 1) for k2, v2 in link.items()},
                "clocks": {k2: ce[k2] for k2 in ("sm_mhz", "power_w", "reasons", "samples")},
                "h2d_bytes_per_step": int(3 * q.numel() * q.element_size()),
                "d2h_bytes_per_step": int(fa.out.numel() * fa.out.element_size()),
