@@ -29,7 +29,8 @@
 //              the norms pass with atomics on a zeroed workspace word), U, m and flag of its 16
 //              Q-blocks, and every row's shift b_i = m_i + alpha*q_i.kbar (m_i per row or per
 //              Q-block)
-// One memset before them zeroes the V-max word and the per-head arrival counters of step 1.
+// One memset before them zeroes the V-max word and the per-head arrival counters of step 1;
+// without centering the finish writes kbar as zeros.
 // Bytes: Q + K + V once each, plus K once more for the mean when centering.
 #include <cuda_bf16.h>
 #include <limits.h>
@@ -1155,7 +1156,8 @@ __global__ void __launch_bounds__(kThreads)
 // floats), so a CTA takes enough rows (8 a thread, their loads issued before that reduction) for
 // the reduction's latency to be paid rarely; the first CTA of a head writes kmax_sq, the first
 // CTA of all copies the V max out of the workspace into vmax_sq.
-// `shift` holds |q_i|^2 on entry (from the norms pass).
+// `shift` holds |q_i|^2 on entry (from the norms pass).  Without centering the first CTA of a
+// head also writes the head's key mean as zeros (kbar_zero; no memset of its own).
 constexpr int kFinishRowsPerThread = 8;
 constexpr int kFinishRows = kThreads * kFinishRowsPerThread;  // 2048 rows, 16 Q-blocks
 constexpr int kFinishBlocks = kFinishRows / kQRows;
@@ -1164,10 +1166,11 @@ __global__ void __launch_bounds__(kThreads)
     finish_shift_kernel(int64_t H, int64_t Sq, int64_t nqb, int64_t nkb, const float *kblk, const float *vmax_all,
                         double alpha, int C, int gate, int per_row, const float *qmax_sq, float *kmax_sq,
                         float *vmax_sq, int32_t *m, uint8_t *flag, const float *qkbar, float *shift,
-                        int kmax_given) {
+                        int kmax_given, float *kbar_zero, int D) {
   pdl_wait();  // inputs written by the kernels before this one
   pdl_trigger();
   const int64_t bh = blockIdx.z * H + blockIdx.y;
+  if (kbar_zero && blockIdx.x == 0 && threadIdx.x < D) kbar_zero[bh * D + threadIdx.x] = 0.f;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   __shared__ float red[kWarps];
   __shared__ int32_t mblk[kFinishBlocks];
@@ -1573,9 +1576,11 @@ cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st
   unsigned int *count = reinterpret_cast<unsigned int *>(ws + w.off_zero + 16);
   cudaError_t e = cudaMemsetAsync(ws + w.off_zero, 0, w.zero_bytes, st);
   if (e != cudaSuccess) return e;
+  // without centering no kernel reads the key mean: the finish writes it as zeros
+  const bool kbar_by_finish = !a.centering && a.q.D <= kThreads;
   if (a.centering && N > 0) {
     e = launch_ksum<T, EPL, CONTIG>(a.k, w.P, part, count, N, a.kbar, st);
-  } else {
+  } else if (!kbar_by_finish) {
     e = cudaMemsetAsync(a.kbar, 0, sizeof(float) * (size_t)(B * H * a.q.D), st);
   }
   if (e != cudaSuccess) return e;
@@ -1590,7 +1595,8 @@ cudaError_t launch_typed(const BoundsArgs &a, const WsLayout &w, cudaStream_t st
   const int64_t nx = ceil_div(a.q.S, kFinishRows) > 0 ? ceil_div(a.q.S, kFinishRows) : 1;
   e = launch_pdl(finish_shift_kernel, dim3((unsigned)nx, (unsigned)H, (unsigned)B), dim3(kThreads), 0, st, H, a.q.S,
                  a.nqb, w.nkb, kblk, vmax_ws, a.alpha, a.C, a.gate, a.per_row, a.qmax_sq, a.kmax_sq, a.vmax_sq, a.m,
-                 a.flag, a.qkbar, a.shift, (int)(a.n_sink > 0));
+                 a.flag, a.qkbar, a.shift, (int)(a.n_sink > 0), kbar_by_finish ? a.kbar : nullptr,
+                 (int)a.q.D);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

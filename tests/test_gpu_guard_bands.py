@@ -52,6 +52,12 @@ class Guarded:
             ok = ok and bool(np.all(body[:, self.shape[-1]:] == pat))
         return ok
 
+    def fully_written(self):
+        """No element of the tensor itself still holds the fill pattern."""
+        bits = self.flat_bits.cpu().numpy().astype(np.int64) & ((1 << (8 * self.flat_bits.element_size())) - 1)
+        body = bits[GUARD:GUARD + self.n_inner].reshape(-1, self.shape[-1] + self.pad)[:, :self.shape[-1]]
+        return bool(np.all(body != self.pattern))
+
 
 def guarded_bounds(B, H, Sq, D, dev):
     """fm.Bounds whose device arrays live inside guard bands; returns (bounds, guards)."""
@@ -152,6 +158,13 @@ def test_no_write_outside_any_buffer(dev, Sq, path):
     fm.fm_sync_status()
     broken = [name for name, g in guards.items() if not g.intact()]
     assert not broken, f"writes outside {broken} (Sq={Sq}, path={path})"
+    # every bounds array the pass fills is written in full (each started as the fill pattern),
+    # the key mean included: the oracle's with centering, zeros without
+    unwritten = [n for n in ("m", "flag", "qmax_sq", "kmax_sq", "kbar", "qkbar", "shift", "vmax_sq")
+                 if not guards[n].fully_written()]
+    assert not unwritten, f"bounds arrays not fully written: {unwritten} (Sq={Sq}, path={path})"
+    ob = oracle.bounds(q, k, v, centering=path == "online")
+    np.testing.assert_allclose(bounds.kbar.cpu().numpy(), ob["kbar"], rtol=1e-5, atol=2e-6)
     got = out.t.float().cpu().numpy()
     if dtype == torch.float32:  # 1e-5, widened for the head whose keys are a hundred times louder
         for h in range(H):
