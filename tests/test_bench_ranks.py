@@ -37,7 +37,7 @@ def test_two_gloo_ranks_take_the_slowest_time():
     world = 2
     times = [80.0, 95.5]
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of this (threaded) process
         out = m.dict()
         mp.start_processes(_rank, args=(world, port, times, out), nprocs=world, start_method="spawn", join=True)
         res = dict(out)

@@ -125,7 +125,7 @@ def _rank(rank, world, port, centering, prefetch, results):
 @pytest.mark.parametrize("world,centering,prefetch", [(2, True, 2), (3, True, 2), (3, False, 1)])
 def test_ring_delivers_every_shard_in_order_with_its_offset(world, centering, prefetch):
     port = _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of this (threaded) process
         results = m.dict()
         mp.start_processes(_rank, args=(world, port, centering, prefetch, results), nprocs=world,
                            start_method="spawn", join=True)
