@@ -1,6 +1,6 @@
 """The scale-aware parity bars (tests/parity.py) can fail: CPU checks with oracle outputs only.
 
-At the pages' workloads |o| is about as large as the benchmark spec's 2e-2 bar, so that bar alone
+At the pages' workloads |o| is about as large as the absolute 2e-2 bar, so that bar alone
 passes an all-zero output.  These tests show that the added bars reject the outputs a broken
 kernel would produce -- zero, scaled by 0.9, ten times noisier than bf16 P, a row from the
 wrong query, a chunk of keys left out -- and accept the oracle's own bf16-P reference and
@@ -36,7 +36,7 @@ def test_accepts_bf16_references(case):
 def test_zero_output_passes_the_absolute_bar_but_not_these(case):
     _, _, _, ref = case
     zero = np.zeros_like(ref.o)
-    assert np.abs(zero - ref.o).max() <= parity.TOL_BF16  # what the benchmark spec's bar alone lets through
+    assert np.abs(zero - ref.o).max() <= parity.TOL_BF16  # what the absolute bar alone lets through
     with pytest.raises(AssertionError):
         parity.assert_bf16_parity(zero, ref.o, ref.model, ref.abs_v)
 
@@ -78,7 +78,7 @@ def test_a_non_finite_element_fails(case):
         parity.assert_bf16_parity(bad, ref.o, ref.model, ref.abs_v)
 
 
-def test_f32_bar_is_north_stars_at_the_fp32_workload():
+def test_f32_bar_is_the_plain_1e5_at_the_fp32_workload():
     q, k, _ = workloads.make_inputs("tiny")
     assert parity.f32_bar(q[0], k[0]) == parity.TOL_F32
     # a key a hundred times louder widens it in proportion to the bound U
